@@ -1,0 +1,483 @@
+"""Benchmark of the tree verify step on one GB300 (or N independent replicas).
+
+One step = one pass of the whole hot path over one batch of the long-context
+verify workload (4 requests, 32 q / 8 kv heads, d 128, prefix 32768, 32-node
+trees, vocab 152064, 64 layers):
+
+  1. tree-masked GQA attention of one layer (tree_attn_forward),
+  2. greedy acceptance over the vocab logits (tree_accept_greedy),
+  3. target-side re-root + KV compaction over 64 layers (tree_cache_compact),
+  4. draft-side re-root + KV compaction of the 64-node draft trees over the
+     draft cache's 64 layers (tree_cache_compact).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.  With torchrun and N > 1 every
+rank runs its own replica of the workload (no data exchange: requests are
+independent), and the value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tree tokens/s and achieved HBM GB/s (fraction of ~8 TB/s) per attention layer"
+UNIT = "tree tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="longctx_verify_b4_p32k",
+                    choices=["longctx_verify_b4_p32k", "verify_b8_tree16", "chain_verify_b16_paged",
+                             "expand_w8_prefix2048", "tree16_prefix128"])
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}", "--format=csv,noheader",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1].split()[0]), float(parts[2].split()[0]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+def attn_algorithmic_bytes(case) -> int:
+    """K and V rows each read once per (request, KV head), Q read, O and lse written, metadata."""
+    keys = sum(int(case.prefix_len[b]) + int(case.n_tree[b]) for b in range(case.num_req))
+    kv = keys * case.num_kv_heads * case.head_dim * 2 * 2
+    qo = 2 * case.num_req * case.n_query * case.num_q_heads * case.head_dim * 2
+    lse = case.num_req * case.num_q_heads * case.n_query * 4
+    meta = case.num_req * (case.n_tree_max + 2) * 4
+    if case.paged:
+        meta += case.block_table.size * 4
+    return kv + qo + lse + meta
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_forward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, path: str):
+    """Per-launch DRAM bytes of the attention kernels from a committed ncu summary, if still current."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(workload, {}).get(path)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e["dram_bytes_per_launch"]
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+def build_step(args, torch, ts, W, device):
+    """Allocate the workload on the device and return (step_fn, info)."""
+    wl = getattr(W, args.workload)
+    kw = {"num_layers": args.layers} if args.workload.startswith("longctx") else {}
+    w = wl(**kw)
+    from tests.gpu_util import attn_inputs, i32_dev  # noqa: E402
+    stream = torch.cuda.current_stream()
+    calls = []        # (name, fn) run in order each step
+    info = {"workload": w.name, "attn_cases": w.attn}
+    tokens_per_step = 0
+    attn_bytes = 0
+    attn_calls = []
+    for case in w.attn:
+        d = attn_inputs(case)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((case.num_req, case.num_q_heads, case.n_query), dtype=torch.float32, device=device)
+        a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"], out, lse,
+                         d.get("block_table"), case.softmax_scale, args.force_path)
+        ws = ts.new_workspace(ts.tree_attn_workspace_size(a), device)
+        attn_calls.append((a, ws, d, out, lse))
+        tokens_per_step += case.num_req * case.n_query
+        attn_bytes += attn_algorithmic_bytes(case)
+    info["attn_bytes"] = attn_bytes
+    info["attn_inputs"] = attn_calls
+    launches = 2 * len(attn_calls)
+
+    acc_state = None
+    if w.accept is not None:
+        A = w.accept
+        logits = torch.from_numpy(A.logits).to(device)
+        tok = i32_dev(A.tokens)
+        res = {k: torch.empty(s, dtype=torch.int32, device=device) for k, s in [
+            ("argmax", (A.num_req, A.n_tree_max)), ("path", (A.num_req, A.n_tree_max)),
+            ("accept_len", (A.num_req,)), ("bonus", (A.num_req,)), ("verified", (A.num_req, A.n_tree_max + 1)),
+            ("verified_len", (A.num_req,))]}
+        par = attn_calls[0][2]["parent"] if attn_calls else i32_dev(A.parent)
+        ntree = attn_calls[0][2]["n_tree"] if attn_calls else i32_dev(A.n_tree)
+        aa = ts.accept_args(logits, tok, par, ntree, **res)
+        aws = ts.new_workspace(ts.tree_accept_workspace_size(aa), device)
+        acc_state = (aa, aws, logits, tok, res)
+        launches += 2
+        info["accept_bytes"] = A.logits.nbytes
+
+    comp_states = []
+    if w.compact is not None and acc_state is not None:
+        res = acc_state[4]
+        for side, C in (("target", w.compact), ("draft", w.compact_draft)):
+            if C is None:
+                continue
+            layers = w.num_layers
+            case0 = w.attn[0]
+            max_kv = int(C.prefix_len.max()) + C.n_tree_max
+            hkv, d = case0.num_kv_heads, case0.head_dim
+            g = torch.Generator(device=device)
+            g.manual_seed(1 + len(comp_states))
+            shape = (C.num_req, max_kv, hkv, d)
+            kl, vl = [], []
+            for li in range(layers):
+                if side == "target" and li == 0 and not case0.paged and case0.max_kv_len == max_kv:
+                    kl.append(attn_calls[0][2]["k_cache"])
+                    vl.append(attn_calls[0][2]["v_cache"])
+                    continue
+                kl.append(torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16))
+                vl.append(torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16))
+            kp, vp = ts.layer_pointer_table(kl, device), ts.layer_pointer_table(vl, device)
+            outs = {k: torch.empty(s, dtype=torch.int32, device=device) for k, s in [
+                ("new_prefix_len", (C.num_req,)), ("new_n_tree", (C.num_req,)),
+                ("new_parent", (C.num_req, C.n_tree_max)), ("new_tokens", (C.num_req, C.n_tree_max)),
+                ("src_rows", (C.num_req, C.n_tree_max))]}
+            P, N, par, tok = i32_dev(C.prefix_len), i32_dev(C.n_tree), i32_dev(C.parent), i32_dev(C.tokens)
+            ca = ts.compact_args(kp, vp, layers, hkv, d, P, N, par, tok, res["verified"], res["verified_len"],
+                                 outs["new_prefix_len"], outs["new_n_tree"], outs["new_parent"], outs["new_tokens"],
+                                 outs["src_rows"], max_kv)
+            cws = ts.new_workspace(ts.tree_compact_workspace_size(ca), device)
+            comp_states.append((ca, cws, kl, vl, kp, vp, P, N, par, tok, outs, side))
+            launches += 2
+
+    def step():
+        for a, ws, *_ in attn_calls:
+            ts.tree_attn_forward_args(a, ws)
+        if acc_state is not None:
+            ts.tree_accept_greedy_args(acc_state[0], acc_state[1])
+        for st in comp_states:
+            ts.tree_cache_compact_args(st[0], st[1])
+
+    info.update(tokens_per_step=tokens_per_step, launches=launches, acc_state=acc_state, comp_states=comp_states,
+                workload_obj=w)
+    return step, info
+
+
+def e2e_measure(args, torch, ts, info, steps, warmup):
+    """Same step through the public API with host (pinned) inputs copied in and results copied out every step."""
+    dev_bufs, host_bufs = [], []
+    for a, ws, d, out, lse in info["attn_inputs"]:
+        dev_bufs.append(d["q"])
+    acc = info["acc_state"]
+    if acc is not None:
+        dev_bufs += [acc[2], acc[3]]
+    for st in info["comp_states"]:
+        dev_bufs += [st[8], st[9]]          # parent, tokens (tree metadata)
+    for t in dev_bufs:
+        host_bufs.append(torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()))
+    outs = [o for *_, o, l in info["attn_inputs"]] + [l for *_, l in info["attn_inputs"]]
+    if acc is not None:
+        outs += list(acc[4].values())
+    for st in info["comp_states"]:
+        outs += list(st[10].values())
+    host_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_bufs)
+    d2h = sum(t.numel() * t.element_size() for t in host_outs)
+
+    def step():
+        for h, dv in zip(host_bufs, dev_bufs):
+            dv.copy_(h, non_blocking=True)
+        info["step"]()
+        for dv, h in zip(outs, host_outs):
+            h.copy_(dv, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """Inputs of one request of the long-context workload for timing the CPU oracle."""
+
+    def __init__(self, layers: int):
+        import numpy as np
+
+        import workloads as W
+        from oracle import attention as OA
+        self.layers = layers
+        case = W.random_attn_case(0, num_req=1, hq=32, hkv=8, d=128, n_tree_max=32, prefix_range=(32768, 32768))
+        self.case = case
+        keys = 32768 + 32
+        # widening the bf16 inputs to fp64 is input preparation, done once
+        self.q = OA.bf16_bits_to_f64(case.q[0])
+        self.k = OA.bf16_bits_to_f64(case.k[0, :keys])
+        self.v = OA.bf16_bits_to_f64(case.v[0, :keys])
+        self.acc = W.random_accept_case(0, num_req=1, n_tree_max=32, vocab=152064, p_accept=0.8, ragged_tree=False)
+        self.rows = np.zeros((keys + 32, 8, 128), np.uint16)
+
+    def run(self, heads, one_query: bool = False):
+        """Times the oracle on `heads` q heads of attention (all 32 queries, or only the last
+        node's query), one acceptance, one re-root and one row compaction.
+
+        Returns the time of the full step (4 requests x 32 heads x 32 queries, 4
+        acceptances, 2 sides x 4 requests re-roots, 2 sides x 4 requests x layers
+        x {K, V} compactions) extrapolated linearly from the sample, and the
+        sample's wall time."""
+        from oracle import attention as OA
+        from oracle import tree as OT
+        nq = 1 if one_query else 32
+        q = self.q[32 - nq:]
+        t0 = time.perf_counter()
+        OA.tree_attention(q, self.k, self.v, 32768, 32, self.case.parent[0], nq, self.case.scale, heads)
+        t1 = time.perf_counter()
+        r = OT.greedy_accept(self.acc.logits[0], self.acc.tokens[0], self.acc.parent[0], 32)
+        t2 = time.perf_counter()
+        rr = OT.reroot(self.acc.parent[0], self.acc.tokens[0], 32, 32768, r.verified)
+        t3 = time.perf_counter()
+        OT.compact_rows(self.rows, 32768, rr.src)
+        t4 = time.perf_counter()
+        attn_scale = (4 * 32 / len(heads)) * (32 / nq)
+        full = attn_scale * (t1 - t0) + 4 * (t2 - t1) + 8 * (t3 - t2) + 8 * self.layers * 2 * (t4 - t3)
+        return full, t4 - t0
+
+
+def cpu_oracle_sample(args):
+    if not args.workload.startswith("longctx"):
+        return None
+    s = OracleSample(args.layers)
+    full, _ = s.run(list(range(4)))
+    return {"value": 128.0 / full, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": ("request 0 of the workload: fp64 attention of one KV-head group (4 q heads x 32 queries x "
+                       "32800 keys), greedy acceptance of its 32-node tree over 152064 logits, one re-root and one "
+                       "row compaction of one layer; extrapolated to the full step (4 requests x 32 heads, "
+                       "4 acceptances, 8 re-roots, 2 x 4 x %d layers x {K,V} compactions)" % args.layers)}
+
+
+def reference_arm(args):
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    if not args.workload.startswith("longctx"):
+        print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle sample is defined for the "
+                          "long-context workload only"}))
+        return
+    s = OracleSample(args.layers)
+    fulls = []
+    for i in range(args.warmup + args.steps):
+        full, _ = s.run([i % 32])   # one q head per step, all 32 queries; heads cycle
+        if i >= args.warmup:
+            fulls.append(full)
+    t = statistics.mean(fulls)
+    v = 128.0 / t
+    sample = ("per step: fp64 oracle attention of one q head of request 0 (32 queries x 32800 keys), greedy "
+              "acceptance of its 32-node tree over 152064 logits, one re-root and one row compaction of one "
+              "layer; extrapolated to the full step (4 requests x 32 heads x 32 queries, 4 acceptances, 8 re-roots, "
+              "2 x 4 x %d layers x {K,V} compactions)" % args.layers)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import torch
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    import speculative_decoding_tree_forward_gb300 as ts
+    import workloads as W
+
+    step, info = build_step(args, torch, ts, W, device)
+    info["step"] = step
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    for _, ws, *_ in info["attn_inputs"]:
+        code = ts.read_device_error(ws)
+        assert code == 0, f"device error word {code:#x}"
+
+    # attention launches timed on the launching stream inside the timed region
+    n_attn = len(info["attn_inputs"])
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        for a, ws, *_ in info["attn_inputs"]:
+            ts.tree_attn_forward_args(a, ws)
+        ev[i][1].record(stream)
+        if info["acc_state"] is not None:
+            ts.tree_accept_greedy_args(info["acc_state"][0], info["acc_state"][1])
+        for st in info["comp_states"]:
+            ts.tree_cache_compact_args(st[0], st[1])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop() if clocks else None
+    ms = t_start.elapsed_time(t_end) / args.steps
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps / n_attn
+    ms_max = max_over_ranks(ms, world)
+
+    tokens = info["tokens_per_step"] * world
+    value = tokens / (ms_max / 1e3)
+    peak, peak_kind = peaks()
+    attn_bytes = info["attn_bytes"] / n_attn
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+    path = ts.tree_attn_selected_path(info["attn_inputs"][0][0])
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(10, min(args.steps, 200))
+        e_ms, h2d, d2h = e2e_measure(args, torch, ts, info, e2e_steps, 3)
+        e_ms = max_over_ranks(e_ms, world)
+        e2e = {"value": tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_sample(args)
+    traffic = measured_traffic(info["workload"], path)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": info["workload"], "requests": info["attn_cases"][0].num_req,
+                   "q_heads": info["attn_cases"][0].num_q_heads, "kv_heads": info["attn_cases"][0].num_kv_heads,
+                   "head_dim": info["attn_cases"][0].head_dim, "tree_nodes": info["attn_cases"][0].n_tree_max,
+                   "layers_compacted": args.layers if info["comp_states"] else 0, "attention_path": path,
+                   "l2": "inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2" % (attn_bytes / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": f"tree_attn_forward ({path} kernel + LSE merge)",
+                     "algorithmic_bytes_per_launch": attn_bytes, "launch_ms": attn_ms},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": info["launches"] * args.steps,
+        "clocks": ck,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

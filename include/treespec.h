@@ -1,0 +1,253 @@
+/*
+ * treespec -- the speculative-decoding verify / expand step on one GB300 GPU.
+ *
+ * C ABI.  Every pointer named "device" is device memory owned by the caller;
+ * the library allocates nothing, keeps no global state besides one cached
+ * driver entry point, and never synchronises the stream it is given.  Every
+ * entry point validates its arguments on the host and returns a ts_status
+ * synchronously; kernels are launched asynchronously on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream).  Kernel-side faults in the
+ * metadata (a parent index out of range, a block-table entry out of range, a
+ * bounded wait that expired) never trap: they clamp the offending value and
+ * OR a TS_DEVERR_* bit into the error word at the start of the workspace,
+ * which ts_read_device_error() reports.
+ *
+ * Workspace: each call that takes one needs `*_workspace_size()` bytes of
+ * device memory, 256-byte aligned.  Its first 4 bytes are the sticky device
+ * error word: zero the whole workspace once before its first use
+ * (cudaMemset); afterwards the library keeps the rest consistent by itself
+ * and only ts_read_device_error(..., clear = 1) resets the word.  Calls that
+ * share one workspace must be ordered on one stream.
+ *
+ * Shapes use the pages' terms: a draft tree of n nodes (n = 1 + D for a
+ * verify block, the SwiftSpec summary's bs), the last n_query nodes as
+ * queries (w new leaves when expanding), G = num_q_heads / num_kv_heads query
+ * heads per KV head (NVIDIA draft-length article), a verified prefix of P
+ * tokens, and a parent array.  The KV cache of a request holds its P prefix
+ * rows followed by its n tree rows: tree node i is row P + i (SwiftSpec
+ * summary, §3.2, the prefix-cache / tree-cache invariant).
+ */
+#ifndef TREESPEC_H
+#define TREESPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TS_API __attribute__((visibility("default")))
+#else
+#define TS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ts_status {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = 1,   /* a null pointer, a negative or inconsistent size */
+  TS_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels implement */
+  TS_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  TS_ERR_WORKSPACE = 4      /* workspace missing, too small or misaligned */
+} ts_status;
+
+typedef enum ts_kv_layout {
+  TS_KV_CONTIGUOUS = 0,     /* [num_requests][max_kv_len][num_kv_heads][head_dim] */
+  TS_KV_PAGED = 1           /* pool [num_blocks][page_size][num_kv_heads][head_dim] + block table */
+} ts_kv_layout;
+
+/* Device error word bits (ts_read_device_error). */
+#define TS_DEVERR_BAD_PARENT 0x1u   /* parent[i] outside [-1, i): treated as -1 */
+#define TS_DEVERR_BAD_LENGTH 0x2u   /* prefix_len / n_tree / m outside its stated bound: clamped */
+#define TS_DEVERR_BAD_BLOCK 0x4u    /* block_table entry outside [0, num_blocks): rows read as zero / not moved */
+#define TS_DEVERR_TIMEOUT 0x8u      /* a bounded wait inside a kernel expired; outputs are invalid */
+
+/* Largest tree the kernels accept (ancestor sets are 128-bit masks). */
+#define TS_MAX_TREE 128
+
+/* ------------------------------------------------------------------------
+ * Tree metadata (depth and ancestor-or-self bitmask of every node).
+ *
+ * SwiftSpec summary, §3.1.3 and Figure 3: a node attends to its ancestors
+ * and itself; the mask row of node i is the set anc(i).  Computed for every
+ * request by one kernel: depth[b][i] = number of proper ancestors,
+ * anc[b][i][w] = bits 32w..32w+31 of the set {j : j is i or an ancestor of i}.
+ *
+ *   parent  device int32 [num_requests][n_tree_max]; parent[i] in [-1, i)
+ *   n_tree  device int32 [num_requests]; n_tree[b] in [0, n_tree_max]
+ *   depth   device int32 [num_requests][n_tree_max]   (out; entries >= n_tree[b] set to -1)
+ *   anc     device uint32 [num_requests][n_tree_max][4] (out; zero beyond n_tree[b])
+ *   workspace  >= tree_meta_workspace_size() bytes (holds the error word)
+ * Errors: TS_ERR_UNSUPPORTED if n_tree_max > TS_MAX_TREE.
+ * ------------------------------------------------------------------------ */
+TS_API size_t tree_meta_workspace_size(void);
+TS_API ts_status tree_build_mask(const int32_t* parent, const int32_t* n_tree, int num_requests,
+                          int n_tree_max, int32_t* depth, uint32_t* anc, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Tree-masked grouped-query attention (verify and expand).
+ *
+ * SwiftSpec summary, §3.1.3 / Figure 3 (non-square mask: query rows are the
+ * new leaves, key columns are the prefix and the whole tree, each leaf sees
+ * the prefix, its ancestors and itself) and §3.3 (one head split across
+ * thread blocks, partial results combined).  For request b, query r is tree
+ * node u = n_tree[b] - n_query + r; query head h reads KV head h / G; keys are
+ * rows [0, prefix_len[b] + n_tree[b]) of the request's cache; key P + j is
+ * visible to u iff j is u or an ancestor of u; every prefix key is visible.
+ *   out[b][r][h] = sum_j softmax_j(scale * q.k_j) v_j   (bf16, fp32 accumulation)
+ *   lse[b][h][r] = log sum_j exp(scale * q.k_j)         (fp32, natural log)
+ * The caller has already written the tree's K/V rows at P .. P + n - 1.
+ * ------------------------------------------------------------------------ */
+typedef struct ts_attn_args {
+  int num_requests;
+  int num_q_heads;            /* Hq */
+  int num_kv_heads;           /* Hkv; Hq % Hkv == 0, G = Hq / Hkv */
+  int head_dim;               /* 64 or 128 */
+  int n_tree_max;             /* row stride of `parent`; <= TS_MAX_TREE */
+  int n_query;                /* query rows per request, 1 <= n_query <= n_tree[b] */
+  int max_kv_len;             /* contiguous: rows allocated per request (>= P + n);
+                                 paged: max_blocks_per_req * page_size */
+  int kv_layout;              /* ts_kv_layout */
+  int page_size;              /* paged only: 16, 32 or 64 rows per block */
+  int max_blocks_per_req;     /* paged only: row stride of block_table */
+  int num_blocks;             /* paged only: blocks in the pool */
+  const int32_t* prefix_len;  /* device [num_requests]: P >= 0 */
+  const int32_t* n_tree;      /* device [num_requests]: n in [n_query, n_tree_max] */
+  const int32_t* parent;      /* device [num_requests][n_tree_max] */
+  const void* q;              /* device bf16 [num_requests][n_query][Hq][head_dim] */
+  const void* k_cache;        /* device bf16, layout per kv_layout (16-byte aligned) */
+  const void* v_cache;        /* device bf16, same layout as k_cache */
+  const int32_t* block_table; /* device [num_requests][max_blocks_per_req] (paged only) */
+  void* out;                  /* device bf16 [num_requests][n_query][Hq][head_dim] (out) */
+  float* lse;                 /* device fp32 [num_requests][Hq][n_query] (out) or NULL */
+  float softmax_scale;        /* <= 0 selects 1 / sqrt(head_dim) */
+  int force_path;             /* 0 automatic; 1 warp-mma kernel; 2 tcgen05 kernel (G*n_query == 128 only) */
+  int num_ctas;               /* 0 automatic; else the number of split-KV CTAs (testing) */
+} ts_attn_args;
+
+TS_API size_t tree_attn_workspace_size(const ts_attn_args* args);
+/* The kernel tree_attn_forward runs for these arguments: 1 = warp-level MMA,
+ * 2 = tcgen05/TMEM (G * n_query == 128, head_dim 128); -(ts_status) when the
+ * arguments are rejected. */
+TS_API int tree_attn_selected_path(const ts_attn_args* args);
+TS_API ts_status tree_attn_forward(const ts_attn_args* args, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ------------------------------------------------------------------------
+ * Greedy tree acceptance.
+ *
+ * NVIDIA draft-length article ("Speculative Decoding 작동 원리", Acceptance
+ * Length): the target accepts draft tokens up to the first mismatch and adds
+ * one of its own, so AL is in [1, 1 + D].  SwiftSpec summary Figure 2: the
+ * target picks one path of the tree.  For each request b:
+ *   argmax[b][i] = argmax_v logits[b][i][v]      (lowest v on ties)
+ *   node 0 (the root = last verified token) is accepted; node i >= 1 is
+ *   accepted iff parent[i] >= 0 is accepted and tokens[i] == argmax[parent[i]];
+ *   path = the longest accepted root path (ties: smallest last index),
+ *   accept_len = |path| (AL), bonus = argmax[last node of path],
+ *   verified = tokens[path[0..AL-1]] ++ [bonus], verified_len = AL + 1.
+ * An empty tree gives accept_len = 0, bonus = -1, verified_len = 0.
+ *   logits   device fp32 [num_requests][n_tree_max][vocab] (rows >= n_tree[b] unread)
+ *   tokens, parent  device int32 [num_requests][n_tree_max]
+ *   n_tree   device int32 [num_requests]
+ *   argmax, path    device int32 [num_requests][n_tree_max] (out; unused entries -1)
+ *   accept_len, bonus  device int32 [num_requests] (out)
+ *   verified device int32 [num_requests][n_tree_max + 1] (out) or NULL
+ *   verified_len device int32 [num_requests] (out) or NULL
+ * ------------------------------------------------------------------------ */
+typedef struct ts_accept_args {
+  int num_requests;
+  int n_tree_max;             /* <= TS_MAX_TREE */
+  int vocab;                  /* >= 1 */
+  const float* logits;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* n_tree;
+  int32_t* argmax;
+  int32_t* path;
+  int32_t* accept_len;
+  int32_t* bonus;
+  int32_t* verified;
+  int32_t* verified_len;
+} ts_accept_args;
+
+TS_API size_t tree_accept_workspace_size(const ts_accept_args* args);
+TS_API ts_status tree_accept_greedy(const ts_accept_args* args, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
+ * Evolving tree cache: re-root and in-place KV compaction.
+ *
+ * SwiftSpec summary, §3.2 (update procedure, Figure 4) and Figure 2's
+ * walkthrough.  For each request b, walk the verified tokens v[0..m) from the
+ * prefix tail: at each step take the lowest-index child of the current node
+ * (the prefix tail at first: parent == -1) whose token equals v[j]; stop at
+ * the first token without such a child.  The matched nodes (`path`) join the
+ * prefix.  If all m tokens matched, the proper descendants of the last one
+ * (all nodes when m == 0) survive as the new tree, in increasing index
+ * order; otherwise nothing survives (a new tree starts from the unmatched
+ * token, whose KV does not exist yet).  Then, for every layer and for K and
+ * V, new row P + j takes old row P + src[j], src = path ++ survivors, in
+ * place; rows below P are not touched; rows at or beyond the new P + n are
+ * left with unspecified content.
+ *   new_prefix_len = P + |path|, new_n_tree = |survivors|,
+ *   new_parent[j] = -1 if the survivor's parent is the last matched node,
+ *   else that parent's new index; new_tokens[j] = tokens of survivor j.
+ *   new_parent / new_tokens may alias parent / tokens (in-place update);
+ *   src_rows (optional) gets src (entries beyond |src| set to -1).
+ * Layers: k_layers / v_layers are device arrays of num_layers device
+ * pointers, each one layer's cache in the given layout; the paged block
+ * table is shared by all layers.  A row is num_kv_heads * head_dim *
+ * elem_bytes bytes, a multiple of 16.
+ * ------------------------------------------------------------------------ */
+typedef struct ts_compact_args {
+  int num_requests;
+  int n_tree_max;             /* <= TS_MAX_TREE */
+  int m_max;                  /* row stride of `verified` */
+  int num_layers;
+  int num_kv_heads;
+  int head_dim;
+  int elem_bytes;             /* bytes per cache element (2 for bf16) */
+  int kv_layout;              /* ts_kv_layout */
+  int max_kv_len;             /* contiguous: rows allocated per request */
+  int page_size;              /* paged only */
+  int max_blocks_per_req;     /* paged only */
+  int num_blocks;             /* paged only */
+  void* const* k_layers;      /* device [num_layers] of device pointers */
+  void* const* v_layers;      /* device [num_layers] of device pointers */
+  const int32_t* block_table; /* device [num_requests][max_blocks_per_req] (paged only) */
+  const int32_t* prefix_len;  /* device [num_requests] */
+  const int32_t* n_tree;      /* device [num_requests] */
+  const int32_t* parent;      /* device [num_requests][n_tree_max] */
+  const int32_t* tokens;      /* device [num_requests][n_tree_max] */
+  const int32_t* verified;    /* device [num_requests][m_max] */
+  const int32_t* m;           /* device [num_requests]: m in [0, m_max] */
+  int32_t* new_prefix_len;    /* device [num_requests] (out) */
+  int32_t* new_n_tree;        /* device [num_requests] (out) */
+  int32_t* new_parent;        /* device [num_requests][n_tree_max] (out, may alias parent) */
+  int32_t* new_tokens;        /* device [num_requests][n_tree_max] (out, may alias tokens) */
+  int32_t* src_rows;          /* device [num_requests][n_tree_max] (out) or NULL */
+} ts_compact_args;
+
+TS_API size_t tree_compact_workspace_size(const ts_compact_args* args);
+TS_API ts_status tree_cache_compact(const ts_compact_args* args, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
+ * Status and error reporting.
+ * ------------------------------------------------------------------------ */
+TS_API const char* ts_status_string(ts_status status);
+
+/* Copies the device error word of `workspace` into *code (TS_DEVERR_* bits)
+ * and, if `clear` is non-zero, resets it.  Synchronises `stream`. */
+TS_API ts_status ts_read_device_error(void* workspace, int* code, int clear, void* stream);
+
+/* Library version, (major << 16) | minor. */
+TS_API int ts_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREESPEC_H */

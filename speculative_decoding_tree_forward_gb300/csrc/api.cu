@@ -1,0 +1,372 @@
+// treespec C ABI: argument validation, workspace layout, TMA descriptors and
+// kernel launches.  Every entry point returns synchronously with a ts_status
+// and launches its kernels asynchronously on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+namespace ts {
+
+int attn_mma_occupancy(int head_dim, int stages, int num_req, int rows_pad);
+int attn_tc_occupancy(int stages, int num_req);
+bool attn_tc_available();
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<void*> fn{nullptr};
+  void* f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn.store(f, std::memory_order_release);
+  }
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+// ------------------------------------------------------------------ attention plan
+struct AttnPlan {
+  bool use_tc;
+  int rows, row_groups, rows_pad, group, stages, num_ctas;
+  int64_t units, slots;
+  size_t ws_bytes, off_o, off_lse;
+};
+
+ts_status validate_attn(const ts_attn_args* a) {
+  if (a == nullptr) return TS_ERR_INVALID_ARG;
+  if (a->num_requests < 1 || a->num_q_heads < 1 || a->num_kv_heads < 1 || a->n_tree_max < 1 || a->n_query < 1 ||
+      a->n_query > a->n_tree_max)
+    return TS_ERR_INVALID_ARG;
+  if (a->num_q_heads % a->num_kv_heads != 0) return TS_ERR_INVALID_ARG;
+  if (a->num_requests > kMaxRequestsAttn) return TS_ERR_UNSUPPORTED;
+  if (a->head_dim != 64 && a->head_dim != 128) return TS_ERR_UNSUPPORTED;
+  if (a->n_tree_max > TS_MAX_TREE) return TS_ERR_UNSUPPORTED;
+  if (a->kv_layout == TS_KV_CONTIGUOUS) {
+    if (a->max_kv_len < 1) return TS_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(a->num_requests) * a->max_kv_len > INT32_MAX - kBlockN) return TS_ERR_UNSUPPORTED;
+  } else if (a->kv_layout == TS_KV_PAGED) {
+    if (a->page_size != 16 && a->page_size != 32 && a->page_size != 64) return TS_ERR_UNSUPPORTED;
+    if (a->max_blocks_per_req < 1 || a->num_blocks < 1 || a->block_table == nullptr) return TS_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(a->num_blocks) * a->page_size > INT32_MAX - kBlockN) return TS_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(a->max_blocks_per_req) * a->page_size > INT32_MAX / 2) return TS_ERR_UNSUPPORTED;
+  } else {
+    return TS_ERR_INVALID_ARG;
+  }
+  if (!a->prefix_len || !a->n_tree || !a->parent || !a->q || !a->k_cache || !a->v_cache || !a->out)
+    return TS_ERR_INVALID_ARG;
+  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 4) || !aligned(a->out, 4) ||
+      !aligned(a->lse, 4))
+    return TS_ERR_INVALID_ARG;
+  if (a->force_path < 0 || a->force_path > 2 || a->num_ctas < 0) return TS_ERR_INVALID_ARG;
+  return TS_OK;
+}
+
+ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
+  ts_status st = validate_attn(a);
+  if (st != TS_OK) return st;
+  const int group = a->num_q_heads / a->num_kv_heads;
+  const int rows = group * a->n_query;
+  pl->group = group;
+  pl->rows = rows;
+  pl->row_groups = (rows + kMaxRowsPerUnit - 1) / kMaxRowsPerUnit;
+  pl->rows_pad = rows >= kMaxRowsPerUnit ? kMaxRowsPerUnit : ((rows + 15) / 16) * 16;
+  const bool tc_shape = (rows == 128) && a->head_dim == 128;
+  if (a->force_path == 2) {
+    if (!tc_shape) return TS_ERR_UNSUPPORTED;
+    if (!attn_tc_available()) return TS_ERR_UNSUPPORTED;
+    pl->use_tc = true;
+  } else if (a->force_path == 1) {
+    pl->use_tc = false;
+  } else {
+    pl->use_tc = tc_shape && attn_tc_available();
+  }
+  pl->units = static_cast<int64_t>(a->num_requests) * a->num_kv_heads * pl->row_groups;
+  const int max_len = a->kv_layout == TS_KV_PAGED ? a->max_blocks_per_req * a->page_size : a->max_kv_len;
+  const int64_t t_max = pl->units * ((max_len + a->n_tree_max + kBlockN - 1) / kBlockN);
+  int occ = 1;
+  if (pl->use_tc) {
+    pl->stages = 4;
+    occ = attn_tc_occupancy(pl->stages, a->num_requests);
+  } else {
+    const int rb = pl->rows_pad / 16;
+    if (a->head_dim == 128) pl->stages = rb <= 4 ? 3 : 5;
+    else pl->stages = rb <= 4 ? 6 : 10;
+    occ = attn_mma_occupancy(a->head_dim, pl->stages, a->num_requests, pl->rows_pad);
+  }
+  if (occ < 1) return TS_ERR_UNSUPPORTED;
+  if (a->num_ctas > 0) {
+    pl->num_ctas = a->num_ctas;
+  } else {
+    const int sms = device_sm_count();
+    if (sms <= 0) return TS_ERR_CUDA;
+    int64_t nc = static_cast<int64_t>(sms) * occ;
+    if (nc > t_max) nc = t_max;
+    pl->num_ctas = static_cast<int>(nc < 1 ? 1 : nc);
+  }
+  pl->slots = pl->num_ctas + pl->units;
+  pl->off_o = kWsHeader;
+  pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
+  pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
+  return TS_OK;
+}
+
+bool encode_kv_map(CUtensorMap* map, const void* base, const ts_attn_args* a) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t rows = a->kv_layout == TS_KV_PAGED
+                              ? static_cast<cuuint64_t>(a->num_blocks) * a->page_size
+                              : static_cast<cuuint64_t>(a->num_requests) * a->max_kv_len;
+  const cuuint32_t box_rows = a->kv_layout == TS_KV_PAGED ? a->page_size : kBlockN;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->head_dim), static_cast<cuuint64_t>(a->num_kv_heads), rows};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(a->head_dim) * 2,
+                           static_cast<cuuint64_t>(a->head_dim) * 2 * a->num_kv_heads};
+  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace ts
+
+using namespace ts;
+
+extern "C" {
+
+int ts_version(void) { return (0 << 16) | 1; }
+
+const char* ts_status_string(ts_status s) {
+  switch (s) {
+    case TS_OK: return "TS_OK";
+    case TS_ERR_INVALID_ARG: return "TS_ERR_INVALID_ARG: invalid argument";
+    case TS_ERR_UNSUPPORTED: return "TS_ERR_UNSUPPORTED: shape or option not implemented";
+    case TS_ERR_CUDA: return "TS_ERR_CUDA: a CUDA call failed";
+    case TS_ERR_WORKSPACE: return "TS_ERR_WORKSPACE: workspace missing, too small or misaligned";
+  }
+  return "unknown ts_status";
+}
+
+ts_status ts_read_device_error(void* workspace, int* code, int clear, void* stream) {
+  if (workspace == nullptr || code == nullptr) return TS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return TS_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TS_ERR_CUDA;
+  *code = static_cast<int>(v);
+  if (clear) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), st) != cudaSuccess) return TS_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TS_ERR_CUDA;
+  }
+  return TS_OK;
+}
+
+// ------------------------------------------------------------------ metadata
+size_t tree_meta_workspace_size(void) { return kWsHeader; }
+
+ts_status tree_build_mask(const int32_t* parent, const int32_t* n_tree, int num_requests, int n_tree_max,
+                          int32_t* depth, uint32_t* anc, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!parent || !n_tree || !depth || !anc || num_requests < 1 || n_tree_max < 1) return TS_ERR_INVALID_ARG;
+  if (n_tree_max > TS_MAX_TREE) return TS_ERR_UNSUPPORTED;
+  if (!aligned(anc, 16)) return TS_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWsHeader || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  cudaError_t e = launch_tree_meta(parent, n_tree, num_requests, n_tree_max, depth, anc,
+                                   static_cast<unsigned*>(workspace), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ attention
+size_t tree_attn_workspace_size(const ts_attn_args* args) {
+  AttnPlan pl;
+  if (plan_attn(args, &pl) != TS_OK) return 0;
+  return pl.ws_bytes;
+}
+
+int tree_attn_selected_path(const ts_attn_args* args) {
+  AttnPlan pl;
+  const ts_status st = plan_attn(args, &pl);
+  if (st != TS_OK) return -static_cast<int>(st);
+  return pl.use_tc ? 2 : 1;
+}
+
+ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  AttnPlan pl;
+  ts_status st = plan_attn(a, &pl);
+  if (st != TS_OK) return st;
+  if (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  CUtensorMap kmap, vmap;
+  if (!encode_kv_map(&kmap, a->k_cache, a) || !encode_kv_map(&vmap, a->v_cache, a)) return TS_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.num_req = a->num_requests;
+  p.hq = a->num_q_heads;
+  p.hkv = a->num_kv_heads;
+  p.group = pl.group;
+  p.head_dim = a->head_dim;
+  p.n_query = a->n_query;
+  p.n_tree_max = a->n_tree_max;
+  p.rows = pl.rows;
+  p.row_groups = pl.row_groups;
+  p.rows_pad = pl.rows_pad;
+  p.max_kv_len = a->max_kv_len;
+  p.paged = a->kv_layout == TS_KV_PAGED;
+  p.page_size = p.paged ? a->page_size : 0;
+  p.max_blocks = p.paged ? a->max_blocks_per_req : 0;
+  p.num_blocks = p.paged ? a->num_blocks : 0;
+  p.num_ctas = pl.num_ctas;
+  p.stages = pl.stages;
+  p.num_units = pl.units;
+  p.prefix_len = a->prefix_len;
+  p.n_tree = a->n_tree;
+  p.parent = a->parent;
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.block_table = a->block_table;
+  p.out = static_cast<__nv_bfloat16*>(a->out);
+  p.lse = a->lse;
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(static_cast<float>(a->head_dim));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+  p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pl.use_tc ? launch_attn_tc(p, kmap, vmap, s) : launch_attn_mma(p, kmap, vmap, s);
+  if (e != cudaSuccess) return TS_ERR_CUDA;
+  e = launch_attn_merge(p, s);
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ acceptance
+static int accept_chunk(int vocab) {
+  const int c = 8192;
+  return vocab <= c ? ((vocab + 3) / 4) * 4 : c;
+}
+
+size_t tree_accept_workspace_size(const ts_accept_args* a) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1) return 0;
+  const int chunk = accept_chunk(a->vocab);
+  const int64_t chunks = (a->vocab + chunk - 1) / chunk;
+  const int64_t rows = static_cast<int64_t>(a->num_requests) * a->n_tree_max;
+  return kWsHeader + align256(rows * chunks * sizeof(float)) + align256(rows * chunks * sizeof(int32_t));
+}
+
+ts_status tree_accept_greedy(const ts_accept_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1) return TS_ERR_INVALID_ARG;
+  if (a->n_tree_max > TS_MAX_TREE) return TS_ERR_UNSUPPORTED;
+  if (!a->logits || !a->tokens || !a->parent || !a->n_tree || !a->argmax || !a->path || !a->accept_len || !a->bonus)
+    return TS_ERR_INVALID_ARG;
+  if (!aligned(a->logits, (a->vocab % 4 == 0) ? 16 : 4)) return TS_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a->num_requests) * a->n_tree_max > INT32_MAX) return TS_ERR_UNSUPPORTED;
+  const size_t need = tree_accept_workspace_size(a);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AcceptParams p;
+  p.num_req = a->num_requests;
+  p.n_tree_max = a->n_tree_max;
+  p.vocab = a->vocab;
+  p.chunk = accept_chunk(a->vocab);
+  p.num_chunks = (a->vocab + p.chunk - 1) / p.chunk;
+  p.logits = a->logits;
+  p.tokens = a->tokens;
+  p.parent = a->parent;
+  p.n_tree = a->n_tree;
+  p.argmax = a->argmax;
+  p.path = a->path;
+  p.accept_len = a->accept_len;
+  p.bonus = a->bonus;
+  p.verified = a->verified;
+  p.verified_len = a->verified_len;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  const int64_t rows = static_cast<int64_t>(a->num_requests) * a->n_tree_max;
+  p.part_val = reinterpret_cast<float*>(ws + kWsHeader);
+  p.part_idx = reinterpret_cast<int32_t*>(ws + kWsHeader + align256(rows * p.num_chunks * sizeof(float)));
+  if (p.num_chunks > 65535) return TS_ERR_UNSUPPORTED;
+  cudaError_t e = launch_accept(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ compaction
+size_t tree_compact_workspace_size(const ts_compact_args* a) {
+  if (a == nullptr || a->num_requests < 1) return 0;
+  return kWsHeader + align256(static_cast<size_t>(a->num_requests) * kPlanStride * sizeof(int32_t));
+}
+
+ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->m_max < 0 || a->num_layers < 1 ||
+      a->num_kv_heads < 1 || a->head_dim < 1 || a->elem_bytes < 1)
+    return TS_ERR_INVALID_ARG;
+  if (a->n_tree_max > TS_MAX_TREE) return TS_ERR_UNSUPPORTED;
+  const int64_t row_bytes = static_cast<int64_t>(a->num_kv_heads) * a->head_dim * a->elem_bytes;
+  if (row_bytes % 16 != 0 || row_bytes > (1 << 20)) return TS_ERR_UNSUPPORTED;
+  if (!a->k_layers || !a->v_layers || !a->prefix_len || !a->n_tree || !a->parent || !a->tokens || !a->m ||
+      !a->new_prefix_len || !a->new_n_tree || !a->new_parent || !a->new_tokens)
+    return TS_ERR_INVALID_ARG;
+  if (a->m_max > 0 && a->verified == nullptr) return TS_ERR_INVALID_ARG;
+  if (a->kv_layout == TS_KV_CONTIGUOUS) {
+    if (a->max_kv_len < 1) return TS_ERR_INVALID_ARG;
+  } else if (a->kv_layout == TS_KV_PAGED) {
+    if (a->page_size < 1 || a->max_blocks_per_req < 1 || a->num_blocks < 1 || !a->block_table)
+      return TS_ERR_INVALID_ARG;
+  } else {
+    return TS_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(a->num_layers) * a->num_requests > INT32_MAX) return TS_ERR_UNSUPPORTED;
+  const size_t need = tree_compact_workspace_size(a);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CompactParams p;
+  p.num_req = a->num_requests;
+  p.n_tree_max = a->n_tree_max;
+  p.m_max = a->m_max;
+  p.num_layers = a->num_layers;
+  p.row_bytes = static_cast<int>(row_bytes);
+  p.paged = a->kv_layout == TS_KV_PAGED;
+  p.max_kv_len = a->max_kv_len;
+  p.page_size = a->page_size;
+  p.max_blocks = a->max_blocks_per_req;
+  p.num_blocks = a->num_blocks;
+  int chunk = (32768 / a->n_tree_max) / 16 * 16;
+  if (chunk < 16) chunk = 16;
+  if (chunk > row_bytes) chunk = static_cast<int>(row_bytes);
+  p.chunk_bytes = chunk;
+  p.num_chunk_groups = static_cast<int>((row_bytes + chunk - 1) / chunk);
+  if (p.num_chunk_groups > 65535) return TS_ERR_UNSUPPORTED;
+  p.k_layers = a->k_layers;
+  p.v_layers = a->v_layers;
+  p.block_table = a->block_table;
+  p.prefix_len = a->prefix_len;
+  p.n_tree = a->n_tree;
+  p.parent = a->parent;
+  p.tokens = a->tokens;
+  p.verified = a->verified;
+  p.m = a->m;
+  p.new_prefix_len = a->new_prefix_len;
+  p.new_n_tree = a->new_n_tree;
+  p.new_parent = a->new_parent;
+  p.new_tokens = a->new_tokens;
+  p.src_rows = a->src_rows;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.plan = reinterpret_cast<int32_t*>(ws + kWsHeader);
+  cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// Pieces shared by the two tree-attention kernels and their merge.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ts {
+
+// Per-request lengths, clamped to the stated bounds (violations reported).
+// Every kernel of one call clamps the same way, so they agree on the schedule.
+__device__ __forceinline__ void attn_lengths(const AttnParams& p, int b, int& P, int& n, bool report) {
+  P = p.prefix_len[b];
+  n = p.n_tree[b];
+  bool bad = false;
+  if (n < p.n_query) { n = p.n_query; bad = true; }
+  if (n > p.n_tree_max) { n = p.n_tree_max; bad = true; }
+  const int cap = p.paged ? p.max_blocks * p.page_size : p.max_kv_len;
+  if (P < 0) { P = 0; bad = true; }
+  if (P > cap - n) { P = max(cap - n, 0); bad = true; }
+  if (bad && report) report_error(p.err, TS_DEVERR_BAD_LENGTH);
+}
+
+// Ancestor-or-self set of node u (bit j = node j) by walking a validated
+// parent array (parent[i] in [-1, i)) held in shared memory.
+__device__ __forceinline__ void ancestor_walk(const int* par, int u, uint32_t a[4]) {
+  uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  while (u >= 0) {
+    const uint32_t bit = 1u << (u & 31);
+    const int w = u >> 5;
+    a0 |= (w == 0) ? bit : 0u;
+    a1 |= (w == 1) ? bit : 0u;
+    a2 |= (w == 2) ? bit : 0u;
+    a3 |= (w == 3) ? bit : 0u;
+    u = par[u];
+  }
+  a[0] = a0;
+  a[1] = a1;
+  a[2] = a2;
+  a[3] = a3;
+}
+
+__device__ __forceinline__ int attn_tiles(int keys) { return (keys + kBlockN - 1) / kBlockN; }
+
+// Visibility of the 64 keys [P + off, P + off + 64) for a query whose
+// ancestor-or-self set is `a` (bit j = tree node j): prefix keys (negative
+// offsets) are visible; tree key j is visible iff bit j is set; keys at or
+// beyond P + n are never visible (their bits are zero in `a`).
+__device__ __forceinline__ uint64_t tile_visibility(const uint32_t a[4], int off) {
+  const uint64_t lo = static_cast<uint64_t>(a[0]) | (static_cast<uint64_t>(a[1]) << 32);
+  const uint64_t hi = static_cast<uint64_t>(a[2]) | (static_cast<uint64_t>(a[3]) << 32);
+  uint64_t tree;
+  if (off >= 128 || off <= -64) tree = 0;
+  else if (off >= 64) tree = hi >> (off - 64);
+  else if (off > 0) tree = (lo >> off) | (hi << (64 - off));
+  else if (off == 0) tree = lo;
+  else tree = lo << (-off);
+  uint64_t pre = 0;
+  if (off < 0) pre = (off <= -64) ? ~0ull : ((1ull << (-off)) - 1ull);
+  return tree | pre;
+}
+
+}  // namespace ts

@@ -1,0 +1,202 @@
+// Device helpers shared by the treespec kernels (sm_103a).
+//
+// Inline-PTX wrappers for mbarriers, TMA tensor loads, ldmatrix and the
+// warp-level bf16 MMA; bounded waits that never hang; the tree-metadata
+// builder (ancestor-or-self bitmasks); and the split-KV schedule used by the
+// attention kernels and their merge.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "treespec.h"
+
+namespace ts {
+
+// A bounded wait gives up after this long (ns of %globaltimer) and reports
+// TS_DEVERR_TIMEOUT instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void report_error(unsigned* err_word, unsigned bits) {
+  if (err_word) atomicOr(err_word, bits);
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, for at most
+// kWaitLimitNs of %globaltimer; returns false when the limit expires.  One
+// PTX block, so the wait adds no register pressure to the loop around it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t.reg .u64 t0, t1;\n\t"
+      "mov.u64 t0, %%globaltimer;\n"
+      "LAB_WAIT:\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+      "@P1 bra.uni DONE;\n\t"
+      "mov.u64 t1, %%globaltimer;\n\t"
+      "sub.u64 t1, t1, t0;\n\t"
+      "setp.lt.u64 P1, t1, %3;\n\t"
+      "@P1 bra.uni LAB_WAIT;\n"
+      "DONE:\n\t"
+      "selp.u32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "l"(kWaitLimitNs)
+      : "memory");
+  return ok != 0;
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- warp MMA
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a tile whose
+// rows are 128 bytes and which TMA wrote with 128-byte swizzling from a
+// 1024-byte-aligned base: chunk index XOR (row mod 8).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
+  return row * 128u + (((chunk ^ row) & 7u) << 4);
+}
+
+// ---------------------------------------------------------------- tree metadata
+// Ancestor-or-self sets of the first n nodes of one tree, as 128-bit masks in
+// shared memory, by pointer jumping: after round k every node has OR-ed in
+// the sets of all ancestors less than 2^k hops away, so ceil(log2 n) rounds
+// cover any depth below n.  A parent outside [-1, i) is reported and treated
+// as -1.  `nthr` threads with ids `tid` in [0, nthr) take part (nthr >= 32);
+// `sync()` must be a barrier over exactly those threads.
+template <class Sync>
+__device__ __forceinline__ void build_ancestor_masks(const int32_t* parent, int n, uint32_t (*anc)[4],
+                                                     int* jmp, int tid, int nthr, unsigned* err_word,
+                                                     Sync sync) {
+  for (int i = tid; i < n; i += nthr) {
+    int p = parent[i];
+    if (p < -1 || p >= i) {
+      report_error(err_word, TS_DEVERR_BAD_PARENT);
+      p = -1;
+    }
+    jmp[i] = p;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) anc[i][w] = (w == (i >> 5)) ? (1u << (i & 31)) : 0u;
+  }
+  sync();
+  int rounds = 0;
+  while ((1 << rounds) < n) ++rounds;
+  for (int r = 0; r < rounds; ++r) {
+    uint32_t a[4][4];
+    int jn[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = tid + k * nthr;
+      if (i < n) {
+        const int q = jmp[i];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) a[k][w] = anc[i][w] | (q >= 0 ? anc[q][w] : 0u);
+        jn[k] = q >= 0 ? jmp[q] : -1;
+      }
+    }
+    sync();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = tid + k * nthr;
+      if (i < n) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) anc[i][w] = a[k][w];
+        jmp[i] = jn[k];
+      }
+    }
+    sync();
+  }
+}
+
+// ---------------------------------------------------------------- split-KV schedule
+// Work is cut into "units" (request b, KV head, row group) and each unit's
+// keys into tiles of kBlockN.  Units are ordered request-major; the tiles of
+// all units form one sequence of T tiles that CTA c takes the contiguous
+// range [c*T/NC, (c+1)*T/NC) of.  A CTA that finishes a unit it did not
+// start (or starts one it does not finish) writes a partial result into slot
+// c + u, which is unique because ranges are monotone in c (if c covers unit u
+// and c' > c covers u' then u' >= u).
+__host__ __device__ __forceinline__ int64_t sched_begin(int c, int64_t T, int NC) {
+  return (static_cast<int64_t>(c) * T) / NC;
+}
+// The CTA whose range holds tile t: the largest c with sched_begin(c) <= t.
+__host__ __device__ __forceinline__ int sched_cta_of(int64_t t, int64_t T, int NC) {
+  return static_cast<int>(((t + 1) * NC + T - 1) / T - 1);
+}
+
+}  // namespace ts

@@ -1,0 +1,98 @@
+// Host/device parameter blocks and launchers shared by the treespec .cu files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "treespec.h"
+
+namespace ts {
+
+constexpr int kBlockN = 64;        // keys per K/V tile
+constexpr int kMaxRowsPerUnit = 128;  // packed query rows handled by one CTA
+constexpr int kMaxRequestsAttn = 1024;
+constexpr size_t kWsHeader = 256;  // error word + padding at the start of every workspace
+
+// Parameters of one tree_attn_forward call as the kernels see them.
+struct AttnParams {
+  int num_req, hq, hkv, group, head_dim, n_query, n_tree_max;
+  int rows;          // R = G * n_query packed rows per KV head
+  int row_groups;    // ceil(R / 128)
+  int rows_pad;      // rows per unit rounded up to 16 (<= 128)
+  int max_kv_len;
+  int paged, page_size, max_blocks, num_blocks;
+  int num_ctas;      // NC
+  int stages;
+  int64_t num_units; // num_req * hkv * row_groups
+  const int32_t* prefix_len;
+  const int32_t* n_tree;
+  const int32_t* parent;
+  const __nv_bfloat16* q;
+  const int32_t* block_table;
+  __nv_bfloat16* out;
+  float* lse;
+  float scale_log2;  // softmax scale * log2(e)
+  unsigned* err;     // workspace error word
+  float* part_o;     // [slots][rows_pad][head_dim]
+  float* part_lse;   // [slots][rows_pad] (log2 domain)
+};
+
+// Launchers (one per kernel family); return cudaGetLastError().
+cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream);
+cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream);
+cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream);
+size_t attn_mma_smem_bytes(int head_dim, int stages, int num_req, int rows_pad);
+size_t attn_tc_smem_bytes(int stages, int num_req);
+int attn_mma_threads(int rows_pad);
+int attn_tc_threads();
+
+cudaError_t launch_tree_meta(const int32_t* parent, const int32_t* n_tree, int num_req, int n_tree_max,
+                             int32_t* depth, uint32_t* anc, unsigned* err, cudaStream_t stream);
+
+struct AcceptParams {
+  int num_req, n_tree_max, vocab, chunk, num_chunks;
+  const float* logits;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* n_tree;
+  int32_t* argmax;
+  int32_t* path;
+  int32_t* accept_len;
+  int32_t* bonus;
+  int32_t* verified;
+  int32_t* verified_len;
+  unsigned* err;
+  float* part_val;   // [num_req * n_tree_max][num_chunks]
+  int32_t* part_idx; // [num_req * n_tree_max][num_chunks]
+};
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
+
+struct CompactParams {
+  int num_req, n_tree_max, m_max, num_layers, row_bytes;
+  int paged, max_kv_len, page_size, max_blocks, num_blocks;
+  int chunk_bytes, num_chunk_groups;
+  void* const* k_layers;
+  void* const* v_layers;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* n_tree;
+  const int32_t* parent;
+  const int32_t* tokens;
+  const int32_t* verified;
+  const int32_t* m;
+  int32_t* new_prefix_len;
+  int32_t* new_n_tree;
+  int32_t* new_parent;
+  int32_t* new_tokens;
+  int32_t* src_rows;
+  unsigned* err;
+  int32_t* plan;     // per request: [0] = old P, [1] = rows in src list, [2..] = src list
+};
+constexpr int kPlanStride = TS_MAX_TREE + 4;
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream);
+
+}  // namespace ts

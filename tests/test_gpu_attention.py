@@ -1,0 +1,155 @@
+"""GPU parity: tree_attn_forward (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():   # on a GPU machine a missing library is an error, not a skip
+    import speculative_decoding_tree_forward_gb300 as ts
+else:
+    ts = None
+from gpu_util import attn_inputs, bf16_dev, bf16_host_f64, check_attention  # noqa: E402
+
+
+def run(case, **kw):
+    d = attn_inputs(case)
+    out, lse = ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
+                                    block_table=d.get("block_table"), softmax_scale=case.softmax_scale, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+SMALL = [
+    dict(num_req=2, hq=8, hkv=2, d=64, n_tree_max=16, prefix_range=(0, 200)),
+    dict(num_req=3, hq=8, hkv=2, d=128, n_tree_max=16, prefix_range=(50, 300)),
+    dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=40, n_query=8, prefix_range=(100, 400)),   # expansion
+    dict(num_req=4, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(60, 300), chain=True),   # R = 40
+    dict(num_req=2, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(0, 500)),              # R = 128
+    dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=32, prefix_range=(0, 300)),              # R = 128
+    dict(num_req=2, hq=16, hkv=2, d=64, n_tree_max=40, n_query=32, prefix_range=(0, 100)),    # R = 256, 2 row groups
+    dict(num_req=3, hq=12, hkv=4, d=64, n_tree_max=20, n_query=7, ragged_tree=True, prefix_range=(0, 150)),  # G=3
+    dict(num_req=2, hq=4, hkv=4, d=128, n_tree_max=128, prefix_range=(0, 70)),                # max tree, G=1
+    dict(num_req=2, hq=8, hkv=1, d=64, n_tree_max=24, prefix_range=(0, 0)),                   # no prefix
+]
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("cfg", range(len(SMALL)))
+def test_small_cases_match_oracle(cfg, paged):
+    case = W.random_attn_case(100 + cfg, paged=paged, **SMALL[cfg])
+    out, lse = run(case, force_path=1)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 1000])
+def test_split_counts_match_oracle(num_ctas):
+    """Every split of the key range (one CTA for everything up to one tile per CTA) merges to the same result."""
+    case = W.random_attn_case(7, num_req=3, hq=16, hkv=4, d=128, n_tree_max=12, prefix_range=(10, 400),
+                              ragged_tree=True, n_query=6)
+    out, lse = run(case, force_path=1, num_ctas=num_ctas)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
+def test_single_node_single_key():
+    case = W.random_attn_case(3, num_req=1, hq=2, hkv=2, d=64, n_tree_max=1, prefix_range=(0, 0))
+    out, lse = run(case)
+    np.testing.assert_array_equal(bf16_host_f64(out)[0, 0], A.bf16_bits_to_f64(case.v[0, 0]))
+
+
+def test_masked_tree_rows_do_not_leak():
+    """Non-ancestor tree K/V replaced by large finite garbage: outputs stay bit-identical."""
+    case = W.random_attn_case(11, num_req=2, hq=8, hkv=2, d=128, n_tree_max=16, prefix_range=(30, 90))
+    out1, lse1 = run(case)
+    u = 15
+    for b in range(case.num_req):
+        P = int(case.prefix_len[b])
+        anc = set()
+        x = u
+        while x != -1:
+            anc.add(x)
+            x = int(case.parent[b][x])
+        for j in range(16):
+            if j not in anc:
+                case.k[b, P + j] = W.f32_to_bf16_bits(np.full(case.k.shape[2:], 300.0, np.float32))
+                case.v[b, P + j] = W.f32_to_bf16_bits(np.full(case.v.shape[2:], -3e4, np.float32))
+    out2, lse2 = run(case)
+    assert torch.equal(out1[:, u], out2[:, u]) and torch.equal(lse1[:, :, u], lse2[:, :, u])
+
+
+def test_rows_past_the_last_key_may_hold_nan():
+    """Memory after P + n (next request, unwritten rows) never reaches the output, even as NaN/Inf."""
+    case = W.random_attn_case(12, num_req=2, hq=8, hkv=2, d=64, n_tree_max=10, prefix_range=(20, 40))
+    d = attn_inputs(case)
+    ref = A.attention_case(case)
+    for b in range(case.num_req):
+        end = int(case.prefix_len[b] + case.n_tree[b])
+        d["k_cache"][b, end:] = float("nan")
+        d["v_cache"][b, end:] = float("inf")
+    out, lse = ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"])
+    torch.cuda.synchronize()
+    check_attention(case, out, lse, ref)
+
+
+def test_bad_parent_is_reported_not_trapped():
+    case = W.random_attn_case(13, num_req=1, hq=4, hkv=1, d=64, n_tree_max=6, prefix_range=(5, 5))
+    case.parent[0, 3] = 5   # not an earlier node
+    d = attn_inputs(case)
+    ws = ts.new_workspace(ts.tree_attn_workspace_size(ts.attn_args(
+        d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"], torch.empty_like(d["q"]))))
+    ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"], workspace=ws)
+    code = ts.read_device_error(ws)
+    assert code & ts.TS_DEVERR_BAD_PARENT
+    assert ts.read_device_error(ws) == 0
+
+
+def test_invalid_arguments_are_rejected():
+    case = W.random_attn_case(14, num_req=1, hq=6, hkv=4, d=64, n_tree_max=4, prefix_range=(3, 3))
+    d = attn_inputs(case)
+    with pytest.raises(ts.TreeSpecError):   # Hq % Hkv != 0
+        ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"])
+
+
+# ------------------------------------------------------------------ named workloads
+def _sampled(case, requests, heads, **kw):
+    out, lse = run(case, **kw)
+    ref = A.attention_case(case, requests=requests, heads=heads)
+    check_attention(case, out, lse, ref, heads=heads)
+
+
+def test_workload_tree16_prefix128():
+    w = W.tree16_prefix128()
+    _sampled(w.attn[0], None, None)
+
+
+def test_workload_expand_w8_prefix2048():
+    w = W.expand_w8_prefix2048()
+    for case in w.attn:
+        _sampled(case, None, None)
+
+
+@pytest.mark.slow
+def test_workload_verify_b8_tree16():
+    w = W.verify_b8_tree16()
+    _sampled(w.attn[0], [0, 3, 7], [0, 9, 63])
+
+
+@pytest.mark.slow
+def test_workload_verify_b8_tree16_mma_path():
+    w = W.verify_b8_tree16()
+    _sampled(w.attn[0], [1, 6], [5, 40], force_path=1)
+
+
+@pytest.mark.slow
+def test_workload_chain_verify_b16_paged():
+    w = W.chain_verify_b16_paged()
+    _sampled(w.attn[0], [0, 5, 15], [0, 17, 63])
+
+
+@pytest.mark.slow
+def test_workload_longctx_verify_b4_p32k():
+    w = W.longctx_verify_b4_p32k(num_layers=1)
+    _sampled(w.attn[0], [0, 3], [0, 31])

@@ -1,0 +1,196 @@
+"""GPU parity: tree metadata, greedy acceptance and re-root/compaction against the oracle (bit-exact)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+from oracle import tree as T
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import speculative_decoding_tree_forward_gb300 as ts
+else:
+    ts = None
+from gpu_util import i32_dev  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ metadata
+@pytest.mark.parametrize("seed", range(4))
+def test_tree_masks_match_oracle(seed):
+    case = W.random_accept_case(seed, num_req=5, n_tree_max=128 if seed == 0 else 37)
+    depth, anc = ts.tree_build_mask(i32_dev(case.parent), i32_dev(case.n_tree))
+    depth, anc = depth.cpu().numpy(), anc.cpu().numpy().view(np.uint32)
+    for b in range(case.num_req):
+        n = int(case.n_tree[b])
+        for u in range(n):
+            expect = set(T.ancestors_or_self(case.parent[b], u))
+            bits = {j for j in range(128) if (int(anc[b, u, j >> 5]) >> (j & 31)) & 1}
+            assert bits == expect
+            assert depth[b, u] == T.depth(case.parent[b], u)
+        assert (depth[b, n:] == -1).all() and (anc[b, n:] == 0).all()
+
+
+def test_fig3_mask_on_gpu():
+    with open(os.path.join(GOLDEN, "fig3_mask.json")) as f:
+        g = json.load(f)
+    depth, anc = ts.tree_build_mask(i32_dev([g["parent"]]), i32_dev([10]))
+    a = int(anc.cpu().numpy().view(np.uint32)[0, g["tokens"].index("t7"), 0])
+    assert [g["tokens"][j] for j in range(10) if (a >> j) & 1] == g["visible"]
+
+
+# ------------------------------------------------------------------ acceptance
+def check_accept(case, res):
+    got = {k: v.cpu().numpy() for k, v in res.items()}
+    for b in range(case.num_req):
+        n = int(case.n_tree[b])
+        r = T.greedy_accept(case.logits[b][:n], case.tokens[b][:n], case.parent[b][:n], n)
+        assert list(got["argmax"][b][:n]) == r.argmax
+        assert (got["argmax"][b][n:] == -1).all()
+        assert got["accept_len"][b] == r.accept_len and got["bonus"][b] == r.bonus
+        assert list(got["path"][b][: r.accept_len]) == r.path and (got["path"][b][r.accept_len:] == -1).all()
+        assert got["verified_len"][b] == len(r.verified)
+        assert list(got["verified"][b][: len(r.verified)]) == r.verified
+
+
+def run_accept(case):
+    res = ts.tree_accept_greedy(torch.from_numpy(case.logits).cuda(), i32_dev(case.tokens), i32_dev(case.parent),
+                                i32_dev(case.n_tree))
+    torch.cuda.synchronize()
+    return res
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_accept_random_trees(seed):
+    kw = [dict(vocab=1000), dict(vocab=7, distinct_siblings=False), dict(vocab=50000, n_tree_max=128),
+          dict(vocab=8193, chain=True, p_accept=0.9), dict(vocab=4097, p_accept=1.0), dict(vocab=3)][seed]
+    case = W.random_accept_case(seed, num_req=6, **kw)
+    check_accept(case, run_accept(case))
+
+
+def test_accept_argmax_ties_take_lowest_index():
+    case = W.random_accept_case(1, num_req=2, n_tree_max=8, vocab=20000)
+    case.logits[:, :, 17] = 9.0
+    case.logits[:, :, 12345] = 9.0
+    case.logits[:, :, 19999] = 9.0
+    check_accept(case, run_accept(case))
+
+
+def test_accept_fig2_target_verify():
+    with open(os.path.join(GOLDEN, "fig2_walkthrough.json")) as f:
+        g = json.load(f)["target_verify"]
+    lg = np.zeros((1, 4, g["vocab"]), np.float32)
+    for i, a in enumerate(g["argmax"]):
+        lg[0, i, a] = 1.0
+    res = ts.tree_accept_greedy(torch.from_numpy(lg).cuda(), i32_dev([g["tokens"]]), i32_dev([g["parent"]]),
+                                i32_dev([4]))
+    e = g["expect"]
+    assert res["accept_len"].item() == e["accept_len"] and res["bonus"].item() == e["bonus"]
+    assert res["path"][0, :2].tolist() == e["path"] and res["verified"][0, :3].tolist() == e["verified"]
+
+
+def test_accept_empty_tree():
+    case = W.random_accept_case(2, num_req=2, n_tree_max=4, vocab=64)
+    case.n_tree[1] = 0
+    check_accept(case, run_accept(case))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl", ["verify_b8_tree16", "longctx_verify_b4_p32k", "tree16_prefix128"])
+def test_accept_named_workloads(wl):
+    w = getattr(W, wl)(**({"with_kv": False} if wl.startswith("longctx") else {}))
+    check_accept(w.accept, run_accept(w.accept))
+
+
+# ------------------------------------------------------------------ compaction
+def _logical(cache, b, nrows, table):
+    return A.logical_rows(cache, b, nrows, table)
+
+
+def run_compact_case(case, layers=3, hkv=2, d=64, paged=False, seed=0, max_rows=None):
+    """Random KV for `layers` layers; compaction on GPU vs oracle (metadata + bytes)."""
+    rng = np.random.default_rng(seed)
+    B = case.num_req
+    rows = case.prefix_len + case.n_tree
+    if paged:
+        nblk = [(int(r) + 15) // 16 for r in rows]
+        perm = rng.permutation(sum(nblk) + 2)
+        table = np.full((B, max(max(nblk), 1)), -1, np.int32)
+        off = 0
+        for b in range(B):
+            table[b, :nblk[b]] = perm[off:off + nblk[b]]
+            off += nblk[b]
+        shape = (len(perm), 16, hkv, d)
+    else:
+        table = None
+        shape = (B, int(rows.max()) + 3, hkv, d)
+    ks = [rng.integers(0, 65535, size=shape, dtype=np.uint16) for _ in range(layers)]
+    vs = [rng.integers(0, 65535, size=shape, dtype=np.uint16) for _ in range(layers)]
+    kd = [torch.from_numpy(x.view(np.int16)).cuda() for x in ks]
+    vd = [torch.from_numpy(x.view(np.int16)).cuda() for x in vs]
+    res = ts.tree_cache_compact(kd, vd, i32_dev(case.prefix_len), i32_dev(case.n_tree), i32_dev(case.parent),
+                                i32_dev(case.tokens), i32_dev(case.verified), i32_dev(case.m),
+                                block_table=None if table is None else i32_dev(table))
+    torch.cuda.synchronize()
+    got = {k: v.cpu().numpy() for k, v in res.items() if not k.startswith("_")}
+    for b in range(B):
+        n, P = int(case.n_tree[b]), int(case.prefix_len[b])
+        r = T.reroot(case.parent[b][:n], case.tokens[b][:n], n, P, case.verified[b][: int(case.m[b])])
+        assert got["new_prefix_len"][b] == r.new_prefix_len and got["new_n_tree"][b] == r.new_n_tree
+        assert list(got["new_parent"][b][: r.new_n_tree]) == r.new_parent
+        assert list(got["new_tokens"][b][: r.new_n_tree]) == r.new_tokens
+        assert list(got["src_rows"][b][: len(r.src)]) == r.src
+        keep = P + len(r.src)
+        for li in range(layers):
+            for host, dev in ((ks[li], kd[li]), (vs[li], vd[li])):
+                before = _logical(host, b, P + n, table)
+                expect = T.compact_rows(before, P, r.src)[:keep]
+                after = _logical(dev.cpu().numpy().view(np.uint16), b, keep, table)
+                assert np.array_equal(after, expect), f"request {b} layer {li}"
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("paged", [False, True])
+def test_compact_random(seed, paged):
+    case = W.random_compact_case(seed, num_req=5, n_tree_max=24 if seed else 128, forest=bool(seed % 2))
+    run_compact_case(case, layers=2 + seed % 3, hkv=2 if seed % 2 else 8, d=64 if seed < 3 else 128,
+                     paged=paged, seed=seed)
+
+
+def test_compact_fig4_on_gpu():
+    with open(os.path.join(GOLDEN, "fig4_compaction.json")) as f:
+        g = json.load(f)
+    case = W.CompactCase(1, 8, np.array([4], np.int32), np.array([8], np.int32), np.array([g["parent"]], np.int32),
+                         np.array([g["tokens"]], np.int32), np.array([g["verified"]], np.int32),
+                         np.array([2], np.int32))
+    run_compact_case(case, layers=2)
+
+
+def test_compact_target_side_after_accept():
+    """accept -> compact chained on the device: the accepted path becomes prefix, nothing survives."""
+    acc = W.random_accept_case(9, num_req=4, n_tree_max=16, vocab=300, p_accept=0.8)
+    res = run_accept(acc)
+    case = W.CompactCase(4, 16, np.full(4, 50, np.int32), acc.n_tree, acc.parent, acc.tokens,
+                         res["verified"].cpu().numpy(), res["verified_len"].cpu().numpy())
+    run_compact_case(case, layers=2)
+
+
+def test_compact_in_place_metadata():
+    case = W.random_compact_case(3, num_req=4, n_tree_max=20)
+    par, tok = i32_dev(case.parent), i32_dev(case.tokens)
+    k = [torch.zeros((4, 80, 2, 64), dtype=torch.int16, device="cuda")]
+    res = ts.tree_cache_compact(k, [torch.zeros_like(k[0])], i32_dev(case.prefix_len), i32_dev(case.n_tree), par,
+                                tok, i32_dev(case.verified), i32_dev(case.m), in_place_metadata=True)
+    torch.cuda.synchronize()
+    for b in range(4):
+        n = int(case.n_tree[b])
+        r = T.reroot(case.parent[b][:n], case.tokens[b][:n], n, int(case.prefix_len[b]),
+                     case.verified[b][: int(case.m[b])])
+        assert par[b, : r.new_n_tree].tolist() == r.new_parent and tok[b, : r.new_n_tree].tolist() == r.new_tokens
+    assert res["new_parent"].data_ptr() == par.data_ptr()
