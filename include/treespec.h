@@ -115,7 +115,7 @@ typedef struct ts_attn_args {
   const int32_t* prefix_len;  /* device [num_requests]: P >= 0 */
   const int32_t* n_tree;      /* device [num_requests]: n in [n_query, n_tree_max] */
   const int32_t* parent;      /* device [num_requests][n_tree_max] */
-  const void* q;              /* device bf16 [num_requests][n_query][Hq][head_dim] */
+  const void* q;              /* device bf16 [num_requests][n_query][Hq][head_dim] (16-byte aligned) */
   const void* k_cache;        /* device bf16, layout per kv_layout (16-byte aligned) */
   const void* v_cache;        /* device bf16, same layout as k_cache */
   const int32_t* block_table; /* device [num_requests][max_blocks_per_req] (paged only) */

@@ -71,7 +71,7 @@ ts_status validate_attn(const ts_attn_args* a) {
   }
   if (!a->prefix_len || !a->n_tree || !a->parent || !a->q || !a->k_cache || !a->v_cache || !a->out)
     return TS_ERR_INVALID_ARG;
-  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 4) || !aligned(a->out, 4) ||
+  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 16) || !aligned(a->out, 4) ||
       !aligned(a->lse, 4))
     return TS_ERR_INVALID_ARG;
   if (a->force_path < 0 || a->force_path > 2 || a->num_ctas < 0) return TS_ERR_INVALID_ARG;

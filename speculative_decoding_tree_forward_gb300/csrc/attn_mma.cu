@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
     }
     // visibility of this thread's 16 columns (nb*8 + 2*t4 + e) as bit nb*2+e
     uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-    if (key0 + kBlockN > P) {
+    const bool tree_tile = key0 + kBlockN > P;
+    if (tree_tile) {
       const uint64_t w0 = tile_visibility(anc0, key0 - P) >> (2 * t4);
       const uint64_t w1 = tile_visibility(anc1, key0 - P) >> (2 * t4);
       vm0 = 0;
@@ -369,8 +370,12 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
       m1 = mn1;
       // probabilities -> bf16 A fragments of P (the m16n8 C layout of two
       // adjacent n8 blocks is the m16k16 A layout)
+      // On tiles that hold tree keys a query may see only a few keys, whose V
+      // rows can cancel; there the bf16 rounding residual of P is carried by
+      // a second PV product (P = hi + lo), so rows with few keys keep fp32-like
+      // accuracy.  Prefix-only tiles use P rounded once.
       float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pa[2][4];
+      uint32_t pa[2][4], pl[2][4];
 #pragma unroll
       for (int kc = 0; kc < 2; ++kc) {
 #pragma unroll
@@ -382,6 +387,8 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
           rs1 += e2 + e3;
           pa[kc][2 * hb + 0] = pack_bf16x2(e0, e1);
           pa[kc][2 * hb + 1] = pack_bf16x2(e2, e3);
+          pl[kc][2 * hb + 0] = bf16x2_residual(pa[kc][2 * hb + 0], e0, e1);
+          pl[kc][2 * hb + 1] = bf16x2_residual(pa[kc][2 * hb + 1], e2, e3);
         }
       }
       l0 = l0 * alpha0 + rs0;
@@ -407,6 +414,10 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
           ldsm_x4_t(addr, r0, r1, r2, r3);
           mma_16816(o[2 * dp], pa[kc], r0, r1);
           mma_16816(o[2 * dp + 1], pa[kc], r2, r3);
+          if (tree_tile) {
+            mma_16816(o[2 * dp], pl[kc], r0, r1);
+            mma_16816(o[2 * dp + 1], pl[kc], r2, r3);
+          }
         }
       }
     }
@@ -530,13 +541,18 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
   const int rows_here = min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit);
   const float ln2 = 0.69314718055994530942f;
   for (int rl = warp; rl < rows_here; rl += blockDim.x / 32) {
+    // CTAs with an empty tile range (possible when there are more CTAs than
+    // tiles) wrote no partial: skip their slots.
     float mx = -INFINITY;
-    for (int c = c_lo + lane; c <= c_hi; c += 32) mx = fmaxf(mx, p.part_lse[(c + unit) * p.rows_pad + rl]);
+    for (int c = c_lo + lane; c <= c_hi; c += 32)
+      if (sched_begin(c, T, p.num_ctas) < sched_begin(c + 1, T, p.num_ctas))
+        mx = fmaxf(mx, p.part_lse[(c + unit) * p.rows_pad + rl]);
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     const float base = (mx == -INFINITY) ? 0.f : mx;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float wsum = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
+      if (sched_begin(c, T, p.num_ctas) == sched_begin(c + 1, T, p.num_ctas)) continue;
       const int64_t slot = c + unit;
       const float w = exp2f(p.part_lse[slot * p.rows_pad + rl] - base);
       wsum += w;

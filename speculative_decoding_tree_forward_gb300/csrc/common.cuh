@@ -125,6 +125,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// bf16 pair holding (lo - bf16(lo), hi - bf16(hi)) given `rounded` = the
+// bf16 pair of (lo, hi): the part of two fp32 values that one bf16 rounding drops.
+__device__ __forceinline__ uint32_t bf16x2_residual(uint32_t rounded, float lo, float hi) {
+  const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&rounded);
+  return pack_bf16x2(lo - __low2float(r), hi - __high2float(r));
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a tile whose
 // rows are 128 bytes and which TMA wrote with 128-byte swizzling from a
 // 1024-byte-aligned base: chunk index XOR (row mod 8).
