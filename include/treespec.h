@@ -134,6 +134,25 @@ TS_API int tree_attn_selected_path(const ts_attn_args* args);
 TS_API ts_status tree_attn_forward(const ts_attn_args* args, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* Allocation-free variant of tree_attn_forward (the pages have no
+ * counterpart: this is a library convenience).  For callers that cannot
+ * allocate device memory -- code inside a host framework that owns all device
+ * memory through its own pool, or latency-critical loops where cudaMalloc
+ * would synchronize the device -- and so cannot pass a workspace.  The
+ * split-KV scratch is a 16 MiB array in device memory that the library
+ * reserves on every GPU that loads it, until the process exits.  The first
+ * call on each device (with that device current) looks up the array's device
+ * address; make that first call before any stream capture.  Same arguments,
+ * results and tolerance as tree_attn_forward; when the partials of the
+ * requested split would not fit, fewer split-KV CTAs are used; arguments whose
+ * partials exceed 16 MiB even unsplit return TS_ERR_UNSUPPORTED.  No
+ * cudaMalloc, cudaFree or allocating library call is made.  Every call shares
+ * the one array, so calls that overlap on the GPU (other streams, other host
+ * threads) race and corrupt each other's results: serialize them.  Device
+ * error bits of this variant are cleared at the start of each call and are
+ * not reported; use tree_attn_forward with a workspace to read them. */
+TS_API ts_status tree_attn_forward_noalloc(const ts_attn_args* args, void* stream);
+
 /* ------------------------------------------------------------------------
  * Greedy tree acceptance.
  *

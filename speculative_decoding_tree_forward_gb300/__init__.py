@@ -70,6 +70,7 @@ _build_mask = _sig("tree_build_mask", _i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp
 _attn_ws = _sig("tree_attn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(AttnArgs)])
 _attn_path = _sig("tree_attn_selected_path", _i32, [ctypes.POINTER(AttnArgs)])
 _attn = _sig("tree_attn_forward", _i32, [ctypes.POINTER(AttnArgs), _vp, ctypes.c_size_t, _vp])
+_attn_noalloc = _sig("tree_attn_forward_noalloc", _i32, [ctypes.POINTER(AttnArgs), _vp])
 _acc_ws = _sig("tree_accept_workspace_size", ctypes.c_size_t, [ctypes.POINTER(AcceptArgs)])
 _acc = _sig("tree_accept_greedy", _i32, [ctypes.POINTER(AcceptArgs), _vp, ctypes.c_size_t, _vp])
 _cmp_ws = _sig("tree_compact_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CompactArgs)])
@@ -79,7 +80,7 @@ _read_err = _sig("ts_read_device_error", _i32, [_vp, ctypes.POINTER(_i32), _i32,
 _version = _sig("ts_version", _i32, [])
 
 EXPORTED = ["tree_meta_workspace_size", "tree_build_mask", "tree_attn_workspace_size", "tree_attn_selected_path",
-            "tree_attn_forward",
+            "tree_attn_forward", "tree_attn_forward_noalloc",
             "tree_accept_workspace_size", "tree_accept_greedy", "tree_compact_workspace_size",
             "tree_cache_compact", "ts_status_string", "ts_read_device_error", "ts_version"]
 
@@ -201,6 +202,20 @@ def tree_attn_forward(q, k_cache, v_cache, prefix_len, n_tree, parent, out=None,
     if workspace is None:
         workspace = new_workspace(tree_attn_workspace_size(a), q.device)
     tree_attn_forward_args(a, workspace, stream)
+    return out, lse
+
+
+def tree_attn_forward_noalloc(q, k_cache, v_cache, prefix_len, n_tree, parent, out, lse=None, block_table=None,
+                              softmax_scale: float = 0.0, stream=None, force_path: int = 0, num_ctas: int = 0):
+    """tree_attn_forward for callers that cannot allocate device memory.
+
+    The library keeps the split-KV scratch in its own 16 MiB device array, so
+    the caller passes only inputs and preallocated outputs (``out`` and
+    optionally ``lse``).  Calls that overlap on the GPU race on that array.
+    """
+    a = attn_args(q, k_cache, v_cache, prefix_len, n_tree, parent, out, lse, block_table, softmax_scale,
+                  force_path, num_ctas)
+    _check(_attn_noalloc(ctypes.byref(a), _stream(stream)), "tree_attn_forward_noalloc")
     return out, lse
 
 
