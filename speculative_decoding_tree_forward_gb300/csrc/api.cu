@@ -145,6 +145,24 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const ts_attn_args* a) {
   return r == CUDA_SUCCESS;
 }
 
+// Q as a 3-D tensor (head_dim, Hq, num_requests * n_query); one box of
+// (64, G, n_query) is the 128 packed rows (node-major, head within the group)
+// of one KV head, in two 64-column halves.
+bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, int group) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->head_dim), static_cast<cuuint64_t>(a->num_q_heads),
+                        static_cast<cuuint64_t>(a->num_requests) * a->n_query};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(a->head_dim) * 2,
+                           static_cast<cuuint64_t>(a->head_dim) * 2 * a->num_q_heads};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(a->n_query)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace ts
 
@@ -248,7 +266,14 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pl.use_tc ? launch_attn_tc(p, kmap, vmap, s) : launch_attn_mma(p, kmap, vmap, s);
+  cudaError_t e;
+  if (pl.use_tc) {
+    CUtensorMap qmap;
+    if (!encode_q_map(&qmap, a, pl.group)) return TS_ERR_CUDA;
+    e = launch_attn_tc(p, kmap, vmap, qmap, s);
+  } else {
+    e = launch_attn_mma(p, kmap, vmap, s);
+  }
   if (e != cudaSuccess) return TS_ERR_CUDA;
   e = launch_attn_merge(p, s);
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;

@@ -43,7 +43,7 @@ struct AttnParams {
 cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           cudaStream_t stream);
+                           const CUtensorMap& qmap, cudaStream_t stream);
 cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream);
 size_t attn_mma_smem_bytes(int head_dim, int stages, int num_req, int rows_pad);
 size_t attn_tc_smem_bytes(int stages, int num_req);

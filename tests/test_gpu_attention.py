@@ -45,6 +45,69 @@ def test_small_cases_match_oracle(cfg, paged):
     check_attention(case, out, lse, A.attention_case(case))
 
 
+# packed rows R = G * n_query = 128 with head_dim 128: the tcgen05 / TMEM kernel
+TC = [
+    dict(num_req=2, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(0, 500)),
+    dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=32, prefix_range=(0, 300)),
+    dict(num_req=3, hq=16, hkv=1, d=128, n_tree_max=24, n_query=8, ragged_tree=True, prefix_range=(10, 400)),
+    dict(num_req=2, hq=128, hkv=1, d=128, n_tree_max=3, n_query=1, prefix_range=(0, 200)),
+    dict(num_req=1, hq=2, hkv=2, d=128, n_tree_max=128, prefix_range=(0, 150)),
+    dict(num_req=2, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(0, 0)),
+]
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("cfg", range(len(TC)))
+def test_tcgen05_cases_match_oracle(cfg, paged):
+    case = W.random_attn_case(200 + cfg, paged=paged, **TC[cfg])
+    out, lse = run(case, force_path=2)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 64, 1000])
+def test_tcgen05_split_counts_match_oracle(num_ctas):
+    case = W.random_attn_case(8, num_req=3, hq=16, hkv=4, d=128, n_tree_max=40, n_query=32, prefix_range=(10, 700),
+                              ragged_tree=True)
+    out, lse = run(case, force_path=2, num_ctas=num_ctas)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_large_scores_rescale_running_max(path):
+    """Scale 2.0 makes scores grow by far more than 2^8 across tiles: the running max is raised many times."""
+    case = W.random_attn_case(9, num_req=2, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(300, 900),
+                              scale=2.0)
+    out, lse = run(case, force_path=path)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
+def test_tcgen05_rows_past_the_last_key_may_hold_nan():
+    case = W.random_attn_case(15, num_req=2, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(20, 100))
+    d = attn_inputs(case)
+    ref = A.attention_case(case)
+    for b in range(case.num_req):
+        end = int(case.prefix_len[b] + case.n_tree[b])
+        d["k_cache"][b, end:] = float("nan")
+        d["v_cache"][b, end:] = float("inf")
+    out, lse = ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
+                                    force_path=2)
+    torch.cuda.synchronize()
+    check_attention(case, out, lse, ref)
+
+
+def test_automatic_path_choice():
+    case = W.random_attn_case(16, num_req=1, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(5, 5))
+    d = attn_inputs(case)
+    a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
+                     torch.empty_like(d["q"]))
+    assert ts.tree_attn_selected_path(a) == "tcgen05"
+    case2 = W.random_attn_case(16, num_req=1, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(5, 5))
+    d2 = attn_inputs(case2)
+    a2 = ts.attn_args(d2["q"], d2["k_cache"], d2["v_cache"], d2["prefix_len"], d2["n_tree"], d2["parent"],
+                      torch.empty_like(d2["q"]))
+    assert ts.tree_attn_selected_path(a2) == "mma"
+
+
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 1000])
 def test_split_counts_match_oracle(num_ctas):
     """Every split of the key range (one CTA for everything up to one tile per CTA) merges to the same result."""
