@@ -46,7 +46,7 @@ struct AttnPlan {
   bool use_tc;
   int rows, row_groups, rows_pad, group, stages, num_ctas;
   int64_t units, slots;
-  size_t ws_bytes, off_o, off_lse;
+  size_t ws_bytes, off_cnt, off_o, off_lse;
 };
 
 ts_status validate_attn(const ts_attn_args* a) {
@@ -121,7 +121,8 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
     pl->num_ctas = static_cast<int>(nc < 1 ? 1 : nc);
   }
   pl->slots = pl->num_ctas + pl->units;
-  pl->off_o = kWsHeader;
+  pl->off_cnt = kWsHeader;
+  pl->off_o = pl->off_cnt + align256(static_cast<size_t>(pl->units) * sizeof(int));
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
   pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
   return TS_OK;
@@ -164,6 +165,15 @@ bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, int group) {
 }
 
 }  // namespace
+
+// Leading workspace bytes that must be zero when a call starts (error word
+// and split-KV counters); 0 when the arguments are rejected.
+size_t attn_zero_prefix_bytes(const ts_attn_args* a) {
+  AttnPlan pl;
+  if (plan_attn(a, &pl) != TS_OK) return 0;
+  return pl.off_o;
+}
+
 }  // namespace ts
 
 using namespace ts;
@@ -263,6 +273,7 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(static_cast<float>(a->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = reinterpret_cast<unsigned*>(ws);
+  p.counters = reinterpret_cast<int*>(ws + pl.off_cnt);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -274,8 +285,6 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   } else {
     e = launch_attn_mma(p, kmap, vmap, s);
   }
-  if (e != cudaSuccess) return TS_ERR_CUDA;
-  e = launch_attn_merge(p, s);
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 

@@ -11,7 +11,8 @@
 // CTA's key range through QK^T, an online softmax in the exp2 domain and PV.
 // Keys are split across CTAs by the stream-K schedule in common.cuh; a CTA
 // that holds a whole unit writes the bf16 output directly, otherwise it
-// writes a normalised fp32 partial and its log2-sum-exp for the merge.
+// writes a normalised fp32 partial and its log2-sum-exp, and the last CTA to
+// finish its share of the unit combines the partials (attn_common.cuh).
 #include "attn_common.cuh"
 
 namespace ts {
@@ -43,6 +44,19 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
+struct ConsumerSync {
+  int n;
+  __device__ void operator()() const { consumer_sync(n); }
+};
+
+// The combine runs rarely (once per split unit) and outside the hot loop:
+// kept out of line so it adds nothing to the loop's register budget.
+__device__ __noinline__ void merge_unit_rows_mma(const AttnParams& p, int64_t unit, int b, int kvh, int rg, int64_t T,
+                                                 int64_t first, int tiles, int tid, int nthr, float* wbuf,
+                                                 int wbuf_floats) {
+  merge_unit_rows(p, unit, b, kvh, rg, T, first, tiles, tid, nthr, wbuf, wbuf_floats, ConsumerSync{nthr});
+}
+
 template <int D>
 __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                                                        const __grid_constant__ CUtensorMap vmap,
@@ -54,6 +68,7 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
   uint64_t* empty_bar = full_bar + p.stages;
   int64_t* cum = reinterpret_cast<int64_t*>(smem + L.cum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
+  volatile int* merge_flag = abort_flag + 1;
 
   const int tid = threadIdx.x;
   const int warp = tid / kThreadsPerWarp;
@@ -475,6 +490,11 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
           pl[rl0] = L0 > 0.f ? m0 + log2f(L0) : -INFINITY;
           pl[rl1] = L1 > 0.f ? m1 + log2f(L1) : -INFINITY;
         }
+        const int64_t first = cum[b] + static_cast<int64_t>(uir) * tiles;
+        if (split_arrive(p, unit, T, first, tiles, ctid, merge_flag, [&]() { consumer_sync(n_consumers); }))
+          // the Q tile is idle between units: it holds the merge weights
+          merge_unit_rows_mma(p, unit, b, kvh, rg, T, first, tiles, ctid, n_consumers,
+                              reinterpret_cast<float*>(smem + L.qs), p.rows_pad * D / 2);
       }
       if (last_of_cta) break;
       if (++uir == units_per_req) {
@@ -489,83 +509,6 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
     } else {
       ++tile;
     }
-  }
-}
-
-// ---------------------------------------------------------------- merge
-// One CTA per unit; a warp per packed row, lanes over the head dim.
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
-  const int64_t unit = blockIdx.x;
-  const int units_per_req = p.hkv * p.row_groups;
-  const int b = static_cast<int>(unit / units_per_req);
-  const int uir = static_cast<int>(unit % units_per_req);
-  const int kvh = uir / p.row_groups;
-  const int rg = uir % p.row_groups;
-  __shared__ long long part[256];
-  __shared__ int64_t base_s, total_s;
-  long long before = 0, total = 0;
-  for (int bb = threadIdx.x; bb < p.num_req; bb += blockDim.x) {
-    int P, n;
-    attn_lengths(p, bb, P, n, false);
-    const long long tl = static_cast<long long>(attn_tiles(P + n)) * units_per_req;
-    total += tl;
-    if (bb < b) before += tl;
-  }
-  part[threadIdx.x] = before;
-  __syncthreads();
-  for (int s = 128; s > 0; s >>= 1) {
-    if (threadIdx.x < s) part[threadIdx.x] += part[threadIdx.x + s];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) base_s = part[0];
-  __syncthreads();
-  part[threadIdx.x] = total;
-  __syncthreads();
-  for (int s = 128; s > 0; s >>= 1) {
-    if (threadIdx.x < s) part[threadIdx.x] += part[threadIdx.x + s];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) total_s = part[0];
-  __syncthreads();
-  int P, n;
-  attn_lengths(p, b, P, n, false);
-  const int tiles = attn_tiles(P + n);
-  const int64_t T = total_s;
-  const int64_t first = base_s + static_cast<int64_t>(uir) * tiles;
-  const int c_lo = sched_cta_of(first, T, p.num_ctas);
-  const int c_hi = sched_cta_of(first + tiles - 1, T, p.num_ctas);
-  if (c_lo == c_hi) return;  // one CTA held the whole unit and wrote it
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int D = p.head_dim;
-  const int rows_here = min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit);
-  const float ln2 = 0.69314718055994530942f;
-  for (int rl = warp; rl < rows_here; rl += blockDim.x / 32) {
-    // CTAs with an empty tile range (possible when there are more CTAs than
-    // tiles) wrote no partial: skip their slots.
-    float mx = -INFINITY;
-    for (int c = c_lo + lane; c <= c_hi; c += 32)
-      if (sched_begin(c, T, p.num_ctas) < sched_begin(c + 1, T, p.num_ctas))
-        mx = fmaxf(mx, p.part_lse[(c + unit) * p.rows_pad + rl]);
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float base = (mx == -INFINITY) ? 0.f : mx;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float wsum = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      if (sched_begin(c, T, p.num_ctas) == sched_begin(c + 1, T, p.num_ctas)) continue;
-      const int64_t slot = c + unit;
-      const float w = exp2f(p.part_lse[slot * p.rows_pad + rl] - base);
-      wsum += w;
-      const float* po = p.part_o + (slot * p.rows_pad + rl) * D;
-      for (int j = 0; j < D / 32; ++j) acc[j] += w * po[lane + 32 * j];
-    }
-    const float inv = wsum > 0.f ? __frcp_rn(wsum) : 0.f;
-    const int r = rg * kMaxRowsPerUnit + rl;
-    const int i = r / p.group, h = kvh * p.group + r % p.group;
-    __nv_bfloat16* orow = p.out + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * D;
-    for (int j = 0; j < D / 32; ++j) orow[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
-    if (p.lse != nullptr && lane == 0)
-      p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (base + log2f(wsum)) * ln2;
   }
 }
 
@@ -588,11 +531,6 @@ cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const 
     cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     attn_mma_kernel<64><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream) {
-  attn_merge_kernel<<<static_cast<unsigned>(p.num_units), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -21,7 +21,8 @@
 //              O += P_j V_j (M 128, N 128, K 64, V read MN-major) into TMEM O;
 //              completion is signalled with tcgen05.commit on mbarriers.
 // TMEM: 256 columns = S0 [0, 64) | S1 [64, 128) | O [128, 256).
-// The split-KV schedule and the merge are those of the warp-MMA kernel.
+// The split-KV schedule and the in-kernel combine of partials are those of
+// the warp-MMA kernel (attn_common.cuh).
 #include "attn_common.cuh"
 #include "tcgen05.cuh"
 
@@ -51,14 +52,15 @@ struct TcCtrl {
   uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, o_done, o_free, fin;
   uint32_t tmem_base;
   int abort;
+  int merge_flag;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int num_req) {
   TcLayout L;
   L.q = 0;
   L.kv = L.q + TcLayout::kQBytes;
-  L.p_hi = L.kv + kTcStages * TcLayout::kStageBytes;
-  L.p_lo = L.p_hi + TcLayout::kPBytes;
+  L.p_hi = L.kv + kTcStages * TcLayout::kStageBytes;  // two buffers, alternating tiles
+  L.p_lo = L.p_hi + 2 * TcLayout::kPBytes;
   L.ctrl = L.p_lo + TcLayout::kPBytes;
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.cum = L.par + TS_MAX_TREE * 4;
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const uint32_t vs = skv + cp.st * TcLayout::kStageBytes + TcLayout::kKvBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tbase + kColO, smem_desc_sw128(sph + kk * 32, 16, 1024),
+          tc_mma_bf16(tbase + kColO, smem_desc_sw128(sph + (j & 1) * TcLayout::kPBytes + kk * 32, 16, 1024),
                       smem_desc_sw128(vs + kk * 2048, TcLayout::kKvBytes / 2, 1024), kIdescPV,
                       (unit_first && kk == 0) ? 0u : 1u);
         if (tree_tile) {
@@ -349,50 +351,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       tc_fence_after();
       float x[64];
       {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + (it & 1) * 64, v);
+        uint32_t v0[32], v1[32];
+        tmem_ld32(lane_addr + (it & 1) * 64, v0);
+        tmem_ld32(lane_addr + (it & 1) * 64 + 32, v1);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
-        tmem_ld32(lane_addr + (it & 1) * 64 + 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[32 + e] = __uint_as_float(v[e]);
+        for (int e = 0; e < 32; ++e) {
+          x[e] = __uint_as_float(v0[e]);
+          x[32 + e] = __uint_as_float(v1[e]);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_free[it & 1]);
 
-      // ---- scale, ancestor mask, lazily-updated running max
+      // ---- ancestor mask (tiles holding tree keys only), running max in log2 units
       const int key0 = c.tile * kBlockN;
       const bool tree_tile = key0 + kBlockN > c.P;
-      const uint64_t vis = tree_tile ? tile_visibility(anc, key0 - c.P) : ~0ull;
       float mx = -INFINITY;
+      if (tree_tile) {
+        const uint64_t vis = tile_visibility(anc, key0 - c.P);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float s = ((vis >> e) & 1ull) ? x[e] * p.scale_log2 : -INFINITY;
-        x[e] = s;
-        mx = fmaxf(mx, s);
+        for (int e = 0; e < 64; ++e) {
+          x[e] = ((vis >> e) & 1ull) ? x[e] : -INFINITY;
+          mx = fmaxf(mx, x[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
       }
+      const float mxs = mx * p.scale_log2;  // scale > 0, so the max commutes with it
       float alpha = 1.f;
       bool rescale = false;
       if (m_used == -INFINITY) {
-        m_used = mx;  // O and l hold nothing for this row yet
-      } else if (mx > m_used + kRescaleThreshold) {
-        alpha = exp2f(m_used - mx);
-        m_used = mx;
+        m_used = mxs;  // O and l hold nothing for this row yet
+      } else if (mxs > m_used + kRescaleThreshold) {
+        alpha = ex2_approx(m_used - mxs);
+        m_used = mxs;
         rescale = !unit_first;
       }
-      const float base = (m_used == -INFINITY) ? 0.f : m_used;
+      const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
 
-      // the P tile (and O, for a rescale) may be reused once PV of the previous tile is done
-      if (it > 0 && !mbar_wait(&ctl->o_done, (it - 1) & 1)) {
-        report_error(p.err, TS_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-        break;
+      // PV of the previous tile must be complete before O is rescaled or the
+      // single residual tile is rewritten.  The bf16 P tile alternates between
+      // two buffers: PV of tile it-2 had completed before S of tile it was
+      // signalled, so it is written without waiting.  Completion of PV it-1 is
+      // confirmed in every iteration before P of tile it is released, so the
+      // o_done parity waits never fall two phases behind.
+      const bool need_rescale = __any_sync(0xffffffffu, rescale);
+      bool pv_prev_done = (it == 0);
+      if (!pv_prev_done && (need_rescale || tree_tile)) {
+        if (!mbar_wait(&ctl->o_done, (it - 1) & 1)) {
+          report_error(p.err, TS_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        pv_prev_done = true;
       }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale)) {
+      if (need_rescale) {
         const float a = rescale ? alpha : 1.f;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -405,26 +422,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         tmem_st_wait();
       }
-      l *= alpha;
 
-      // ---- probabilities -> bf16 P tile (row r, 128-byte swizzled), residual on tree tiles
+      // ---- probabilities 2^(s*scale - m) -> bf16 P tile (row r, 128-byte swizzled),
+      //      plus the bf16 rounding residual on tiles holding tree keys
       float rs = 0.f;
+      uint8_t* prow = sph + (it & 1) * TcLayout::kPBytes;
 #pragma unroll
       for (int ck = 0; ck < 8; ++ck) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float e0 = exp2f(x[ck * 8 + 2 * q] - base);
-          const float e1 = exp2f(x[ck * 8 + 2 * q + 1] - base);
+          const float e0 = ex2_approx(fmaf(x[8 * ck + 2 * q], p.scale_log2, nbase));
+          const float e1 = ex2_approx(fmaf(x[8 * ck + 2 * q + 1], p.scale_log2, nbase));
           rs += e0 + e1;
           hi[q] = pack_bf16x2(e0, e1);
-          lo[q] = bf16x2_residual(hi[q], e0, e1);
+          if (tree_tile) lo[q] = bf16x2_residual(hi[q], e0, e1);
         }
         const uint32_t off = sw128(r, ck);
-        *reinterpret_cast<uint4*>(sph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         if (tree_tile) *reinterpret_cast<uint4*>(spl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      l += rs;
+      l = l * alpha + rs;
       // rows past the last key may hold anything; their probability is 0 but
       // 0 * NaN is NaN, so zero them in the V tile before PV reads it
       const int keys = c.P + c.n;
@@ -435,6 +453,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         for (int h = 0; h < 2; ++h)
           for (int xv = r; xv < nvec; xv += kSoftmaxThreads)
             reinterpret_cast<uint4*>(vs + h * (TcLayout::kKvBytes / 2) + first * 128)[xv] = make_uint4(0, 0, 0, 0);
+      }
+      if (!pv_prev_done && !mbar_wait(&ctl->o_done, (it - 1) & 1)) {
+        report_error(p.err, TS_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -482,15 +505,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           }
         }
         const float lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->o_free);  // O has been read: the next unit's PV may overwrite it
         if (complete) {
           if (p.lse != nullptr)
             p.lse[(static_cast<int64_t>(c.b) * p.hq + h) * p.n_query + i] = lse2 * 0.69314718055994530942f;
         } else {
           p.part_lse[slot * 128 + r] = lse2;
+          const int64_t first = cum[c.b] + static_cast<int64_t>(c.uir) * c.tiles;
+          if (split_arrive(p, unit, T, first, c.tiles, r, &ctl->merge_flag, softmax_sync))
+            // the residual P tile is idle here (PV of this tile is done, the
+            // next P is not yet released): it holds the merge weights
+            merge_unit_rows(p, unit, c.b, kvh, 0, T, first, c.tiles, r, kSoftmaxThreads,
+                            reinterpret_cast<float*>(spl), TcLayout::kPBytes / 4, softmax_sync);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->o_free);
         seg_first = 0;
       }
       c.advance(p, units_per_req);

@@ -125,6 +125,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^x by the hardware approximation (ex2.approx, flush-to-zero): exact 0
+// for x = -inf, relative error of a few ulp, far below the bf16 rounding the
+// probabilities go through.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // bf16 pair holding (lo - bf16(lo), hi - bf16(hi)) given `rounded` = the
 // bf16 pair of (lo, hi): the part of two fp32 values that one bf16 rounding drops.
 __device__ __forceinline__ uint32_t bf16x2_residual(uint32_t rounded, float lo, float hi) {

@@ -72,6 +72,14 @@ def test_tcgen05_split_counts_match_oracle(num_ctas):
     check_attention(case, out, lse, A.attention_case(case))
 
 
+@pytest.mark.parametrize("num_ctas", [190, 300, 400])
+def test_tcgen05_first_call_many_short_splits(num_ctas):
+    """A fresh workspace and two to four tiles per CTA: every unit is combined from many partials."""
+    case = W.random_attn_case(21, num_req=8, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(300, 1200))
+    out, lse = run(case, force_path=2, num_ctas=num_ctas)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
 @pytest.mark.parametrize("path", [1, 2])
 def test_large_scores_rescale_running_max(path):
     """Scale 2.0 makes scores grow by far more than 2^8 across tiles: the running max is raised many times."""
