@@ -368,18 +368,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // ---- ancestor mask (tiles holding tree keys only), running max in log2 units
       const int key0 = c.tile * kBlockN;
       const bool tree_tile = key0 + kBlockN > c.P;
-      float mx = -INFINITY;
       if (tree_tile) {
         const uint64_t vis = tile_visibility(anc, key0 - c.P);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          x[e] = ((vis >> e) & 1ull) ? x[e] : -INFINITY;
-          mx = fmaxf(mx, x[e]);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
+        for (int e = 0; e < 64; ++e) x[e] = ((vis >> e) & 1ull) ? x[e] : -INFINITY;
       }
+      // eight independent partial maxima keep the dependency chain short
+      float pm[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) pm[q] = x[q];
+#pragma unroll
+      for (int e = 8; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], x[e]);
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       const float mxs = mx * p.scale_log2;  // scale > 0, so the max commutes with it
       float alpha = 1.f;
       bool rescale = false;
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
       // ---- probabilities 2^(s*scale - m) -> bf16 P tile (row r, 128-byte swizzled),
       //      plus the bf16 rounding residual on tiles holding tree keys
-      float rs = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};  // partial row sums
       uint8_t* prow = sph + (it & 1) * TcLayout::kPBytes;
 #pragma unroll
       for (int ck = 0; ck < 8; ++ck) {
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         for (int q = 0; q < 4; ++q) {
           const float e0 = ex2_approx(fmaf(x[8 * ck + 2 * q], p.scale_log2, nbase));
           const float e1 = ex2_approx(fmaf(x[8 * ck + 2 * q + 1], p.scale_log2, nbase));
-          rs += e0 + e1;
+          ps[q] += e0 + e1;
           hi[q] = pack_bf16x2(e0, e1);
           if (tree_tile) lo[q] = bf16x2_residual(hi[q], e0, e1);
         }
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         if (tree_tile) *reinterpret_cast<uint4*>(spl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      l = l * alpha + rs;
+      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       // rows past the last key may hold anything; their probability is 0 but
       // 0 * NaN is NaN, so zero them in the V tile before PV reads it
       const int keys = c.P + c.n;
