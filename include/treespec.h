@@ -3,7 +3,9 @@
  *
  * C ABI.  Every pointer named "device" is device memory owned by the caller;
  * the library allocates nothing, keeps no global state besides one cached
- * driver entry point, and never synchronises the stream it is given.  Every
+ * driver entry point and per-device launch facts (SM count, kernel
+ * occupancy; computed on first use, guarded by a mutex), and never
+ * synchronises the stream it is given.  Every
  * entry point validates its arguments on the host and returns a ts_status
  * synchronously; kernels are launched asynchronously on `stream` (a
  * cudaStream_t; NULL = the legacy default stream).  Kernel-side faults in the
@@ -119,7 +121,7 @@ typedef struct ts_attn_args {
   const void* k_cache;        /* device bf16, layout per kv_layout (16-byte aligned) */
   const void* v_cache;        /* device bf16, same layout as k_cache */
   const int32_t* block_table; /* device [num_requests][max_blocks_per_req] (paged only) */
-  void* out;                  /* device bf16 [num_requests][n_query][Hq][head_dim] (out) */
+  void* out;                  /* device bf16 [num_requests][n_query][Hq][head_dim] (out, 16-byte aligned) */
   float* lse;                 /* device fp32 [num_requests][Hq][n_query] (out) or NULL */
   float softmax_scale;        /* <= 0 selects 1 / sqrt(head_dim) */
   int force_path;             /* 0 automatic; 1 warp-mma kernel; 2 tcgen05 kernel (G*n_query == 128 only) */

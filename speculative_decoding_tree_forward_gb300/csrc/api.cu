@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -34,11 +35,52 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
+// Per-device launch facts, computed once per device and kept for the
+// process: SM count and the occupancy of each kernel shape (computing the
+// occupancy also raises the kernel's dynamic shared-memory limit, which the
+// launches rely on).
+struct OccEntry {
+  int key;  // (tc ? 1 << 20 : 0) | head_dim << 12 | stages << 7 | rows_pad
+  int occ;
+};
+struct DeviceFacts {
+  int sms = 0;
+  int n = 0;
+  OccEntry e[32];
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_facts_mutex;
+DeviceFacts g_facts[kMaxDevices];
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
 int device_sm_count() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return sms;
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(g_facts_mutex);
+  if (g_facts[dev].sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_facts[dev].sms = sms;
+  }
+  return g_facts[dev].sms;
+}
+
+int cached_occupancy(bool tc, int head_dim, int stages, int rows_pad, int num_req) {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  const int key = (tc ? 1 << 20 : 0) | head_dim << 12 | stages << 7 | rows_pad;
+  std::lock_guard<std::mutex> lock(g_facts_mutex);
+  DeviceFacts& f = g_facts[dev];
+  for (int i = 0; i < f.n; ++i)
+    if (f.e[i].key == key) return f.e[i].occ;
+  const int occ = tc ? attn_tc_occupancy(stages, num_req) : attn_mma_occupancy(head_dim, stages, num_req, rows_pad);
+  if (occ > 0 && f.n < 32) f.e[f.n++] = OccEntry{key, occ};
+  return occ;
 }
 
 // ------------------------------------------------------------------ attention plan
@@ -46,7 +88,7 @@ struct AttnPlan {
   bool use_tc;
   int rows, row_groups, rows_pad, group, stages, num_ctas;
   int64_t units, slots;
-  size_t ws_bytes, off_cnt, off_o, off_lse;
+  size_t ws_bytes, off_o, off_lse;
 };
 
 ts_status validate_attn(const ts_attn_args* a) {
@@ -71,7 +113,7 @@ ts_status validate_attn(const ts_attn_args* a) {
   }
   if (!a->prefix_len || !a->n_tree || !a->parent || !a->q || !a->k_cache || !a->v_cache || !a->out)
     return TS_ERR_INVALID_ARG;
-  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 16) || !aligned(a->out, 4) ||
+  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 16) || !aligned(a->out, 16) ||
       !aligned(a->lse, 4))
     return TS_ERR_INVALID_ARG;
   if (a->force_path < 0 || a->force_path > 2 || a->num_ctas < 0) return TS_ERR_INVALID_ARG;
@@ -103,12 +145,12 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   int occ = 1;
   if (pl->use_tc) {
     pl->stages = 4;
-    occ = attn_tc_occupancy(pl->stages, a->num_requests);
+    occ = cached_occupancy(true, a->head_dim, pl->stages, pl->rows_pad, a->num_requests);
   } else {
     const int rb = pl->rows_pad / 16;
     if (a->head_dim == 128) pl->stages = rb <= 4 ? 3 : 5;
     else pl->stages = rb <= 4 ? 6 : 10;
-    occ = attn_mma_occupancy(a->head_dim, pl->stages, a->num_requests, pl->rows_pad);
+    occ = cached_occupancy(false, a->head_dim, pl->stages, pl->rows_pad, a->num_requests);
   }
   if (occ < 1) return TS_ERR_UNSUPPORTED;
   if (a->num_ctas > 0) {
@@ -121,8 +163,7 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
     pl->num_ctas = static_cast<int>(nc < 1 ? 1 : nc);
   }
   pl->slots = pl->num_ctas + pl->units;
-  pl->off_cnt = kWsHeader;
-  pl->off_o = pl->off_cnt + align256(static_cast<size_t>(pl->units) * sizeof(int));
+  pl->off_o = kWsHeader;
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
   pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
   return TS_OK;
@@ -166,8 +207,8 @@ bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, int group) {
 
 }  // namespace
 
-// Leading workspace bytes that must be zero when a call starts (error word
-// and split-KV counters); 0 when the arguments are rejected.
+// Leading workspace bytes that must be zero when a call starts (the error
+// word); 0 when the arguments are rejected.
 size_t attn_zero_prefix_bytes(const ts_attn_args* a) {
   AttnPlan pl;
   if (plan_attn(a, &pl) != TS_OK) return 0;
@@ -273,7 +314,6 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(static_cast<float>(a->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = reinterpret_cast<unsigned*>(ws);
-  p.counters = reinterpret_cast<int*>(ws + pl.off_cnt);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -285,6 +325,8 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   } else {
     e = launch_attn_mma(p, kmap, vmap, s);
   }
+  if (e != cudaSuccess) return TS_ERR_CUDA;
+  e = launch_attn_merge(p, s);
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 

@@ -11,8 +11,8 @@
 // CTA's key range through QK^T, an online softmax in the exp2 domain and PV.
 // Keys are split across CTAs by the stream-K schedule in common.cuh; a CTA
 // that holds a whole unit writes the bf16 output directly, otherwise it
-// writes a normalised fp32 partial and its log2-sum-exp, and the last CTA to
-// finish its share of the unit combines the partials (attn_common.cuh).
+// writes a normalised fp32 partial and its log2-sum-exp, which the combine
+// kernel (attn_merge.cu) merges.
 #include "attn_common.cuh"
 
 namespace ts {
@@ -35,26 +35,14 @@ __host__ __device__ inline SmemLayout mma_layout(int head_dim, int stages, int n
   L.par = L.bars + 2 * 8 * stages;
   L.cum = L.par + static_cast<uint32_t>(rows_pad / 16) * TS_MAX_TREE * 4;
   L.cum = (L.cum + 7) & ~7u;
-  L.flag = L.cum + 8 * (num_req + 1);
+  L.flag = L.cum + 8 * (kMaxRequestsAttn + 1);  // fixed: launch shape independent of the batch
+  (void)num_req;
   L.total = L.flag + 16;
   return L;
 }
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-struct ConsumerSync {
-  int n;
-  __device__ void operator()() const { consumer_sync(n); }
-};
-
-// The combine runs rarely (once per split unit) and outside the hot loop:
-// kept out of line so it adds nothing to the loop's register budget.
-__device__ __noinline__ void merge_unit_rows_mma(const AttnParams& p, int64_t unit, int b, int kvh, int rg, int64_t T,
-                                                 int64_t first, int tiles, int tid, int nthr, float* wbuf,
-                                                 int wbuf_floats) {
-  merge_unit_rows(p, unit, b, kvh, rg, T, first, tiles, tid, nthr, wbuf, wbuf_floats, ConsumerSync{nthr});
 }
 
 template <int D>
@@ -68,7 +56,6 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
   uint64_t* empty_bar = full_bar + p.stages;
   int64_t* cum = reinterpret_cast<int64_t*>(smem + L.cum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
-  volatile int* merge_flag = abort_flag + 1;
 
   const int tid = threadIdx.x;
   const int warp = tid / kThreadsPerWarp;
@@ -490,11 +477,6 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
           pl[rl0] = L0 > 0.f ? m0 + log2f(L0) : -INFINITY;
           pl[rl1] = L1 > 0.f ? m1 + log2f(L1) : -INFINITY;
         }
-        const int64_t first = cum[b] + static_cast<int64_t>(uir) * tiles;
-        if (split_arrive(p, unit, T, first, tiles, ctid, merge_flag, [&]() { consumer_sync(n_consumers); }))
-          // the Q tile is idle between units: it holds the merge weights
-          merge_unit_rows_mma(p, unit, b, kvh, rg, T, first, tiles, ctid, n_consumers,
-                              reinterpret_cast<float*>(smem + L.qs), p.rows_pad * D / 2);
       }
       if (last_of_cta) break;
       if (++uir == units_per_req) {
@@ -520,29 +502,35 @@ size_t attn_mma_smem_bytes(int head_dim, int stages, int num_req, int rows_pad) 
 
 int attn_mma_threads(int rows_pad) { return kThreadsPerWarp * (1 + rows_pad / 16); }
 
+// The dynamic shared-memory attribute was raised by attn_mma_occupancy, which
+// the host plan runs (once per device and shape) before any launch.
 cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
   const size_t smem = attn_mma_smem_bytes(p.head_dim, p.stages, p.num_req, p.rows_pad);
   const int threads = attn_mma_threads(p.rows_pad);
-  if (p.head_dim == 128) {
-    cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    attn_mma_kernel<128><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
-  } else {
-    cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    attn_mma_kernel<64><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
-  }
+  if (p.head_dim == 128) attn_mma_kernel<128><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
+  else attn_mma_kernel<64><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
 int attn_mma_occupancy(int head_dim, int stages, int num_req, int rows_pad) {
+  // raise the kernel's dynamic shared-memory limit to the device maximum once,
+  // so every shape's launch fits; occupancy uses this shape's size
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return 0;
   int nb = 0;
   const size_t smem = attn_mma_smem_bytes(head_dim, stages, num_req, rows_pad);
+  if (smem > static_cast<size_t>(optin)) return 0;
   const int threads = attn_mma_threads(rows_pad);
   if (head_dim == 128) {
-    cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+      return 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_mma_kernel<128>, threads, smem);
   } else {
-    cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+      return 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_mma_kernel<64>, threads, smem);
   }
   return nb;

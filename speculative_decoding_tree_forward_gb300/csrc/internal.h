@@ -35,7 +35,6 @@ struct AttnParams {
   float* lse;
   float scale_log2;  // softmax scale * log2(e)
   unsigned* err;     // workspace error word
-  int* counters;     // [num_units] split-KV arrivals, zero between calls
   float* part_o;     // [slots][rows_pad][head_dim]
   float* part_lse;   // [slots][rows_pad] (log2 domain)
 };
@@ -46,6 +45,7 @@ cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const 
 cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& qmap, cudaStream_t stream);
 size_t attn_zero_prefix_bytes(const ts_attn_args* a);
+cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream);
 size_t attn_mma_smem_bytes(int head_dim, int stages, int num_req, int rows_pad);
 size_t attn_tc_smem_bytes(int stages, int num_req);
 int attn_mma_threads(int rows_pad);

@@ -71,9 +71,8 @@ extern "C" TS_API ts_status tree_attn_forward_noalloc(const ts_attn_args* args, 
     }
     a.num_ctas = lo;
   }
-  // The array keeps the previous call's contents; the error word and the
-  // split-KV arrival counters must start at zero (partial slots are written
-  // before they are read).
+  // The array keeps the previous call's contents; the error word must start
+  // at zero (partial slots are written before they are read).
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t zero_bytes = ts::attn_zero_prefix_bytes(&a);
   if (zero_bytes == 0 || cudaMemsetAsync(scratch, 0, zero_bytes, s) != cudaSuccess) return TS_ERR_CUDA;
