@@ -5,29 +5,40 @@
 // of 128); the ancestor mask is the SwiftSpec summary's Figure 3 and the key
 // split with a combine its §3.3.
 //
-// One CTA per SM, 320 threads, warp-specialised:
+// One CTA per SM, 352 threads, warp-specialised:
 //   warps 0-3 and 4-7  two softmax warpgroups.  Tile k of the CTA's range
 //              belongs to warpgroup k % 2; thread t of a warpgroup owns
 //              packed row t (TMEM lane t).  Per 64-key tile it reads its row
 //              of S = QK^T from TMEM, applies the scale and the ancestor mask,
 //              keeps a lazily-updated running max (its O is rescaled in TMEM
 //              only when the max grows by more than 2^8), and writes the
-//              probabilities as bf16 pairs into TMEM (plus the bf16 rounding
-//              residual on tiles that hold tree keys).  Each warpgroup keeps
-//              its own O, max and sum; at the end of a unit segment the
-//              warpgroup that owns its last tile combines both and writes the
-//              bf16 output or an fp32 split-KV partial (merged afterwards by
-//              the combine kernel, attn_merge.cu).
-//   warp 8     TMA producer: Q once per unit (3-D box G x n_query rows), K and
-//              V tiles into a 5-stage ring of shared-memory stages.
-//   warp 9     MMA issuer (one lane), an event loop over two streams:
-//              S_k = Q K_k^T (M 128, N 64, K 128, both operands in shared
-//              memory) into warpgroup k % 2's S as soon as that S is free, and
-//              O_w += P_k V_k (M 128, N 128, K 64; P from TMEM, V read
-//              MN-major from shared memory) as soon as P_k is written.
-//              Completion is signalled with tcgen05.commit on mbarriers.
-// TMEM (512 columns): S0 S1 [0,128) | O0 O1 [128,384) | P0 P1 [384,448) |
-// P-residual 0 1 [448,512).
+//              probabilities as bf16 pairs over the S they came from (plus
+//              the bf16 rounding residual on tiles that hold tree keys).  Each
+//              warpgroup keeps its own O, max and sum; at the end of a unit
+//              segment the warpgroup that owns its last tile combines both and
+//              writes the bf16 output or an fp32 split-KV partial (merged
+//              afterwards by the combine kernel, attn_merge.cu).
+//   warp 8     TMA producer: Q once per unit (3-D box G x n_query rows), then
+//              per tile its K and V.  Tile k uses S/P buffer b = (k / 2) % 2
+//              of warpgroup w = k % 2, and K and V slot 2 b + w; two adjacent
+//              K slots form one 128-row operand.
+//   warp 9     QK^T issuer (one lane): S = Q K^T (M 128, K 128, both
+//              operands in shared memory) for two consecutive tiles of one
+//              unit as one N = 128 product, else N = 64 for a single tile.
+//              An M = 128 instruction costs about the same at N = 64 as at
+//              N = 128, so pairing halves the tensor time of QK^T.
+//   warp 10    PV issuer (one lane): O_w += P_k V_k (M 128, N 128, K 64; P
+//              from TMEM, V read MN-major from shared memory).
+//              The two issuers run on different schedulers, so the waits and
+//              commits of one do not leave the tensor pipe idle while the
+//              other has work.  Completion is signalled with tcgen05.commit:
+//              one "S ready" barrier (its K slot is then free too) and one
+//              "PV done" barrier (its P buffer and V slot are then free, O is
+//              up to date) per buffer.
+// TMEM (512 columns): S buffers [0,256), buffer b of warpgroup w at column
+// 128 b + 64 w (S as fp32; then, per 32-key chunk j, P as bf16 pairs in
+// columns 32 j .. 32 j + 15 and the P residual in 32 j + 16 .. 32 j + 31) |
+// O0 [256,384) | O1 [384,512).
 // Every mbarrier wait waits for a phase at most one ahead of the last phase
 // the same thread confirmed, so the parity waits are never ambiguous.
 #include "attn_common.cuh"
@@ -36,30 +47,43 @@
 namespace ts {
 namespace {
 
-constexpr int kTcStages = 5;
-constexpr int kTcThreads = 320;
+constexpr int kSlots = 4;  // K and V slots, one per S/P buffer; slots 2i, 2i + 1 form one K pair region
+constexpr int kTcThreads = 352;
 constexpr int kRowsTc = 128;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kQkWarp = 9;
+constexpr int kPvWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
-__host__ __device__ constexpr uint32_t col_s(int w) { return 64u * w; }
-__host__ __device__ constexpr uint32_t col_o(int w) { return 128u + 128u * w; }
-__host__ __device__ constexpr uint32_t col_p(int w) { return 384u + 32u * w; }
-__host__ __device__ constexpr uint32_t col_pl(int w) { return 448u + 32u * w; }
+// tile k of warpgroup w = k % 2 uses S/P buffer b = (k / 2) % 2, and K / V
+// slot k % 4 = 2 b + w, for the (k / 4)-th time
+__host__ __device__ constexpr uint32_t col_s(int w, int b) { return 128u * b + 64u * w; }
+__host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
 
 struct TcLayout {
-  uint32_t q, kv, ctrl, par, xch, cum, total;
+  uint32_t q, k, v, ctrl, par, xch, cum, total;
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
-  static constexpr uint32_t kKvBytes = 64 * 128 * 2;   // one of K or V: two halves of 64 rows
-  static constexpr uint32_t kStageBytes = 2 * kKvBytes;
+  static constexpr uint32_t kTileBytes = 64 * 128 * 2;  // one K or V tile: two halves of 64 rows
+  static constexpr uint32_t kPairBytes = 2 * kTileBytes;  // K pair region: two halves of 128 rows
 };
 
+// half h (columns 64 h .. 64 h + 63) of the K tile in slot s: the pair region
+// holds each half as 128 rows, tile 2i in rows 0-63 and tile 2i + 1 in 64-127
+__device__ __forceinline__ uint32_t k_half_off(int s, int h) {
+  return static_cast<uint32_t>((s >> 1) * TcLayout::kPairBytes + h * (TcLayout::kPairBytes / 2) +
+                               (s & 1) * (TcLayout::kTileBytes / 2));
+}
+// half h of the V tile in slot s
+__device__ __forceinline__ uint32_t v_half_off(int s, int h) {
+  return static_cast<uint32_t>(s * TcLayout::kTileBytes + h * (TcLayout::kTileBytes / 2));
+}
+
 struct TcCtrl {
-  uint64_t kv_full[kTcStages], kv_empty[kTcStages];
+  uint64_t k_full[kSlots], v_full[kSlots];
   uint64_t q_full, q_empty;
-  uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2], xch_full[2], fin;
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
+  uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
   uint32_t tmem_base;
   int abort;
 };
@@ -67,8 +91,9 @@ struct TcCtrl {
 __host__ __device__ inline TcLayout tc_layout(int num_req) {
   TcLayout L;
   L.q = 0;
-  L.kv = L.q + TcLayout::kQBytes;
-  L.ctrl = L.kv + kTcStages * TcLayout::kStageBytes;
+  L.k = L.q + TcLayout::kQBytes;
+  L.v = L.k + (kSlots / 2) * TcLayout::kPairBytes;
+  L.ctrl = L.v + kSlots * TcLayout::kTileBytes;
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
@@ -83,13 +108,11 @@ __device__ __forceinline__ void wg_sync(int w) {
   else asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-// Position of a CTA in its tile sequence: request, unit within the request,
-// tile within the unit, and the K/V ring slot.
+// Position of a CTA in its tile sequence: request, unit within the request
+// and tile within the unit.
 struct Cursor {
   int b, uir, tile, P, n, tiles, unit;  // unit: CTA-local unit index
   int tile0;                            // unit tile at which the CTA's range starts
-  int st;
-  uint32_t phase;
   __device__ void start(const AttnParams& p, int b0, int64_t local) {
     b = b0;
     attn_lengths(p, b, P, n, false);
@@ -98,14 +121,8 @@ struct Cursor {
     tile = static_cast<int>(local % tiles);
     tile0 = tile;
     unit = 0;
-    st = 0;
-    phase = 0;
   }
   __device__ void advance(const AttnParams& p, int units_per_req) {
-    if (++st == kTcStages) {
-      st = 0;
-      ++phase;
-    }
     if (++tile == tiles) {
       tile = 0;
       ++unit;
@@ -127,6 +144,43 @@ struct Cursor {
     return (unit > 0 || tile0 == 0) && (k + tiles - 1 - tile) <= n_tiles - 1;
   }
 };
+
+// Loads one 64-key K or V tile (two 64-column halves) of the cursor's tile,
+// from the contiguous cache or page by page through the block table.  Rows
+// past the pool or the tensor are filled with zeros by the TMA unit.
+__device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, const CUtensorMap* map, uint8_t* dst0,
+                                          uint8_t* dst1, uint64_t* bar) {
+  const int kvh = c.uir;
+  const int key0 = c.tile * kBlockN;
+  if (!p.paged) {
+    const int row = c.b * p.max_kv_len + key0;
+    tma_load_3d(dst0, map, 0, kvh, row, bar);
+    tma_load_3d(dst1, map, 64, kvh, row, bar);
+    return;
+  }
+  const int pages = kBlockN / p.page_size;
+  const int keys = c.P + c.n;
+  for (int pg = 0; pg < pages; ++pg) {
+    const int lb = key0 / p.page_size + pg;
+    int row = p.num_blocks * p.page_size;  // past the pool: TMA fills zeros
+    if (lb * p.page_size < keys) {
+      const int blk = p.block_table[static_cast<int64_t>(c.b) * p.max_blocks + lb];
+      if (blk >= 0 && blk < p.num_blocks) row = blk * p.page_size;
+      else report_error(p.err, TS_DEVERR_BAD_BLOCK);
+    }
+    const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u;
+    tma_load_3d(dst0 + off, map, 0, kvh, row, bar);
+    tma_load_3d(dst1 + off, map, 64, kvh, row, bar);
+  }
+}
+
+// Waits (bounded) for the last copy issued into each slot of a ring.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued) {
+  for (int st = 0; st < slots && st < issued; ++st) {
+    const int last = issued - 1 - ((issued - 1 - st) % slots);
+    mbar_wait(&full[st], static_cast<uint32_t>((last / slots) & 1));
+  }
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
@@ -153,21 +207,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (tid == 0) {
     cum[0] = 0;
     ctl->abort = 0;
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&ctl->kv_full[s], 1);
-      mbar_init(&ctl->kv_empty[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->v_full[s], 1);
     }
     mbar_init(&ctl->q_full, 1);
     mbar_init(&ctl->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->s_free[i], 4);
-      mbar_init(&ctl->p_full[i], 4);
-      mbar_init(&ctl->o_done[i], 1);
+      for (int j = 0; j < 2; ++j) {
+        mbar_init(&ctl->s_full[i][j], 1);
+        mbar_init(&ctl->p_full[i][j], 4);
+        mbar_init(&ctl->pv_done[i][j], 1);
+      }
       mbar_init(&ctl->o_free[i], 4);
       mbar_init(&ctl->xch_full[i], 4);
     }
-    mbar_init(&ctl->fin, 1);
+    mbar_init(&ctl->fin_qk, 1);
+    mbar_init(&ctl->fin_pv, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -190,7 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
   const int64_t local0 = t_begin - cum[b0];
 
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -207,7 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       prefetch_tmap(&qmap);
       Cursor c;
       c.start(p, b0, local0);
-      int issued = 0, q_issued = 0;
+      int k_issued = 0, v_issued = 0, q_issued = 0;
       bool ok = true;
       for (int it = 0; it < n_tiles && ok; ++it) {
         if (it == 0 || c.tile == 0) {
@@ -218,37 +274,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                         c.b * p.n_query, &ctl->q_full);
           ++q_issued;
         }
-        if (it >= kTcStages && !mbar_wait(&ctl->kv_empty[c.st], (c.phase - 1) & 1)) { ok = false; break; }
-        uint8_t* ks = smem + L.kv + c.st * TcLayout::kStageBytes;
-        uint8_t* vs = ks + TcLayout::kKvBytes;
-        const int kvh = c.uir;
-        const int key0 = c.tile * kBlockN;
-        mbar_arrive_expect_tx(&ctl->kv_full[c.st], TcLayout::kStageBytes);
-        if (!p.paged) {
-          const int row = c.b * p.max_kv_len + key0;
-          for (int h = 0; h < 2; ++h) {
-            tma_load_3d(ks + h * (TcLayout::kKvBytes / 2), &kmap, h * 64, kvh, row, &ctl->kv_full[c.st]);
-            tma_load_3d(vs + h * (TcLayout::kKvBytes / 2), &vmap, h * 64, kvh, row, &ctl->kv_full[c.st]);
-          }
-        } else {
-          const int pages = kBlockN / p.page_size;
-          const int keys = c.P + c.n;
-          for (int pg = 0; pg < pages; ++pg) {
-            const int lb = key0 / p.page_size + pg;
-            int row = p.num_blocks * p.page_size;  // past the pool: TMA fills zeros
-            if (lb * p.page_size < keys) {
-              const int blk = p.block_table[static_cast<int64_t>(c.b) * p.max_blocks + lb];
-              if (blk >= 0 && blk < p.num_blocks) row = blk * p.page_size;
-              else report_error(p.err, TS_DEVERR_BAD_BLOCK);
-            }
-            const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u;
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(ks + h * (TcLayout::kKvBytes / 2) + off, &kmap, h * 64, kvh, row, &ctl->kv_full[c.st]);
-              tma_load_3d(vs + h * (TcLayout::kKvBytes / 2) + off, &vmap, h * 64, kvh, row, &ctl->kv_full[c.st]);
-            }
-          }
-        }
-        ++issued;
+        const int sl = it % kSlots, w = it & 1, bb = (it >> 1) & 1;
+        const uint32_t prev = static_cast<uint32_t>(((it >> 2) - 1) & 1);
+        // K slot: free once S of the tile four back is computed
+        if (it >= kSlots && !mbar_wait(&ctl->s_full[w][bb], prev)) { ok = false; break; }
+        mbar_arrive_expect_tx(&ctl->k_full[sl], TcLayout::kTileBytes);
+        load_tile(p, c, &kmap, smem + L.k + k_half_off(sl, 0), smem + L.k + k_half_off(sl, 1), &ctl->k_full[sl]);
+        ++k_issued;
+        // V slot: free once the PV of the tile four back is done
+        if (it >= kSlots && !mbar_wait(&ctl->pv_done[w][bb], prev)) { ok = false; break; }
+        mbar_arrive_expect_tx(&ctl->v_full[sl], TcLayout::kTileBytes);
+        load_tile(p, c, &vmap, smem + L.v + v_half_off(sl, 0), smem + L.v + v_half_off(sl, 1), &ctl->v_full[sl]);
+        ++v_issued;
         c.advance(p, units_per_req);
       }
       if (!ok) {
@@ -257,97 +294,100 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       }
       if (*abort_flag) {
         // never leave with copies into this CTA's shared memory in flight
-        for (int st = 0; st < kTcStages && st < issued; ++st) {
-          const int last = issued - 1 - ((issued - 1 - st) % kTcStages);
-          mbar_wait(&ctl->kv_full[st], static_cast<uint32_t>((last / kTcStages) & 1));
-        }
+        drain_ring(ctl->k_full, kSlots, k_issued);
+        drain_ring(ctl->v_full, kSlots, v_issued);
         if (q_issued > 0) mbar_wait(&ctl->q_full, static_cast<uint32_t>((q_issued - 1) & 1));
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer (event loop) =======================
+  } else if (warp == kQkWarp) {
+    // ======================= QK^T issuer =======================
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
-      const uint32_t sq = smem_u32(smem + L.q);
-      const uint32_t skv = smem_u32(smem + L.kv);
-      Cursor cq, cp;
+      constexpr uint32_t kIdescS1 = idesc_bf16_f32(128, 64, false);
+      constexpr uint32_t kIdescS2 = idesc_bf16_f32(128, 128, false);
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + L.q), 16, 1024);
+      const uint32_t sk = smem_u32(smem + L.k);
+      Cursor cq;
       cq.start(p, b0, local0);
-      cp.start(p, b0, local0);
-      int next_qk = 0, next_pv = 0;
-      int part[2] = {0, 0};  // segments each warpgroup has finished taking part in (o_free phases)
-      uint64_t last_progress = globaltimer_ns();
       bool ok = true;
-      while (next_pv < n_tiles) {
-        bool progressed = false;
-        // ---- S_k = Q K_k^T as soon as the warpgroup's S buffer, K and Q are ready
-        if (next_qk < n_tiles) {
-          const int k = next_qk, w = k & 1;
-          const bool unit_start = (k == 0) || (cq.tile == 0);
-          if ((!unit_start || mbar_test(&ctl->q_full, cq.unit & 1)) &&
-              mbar_test(&ctl->kv_full[cq.st], cq.phase & 1) &&
-              (k < 2 || mbar_test(&ctl->s_free[w], ((k >> 1) - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t ks = skv + cq.st * TcLayout::kStageBytes;
+      for (int k = 0; k < n_tiles;) {
+        if (*abort_flag) { ok = false; break; }
+        const bool pair = (k & 1) == 0 && k + 1 < n_tiles && cq.tile != cq.tiles - 1;
+        const int cnt = pair ? 2 : 1;
+        if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full, cq.unit & 1)) { ok = false; break; }
+        for (int t = k; t < k + cnt && ok; ++t)
+          ok = mbar_wait(&ctl->k_full[t % kSlots], (t >> 2) & 1) &&
+               (t < kSlots || mbar_wait(&ctl->pv_done[t & 1][(t >> 1) & 1], ((t >> 2) - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        // the descriptors of the 8 K-slices differ only in the start address
+        // field (bits 0-13, shared-memory byte address >> 4)
+        const uint64_t kdesc = smem_desc_sw128(sk + k_half_off(k % kSlots, 0), 16, 1024);
+        const uint32_t dst = tbase + col_s(k & 1, (k >> 1) & 1), idesc = pair ? kIdescS2 : kIdescS1;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t half = kk >> 2, off = (kk & 3) * 32;
-              tc_mma_bf16(tbase + col_s(w), smem_desc_sw128(sq + half * (TcLayout::kQBytes / 2) + off, 16, 1024),
-                          smem_desc_sw128(ks + half * (TcLayout::kKvBytes / 2) + off, 16, 1024), kIdescS, kk > 0);
-            }
-            tc_commit(&ctl->s_full[w]);
-            if (cq.tile == cq.tiles - 1 || k == n_tiles - 1) tc_commit(&ctl->q_empty);
-            cq.advance(p, units_per_req);
-            ++next_qk;
-            progressed = true;
-          }
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t a_off = ((kk >> 2) * (TcLayout::kQBytes / 2) + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = ((kk >> 2) * (TcLayout::kPairBytes / 2) + (kk & 3) * 32) >> 4;
+          tc_mma_bf16(dst, qdesc + a_off, kdesc + b_off, idesc, kk > 0);
         }
-        // ---- O_w += P_k V_k as soon as P_k is written (and O_w is free at a segment start)
-        if (next_pv < next_qk) {
-          const int k = next_pv, w = k & 1;
-          const int sf = cp.seg_first(k), sl = cp.seg_last(k, n_tiles);
-          const bool first_owned = (k - sf) < 2;
-          if (mbar_test(&ctl->p_full[w], (k >> 1) & 1) &&
-              (!first_owned || part[w] == 0 || mbar_test(&ctl->o_free[w], (part[w] - 1) & 1))) {
-            tc_fence_after();
-            const bool tree_tile = cp.tile * kBlockN + kBlockN > cp.P;
-            const uint32_t vs = skv + cp.st * TcLayout::kStageBytes + TcLayout::kKvBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16_ts(tbase + col_o(w), tbase + col_p(w) + kk * 8,
-                             smem_desc_sw128(vs + kk * 2048, TcLayout::kKvBytes / 2, 1024), kIdescPV,
-                             (first_owned && kk == 0) ? 0u : 1u);
-            if (tree_tile) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc_mma_bf16_ts(tbase + col_o(w), tbase + col_pl(w) + kk * 8,
-                               smem_desc_sw128(vs + kk * 2048, TcLayout::kKvBytes / 2, 1024), kIdescPV, 1u);
-            }
-            tc_commit(&ctl->o_done[w]);
-            tc_commit(&ctl->kv_empty[cp.st]);
-            if (k == sl) {  // segment ends: both warpgroups' participation counts
-              ++part[sl & 1];
-              if (sl > sf) ++part[(sl & 1) ^ 1];
-            }
-            cp.advance(p, units_per_req);
-            ++next_pv;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          last_progress = globaltimer_ns();
-        } else if (*abort_flag || globaltimer_ns() - last_progress > kWaitLimitNs) {
-          ok = false;
-          break;
-        }
+        for (int t = k; t < k + cnt; ++t) tc_commit(&ctl->s_full[t & 1][(t >> 1) & 1]);
+        if (cq.tile + cnt - 1 == cq.tiles - 1 || k + cnt == n_tiles) tc_commit(&ctl->q_empty);
+        for (int t = 0; t < cnt; ++t) cq.advance(p, units_per_req);
+        k += cnt;
       }
       if (!ok) {
         report_error(p.err, TS_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
       // every MMA this thread issued has completed before TMEM is released
-      tc_commit(&ctl->fin);
-      mbar_wait(&ctl->fin, 0);
+      tc_commit(&ctl->fin_qk);
+      mbar_wait(&ctl->fin_qk, 0);
+    }
+  } else if (warp == kPvWarp) {
+    // ======================= PV issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
+      const uint32_t sv = smem_u32(smem + L.v);
+      Cursor cp;
+      cp.start(p, b0, local0);
+      int part[2] = {0, 0};  // segments each warpgroup has finished taking part in (o_free phases)
+      bool ok = true;
+      for (int k = 0; k < n_tiles; ++k) {
+        if (*abort_flag) { ok = false; break; }
+        const int w = k & 1, bb = (k >> 1) & 1;
+        const int sf = cp.seg_first(k), sl = cp.seg_last(k, n_tiles);
+        const bool first_owned = (k - sf) < 2;
+        if (!mbar_wait(&ctl->p_full[w][bb], (k >> 2) & 1) ||
+            (first_owned && part[w] > 0 && !mbar_wait(&ctl->o_free[w], (part[w] - 1) & 1)) ||
+            !mbar_wait(&ctl->v_full[k % kSlots], (k >> 2) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool tree_tile = cp.tile * kBlockN + kBlockN > cp.P;
+        const uint64_t vdesc = smem_desc_sw128(sv + v_half_off(k % kSlots, 0), TcLayout::kTileBytes / 2, 1024);
+        const uint32_t pa = tbase + col_s(w, bb), dst = tbase + col_o(w);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16_ts(dst, pa + 32 * (kk >> 1) + 8 * (kk & 1), vdesc + ((kk * 2048) >> 4), kIdescPV,
+                         (first_owned && kk == 0) ? 0u : 1u);
+        if (tree_tile) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16_ts(dst, pa + 32 * (kk >> 1) + 16 + 8 * (kk & 1), vdesc + ((kk * 2048) >> 4), kIdescPV, 1u);
+        }
+        tc_commit(&ctl->pv_done[w][bb]);
+        if (k == sl) {  // segment ends: both warpgroups' participation counts
+          ++part[sl & 1];
+          if (sl > sf) ++part[(sl & 1) ^ 1];
+        }
+        cp.advance(p, units_per_req);
+      }
+      if (!ok) {
+        report_error(p.err, TS_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      tc_commit(&ctl->fin_pv);
+      mbar_wait(&ctl->fin_pv, 0);
     }
   } else {
     // ======================= softmax warpgroups =======================
@@ -385,7 +425,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           m_used = -INFINITY;
           l = 0.f;
         }
-        if (*abort_flag || !mbar_wait(&ctl->s_full[wg], (k >> 1) & 1)) {
+        const int bb = (k >> 1) & 1;
+        const uint32_t sbuf = lane_addr + col_s(wg, bb);
+        if (*abort_flag || !mbar_wait(&ctl->s_full[wg][bb], (k >> 2) & 1)) {
           report_error(p.err, TS_DEVERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -395,20 +437,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const bool tree_tile = key0 + kBlockN > c.P;
         const uint64_t vis = tree_tile ? tile_visibility(anc, key0 - c.P) : ~0ull;
 
-        // ---- pass 1: masked row max over the 64 keys
+        // ---- pass 1: row max over the 64 keys (masked on tiles holding tree
+        //      keys; every key of a prefix tile is visible).  S stays in
+        //      registers for pass 2.
+        uint32_t v0[32], v1[32];
+        tmem_ld32(sbuf, v0);
+        tmem_ld32(sbuf + 32, v1);
+        tmem_ld_wait();
         float mx;
         {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(lane_addr + col_s(wg), v0);
-          tmem_ld32(lane_addr + col_s(wg) + 32, v1);
-          tmem_ld_wait();
           float pm[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
+          if (tree_tile) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if ((vis >> e) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v0[e]));
-            if ((vis >> (32 + e)) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v1[e]));
+            for (int e = 0; e < 32; ++e) {
+              if ((vis >> e) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v0[e]));
+              if ((vis >> (32 + e)) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v1[e]));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v0[e]));
+              pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v1[e]));
+            }
           }
           mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
         }
@@ -424,15 +476,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
 
-        // PV of this warpgroup's previous tile must be complete before its P
-        // columns are overwritten or its O is rescaled
-        if (k >= 2 && !mbar_wait(&ctl->o_done[wg], ((k >> 1) - 1) & 1)) {
-          report_error(p.err, TS_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        // O may be rescaled only once every earlier PV into it is done: the
+        // last one was this warpgroup's previous tile, k - 2, in the other
+        // buffer (a rescale implies a previous tile in this segment)
+        const bool need_rescale = __any_sync(0xffffffffu, rescale);
+        if (need_rescale) {
+          if (!mbar_wait(&ctl->pv_done[wg][bb ^ 1], ((k - 2) >> 2) & 1)) {
+            report_error(p.err, TS_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
           const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
           for (int ch = 0; ch < 4; ++ch) {
@@ -445,28 +499,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           }
         }
 
-        // ---- pass 2: probabilities 2^(s*scale - m) as bf16 pairs into TMEM P
-        //      (plus the rounding residual on tiles holding tree keys)
+        // ---- pass 2: probabilities 2^(s*scale - m) as bf16 pairs, written over
+        //      the S chunk they came from: for keys 32 j .. 32 j + 31, P in
+        //      columns 32 j .. 32 j + 15 and the rounding residual (tiles
+        //      holding tree keys) in 32 j + 16 .. 32 j + 31.
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        if (tree_tile) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + col_s(wg) + 32 * h, v);
-          tmem_ld_wait();
-          uint32_t hi[16], lo[16];
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t* v = h == 0 ? v0 : v1;
+            uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int e = 2 * q;
-            const float s0 = ((vis >> (32 * h + e)) & 1ull) ? __uint_as_float(v[e]) : -INFINITY;
-            const float s1 = ((vis >> (32 * h + e + 1)) & 1ull) ? __uint_as_float(v[e + 1]) : -INFINITY;
-            const float e0 = ex2_approx(fmaf(s0, p.scale_log2, nbase));
-            const float e1 = ex2_approx(fmaf(s1, p.scale_log2, nbase));
-            ps[q & 3] += e0 + e1;
-            hi[q] = pack_bf16x2(e0, e1);
-            lo[q] = tree_tile ? bf16x2_residual(hi[q], e0, e1) : 0u;
+            for (int q = 0; q < 16; ++q) {
+              const int e = 2 * q;
+              const float s0 = ((vis >> (32 * h + e)) & 1ull) ? __uint_as_float(v[e]) : -INFINITY;
+              const float s1 = ((vis >> (32 * h + e + 1)) & 1ull) ? __uint_as_float(v[e + 1]) : -INFINITY;
+              const float e0 = ex2_approx(fmaf(s0, p.scale_log2, nbase));
+              const float e1 = ex2_approx(fmaf(s1, p.scale_log2, nbase));
+              ps[q & 3] += e0 + e1;
+              hi[q] = pack_bf16x2(e0, e1);
+              lo[q] = bf16x2_residual(hi[q], e0, e1);
+            }
+            tmem_st16(sbuf + 32 * h, hi);
+            tmem_st16(sbuf + 32 * h + 16, lo);
           }
-          tmem_st16(lane_addr + col_p(wg) + 16 * h, hi);
-          if (tree_tile) tmem_st16(lane_addr + col_pl(wg) + 16 * h, lo);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t* v = h == 0 ? v0 : v1;
+            uint32_t hi[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float e0 = ex2_approx(fmaf(__uint_as_float(v[2 * q]), p.scale_log2, nbase));
+              const float e1 = ex2_approx(fmaf(__uint_as_float(v[2 * q + 1]), p.scale_log2, nbase));
+              ps[q & 3] += e0 + e1;
+              hi[q] = pack_bf16x2(e0, e1);
+            }
+            tmem_st16(sbuf + 32 * h, hi);
+          }
         }
         tmem_st_wait();
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
@@ -474,25 +544,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // 0 * NaN is NaN, so zero them in the V tile before PV reads it
         const int keys = c.P + c.n;
         if (key0 + kBlockN > keys) {
-          uint8_t* vs = smem + L.kv + c.st * TcLayout::kStageBytes + TcLayout::kKvBytes;
+          const int vslot = k % kSlots;
+          if (!mbar_wait(&ctl->v_full[vslot], (k >> 2) & 1)) {  // the tile has landed
+            report_error(p.err, TS_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
           const int first = keys - key0;
           const int nvec = (kBlockN - first) * 8;
           for (int h = 0; h < 2; ++h)
             for (int xv = r; xv < nvec; xv += kRowsTc)
-              reinterpret_cast<uint4*>(vs + h * (TcLayout::kKvBytes / 2) + first * 128)[xv] =
-                  make_uint4(0, 0, 0, 0);
+              reinterpret_cast<uint4*>(smem + L.v + v_half_off(vslot, h) + first * 128)[xv] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ctl->s_free[wg]);
-          mbar_arrive(&ctl->p_full[wg]);
-        }
+        if (lane == 0) mbar_arrive(&ctl->p_full[wg][bb]);
 
         // ---- this warpgroup's last tile of the segment
         if (last_owned) {
-          if (!mbar_wait(&ctl->o_done[wg], (k >> 1) & 1)) {
+          if (!mbar_wait(&ctl->pv_done[wg][bb], (k >> 2) & 1)) {
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -578,7 +649,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
