@@ -5,7 +5,7 @@
 // of 128); the ancestor mask is the SwiftSpec summary's Figure 3 and the key
 // split with a combine its §3.3.
 //
-// One CTA per SM, 352 threads, warp-specialised:
+// One CTA per SM, 384 threads, warp-specialised:
 //   warps 0-3 and 4-7  two softmax warpgroups.  Tile k of the CTA's range
 //              belongs to warpgroup k % 2; thread t of a warpgroup owns
 //              packed row t (TMEM lane t).  Per 64-key tile it reads its row
@@ -18,10 +18,12 @@
 //              segment the warpgroup that owns its last tile combines both and
 //              writes the bf16 output or an fp32 split-KV partial (merged
 //              afterwards by the combine kernel, attn_merge.cu).
-//   warp 8     TMA producer: Q once per unit (3-D box G x n_query rows), then
-//              per tile its K and V.  Tile k uses S/P buffer b = (k / 2) % 2
-//              of warpgroup w = k % 2, and K and V slot 2 b + w; two adjacent
-//              K slots form one 128-row operand.
+//   warps 8, 11  TMA producers: warp 8 loads Q once per unit (3-D box
+//              G x n_query rows) and the K tiles, warp 11 the V tiles, so a K
+//              slot is refilled as soon as its S is computed without waiting
+//              behind a V slot.  Tile k uses S/P buffer b = (k / 2) % 2 of
+//              warpgroup w = k % 2, and K and V slot 2 b + w; two adjacent K
+//              slots form one 128-row operand.
 //   warp 9     QK^T issuer (one lane): S = Q K^T (M 128, K 128, both
 //              operands in shared memory) for two consecutive tiles of one
 //              unit as one N = 128 product, else N = 64 for a single tile.
@@ -48,11 +50,12 @@ namespace ts {
 namespace {
 
 constexpr int kSlots = 4;  // K and V slots, one per S/P buffer; slots 2i, 2i + 1 form one K pair region
-constexpr int kTcThreads = 352;
+constexpr int kTcThreads = 384;
 constexpr int kRowsTc = 128;
-constexpr int kProducerWarp = 8;
+constexpr int kProducerWarp = 8;  // Q and K
 constexpr int kQkWarp = 9;
 constexpr int kPvWarp = 10;
+constexpr int kVProducerWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
@@ -255,18 +258,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
 
-  if (warp == kProducerWarp) {
-    // ======================= TMA producer =======================
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
+    // ======================= TMA producers =======================
     if (lane == 0) {
-      prefetch_tmap(&kmap);
-      prefetch_tmap(&vmap);
-      prefetch_tmap(&qmap);
+      const bool kside = warp == kProducerWarp;
+      const CUtensorMap* map = kside ? &kmap : &vmap;
+      prefetch_tmap(map);
+      if (kside) prefetch_tmap(&qmap);
       Cursor c;
       c.start(p, b0, local0);
-      int k_issued = 0, v_issued = 0, q_issued = 0;
+      int issued = 0, q_issued = 0;
       bool ok = true;
       for (int it = 0; it < n_tiles && ok; ++it) {
-        if (it == 0 || c.tile == 0) {
+        if (kside && (it == 0 || c.tile == 0)) {
           if (c.unit > 0 && !mbar_wait(&ctl->q_empty, (c.unit - 1) & 1)) { ok = false; break; }
           mbar_arrive_expect_tx(&ctl->q_full, TcLayout::kQBytes);
           for (int h = 0; h < 2; ++h)
@@ -275,17 +279,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           ++q_issued;
         }
         const int sl = it % kSlots, w = it & 1, bb = (it >> 1) & 1;
-        const uint32_t prev = static_cast<uint32_t>(((it >> 2) - 1) & 1);
-        // K slot: free once S of the tile four back is computed
-        if (it >= kSlots && !mbar_wait(&ctl->s_full[w][bb], prev)) { ok = false; break; }
-        mbar_arrive_expect_tx(&ctl->k_full[sl], TcLayout::kTileBytes);
-        load_tile(p, c, &kmap, smem + L.k + k_half_off(sl, 0), smem + L.k + k_half_off(sl, 1), &ctl->k_full[sl]);
-        ++k_issued;
-        // V slot: free once the PV of the tile four back is done
-        if (it >= kSlots && !mbar_wait(&ctl->pv_done[w][bb], prev)) { ok = false; break; }
-        mbar_arrive_expect_tx(&ctl->v_full[sl], TcLayout::kTileBytes);
-        load_tile(p, c, &vmap, smem + L.v + v_half_off(sl, 0), smem + L.v + v_half_off(sl, 1), &ctl->v_full[sl]);
-        ++v_issued;
+        // a K slot is free once S of the tile four back is computed, a V slot
+        // once the PV of the tile four back is done
+        if (it >= kSlots &&
+            !mbar_wait(kside ? &ctl->s_full[w][bb] : &ctl->pv_done[w][bb], ((it >> 2) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        uint64_t* full = kside ? &ctl->k_full[sl] : &ctl->v_full[sl];
+        mbar_arrive_expect_tx(full, TcLayout::kTileBytes);
+        if (kside) load_tile(p, c, map, smem + L.k + k_half_off(sl, 0), smem + L.k + k_half_off(sl, 1), full);
+        else load_tile(p, c, map, smem + L.v + v_half_off(sl, 0), smem + L.v + v_half_off(sl, 1), full);
+        ++issued;
         c.advance(p, units_per_req);
       }
       if (!ok) {
@@ -294,8 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       }
       if (*abort_flag) {
         // never leave with copies into this CTA's shared memory in flight
-        drain_ring(ctl->k_full, kSlots, k_issued);
-        drain_ring(ctl->v_full, kSlots, v_issued);
+        drain_ring(kside ? ctl->k_full : ctl->v_full, kSlots, issued);
         if (q_issued > 0) mbar_wait(&ctl->q_full, static_cast<uint32_t>((q_issued - 1) & 1));
       }
     }
