@@ -29,6 +29,8 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
 }
 
 __global__ void __launch_bounds__(kArgmaxThreads) argmax_chunk_kernel(const AcceptParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x;  // b * n_tree_max + i
   const int b = row / p.n_tree_max, i = row % p.n_tree_max;
   int n = p.n_tree[b];
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_chunk_kernel(const Acce
 __device__ __forceinline__ void block_sync() { __syncthreads(); }
 
 __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int i = threadIdx.x;
   __shared__ uint32_t anc[TS_MAX_TREE][4];
@@ -177,9 +181,9 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
 
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   dim3 grid(p.num_req * p.n_tree_max, p.num_chunks);
-  argmax_chunk_kernel<<<grid, kArgmaxThreads, 0, stream>>>(p);
-  accept_scan_kernel<<<p.num_req, TS_MAX_TREE, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(argmax_chunk_kernel, grid, dim3(kArgmaxThreads), 0, stream, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(accept_scan_kernel, dim3(p.num_req), dim3(TS_MAX_TREE), 0, stream, p);
 }
 
 }  // namespace ts

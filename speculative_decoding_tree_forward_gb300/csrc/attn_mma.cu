@@ -49,6 +49,8 @@ template <int D>
 __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                                                        const __grid_constant__ CUtensorMap vmap,
                                                        const AttnParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const SmemLayout L = mma_layout(D, p.stages, p.num_req, p.rows_pad);
@@ -508,9 +510,9 @@ cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const 
                             cudaStream_t stream) {
   const size_t smem = attn_mma_smem_bytes(p.head_dim, p.stages, p.num_req, p.rows_pad);
   const int threads = attn_mma_threads(p.rows_pad);
-  if (p.head_dim == 128) attn_mma_kernel<128><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
-  else attn_mma_kernel<64><<<p.num_ctas, threads, smem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  if (p.head_dim == 128)
+    return launch_pdl(attn_mma_kernel<128>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p);
+  return launch_pdl(attn_mma_kernel<64>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p);
 }
 
 int attn_mma_occupancy(int head_dim, int stages, int num_req, int rows_pad) {

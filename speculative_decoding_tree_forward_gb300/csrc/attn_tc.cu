@@ -189,6 +189,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const AttnParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcLayout L = tc_layout(p.num_req);
@@ -686,8 +688,7 @@ int attn_tc_occupancy(int stages, int num_req) {
 cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = attn_tc_smem_bytes(p.stages, p.num_req);
-  attn_tc_kernel<<<p.num_ctas, kTcThreads, smem, stream>>>(kmap, vmap, qmap, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, qmap, p);
 }
 
 }  // namespace ts

@@ -29,6 +29,8 @@ constexpr int kGatherThreads = 256;
 __device__ __forceinline__ void block_sync() { __syncthreads(); }
 
 __global__ void __launch_bounds__(kWalkThreads) reroot_walk_kernel(const CompactParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int i = threadIdx.x;
   __shared__ int par_s[TS_MAX_TREE];
@@ -138,6 +140,8 @@ __device__ __forceinline__ uint8_t* row_ptr(const CompactParams& p, void* layer,
 }
 
 __global__ void __launch_bounds__(kGatherThreads) compact_gather_kernel(const CompactParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ uint4 buf[];  // [rows][chunk_bytes / 16]
   const int group = blockIdx.z;
   const int kv = blockIdx.y;  // 0 = K, 1 = V
@@ -179,13 +183,13 @@ __global__ void __launch_bounds__(kGatherThreads) compact_gather_kernel(const Co
 }  // namespace
 
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream) {
-  reroot_walk_kernel<<<p.num_req, kWalkThreads, 0, stream>>>(p);
+  cudaError_t e = launch_pdl(reroot_walk_kernel, dim3(p.num_req), dim3(kWalkThreads), 0, stream, p);
+  if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(p.n_tree_max) * p.chunk_bytes;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(compact_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   dim3 grid(p.num_layers * p.num_req, 2, p.num_chunk_groups);
-  compact_gather_kernel<<<grid, kGatherThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(compact_gather_kernel, grid, dim3(kGatherThreads), smem, stream, p);
 }
 
 }  // namespace ts

@@ -10,6 +10,27 @@
 
 namespace ts {
 
+// Launches a kernel with programmatic dependent launch allowed: its CTAs may
+// be scheduled while the previous kernel in the stream drains.  Every kernel
+// of this library begins with pdl_wait() (griddepcontrol.wait), which blocks
+// until the previous grid has completed and its writes are visible, so
+// stream order is kept; only the launch latency is overlapped.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kBlockN = 64;        // keys per K/V tile
 constexpr int kMaxRowsPerUnit = 128;  // packed query rows handled by one CTA
 constexpr int kMaxRequestsAttn = 1024;

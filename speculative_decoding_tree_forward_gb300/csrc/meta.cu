@@ -17,6 +17,8 @@ __device__ __forceinline__ void block_sync() { __syncthreads(); }
 __global__ void __launch_bounds__(TS_MAX_TREE) tree_meta_kernel(const int32_t* parent, const int32_t* n_tree,
                                                                int n_tree_max, int32_t* depth, uint32_t* anc_out,
                                                                unsigned* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ uint32_t anc[TS_MAX_TREE][4];
   __shared__ int jmp[TS_MAX_TREE];
   const int b = blockIdx.x;
@@ -45,8 +47,8 @@ __global__ void __launch_bounds__(TS_MAX_TREE) tree_meta_kernel(const int32_t* p
 
 cudaError_t launch_tree_meta(const int32_t* parent, const int32_t* n_tree, int num_req, int n_tree_max,
                              int32_t* depth, uint32_t* anc, unsigned* err, cudaStream_t stream) {
-  tree_meta_kernel<<<num_req, TS_MAX_TREE, 0, stream>>>(parent, n_tree, n_tree_max, depth, anc, err);
-  return cudaGetLastError();
+  return launch_pdl(tree_meta_kernel, dim3(num_req), dim3(TS_MAX_TREE), 0, stream, parent, n_tree, n_tree_max, depth,
+                    anc, err);
 }
 
 }  // namespace ts
