@@ -101,8 +101,10 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
   if (i < n) {
     float bv = -INFINITY;
     int bi = INT32_MAX;
-    for (int c = 0; c < p.num_chunks; ++c)
-      better(bv, bi, p.part_val[(rowbase + i) * p.num_chunks + c], p.part_idx[(rowbase + i) * p.num_chunks + c]);
+    const float* pv = p.part_val + (rowbase + i) * p.num_chunks;
+    const int* pi = p.part_idx + (rowbase + i) * p.num_chunks;
+#pragma unroll 8
+    for (int c = 0; c < p.num_chunks; ++c) better(bv, bi, pv[c], pi[c]);
     am = bi;
   }
   if (i < p.n_tree_max) p.argmax[rowbase + i] = (i < n) ? am : -1;

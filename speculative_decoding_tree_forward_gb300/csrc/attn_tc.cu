@@ -19,11 +19,12 @@
 //              writes the bf16 output or an fp32 split-KV partial (merged
 //              afterwards by the combine kernel, attn_merge.cu).
 //   warps 8, 11  TMA producers: warp 8 loads Q once per unit (3-D box
-//              G x n_query rows) and the K tiles, warp 11 the V tiles, so a K
-//              slot is refilled as soon as its S is computed without waiting
-//              behind a V slot.  Tile k uses S/P buffer b = (k / 2) % 2 of
-//              warpgroup w = k % 2, and K and V slot 2 b + w; two adjacent K
-//              slots form one 128-row operand.
+//              G x n_query rows) and the K tiles into a 6-slot ring (slots
+//              2i and 2i + 1 form one 128-row operand); warp 11 loads the V
+//              tiles, tile k into V slot 2 b + w of its S/P buffer (b, w)
+//              below.  A K slot is refilled as soon as the S that read it is
+//              computed, without queueing behind a V slot.  Tile k uses S/P
+//              buffer b = (k / 2) % 2 of warpgroup w = k % 2.
 //   warp 9     QK^T issuer (one lane): S = Q K^T (M 128, K 128, both
 //              operands in shared memory) for two consecutive tiles of one
 //              unit as one N = 128 product, else N = 64 for a single tile.
@@ -34,9 +35,9 @@
 //              The two issuers run on different schedulers, so the waits and
 //              commits of one do not leave the tensor pipe idle while the
 //              other has work.  Completion is signalled with tcgen05.commit:
-//              one "S ready" barrier (its K slot is then free too) and one
-//              "PV done" barrier (its P buffer and V slot are then free, O is
-//              up to date) per buffer.
+//              per S/P buffer one "S ready" and one "PV done" barrier (its P
+//              buffer and V slot are then free, O is up to date), and per K
+//              slot one "K slot free" barrier.
 // TMEM (512 columns): S buffers [0,256), buffer b of warpgroup w at column
 // 128 b + 64 w (S as fp32; then, per 32-key chunk j, P as bf16 pairs in
 // columns 32 j .. 32 j + 15 and the P residual in 32 j + 16 .. 32 j + 31) |
@@ -49,7 +50,9 @@
 namespace ts {
 namespace {
 
-constexpr int kSlots = 4;  // K and V slots, one per S/P buffer; slots 2i, 2i + 1 form one K pair region
+constexpr int kSlots = 4;   // V slots, one per S/P buffer
+constexpr int kKSlots = 6;  // K slots (even: slots 2i, 2i + 1 form one 128-row pair region)
+constexpr int kQBufs = 1;   // Q buffers (unit u uses buffer u % kQBufs)
 constexpr int kTcThreads = 384;
 constexpr int kRowsTc = 128;
 constexpr int kProducerWarp = 8;  // Q and K
@@ -65,7 +68,8 @@ __host__ __device__ constexpr uint32_t col_s(int w, int b) { return 128u * b + 6
 __host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
 
 struct TcLayout {
-  uint32_t q, k, v, ctrl, par, xch, cum, total;
+  uint32_t q, k, v, ctrl, par, xch, cum, stg, total;
+  static constexpr uint32_t kStgStride = 36;  // words per staged row: 32 + 4 (16-byte rows, conflict-free float4)
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
   static constexpr uint32_t kTileBytes = 64 * 128 * 2;  // one K or V tile: two halves of 64 rows
   static constexpr uint32_t kPairBytes = 2 * kTileBytes;  // K pair region: two halves of 128 rows
@@ -83,10 +87,11 @@ __device__ __forceinline__ uint32_t v_half_off(int s, int h) {
 }
 
 struct TcCtrl {
-  uint64_t k_full[kSlots], v_full[kSlots];
-  uint64_t q_full, q_empty;
+  uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kSlots];
+  uint64_t q_full[kQBufs], q_empty[kQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
   uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
+  uint64_t stg_free;  // one phase per segment epilogue: the staging rows are reused in segment order
   uint32_t tmem_base;
   int abort;
 };
@@ -94,13 +99,15 @@ struct TcCtrl {
 __host__ __device__ inline TcLayout tc_layout(int num_req) {
   TcLayout L;
   L.q = 0;
-  L.k = L.q + TcLayout::kQBytes;
-  L.v = L.k + (kSlots / 2) * TcLayout::kPairBytes;
+  L.k = L.q + kQBufs * TcLayout::kQBytes;
+  L.v = L.k + (kKSlots / 2) * TcLayout::kPairBytes;
   L.ctrl = L.v + kSlots * TcLayout::kTileBytes;
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
-  L.total = L.cum + 8 * (kMaxRequestsAttn + 1);  // fixed: launch shape independent of the batch
+  // epilogue staging: 32 rows x 32 columns per warp of the finishing warpgroup
+  L.stg = (L.cum + 8 * (kMaxRequestsAttn + 1) + 15) & ~15u;
+  L.total = L.stg + 4 * 32 * TcLayout::kStgStride * 4;  // fixed: launch shape independent of the batch
   (void)num_req;
   return L;
 }
@@ -212,12 +219,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (tid == 0) {
     cum[0] = 0;
     ctl->abort = 0;
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kKSlots; ++s) {
       mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
     }
-    mbar_init(&ctl->q_full, 1);
-    mbar_init(&ctl->q_empty, 1);
+    for (int s = 0; s < kSlots; ++s) mbar_init(&ctl->v_full[s], 1);
+    for (int i = 0; i < kQBufs; ++i) {
+      mbar_init(&ctl->q_full[i], 1);
+      mbar_init(&ctl->q_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       for (int j = 0; j < 2; ++j) {
         mbar_init(&ctl->s_full[i][j], 1);
@@ -227,6 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       mbar_init(&ctl->o_free[i], 4);
       mbar_init(&ctl->xch_full[i], 4);
     }
+    mbar_init(&ctl->stg_free, 4);
     mbar_init(&ctl->fin_qk, 1);
     mbar_init(&ctl->fin_pv, 1);
     fence_mbar_init();
@@ -273,18 +284,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       bool ok = true;
       for (int it = 0; it < n_tiles && ok; ++it) {
         if (kside && (it == 0 || c.tile == 0)) {
-          if (c.unit > 0 && !mbar_wait(&ctl->q_empty, (c.unit - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&ctl->q_full, TcLayout::kQBytes);
+          // buffer u % kQBufs is free once the QK^T of unit u - kQBufs are done
+          const int qb = c.unit % kQBufs;
+          if (c.unit >= kQBufs && !mbar_wait(&ctl->q_empty[qb], ((c.unit / kQBufs) - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&ctl->q_full[qb], TcLayout::kQBytes);
           for (int h = 0; h < 2; ++h)
-            tma_load_3d(smem + L.q + h * (TcLayout::kQBytes / 2), &qmap, h * 64, c.uir * p.group,
-                        c.b * p.n_query, &ctl->q_full);
+            tma_load_3d(smem + L.q + qb * TcLayout::kQBytes + h * (TcLayout::kQBytes / 2), &qmap, h * 64,
+                        c.uir * p.group, c.b * p.n_query, &ctl->q_full[qb]);
           ++q_issued;
         }
-        const int sl = it % kSlots, w = it & 1, bb = (it >> 1) & 1;
-        // a K slot is free once S of the tile four back is computed, a V slot
-        // once the PV of the tile four back is done
-        if (it >= kSlots &&
-            !mbar_wait(kside ? &ctl->s_full[w][bb] : &ctl->pv_done[w][bb], ((it >> 2) - 1) & 1)) {
+        const int sl = kside ? it % kKSlots : it % kSlots, w = it & 1, bb = (it >> 1) & 1;
+        // a K slot is free once the S that read it is computed, a V slot once
+        // the PV of the tile four back (same S/P buffer) is done
+        if (kside ? (it >= kKSlots && !mbar_wait(&ctl->k_empty[sl], ((it / kKSlots) - 1) & 1))
+                  : (it >= kSlots && !mbar_wait(&ctl->pv_done[w][bb], ((it >> 2) - 1) & 1))) {
           ok = false;
           break;
         }
@@ -301,8 +314,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       }
       if (*abort_flag) {
         // never leave with copies into this CTA's shared memory in flight
-        drain_ring(kside ? ctl->k_full : ctl->v_full, kSlots, issued);
-        if (q_issued > 0) mbar_wait(&ctl->q_full, static_cast<uint32_t>((q_issued - 1) & 1));
+        drain_ring(kside ? ctl->k_full : ctl->v_full, kside ? kKSlots : kSlots, issued);
+        for (int u = max(q_issued - kQBufs, 0); u < q_issued; ++u)
+          mbar_wait(&ctl->q_full[u % kQBufs], static_cast<uint32_t>((u / kQBufs) & 1));
       }
     }
   } else if (warp == kQkWarp) {
@@ -310,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     if (lane == 0) {
       constexpr uint32_t kIdescS1 = idesc_bf16_f32(128, 64, false);
       constexpr uint32_t kIdescS2 = idesc_bf16_f32(128, 128, false);
-      const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + L.q), 16, 1024);
+      const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem + L.q), 16, 1024);
       const uint32_t sk = smem_u32(smem + L.k);
       Cursor cq;
       cq.start(p, b0, local0);
@@ -319,24 +333,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (*abort_flag) { ok = false; break; }
         const bool pair = (k & 1) == 0 && k + 1 < n_tiles && cq.tile != cq.tiles - 1;
         const int cnt = pair ? 2 : 1;
-        if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full, cq.unit & 1)) { ok = false; break; }
+        const int qb = cq.unit % kQBufs;
+        if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full[qb], (cq.unit / kQBufs) & 1)) { ok = false; break; }
         for (int t = k; t < k + cnt && ok; ++t)
-          ok = mbar_wait(&ctl->k_full[t % kSlots], (t >> 2) & 1) &&
+          ok = mbar_wait(&ctl->k_full[t % kKSlots], (t / kKSlots) & 1) &&
                (t < kSlots || mbar_wait(&ctl->pv_done[t & 1][(t >> 1) & 1], ((t >> 2) - 1) & 1));
         if (!ok) break;
         tc_fence_after();
         // the descriptors of the 8 K-slices differ only in the start address
         // field (bits 0-13, shared-memory byte address >> 4)
-        const uint64_t kdesc = smem_desc_sw128(sk + k_half_off(k % kSlots, 0), 16, 1024);
+        const uint64_t kdesc = smem_desc_sw128(sk + k_half_off(k % kKSlots, 0), 16, 1024);
         const uint32_t dst = tbase + col_s(k & 1, (k >> 1) & 1), idesc = pair ? kIdescS2 : kIdescS1;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a_off = ((kk >> 2) * (TcLayout::kQBytes / 2) + (kk & 3) * 32) >> 4;
           const uint32_t b_off = ((kk >> 2) * (TcLayout::kPairBytes / 2) + (kk & 3) * 32) >> 4;
-          tc_mma_bf16(dst, qdesc + a_off, kdesc + b_off, idesc, kk > 0);
+          tc_mma_bf16(dst, qdesc0 + qb * (TcLayout::kQBytes >> 4) + a_off, kdesc + b_off, idesc, kk > 0);
         }
-        for (int t = k; t < k + cnt; ++t) tc_commit(&ctl->s_full[t & 1][(t >> 1) & 1]);
-        if (cq.tile + cnt - 1 == cq.tiles - 1 || k + cnt == n_tiles) tc_commit(&ctl->q_empty);
+        for (int t = k; t < k + cnt; ++t) {
+          tc_commit(&ctl->s_full[t & 1][(t >> 1) & 1]);
+          tc_commit(&ctl->k_empty[t % kKSlots]);
+        }
+        if (cq.tile + cnt - 1 == cq.tiles - 1 || k + cnt == n_tiles) tc_commit(&ctl->q_empty[qb]);
         for (int t = 0; t < cnt; ++t) cq.advance(p, units_per_req);
         k += cnt;
       }
@@ -405,6 +423,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     Cursor c;
     c.start(p, b0, local0);
     int nonfin[2] = {0, 0};  // segments in which each warpgroup handed its state to the other
+    int seg_idx = 0;         // CTA-local index of the segment tile k belongs to
     int anc_req = -1;
     uint32_t anc[4] = {0, 0, 0, 0};
     float m_used = -INFINITY, l = 0.f;
@@ -607,8 +626,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             const int i = r / p.group, h = kvh * p.group + r % p.group;
             const int64_t unit = static_cast<int64_t>(c.b) * units_per_req + c.uir;
             const int64_t slot = static_cast<int64_t>(blockIdx.x) + unit;
-            __nv_bfloat16* orow = p.out + ((static_cast<int64_t>(c.b) * p.n_query + i) * p.hq + h) * 128;
-            float* prow = p.part_o + (slot * 128 + r) * 128;
+            // Each 32-column chunk of this warp's 32 rows goes through shared
+            // memory, so the global stores are whole row segments (128 bytes
+            // of fp32 or 64 bytes of bf16 per row) instead of 16-byte pieces
+            // of 32 different rows.
+            float* stg = reinterpret_cast<float*>(smem + L.stg) + (warp & 3) * 32 * TcLayout::kStgStride;
+            const int row0 = (warp & 3) * 32;
+            // finishers of consecutive short segments may be different
+            // warpgroups with no O in common: take the staging rows in turn
+            if (seg_idx > 0 && !mbar_wait(&ctl->stg_free, (seg_idx - 1) & 1)) {
+              report_error(p.err, TS_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
               uint32_t v[32], u[32];
@@ -622,17 +652,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               if (complete) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                  reinterpret_cast<uint4*>(orow + ch * 32)[q] =
+                  reinterpret_cast<uint4*>(stg + lane * TcLayout::kStgStride)[q] =
                       make_uint4(pack_bf16x2(o[8 * q + 0], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
                                  pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {  // 8 rows x 64 bytes per instruction
+                  const int rr = it * 8 + (lane >> 2), c4 = lane & 3;
+                  const int row = row0 + rr;
+                  const int ii = row / p.group, hh = kvh * p.group + row % p.group;
+                  const uint4 val = reinterpret_cast<const uint4*>(stg + rr * TcLayout::kStgStride)[c4];
+                  reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(c.b) * p.n_query + ii) * p.hq + hh) * 128 +
+                                           ch * 32)[c4] = val;
+                }
               } else {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                  reinterpret_cast<float4*>(prow + ch * 32)[q] =
+                  reinterpret_cast<float4*>(stg + lane * TcLayout::kStgStride)[q] =
                       make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {  // 4 rows x 128 bytes per instruction
+                  const int rr = it * 4 + (lane >> 3), c4 = lane & 7;
+                  const float4 val = reinterpret_cast<const float4*>(stg + rr * TcLayout::kStgStride)[c4];
+                  reinterpret_cast<float4*>(p.part_o + (slot * 128 + row0 + rr) * 128 + ch * 32)[c4] = val;
+                }
               }
+              __syncwarp();  // the next chunk rewrites the staging rows
             }
-            tc_fence_before();
+            if (lane == 0) mbar_arrive(&ctl->stg_free);            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(&ctl->o_free[wg]);  // both O accumulators have been read
@@ -649,6 +697,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
       }
       if (k == sl && sl > sf) ++nonfin[(sl & 1) ^ 1];  // the non-finishing warpgroup handed over
+      if (k == sl) ++seg_idx;
       c.advance(p, units_per_req);
     }
   }

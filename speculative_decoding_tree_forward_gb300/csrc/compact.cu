@@ -38,8 +38,9 @@ __global__ void __launch_bounds__(kWalkThreads) reroot_walk_kernel(const Compact
   __shared__ uint32_t anc[TS_MAX_TREE][4];
   __shared__ int jmp[TS_MAX_TREE];
   __shared__ int path_s[TS_MAX_TREE + 1];
-  __shared__ int red[kWalkThreads / 32];
+  __shared__ int red[2 * (kWalkThreads / 32)];
   __shared__ int cnt[kWalkThreads / 32];
+  __shared__ int ver_s[TS_MAX_TREE + 1];
 
   const int64_t rowbase = static_cast<int64_t>(b) * p.n_tree_max;
   int n = p.n_tree[b];
@@ -52,6 +53,11 @@ __global__ void __launch_bounds__(kWalkThreads) reroot_walk_kernel(const Compact
   if (P < 0 || P + n > cap) { P = min(max(P, 0), max(cap - n, 0)); bad = true; }
   if (bad && i == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
 
+  // the verified tokens, loaded once (the walk below reads one per step).
+  // A walk step matches at most one node, so with n <= TS_MAX_TREE nodes the
+  // walk has always ended by step TS_MAX_TREE + 1: later tokens are never read.
+  const int mw = min(m, TS_MAX_TREE + 1);
+  for (int j = i; j < mw; j += kWalkThreads) ver_s[j] = p.verified[static_cast<int64_t>(b) * p.m_max + j];
   int my_par = -1, my_tok = 0;
   if (i < n) {
     my_par = p.parent[rowbase + i];
@@ -68,15 +74,16 @@ __global__ void __launch_bounds__(kWalkThreads) reroot_walk_kernel(const Compact
   // ---- walk the verified tokens from the prefix tail
   int cur = -1, plen = 0;
   bool matched_all = true;
-  for (int j = 0; j < m; ++j) {
-    const int v = p.verified[static_cast<int64_t>(b) * p.m_max + j];
+  for (int j = 0; j < mw; ++j) {
+    const int v = ver_s[j];
     int cand = (i < n && my_par == cur && my_tok == v) ? i : INT32_MAX;
     for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-    if ((i & 31) == 0) red[i >> 5] = cand;
+    // two slot sets: set j % 2 is rewritten at step j + 2, after every
+    // thread has passed the barrier of step j + 1 and so finished reading it
+    if ((i & 31) == 0) red[(j & 1) * (kWalkThreads / 32) + (i >> 5)] = cand;
     __syncthreads();
-    int c = red[0];
-    for (int w = 1; w < kWalkThreads / 32; ++w) c = min(c, red[w]);
-    __syncthreads();
+    int c = red[(j & 1) * (kWalkThreads / 32)];
+    for (int w = 1; w < kWalkThreads / 32; ++w) c = min(c, red[(j & 1) * (kWalkThreads / 32) + w]);
     if (c == INT32_MAX) {
       matched_all = false;
       break;
@@ -143,40 +150,58 @@ __global__ void __launch_bounds__(kGatherThreads) compact_gather_kernel(const Co
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ uint4 buf[];  // [rows][chunk_bytes / 16]
+  __shared__ int plan_s[kPlanStride];
   const int group = blockIdx.z;
   const int kv = blockIdx.y;  // 0 = K, 1 = V
   const int layer = blockIdx.x / p.num_req;
   const int b = blockIdx.x % p.num_req;
   const int32_t* plan = p.plan + static_cast<int64_t>(b) * kPlanStride;
-  const int P = plan[0];
-  const int L = plan[1];
+  for (int x = threadIdx.x; x < kPlanStride; x += blockDim.x) plan_s[x] = plan[x];
+  __syncthreads();
+  const int P = plan_s[0];
+  const int L = min(max(plan_s[1], 0), TS_MAX_TREE);
   void* base = kv == 0 ? p.k_layers[layer] : p.v_layers[layer];
   const int vecs = p.chunk_bytes / 16;
   const int c0 = group * p.chunk_bytes;
   const int nvec = min(vecs, (p.row_bytes - c0) / 16);
   if (nvec <= 0) return;
-  // load phase
-  for (int x = threadIdx.x; x < L * nvec; x += blockDim.x) {
-    const int j = x / nvec, v = x % nvec;
-    const int src = plan[2 + j];
-    if (src == j) continue;
-    const uint8_t* s = row_ptr(p, base, b, P + src);
-    if (s == nullptr) {
-      report_error(p.err, TS_DEVERR_BAD_BLOCK);
-      continue;
+  const int total = L * nvec;
+  // load phase: four independent 16-byte loads in flight per thread
+  for (int x0 = threadIdx.x; x0 < total; x0 += 4 * kGatherThreads) {
+    uint4 v[4];
+    int slot[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int x = x0 + q * kGatherThreads;
+      slot[q] = -1;
+      if (x < total) {
+        const int j = x / nvec, e = x % nvec;
+        const int src = plan_s[2 + j];
+        if (src != j) {
+          const uint8_t* sp = row_ptr(p, base, b, P + src);
+          if (sp == nullptr) {
+            report_error(p.err, TS_DEVERR_BAD_BLOCK);
+          } else {
+            v[q] = *reinterpret_cast<const uint4*>(sp + c0 + 16 * e);
+            slot[q] = j * vecs + e;
+          }
+        }
+      }
     }
-    buf[j * vecs + v] = *reinterpret_cast<const uint4*>(s + c0 + 16 * v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (slot[q] >= 0) buf[slot[q]] = v[q];
   }
   __syncthreads();
   // store phase
-  for (int x = threadIdx.x; x < L * nvec; x += blockDim.x) {
-    const int j = x / nvec, v = x % nvec;
-    const int src = plan[2 + j];
+  for (int x = threadIdx.x; x < total; x += kGatherThreads) {
+    const int j = x / nvec, e = x % nvec;
+    const int src = plan_s[2 + j];
     if (src == j) continue;
     uint8_t* d = row_ptr(p, base, b, P + j);
-    const uint8_t* s = row_ptr(p, base, b, P + src);
-    if (d == nullptr || s == nullptr) continue;
-    *reinterpret_cast<uint4*>(d + c0 + 16 * v) = buf[j * vecs + v];
+    const uint8_t* sp = row_ptr(p, base, b, P + src);
+    if (d == nullptr || sp == nullptr) continue;
+    *reinterpret_cast<uint4*>(d + c0 + 16 * e) = buf[j * vecs + e];
   }
 }
 
