@@ -129,7 +129,8 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   pl->rows = rows;
   pl->row_groups = (rows + kMaxRowsPerUnit - 1) / kMaxRowsPerUnit;
   pl->rows_pad = rows >= kMaxRowsPerUnit ? kMaxRowsPerUnit : ((rows + 15) / 16) * 16;
-  const bool tc_shape = (rows == 128) && a->head_dim == 128;
+  // the tcgen05 kernel takes any R <= 128 as one 128-row tile (padded)
+  const bool tc_shape = (rows <= kMaxRowsPerUnit) && a->head_dim == 128;
   if (a->force_path == 2) {
     if (!tc_shape) return TS_ERR_UNSUPPORTED;
     if (!attn_tc_available()) return TS_ERR_UNSUPPORTED;
@@ -139,6 +140,7 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   } else {
     pl->use_tc = tc_shape && attn_tc_available();
   }
+  if (pl->use_tc) pl->rows_pad = kMaxRowsPerUnit;  // partial rows laid out as the 128-row tile
   pl->units = static_cast<int64_t>(a->num_requests) * a->num_kv_heads * pl->row_groups;
   const int max_len = a->kv_layout == TS_KV_PAGED ? a->max_blocks_per_req * a->page_size : a->max_kv_len;
   const int64_t t_max = pl->units * ((max_len + a->n_tree_max + kBlockN - 1) / kBlockN);
@@ -200,6 +202,21 @@ bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, int group) {
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(a->n_query)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// fp32 split-KV partial O as a 2-D tensor (head_dim 128, slots * 128 rows);
+// the tcgen05 kernel stores one box of 32 columns x 32 rows per warp.
+bool encode_partial_map(CUtensorMap* map, float* part_o, int64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {128 * sizeof(float)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -308,6 +325,8 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.n_tree = a->n_tree;
   p.parent = a->parent;
   p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.k_cache = a->k_cache;
+  p.v_cache = a->v_cache;
   p.block_table = a->block_table;
   p.out = static_cast<__nv_bfloat16*>(a->out);
   p.lse = a->lse;
@@ -319,9 +338,10 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.use_tc) {
-    CUtensorMap qmap;
+    CUtensorMap qmap, pmap;
     if (!encode_q_map(&qmap, a, pl.group)) return TS_ERR_CUDA;
-    e = launch_attn_tc(p, kmap, vmap, qmap, s);
+    if (!encode_partial_map(&pmap, p.part_o, pl.slots * pl.rows_pad)) return TS_ERR_CUDA;
+    e = launch_attn_tc(p, kmap, vmap, pmap, qmap, s);
   } else {
     e = launch_attn_mma(p, kmap, vmap, s);
   }

@@ -1,6 +1,8 @@
 // Tree-masked GQA attention on the fifth-generation tensor cores (tcgen05,
-// accumulators in tensor memory), for KV heads whose packed query rows fill
-// one 128-row tile: R = G * n_query = 128, head_dim 128.  This is the NVIDIA
+// accumulators in tensor memory), for KV heads whose packed query rows fit
+// one 128-row tile: R = G * n_query <= 128, head_dim 128.  Rows R..127 of the
+// tile are padding: an M = 128 instruction costs the same for any R, and the
+// kernel is bound by the K/V stream, not by the tensor pipe.  This is the NVIDIA
 // draft-length article's tile rule (D = 128 / G - 1, G x (1 + D) a multiple
 // of 128); the ancestor mask is the SwiftSpec summary's Figure 3 and the key
 // split with a combine its §3.3.
@@ -69,7 +71,7 @@ __host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
 
 struct TcLayout {
   uint32_t q, k, v, ctrl, par, xch, cum, stg, total;
-  static constexpr uint32_t kStgStride = 36;  // words per staged row: 32 + 4 (16-byte rows, conflict-free float4)
+  static constexpr uint32_t kStgWarpBytes = 32 * 128;  // 32 rows x 128 bytes, 128-byte swizzle
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
   static constexpr uint32_t kTileBytes = 64 * 128 * 2;  // one K or V tile: two halves of 64 rows
   static constexpr uint32_t kPairBytes = 2 * kTileBytes;  // K pair region: two halves of 128 rows
@@ -105,9 +107,10 @@ __host__ __device__ inline TcLayout tc_layout(int num_req) {
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
-  // epilogue staging: 32 rows x 32 columns per warp of the finishing warpgroup
-  L.stg = (L.cum + 8 * (kMaxRequestsAttn + 1) + 15) & ~15u;
-  L.total = L.stg + 4 * 32 * TcLayout::kStgStride * 4;  // fixed: launch shape independent of the batch
+  // epilogue staging: 32 rows x 32 fp32 columns per warp of the finishing
+  // warpgroup, 1024-byte aligned for the swizzled TMA store
+  L.stg = (L.cum + 8 * (kMaxRequestsAttn + 1) + 1023) & ~1023u;
+  L.total = L.stg + 4 * TcLayout::kStgWarpBytes;  // fixed: launch shape independent of the batch
   (void)num_req;
   return L;
 }
@@ -155,11 +158,31 @@ struct Cursor {
   }
 };
 
+// Pages per 64-key tile at the smallest supported page size (16 rows).
+constexpr int kMaxPagesPerTile = kBlockN / 16;
+
+// Block-table entries of the cursor's tile for paged K/V: the row of each
+// page in the pool, or one past the pool (the TMA unit fills zeros there)
+// for pages past the request's keys or with an invalid block id.  The loads
+// are independent, so they overlap; the producer issues them one tile ahead.
+__device__ __forceinline__ void tile_pages(const AttnParams& p, const Cursor& c, int (&row)[kMaxPagesPerTile]) {
+  const int pages = kBlockN / p.page_size;
+  const int keys = c.P + c.n;
+  const int key0 = c.tile * kBlockN;
+#pragma unroll
+  for (int pg = 0; pg < kMaxPagesPerTile; ++pg) {
+    const int lb = key0 / p.page_size + pg;
+    row[pg] = -1;
+    if (pg < pages && lb * p.page_size < keys) row[pg] = p.block_table[static_cast<int64_t>(c.b) * p.max_blocks + lb];
+  }
+}
+
 // Loads one 64-key K or V tile (two 64-column halves) of the cursor's tile,
-// from the contiguous cache or page by page through the block table.  Rows
-// past the pool or the tensor are filled with zeros by the TMA unit.
+// from the contiguous cache or page by page (block-table entries `blk` from
+// tile_pages).  Rows past the pool or the tensor are filled with zeros by
+// the TMA unit.
 __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, const CUtensorMap* map, uint8_t* dst0,
-                                          uint8_t* dst1, uint64_t* bar) {
+                                          uint8_t* dst1, uint64_t* bar, const int (&blk)[kMaxPagesPerTile]) {
   const int kvh = c.uir;
   const int key0 = c.tile * kBlockN;
   if (!p.paged) {
@@ -170,18 +193,41 @@ __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, 
   }
   const int pages = kBlockN / p.page_size;
   const int keys = c.P + c.n;
-  for (int pg = 0; pg < pages; ++pg) {
+#pragma unroll
+  for (int pg = 0; pg < kMaxPagesPerTile; ++pg) {
+    if (pg >= pages) break;
     const int lb = key0 / p.page_size + pg;
     int row = p.num_blocks * p.page_size;  // past the pool: TMA fills zeros
     if (lb * p.page_size < keys) {
-      const int blk = p.block_table[static_cast<int64_t>(c.b) * p.max_blocks + lb];
-      if (blk >= 0 && blk < p.num_blocks) row = blk * p.page_size;
+      if (blk[pg] >= 0 && blk[pg] < p.num_blocks) row = blk[pg] * p.page_size;
       else report_error(p.err, TS_DEVERR_BAD_BLOCK);
     }
     const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u;
     tma_load_3d(dst0 + off, map, 0, kvh, row, bar);
     tma_load_3d(dst1 + off, map, 64, kvh, row, bar);
   }
+}
+
+// Paged K or V tile: lane l < 2 * pages issues the TMA box of page l / 2,
+// half l % 2 (one page-head slice of 16 rows is one 2 KB box per half).
+__device__ __forceinline__ void load_tile_paged_lanes(const AttnParams& p, const Cursor& c, const CUtensorMap* map,
+                                                      uint8_t* dst0, uint8_t* dst1, uint64_t* bar,
+                                                      const int (&blk)[kMaxPagesPerTile], int lane) {
+  const int pages = kBlockN / p.page_size;
+  if (lane >= 2 * pages) return;
+  const int pg = lane >> 1, h = lane & 1;
+  const int kvh = c.uir;
+  const int key0 = c.tile * kBlockN;
+  const int keys = c.P + c.n;
+  const int lb = key0 / p.page_size + pg;
+  const int b = pg == 0 ? blk[0] : pg == 1 ? blk[1] : pg == 2 ? blk[2] : blk[3];
+  int row = p.num_blocks * p.page_size;  // past the pool: TMA fills zeros
+  if (lb * p.page_size < keys) {
+    if (b >= 0 && b < p.num_blocks) row = b * p.page_size;
+    else report_error(p.err, TS_DEVERR_BAD_BLOCK);
+  }
+  const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u;
+  tma_load_3d((h == 0 ? dst0 : dst1) + off, map, h * 64, kvh, row, bar);
 }
 
 // Waits (bounded) for the last copy issued into each slot of a ring.
@@ -194,6 +240,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued
 
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
+                                                                const __grid_constant__ CUtensorMap pmap,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const AttnParams p) {
   pdl_wait();
@@ -262,6 +309,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
   const int64_t local0 = t_begin - cum[b0];
 
+  // fewer than 128 packed rows: the Q loads fill rows 0 .. R-1 only, so the
+  // rest of each Q buffer is zeroed once (before any copy into it)
+  if (p.rows < kRowsTc) {
+    for (int x = tid; x < kQBufs * static_cast<int>(TcLayout::kQBytes / 16); x += kTcThreads)
+      reinterpret_cast<uint4*>(smem + L.q)[x] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
   if (warp == kQkWarp) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -272,48 +326,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const uint32_t tbase = ctl->tmem_base;
 
   if (warp == kProducerWarp || warp == kVProducerWarp) {
-    // ======================= TMA producers =======================
+    // ======================= K / V producers =======================
+    // Lane 0 waits for slots and issues the TMA loads; a paged tile's page
+    // boxes are issued by several lanes at once.
+    const bool kside = warp == kProducerWarp;
+    const CUtensorMap* map = kside ? &kmap : &vmap;
     if (lane == 0) {
-      const bool kside = warp == kProducerWarp;
-      const CUtensorMap* map = kside ? &kmap : &vmap;
       prefetch_tmap(map);
       if (kside) prefetch_tmap(&qmap);
-      Cursor c;
-      c.start(p, b0, local0);
-      int issued = 0, q_issued = 0;
-      bool ok = true;
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        if (kside && (it == 0 || c.tile == 0)) {
-          // buffer u % kQBufs is free once the QK^T of unit u - kQBufs are done
-          const int qb = c.unit % kQBufs;
-          if (c.unit >= kQBufs && !mbar_wait(&ctl->q_empty[qb], ((c.unit / kQBufs) - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&ctl->q_full[qb], TcLayout::kQBytes);
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(smem + L.q + qb * TcLayout::kQBytes + h * (TcLayout::kQBytes / 2), &qmap, h * 64,
-                        c.uir * p.group, c.b * p.n_query, &ctl->q_full[qb]);
-          ++q_issued;
+    }
+    Cursor c;
+    c.start(p, b0, local0);
+    int issued = 0, q_issued = 0;
+    int blk[kMaxPagesPerTile];
+    if (p.paged) tile_pages(p, c, blk);
+    bool ok = true;
+    for (int it = 0; it < n_tiles; ++it) {
+      if (kside && (it == 0 || c.tile == 0)) {
+        // buffer u % kQBufs is free once the QK^T of unit u - kQBufs are done
+        const int qb = c.unit % kQBufs;
+        if (lane == 0) {
+          ok = c.unit < kQBufs || mbar_wait(&ctl->q_empty[qb], ((c.unit / kQBufs) - 1) & 1);
+          if (ok) {
+            mbar_arrive_expect_tx(&ctl->q_full[qb], static_cast<uint32_t>(p.rows) * 256u);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(smem + L.q + qb * TcLayout::kQBytes + h * (TcLayout::kQBytes / 2), &qmap, h * 64,
+                          c.uir * p.group, c.b * p.n_query, &ctl->q_full[qb]);
+          }
         }
-        const int sl = kside ? it % kKSlots : it % kSlots, w = it & 1, bb = (it >> 1) & 1;
-        // a K slot is free once the S that read it is computed, a V slot once
-        // the PV of the tile four back (same S/P buffer) is done
-        if (kside ? (it >= kKSlots && !mbar_wait(&ctl->k_empty[sl], ((it / kKSlots) - 1) & 1))
-                  : (it >= kSlots && !mbar_wait(&ctl->pv_done[w][bb], ((it >> 2) - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        uint64_t* full = kside ? &ctl->k_full[sl] : &ctl->v_full[sl];
-        mbar_arrive_expect_tx(full, TcLayout::kTileBytes);
-        if (kside) load_tile(p, c, map, smem + L.k + k_half_off(sl, 0), smem + L.k + k_half_off(sl, 1), full);
-        else load_tile(p, c, map, smem + L.v + v_half_off(sl, 0), smem + L.v + v_half_off(sl, 1), full);
-        ++issued;
-        c.advance(p, units_per_req);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++q_issued;
       }
-      if (!ok) {
-        report_error(p.err, TS_DEVERR_TIMEOUT);
-        *abort_flag = 1;
+      const int sl = kside ? it % kKSlots : it % kSlots, w = it & 1, bb = (it >> 1) & 1;
+      // a K slot is free once the S that read it is computed, a V slot once
+      // the PV of the tile four back (same S/P buffer) is done
+      if (lane == 0)
+        ok = kside ? (it < kKSlots || mbar_wait(&ctl->k_empty[sl], ((it / kKSlots) - 1) & 1))
+                   : (it < kSlots || mbar_wait(&ctl->pv_done[w][bb], ((it >> 2) - 1) & 1));
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      uint64_t* full = kside ? &ctl->k_full[sl] : &ctl->v_full[sl];
+      uint8_t* dst0 = smem + (kside ? L.k + k_half_off(sl, 0) : L.v + v_half_off(sl, 0));
+      uint8_t* dst1 = smem + (kside ? L.k + k_half_off(sl, 1) : L.v + v_half_off(sl, 1));
+      if (lane == 0) mbar_arrive_expect_tx(full, TcLayout::kTileBytes);
+      if (!p.paged) {
+        if (lane == 0) load_tile(p, c, map, dst0, dst1, full, blk);
+      } else {
+        __syncwarp();  // the transaction count is armed before any box lands
+        load_tile_paged_lanes(p, c, map, dst0, dst1, full, blk, lane);
       }
-      if (*abort_flag) {
-        // never leave with copies into this CTA's shared memory in flight
+      ++issued;
+      c.advance(p, units_per_req);
+      // next tile's block-table entries: in flight while lane 0 waits for the slot
+      if (p.paged && it + 1 < n_tiles) tile_pages(p, c, blk);
+    }
+    if (!ok && lane == 0) {
+      report_error(p.err, TS_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    __syncwarp();
+    if (*abort_flag) {
+      // never leave with copies into this CTA's shared memory in flight
+      if (lane == 0) {
         drain_ring(kside ? ctl->k_full : ctl->v_full, kside ? kKSlots : kSlots, issued);
         for (int u = max(q_issued - kQBufs, 0); u < q_issued; ++u)
           mbar_wait(&ctl->q_full[u % kQBufs], static_cast<uint32_t>((u / kQBufs) & 1));
@@ -446,7 +521,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             wg_sync(wg);
             anc_req = c.b;
           }
-          ancestor_walk(par, c.n - p.n_query + r / p.group, anc);
+          if (r < p.rows) {
+            ancestor_walk(par, c.n - p.n_query + r / p.group, anc);
+          } else {  // padding row: sees no tree key, its output is discarded
+#pragma unroll
+            for (int w = 0; w < 4; ++w) anc[w] = 0u;
+          }
           m_used = -INFINITY;
           l = 0.f;
         }
@@ -627,10 +707,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             const int64_t unit = static_cast<int64_t>(c.b) * units_per_req + c.uir;
             const int64_t slot = static_cast<int64_t>(blockIdx.x) + unit;
             // Each 32-column chunk of this warp's 32 rows goes through shared
-            // memory, so the global stores are whole row segments (128 bytes
-            // of fp32 or 64 bytes of bf16 per row) instead of 16-byte pieces
-            // of 32 different rows.
-            float* stg = reinterpret_cast<float*>(smem + L.stg) + (warp & 3) * 32 * TcLayout::kStgStride;
+            // memory (128-byte rows, 16-byte chunk c of row r at c ^ (r % 8)):
+            // fp32 partials leave as one TMA store per chunk, so the warp waits
+            // only until the tile has been read; bf16 outputs leave as whole
+            // 64-byte row segments.
+            uint8_t* stg = smem + L.stg + (warp & 3) * TcLayout::kStgWarpBytes;
             const int row0 = (warp & 3) * 32;
             // finishers of consecutive short segments may be different
             // warpgroups with no O in common: take the staging rows in turn
@@ -652,7 +733,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               if (complete) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                  reinterpret_cast<uint4*>(stg + lane * TcLayout::kStgStride)[q] =
+                  *reinterpret_cast<uint4*>(stg + sw128(lane, q)) =
                       make_uint4(pack_bf16x2(o[8 * q + 0], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
                                  pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
                 __syncwarp();
@@ -660,25 +741,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 for (int it = 0; it < 4; ++it) {  // 8 rows x 64 bytes per instruction
                   const int rr = it * 8 + (lane >> 2), c4 = lane & 3;
                   const int row = row0 + rr;
+                  if (row >= p.rows) continue;
                   const int ii = row / p.group, hh = kvh * p.group + row % p.group;
-                  const uint4 val = reinterpret_cast<const uint4*>(stg + rr * TcLayout::kStgStride)[c4];
+                  const uint4 val = *reinterpret_cast<const uint4*>(stg + sw128(rr, c4));
                   reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(c.b) * p.n_query + ii) * p.hq + hh) * 128 +
                                            ch * 32)[c4] = val;
                 }
+                __syncwarp();  // the next chunk rewrites the staging rows
               } else {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                  reinterpret_cast<float4*>(stg + lane * TcLayout::kStgStride)[q] =
+                  *reinterpret_cast<float4*>(stg + sw128(lane, q)) =
                       make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                fence_proxy_async_smem();
                 __syncwarp();
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {  // 4 rows x 128 bytes per instruction
-                  const int rr = it * 4 + (lane >> 3), c4 = lane & 7;
-                  const float4 val = reinterpret_cast<const float4*>(stg + rr * TcLayout::kStgStride)[c4];
-                  reinterpret_cast<float4*>(p.part_o + (slot * 128 + row0 + rr) * 128 + ch * 32)[c4] = val;
+                if (lane == 0) {
+                  tma_store_2d(&pmap, stg, ch * 32, static_cast<int>(slot * 128 + row0));
+                  bulk_commit();
+                  bulk_wait_read_all();  // the staging rows may be rewritten
                 }
+                __syncwarp();
               }
-              __syncwarp();  // the next chunk rewrites the staging rows
             }
             if (lane == 0) mbar_arrive(&ctl->stg_free);            tc_fence_before();
             __syncwarp();
@@ -687,11 +770,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               if (other_in) mbar_arrive(&ctl->o_free[oth]);
             }
             const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
-            if (complete) {
-              if (p.lse != nullptr)
-                p.lse[(static_cast<int64_t>(c.b) * p.hq + h) * p.n_query + i] = lse2 * 0.69314718055994530942f;
-            } else {
-              p.part_lse[slot * 128 + r] = lse2;
+            if (r < p.rows) {
+              if (complete) {
+                if (p.lse != nullptr)
+                  p.lse[(static_cast<int64_t>(c.b) * p.hq + h) * p.n_query + i] = lse2 * 0.69314718055994530942f;
+              } else {
+                p.part_lse[slot * 128 + r] = lse2;
+              }
             }
           }
         }
@@ -702,6 +787,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
   }
 
+  bulk_wait_all();  // partial stores issued by this thread have completed
   tc_fence_before();
   __syncthreads();
   if (warp == kQkWarp) {
@@ -734,10 +820,10 @@ int attn_tc_occupancy(int stages, int num_req) {
 
 // The dynamic shared-memory attribute was raised by attn_tc_occupancy, which
 // the host plan runs (once per device) before any launch.
-cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& pmap,
                            const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = attn_tc_smem_bytes(p.stages, p.num_req);
-  return launch_pdl(attn_tc_kernel, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, qmap, p);
+  return launch_pdl(attn_tc_kernel, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, pmap, qmap, p);
 }
 
 }  // namespace ts

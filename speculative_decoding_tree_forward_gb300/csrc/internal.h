@@ -51,6 +51,8 @@ struct AttnParams {
   const int32_t* n_tree;
   const int32_t* parent;
   const __nv_bfloat16* q;
+  const void* k_cache;   // K / V base (the paged tcgen05 path gathers rows with cp.async)
+  const void* v_cache;
   const int32_t* block_table;
   __nv_bfloat16* out;
   float* lse;
@@ -63,7 +65,7 @@ struct AttnParams {
 // Launchers (one per kernel family); return cudaGetLastError().
 cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream);
-cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& pmap,
                            const CUtensorMap& qmap, cudaStream_t stream);
 size_t attn_zero_prefix_bytes(const ts_attn_args* a);
 cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream);

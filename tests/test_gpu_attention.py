@@ -56,6 +56,32 @@ TC = [
 ]
 
 
+# R < 128: the tcgen05 kernel pads the packed rows to one 128-row tile
+TC_SMALL_R = [
+    dict(num_req=4, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(60, 700), chain=True),          # R = 40
+    dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=40, n_query=8, prefix_range=(100, 400)),         # R = 32
+    dict(num_req=3, hq=4, hkv=4, d=128, n_tree_max=20, n_query=8, ragged_tree=True, prefix_range=(0, 300)),  # R = 8
+    dict(num_req=2, hq=2, hkv=2, d=128, n_tree_max=6, n_query=1, prefix_range=(0, 260)),             # R = 1
+    dict(num_req=2, hq=16, hkv=4, d=128, n_tree_max=30, n_query=25, prefix_range=(0, 200)),          # R = 100
+    dict(num_req=1, hq=127, hkv=1, d=128, n_tree_max=9, n_query=1, prefix_range=(30, 90)),           # R = 127
+]
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("cfg", range(len(TC_SMALL_R)))
+def test_tcgen05_fewer_rows_match_oracle(cfg, paged):
+    case = W.random_attn_case(250 + cfg, paged=paged, **TC_SMALL_R[cfg])
+    out, lse = run(case, force_path=2)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 5, 64, 700])
+def test_tcgen05_fewer_rows_split_counts(num_ctas):
+    case = W.random_attn_case(260, num_req=3, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(10, 900), chain=True)
+    out, lse = run(case, force_path=2, num_ctas=num_ctas)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
 @pytest.mark.parametrize("paged", [False, True])
 @pytest.mark.parametrize("cfg", range(len(TC)))
 def test_tcgen05_cases_match_oracle(cfg, paged):
@@ -109,11 +135,23 @@ def test_automatic_path_choice():
     a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
                      torch.empty_like(d["q"]))
     assert ts.tree_attn_selected_path(a) == "tcgen05"
+    # R = 40 (chain verify, G = 8): one padded 128-row tile on the tcgen05 path
     case2 = W.random_attn_case(16, num_req=1, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(5, 5))
     d2 = attn_inputs(case2)
     a2 = ts.attn_args(d2["q"], d2["k_cache"], d2["v_cache"], d2["prefix_len"], d2["n_tree"], d2["parent"],
                       torch.empty_like(d2["q"]))
-    assert ts.tree_attn_selected_path(a2) == "mma"
+    assert ts.tree_attn_selected_path(a2) == "tcgen05"
+    # head_dim 64 and R > 128 stay on the warp-MMA kernel
+    case3 = W.random_attn_case(16, num_req=1, hq=8, hkv=2, d=64, n_tree_max=16, prefix_range=(5, 5))
+    d3 = attn_inputs(case3)
+    a3 = ts.attn_args(d3["q"], d3["k_cache"], d3["v_cache"], d3["prefix_len"], d3["n_tree"], d3["parent"],
+                      torch.empty_like(d3["q"]))
+    assert ts.tree_attn_selected_path(a3) == "mma"
+    case4 = W.random_attn_case(16, num_req=1, hq=16, hkv=1, d=128, n_tree_max=16, prefix_range=(5, 5))
+    d4 = attn_inputs(case4)
+    a4 = ts.attn_args(d4["q"], d4["k_cache"], d4["v_cache"], d4["prefix_len"], d4["n_tree"], d4["parent"],
+                      torch.empty_like(d4["q"]))
+    assert ts.tree_attn_selected_path(a4) == "mma"   # R = 256
 
 
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 64, 1000])
