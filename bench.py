@@ -66,13 +66,21 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value over the ranks (the slowest replica's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(tokens_per_step, world, ms_max):
+    """Whole-job throughput: every rank runs its own replica of the step, so the
+    job verifies world x tokens_per_step tokens in the slowest rank's step time."""
+    return tokens_per_step * world / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------------------
@@ -474,7 +482,7 @@ def main():
     ms_max = max_over_ranks(ms, world)
 
     tokens = info["tokens_per_step"] * world
-    value = tokens / (ms_max / 1e3)
+    value = replica_value(info["tokens_per_step"], world, ms_max)
     peak, peak_kind = peaks()
     attn_bytes = info["attn_bytes"] / n_attn
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
