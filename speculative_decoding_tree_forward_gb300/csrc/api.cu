@@ -86,7 +86,7 @@ int cached_occupancy(bool tc, int head_dim, int stages, int rows_pad, int num_re
 // ------------------------------------------------------------------ attention plan
 struct AttnPlan {
   bool use_tc;
-  int rows, row_groups, rows_pad, group, stages, num_ctas;
+  int rows, row_groups, rows_pad, group, stages, num_ctas, hp;
   int64_t units, slots;
   size_t ws_bytes, off_o, off_lse;
 };
@@ -140,8 +140,11 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   } else {
     pl->use_tc = tc_shape && attn_tc_available();
   }
+  // the tcgen05 kernel packs two adjacent KV heads into one 128-row tile when
+  // their rows fit (R <= 64): one TMA box then carries both heads' keys
+  pl->hp = (pl->use_tc && rows <= kMaxRowsPerUnit / 2 && a->num_kv_heads % 2 == 0) ? 2 : 1;
   if (pl->use_tc) pl->rows_pad = kMaxRowsPerUnit;  // partial rows laid out as the 128-row tile
-  pl->units = static_cast<int64_t>(a->num_requests) * a->num_kv_heads * pl->row_groups;
+  pl->units = static_cast<int64_t>(a->num_requests) * (a->num_kv_heads / pl->hp) * pl->row_groups;
   const int max_len = a->kv_layout == TS_KV_PAGED ? a->max_blocks_per_req * a->page_size : a->max_kv_len;
   const int64_t t_max = pl->units * ((max_len + a->n_tree_max + kBlockN - 1) / kBlockN);
   int occ = 1;
@@ -171,7 +174,9 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   return TS_OK;
 }
 
-bool encode_kv_map(CUtensorMap* map, const void* base, const ts_attn_args* a) {
+// K or V as a 3-D tensor (head_dim, Hkv, rows); a box is 64 columns of `hp`
+// adjacent heads for 64 rows (contiguous) or one page (paged).
+bool encode_kv_map(CUtensorMap* map, const void* base, const ts_attn_args* a, int hp) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t rows = a->kv_layout == TS_KV_PAGED
@@ -181,7 +186,7 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const ts_attn_args* a) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->head_dim), static_cast<cuuint64_t>(a->num_kv_heads), rows};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(a->head_dim) * 2,
                            static_cast<cuuint64_t>(a->head_dim) * 2 * a->num_kv_heads};
-  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(hp), box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -299,7 +304,7 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   if (st != TS_OK) return st;
   if (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
   CUtensorMap kmap, vmap;
-  if (!encode_kv_map(&kmap, a->k_cache, a) || !encode_kv_map(&vmap, a->v_cache, a)) return TS_ERR_CUDA;
+  if (!encode_kv_map(&kmap, a->k_cache, a, pl.hp) || !encode_kv_map(&vmap, a->v_cache, a, pl.hp)) return TS_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
@@ -311,6 +316,7 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.n_query = a->n_query;
   p.n_tree_max = a->n_tree_max;
   p.rows = pl.rows;
+  p.hp = pl.hp;
   p.row_groups = pl.row_groups;
   p.rows_pad = pl.rows_pad;
   p.max_kv_len = a->max_kv_len;

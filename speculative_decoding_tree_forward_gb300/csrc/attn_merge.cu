@@ -27,14 +27,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t unit = blockIdx.x;
-  const int units_per_req = p.hkv * p.row_groups;
+  // a unit is (request, group of hp KV heads, row group); with hp = 2 the
+  // unit's rows are two heads' R <= 64 rows at 0 and 64
+  const int units_per_req = (p.hkv / p.hp) * p.row_groups;
   const int b = static_cast<int>(unit / units_per_req);
   const int uir = static_cast<int>(unit % units_per_req);
-  const int kvh = uir / p.row_groups;
+  const int kvh = uir / p.row_groups;  // head group
   const int rg = uir % p.row_groups;
-  const int rows_here = min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit);
   const int rl = blockIdx.y * kMergeWarps + warp;
-  if (rl >= rows_here) return;
+  const int hj = p.hp == 2 ? rl >> 6 : 0, loc = p.hp == 2 ? rl & 63 : rl;
+  if (p.hp == 2 ? loc >= p.rows : rl >= min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit)) return;
   // tiles before this unit and in total (same clamped lengths as the attention kernels)
   long long before = 0, total = 0;
   for (int bb = lane; bb < p.num_req; bb += 32) {
@@ -110,8 +112,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   const float inv = wsum > 0.f ? __frcp_rn(wsum) : 0.f;
-  const int r = rg * kMaxRowsPerUnit + rl;
-  const int i = r / p.group, h = kvh * p.group + r % p.group;
+  const int r = rg * kMaxRowsPerUnit + loc;
+  const int i = r / p.group, h = (p.hp * kvh + hj) * p.group + r % p.group;
   if (active) {
     uint2* dst = reinterpret_cast<uint2*>(p.out + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * D + lane * 4);
     *dst = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));

@@ -52,9 +52,9 @@
 namespace ts {
 namespace {
 
-constexpr int kSlots = 4;   // V slots, one per S/P buffer
-constexpr int kKSlots = 6;  // K slots (even: slots 2i, 2i + 1 form one 128-row pair region)
-constexpr int kQBufs = 1;   // Q buffers (unit u uses buffer u % kQBufs)
+constexpr int kMaxVSlots = 4;  // V slots (one per S/P buffer)
+constexpr int kMaxKSlots = 6;  // K slots
+constexpr int kQBufs = 1;      // Q buffers (unit u uses buffer u % kQBufs)
 constexpr int kTcThreads = 384;
 constexpr int kRowsTc = 128;
 constexpr int kProducerWarp = 8;  // Q and K
@@ -64,32 +64,50 @@ constexpr int kVProducerWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
-// tile k of warpgroup w = k % 2 uses S/P buffer b = (k / 2) % 2, and K / V
-// slot k % 4 = 2 b + w, for the (k / 4)-th time
-__host__ __device__ constexpr uint32_t col_s(int w, int b) { return 128u * b + 64u * w; }
 __host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
+
+// Shape of the pipeline for HP KV heads per unit.  HP = 1: a tile is 64 keys
+// of one head; each warpgroup has two 64-column S/P buffers (tile k of
+// warpgroup w = k % 2 uses buffer (k / 2) % 2 and V slot k % 4); K lives in
+// six 16 KB slots, two adjacent slots forming the 128-row operand of a tile
+// pair.  HP = 2 (packed rows R <= 64, two adjacent KV heads share one CTA):
+// a tile is 64 keys of both heads, loaded as one TMA box per page-half (keys
+// interleaved by head: shared-memory row 2 key + head); each warpgroup has one
+// 128-column S/P buffer; K lives in three 32 KB slots and V in two.
+template <int HP>
+struct TcShape {
+  static constexpr int kKSlots = HP == 1 ? 6 : 3;
+  static constexpr int kVSlots = HP == 1 ? 4 : 2;     // = S/P buffers in all: slot of tile k is k % kVSlots
+  static constexpr uint32_t kTileBytes = 64u * 128u * 2u * HP;  // one K or V tile (two 64-column halves)
+  static constexpr uint32_t kHalfRows = 64u * HP;    // shared-memory rows of one half of a tile
+  __device__ static uint32_t col_s(int w, int b) { return HP == 1 ? 128u * b + 64u * w : 128u * w; }
+  __device__ static int buf(int k) { return HP == 1 ? (k >> 1) & 1 : 0; }
+  __device__ static int use(int k) { return HP == 1 ? k >> 2 : k >> 1; }  // earlier tiles in the same buffer
+  // half h (columns 64 h .. 64 h + 63) of the K tile in slot s; for HP = 1
+  // the pair region holds each half as 128 rows, tile 2i in rows 0-63 and
+  // tile 2i + 1 in 64-127
+  __device__ static uint32_t k_half_off(int s, int h) {
+    return HP == 1 ? static_cast<uint32_t>((s >> 1) * 32768 + h * 16384 + (s & 1) * 8192)
+                   : static_cast<uint32_t>(s * 32768 + h * 16384);
+  }
+  __device__ static uint32_t v_half_off(int s, int h) {
+    return static_cast<uint32_t>(s * kTileBytes + h * (kTileBytes / 2));
+  }
+  // packed row r of the tile: head within the unit and row within the head
+  __device__ static int head_of(int r) { return HP == 1 ? 0 : r >> 6; }
+  __device__ static int local_of(int r) { return HP == 1 ? r : r & 63; }
+};
 
 struct TcLayout {
   uint32_t q, k, v, ctrl, par, xch, cum, stg, total;
   static constexpr uint32_t kStgWarpBytes = 32 * 128;  // 32 rows x 128 bytes, 128-byte swizzle
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
-  static constexpr uint32_t kTileBytes = 64 * 128 * 2;  // one K or V tile: two halves of 64 rows
-  static constexpr uint32_t kPairBytes = 2 * kTileBytes;  // K pair region: two halves of 128 rows
+  static constexpr uint32_t kKBytes = 96 * 1024;       // K ring (same bytes for HP = 1 and 2)
+  static constexpr uint32_t kVBytes = 64 * 1024;       // V ring
 };
 
-// half h (columns 64 h .. 64 h + 63) of the K tile in slot s: the pair region
-// holds each half as 128 rows, tile 2i in rows 0-63 and tile 2i + 1 in 64-127
-__device__ __forceinline__ uint32_t k_half_off(int s, int h) {
-  return static_cast<uint32_t>((s >> 1) * TcLayout::kPairBytes + h * (TcLayout::kPairBytes / 2) +
-                               (s & 1) * (TcLayout::kTileBytes / 2));
-}
-// half h of the V tile in slot s
-__device__ __forceinline__ uint32_t v_half_off(int s, int h) {
-  return static_cast<uint32_t>(s * TcLayout::kTileBytes + h * (TcLayout::kTileBytes / 2));
-}
-
 struct TcCtrl {
-  uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kSlots];
+  uint64_t k_full[kMaxKSlots], k_empty[kMaxKSlots], v_full[kMaxVSlots];
   uint64_t q_full[kQBufs], q_empty[kQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
   uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
@@ -102,8 +120,8 @@ __host__ __device__ inline TcLayout tc_layout(int num_req) {
   TcLayout L;
   L.q = 0;
   L.k = L.q + kQBufs * TcLayout::kQBytes;
-  L.v = L.k + (kKSlots / 2) * TcLayout::kPairBytes;
-  L.ctrl = L.v + kSlots * TcLayout::kTileBytes;
+  L.v = L.k + TcLayout::kKBytes;
+  L.ctrl = L.v + TcLayout::kVBytes;
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
@@ -181,9 +199,10 @@ __device__ __forceinline__ void tile_pages(const AttnParams& p, const Cursor& c,
 // from the contiguous cache or page by page (block-table entries `blk` from
 // tile_pages).  Rows past the pool or the tensor are filled with zeros by
 // the TMA unit.
+template <int HP>
 __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, const CUtensorMap* map, uint8_t* dst0,
                                           uint8_t* dst1, uint64_t* bar, const int (&blk)[kMaxPagesPerTile]) {
-  const int kvh = c.uir;
+  const int kvh = HP * c.uir;  // first KV head of the unit (the box covers HP heads)
   const int key0 = c.tile * kBlockN;
   if (!p.paged) {
     const int row = c.b * p.max_kv_len + key0;
@@ -202,21 +221,22 @@ __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, 
       if (blk[pg] >= 0 && blk[pg] < p.num_blocks) row = blk[pg] * p.page_size;
       else report_error(p.err, TS_DEVERR_BAD_BLOCK);
     }
-    const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u;
+    const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u * HP;
     tma_load_3d(dst0 + off, map, 0, kvh, row, bar);
     tma_load_3d(dst1 + off, map, 64, kvh, row, bar);
   }
 }
 
 // Paged K or V tile: lane l < 2 * pages issues the TMA box of page l / 2,
-// half l % 2 (one page-head slice of 16 rows is one 2 KB box per half).
+// half l % 2 (16 rows of HP heads: a 2 KB box per half for one head).
+template <int HP>
 __device__ __forceinline__ void load_tile_paged_lanes(const AttnParams& p, const Cursor& c, const CUtensorMap* map,
                                                       uint8_t* dst0, uint8_t* dst1, uint64_t* bar,
                                                       const int (&blk)[kMaxPagesPerTile], int lane) {
   const int pages = kBlockN / p.page_size;
   if (lane >= 2 * pages) return;
   const int pg = lane >> 1, h = lane & 1;
-  const int kvh = c.uir;
+  const int kvh = HP * c.uir;
   const int key0 = c.tile * kBlockN;
   const int keys = c.P + c.n;
   const int lb = key0 / p.page_size + pg;
@@ -226,8 +246,63 @@ __device__ __forceinline__ void load_tile_paged_lanes(const AttnParams& p, const
     if (b >= 0 && b < p.num_blocks) row = b * p.page_size;
     else report_error(p.err, TS_DEVERR_BAD_BLOCK);
   }
-  const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u;
+  const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u * HP;
   tma_load_3d((h == 0 ? dst0 : dst1) + off, map, h * 64, kvh, row, bar);
+}
+
+// Pass 2 of the softmax for one row: P = 2^(s * scale_log2 + nbase) (keys
+// whose bit in vis is clear count as -inf on tiles holding tree keys),
+// written as bf16 pairs over the S chunks they came from (16 pairs per
+// 32-column chunk; the chunk's other 16 columns get the bf16 rounding
+// residual on tree tiles); the sum of the fp32 probabilities goes to ps.
+// HP = 1: the row's 64 scores sv are in registers; a chunk is keys
+// 32 ch .. 32 ch + 31, two keys per pair.
+template <bool TREE>
+__device__ __forceinline__ void write_p1(const float (&sv)[64], uint64_t vis, float scale_log2, float nbase,
+                                         uint32_t sbuf, float (&ps)[4]) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = 32 * ch + 2 * q;
+      const float s0 = (!TREE || ((vis >> e) & 1ull)) ? sv[e] : -INFINITY;
+      const float s1 = (!TREE || ((vis >> (e + 1)) & 1ull)) ? sv[e + 1] : -INFINITY;
+      const float x0 = ex2_approx(fmaf(s0, scale_log2, nbase));
+      const float x1 = ex2_approx(fmaf(s1, scale_log2, nbase));
+      ps[q & 3] += x0 + x1;
+      hi[q] = pack_bf16x2(x0, x1);
+      if constexpr (TREE) lo[q] = bf16x2_residual(hi[q], x0, x1);
+    }
+    tmem_st16(sbuf + 32 * ch, hi);
+    if constexpr (TREE) tmem_st16(sbuf + 32 * ch + 16, lo);
+  }
+}
+// HP = 2: S is re-read chunk by chunk; chunk ch holds keys 16 ch .. 16 ch + 15
+// of both heads (column 2 key + head), and pair q of the chunk is key
+// 16 ch + q (V rows 2 key, 2 key + 1) with the other head's half zero.
+template <bool TREE>
+__device__ __forceinline__ void write_p2(uint64_t vis, float scale_log2, float nbase, int hj, uint32_t sbuf,
+                                         float (&ps)[4]) {
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(sbuf + 32 * ch, v);
+    tmem_ld_wait();
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = 16 * ch + q;
+      const float s0 = (!TREE || ((vis >> e) & 1ull)) ? __uint_as_float(hj ? v[2 * q + 1] : v[2 * q]) : -INFINITY;
+      const float e0 = ex2_approx(fmaf(s0, scale_log2, nbase));
+      ps[q & 3] += e0;
+      const float x0 = hj ? 0.f : e0, x1 = hj ? e0 : 0.f;
+      hi[q] = pack_bf16x2(x0, x1);
+      if constexpr (TREE) lo[q] = bf16x2_residual(hi[q], x0, x1);
+    }
+    tmem_st16(sbuf + 32 * ch, hi);
+    if constexpr (TREE) tmem_st16(sbuf + 32 * ch + 16, lo);
+  }
 }
 
 // Waits (bounded) for the last copy issued into each slot of a ring.
@@ -238,6 +313,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued
   }
 }
 
+template <int HP>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const __grid_constant__ CUtensorMap pmap,
@@ -255,7 +331,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const int tid = threadIdx.x;
   const int warp = tid / 32;
   const int lane = tid % 32;
-  const int units_per_req = p.hkv;  // one row group: R == 128
+  using Sh = TcShape<HP>;
+  const int units_per_req = p.hkv / HP;  // one row group: HP heads x R <= 128 rows
 
   // ---- schedule (identical to the warp-MMA kernel) and barrier set-up
   for (int b = tid; b < p.num_req; b += blockDim.x) {
@@ -266,11 +343,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (tid == 0) {
     cum[0] = 0;
     ctl->abort = 0;
-    for (int s = 0; s < kKSlots; ++s) {
+    for (int s = 0; s < Sh::kKSlots; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 1);
     }
-    for (int s = 0; s < kSlots; ++s) mbar_init(&ctl->v_full[s], 1);
+    for (int s = 0; s < Sh::kVSlots; ++s) mbar_init(&ctl->v_full[s], 1);
     for (int i = 0; i < kQBufs; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
@@ -309,9 +386,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
   const int64_t local0 = t_begin - cum[b0];
 
-  // fewer than 128 packed rows: the Q loads fill rows 0 .. R-1 only, so the
-  // rest of each Q buffer is zeroed once (before any copy into it)
-  if (p.rows < kRowsTc) {
+  // fewer than 128 packed rows: the Q loads fill rows 0 .. R-1 of each head's
+  // 128 / HP rows only, so the rest of each Q buffer is zeroed once (before
+  // any copy into it)
+  if (p.rows < kRowsTc / HP) {
     for (int x = tid; x < kQBufs * static_cast<int>(TcLayout::kQBytes / 16); x += kTcThreads)
       reinterpret_cast<uint4*>(smem + L.q)[x] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -348,33 +426,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (lane == 0) {
           ok = c.unit < kQBufs || mbar_wait(&ctl->q_empty[qb], ((c.unit / kQBufs) - 1) & 1);
           if (ok) {
-            mbar_arrive_expect_tx(&ctl->q_full[qb], static_cast<uint32_t>(p.rows) * 256u);
+            mbar_arrive_expect_tx(&ctl->q_full[qb], static_cast<uint32_t>(HP * p.rows) * 256u);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + L.q + qb * TcLayout::kQBytes + h * (TcLayout::kQBytes / 2), &qmap, h * 64,
-                          c.uir * p.group, c.b * p.n_query, &ctl->q_full[qb]);
+              for (int j = 0; j < HP; ++j)  // head j of the unit at packed row 64 j
+                tma_load_3d(smem + L.q + qb * TcLayout::kQBytes + h * (TcLayout::kQBytes / 2) + j * 8192, &qmap,
+                            h * 64, (HP * c.uir + j) * p.group, c.b * p.n_query, &ctl->q_full[qb]);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         ++q_issued;
       }
-      const int sl = kside ? it % kKSlots : it % kSlots, w = it & 1, bb = (it >> 1) & 1;
+      const int sl = kside ? it % Sh::kKSlots : it % Sh::kVSlots, w = it & 1, bb = Sh::buf(it);
       // a K slot is free once the S that read it is computed, a V slot once
-      // the PV of the tile four back (same S/P buffer) is done
+      // the PV of the previous tile in the same S/P buffer is done
       if (lane == 0)
-        ok = kside ? (it < kKSlots || mbar_wait(&ctl->k_empty[sl], ((it / kKSlots) - 1) & 1))
-                   : (it < kSlots || mbar_wait(&ctl->pv_done[w][bb], ((it >> 2) - 1) & 1));
+        ok = kside ? (it < Sh::kKSlots || mbar_wait(&ctl->k_empty[sl], ((it / Sh::kKSlots) - 1) & 1))
+                   : (it < Sh::kVSlots || mbar_wait(&ctl->pv_done[w][bb], (Sh::use(it) - 1) & 1));
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       uint64_t* full = kside ? &ctl->k_full[sl] : &ctl->v_full[sl];
-      uint8_t* dst0 = smem + (kside ? L.k + k_half_off(sl, 0) : L.v + v_half_off(sl, 0));
-      uint8_t* dst1 = smem + (kside ? L.k + k_half_off(sl, 1) : L.v + v_half_off(sl, 1));
-      if (lane == 0) mbar_arrive_expect_tx(full, TcLayout::kTileBytes);
+      uint8_t* dst0 = smem + (kside ? L.k + Sh::k_half_off(sl, 0) : L.v + Sh::v_half_off(sl, 0));
+      uint8_t* dst1 = smem + (kside ? L.k + Sh::k_half_off(sl, 1) : L.v + Sh::v_half_off(sl, 1));
+      if (lane == 0) mbar_arrive_expect_tx(full, Sh::kTileBytes);
       if (!p.paged) {
-        if (lane == 0) load_tile(p, c, map, dst0, dst1, full, blk);
+        if (lane == 0) load_tile<HP>(p, c, map, dst0, dst1, full, blk);
       } else {
         __syncwarp();  // the transaction count is armed before any box lands
-        load_tile_paged_lanes(p, c, map, dst0, dst1, full, blk, lane);
+        load_tile_paged_lanes<HP>(p, c, map, dst0, dst1, full, blk, lane);
       }
       ++issued;
       c.advance(p, units_per_req);
@@ -389,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     if (*abort_flag) {
       // never leave with copies into this CTA's shared memory in flight
       if (lane == 0) {
-        drain_ring(kside ? ctl->k_full : ctl->v_full, kside ? kKSlots : kSlots, issued);
+        drain_ring(kside ? ctl->k_full : ctl->v_full, kside ? Sh::kKSlots : Sh::kVSlots, issued);
         for (int u = max(q_issued - kQBufs, 0); u < q_issued; ++u)
           mbar_wait(&ctl->q_full[u % kQBufs], static_cast<uint32_t>((u / kQBufs) & 1));
       }
@@ -406,28 +485,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       bool ok = true;
       for (int k = 0; k < n_tiles;) {
         if (*abort_flag) { ok = false; break; }
-        const bool pair = (k & 1) == 0 && k + 1 < n_tiles && cq.tile != cq.tiles - 1;
+        // HP = 1: two consecutive tiles of one unit as one N = 128 product
+        const bool pair = HP == 1 && (k & 1) == 0 && k + 1 < n_tiles && cq.tile != cq.tiles - 1;
         const int cnt = pair ? 2 : 1;
         const int qb = cq.unit % kQBufs;
         if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full[qb], (cq.unit / kQBufs) & 1)) { ok = false; break; }
         for (int t = k; t < k + cnt && ok; ++t)
-          ok = mbar_wait(&ctl->k_full[t % kKSlots], (t / kKSlots) & 1) &&
-               (t < kSlots || mbar_wait(&ctl->pv_done[t & 1][(t >> 1) & 1], ((t >> 2) - 1) & 1));
+          ok = mbar_wait(&ctl->k_full[t % Sh::kKSlots], (t / Sh::kKSlots) & 1) &&
+               (t < Sh::kVSlots || mbar_wait(&ctl->pv_done[t & 1][Sh::buf(t)], (Sh::use(t) - 1) & 1));
         if (!ok) break;
         tc_fence_after();
         // the descriptors of the 8 K-slices differ only in the start address
         // field (bits 0-13, shared-memory byte address >> 4)
-        const uint64_t kdesc = smem_desc_sw128(sk + k_half_off(k % kKSlots, 0), 16, 1024);
-        const uint32_t dst = tbase + col_s(k & 1, (k >> 1) & 1), idesc = pair ? kIdescS2 : kIdescS1;
+        const uint64_t kdesc = smem_desc_sw128(sk + Sh::k_half_off(k % Sh::kKSlots, 0), 16, 1024);
+        const uint32_t dst = tbase + Sh::col_s(k & 1, Sh::buf(k));
+        const uint32_t idesc = (pair || HP == 2) ? kIdescS2 : kIdescS1;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a_off = ((kk >> 2) * (TcLayout::kQBytes / 2) + (kk & 3) * 32) >> 4;
-          const uint32_t b_off = ((kk >> 2) * (TcLayout::kPairBytes / 2) + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;  // 128-row halves, 16 KB apart
           tc_mma_bf16(dst, qdesc0 + qb * (TcLayout::kQBytes >> 4) + a_off, kdesc + b_off, idesc, kk > 0);
         }
         for (int t = k; t < k + cnt; ++t) {
-          tc_commit(&ctl->s_full[t & 1][(t >> 1) & 1]);
-          tc_commit(&ctl->k_empty[t % kKSlots]);
+          tc_commit(&ctl->s_full[t & 1][Sh::buf(t)]);
+          tc_commit(&ctl->k_empty[t % Sh::kKSlots]);
         }
         if (cq.tile + cnt - 1 == cq.tiles - 1 || k + cnt == n_tiles) tc_commit(&ctl->q_empty[qb]);
         for (int t = 0; t < cnt; ++t) cq.advance(p, units_per_req);
@@ -452,26 +533,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       bool ok = true;
       for (int k = 0; k < n_tiles; ++k) {
         if (*abort_flag) { ok = false; break; }
-        const int w = k & 1, bb = (k >> 1) & 1;
+        const int w = k & 1, bb = Sh::buf(k);
         const int sf = cp.seg_first(k), sl = cp.seg_last(k, n_tiles);
         const bool first_owned = (k - sf) < 2;
-        if (!mbar_wait(&ctl->p_full[w][bb], (k >> 2) & 1) ||
+        if (!mbar_wait(&ctl->p_full[w][bb], Sh::use(k) & 1) ||
             (first_owned && part[w] > 0 && !mbar_wait(&ctl->o_free[w], (part[w] - 1) & 1)) ||
-            !mbar_wait(&ctl->v_full[k % kSlots], (k >> 2) & 1)) {
+            !mbar_wait(&ctl->v_full[k % Sh::kVSlots], (k / Sh::kVSlots) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const bool tree_tile = cp.tile * kBlockN + kBlockN > cp.P;
-        const uint64_t vdesc = smem_desc_sw128(sv + v_half_off(k % kSlots, 0), TcLayout::kTileBytes / 2, 1024);
-        const uint32_t pa = tbase + col_s(w, bb), dst = tbase + col_o(w);
+        const uint64_t vdesc =
+            smem_desc_sw128(sv + Sh::v_half_off(k % Sh::kVSlots, 0), Sh::kTileBytes / 2, 1024);
+        const uint32_t pa = tbase + Sh::col_s(w, bb), dst = tbase + col_o(w);
+        // K = 16 shared-memory rows per instruction (8 keys of both heads when HP = 2)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < 4 * HP; ++kk)
           tc_mma_bf16_ts(dst, pa + 32 * (kk >> 1) + 8 * (kk & 1), vdesc + ((kk * 2048) >> 4), kIdescPV,
                          (first_owned && kk == 0) ? 0u : 1u);
         if (tree_tile) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < 4 * HP; ++kk)
             tc_mma_bf16_ts(dst, pa + 32 * (kk >> 1) + 16 + 8 * (kk & 1), vdesc + ((kk * 2048) >> 4), kIdescPV, 1u);
         }
         tc_commit(&ctl->pv_done[w][bb]);
@@ -521,8 +604,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             wg_sync(wg);
             anc_req = c.b;
           }
-          if (r < p.rows) {
-            ancestor_walk(par, c.n - p.n_query + r / p.group, anc);
+          if (Sh::local_of(r) < p.rows) {
+            ancestor_walk(par, c.n - p.n_query + Sh::local_of(r) / p.group, anc);
           } else {  // padding row: sees no tree key, its output is discarded
 #pragma unroll
             for (int w = 0; w < 4; ++w) anc[w] = 0u;
@@ -530,9 +613,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           m_used = -INFINITY;
           l = 0.f;
         }
-        const int bb = (k >> 1) & 1;
-        const uint32_t sbuf = lane_addr + col_s(wg, bb);
-        if (*abort_flag || !mbar_wait(&ctl->s_full[wg][bb], (k >> 2) & 1)) {
+        const int bb = Sh::buf(k);
+        const uint32_t sbuf = lane_addr + Sh::col_s(wg, bb);
+        if (*abort_flag || !mbar_wait(&ctl->s_full[wg][bb], Sh::use(k) & 1)) {
           report_error(p.err, TS_DEVERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -543,28 +626,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const uint64_t vis = tree_tile ? tile_visibility(anc, key0 - c.P) : ~0ull;
 
         // ---- pass 1: row max over the 64 keys (masked on tiles holding tree
-        //      keys; every key of a prefix tile is visible).  S stays in
-        //      registers for pass 2.
-        uint32_t v0[32], v1[32];
-        tmem_ld32(sbuf, v0);
-        tmem_ld32(sbuf + 32, v1);
-        tmem_ld_wait();
+        //      keys; every key of a prefix tile is visible).  The row's 64
+        //      scores stay in registers for pass 2: HP = 1 reads S columns
+        //      0..63; HP = 2 reads column 2 key + head of this row's head.
+        //      (HP = 2 re-reads S in pass 2 instead, chunk by chunk.)
+        float sv[HP == 1 ? 64 : 1];
         float mx;
         {
           float pm[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
-          if (tree_tile) {
+          if constexpr (HP == 1) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(sbuf, v0);
+            tmem_ld32(sbuf + 32, v1);
+            tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              if ((vis >> e) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v0[e]));
-              if ((vis >> (32 + e)) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v1[e]));
+              sv[e] = __uint_as_float(v0[e]);
+              sv[32 + e] = __uint_as_float(v1[e]);
+            }
+            if (tree_tile) {
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                if ((vis >> e) & 1ull) pm[e & 7] = fmaxf(pm[e & 7], sv[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], sv[e]);
             }
           } else {
+            const int hj = Sh::head_of(r);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+              uint32_t v[32];
+              tmem_ld32(sbuf + 32 * ch, v);
+              tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v0[e]));
-              pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v1[e]));
+              for (int q = 0; q < 16; ++q) {
+                const int e = 16 * ch + q;
+                if (!tree_tile || ((vis >> e) & 1ull))
+                  pm[q & 7] = fmaxf(pm[q & 7], __uint_as_float(hj ? v[2 * q + 1] : v[2 * q]));
+              }
             }
           }
           mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
@@ -582,11 +684,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
 
         // O may be rescaled only once every earlier PV into it is done: the
-        // last one was this warpgroup's previous tile, k - 2, in the other
-        // buffer (a rescale implies a previous tile in this segment)
+        // last one was this warpgroup's previous tile, k - 2 (a rescale
+        // implies a previous tile in this segment)
         const bool need_rescale = __any_sync(0xffffffffu, rescale);
         if (need_rescale) {
-          if (!mbar_wait(&ctl->pv_done[wg][bb ^ 1], ((k - 2) >> 2) & 1)) {
+          if (!mbar_wait(&ctl->pv_done[wg][Sh::buf(k - 2)], Sh::use(k - 2) & 1)) {
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -605,43 +707,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
 
         // ---- pass 2: probabilities 2^(s*scale - m) as bf16 pairs, written over
-        //      the S chunk they came from: for keys 32 j .. 32 j + 31, P in
-        //      columns 32 j .. 32 j + 15 and the rounding residual (tiles
-        //      holding tree keys) in 32 j + 16 .. 32 j + 31.
+        //      the S chunk they came from: the chunk's first 16 columns hold P,
+        //      the other 16 the bf16 rounding residual (tiles holding tree
+        //      keys).  HP = 1: a chunk is keys 32 j .. 32 j + 31, two keys per
+        //      pair.  HP = 2: a chunk is keys 16 j .. 16 j + 15, one key per
+        //      pair (key k's pair is shared-memory rows 2 k, 2 k + 1 of V),
+        //      with the other head's half zero.
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        if (tree_tile) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t* v = h == 0 ? v0 : v1;
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const int e = 2 * q;
-              const float s0 = ((vis >> (32 * h + e)) & 1ull) ? __uint_as_float(v[e]) : -INFINITY;
-              const float s1 = ((vis >> (32 * h + e + 1)) & 1ull) ? __uint_as_float(v[e + 1]) : -INFINITY;
-              const float e0 = ex2_approx(fmaf(s0, p.scale_log2, nbase));
-              const float e1 = ex2_approx(fmaf(s1, p.scale_log2, nbase));
-              ps[q & 3] += e0 + e1;
-              hi[q] = pack_bf16x2(e0, e1);
-              lo[q] = bf16x2_residual(hi[q], e0, e1);
-            }
-            tmem_st16(sbuf + 32 * h, hi);
-            tmem_st16(sbuf + 32 * h + 16, lo);
-          }
+        if constexpr (HP == 1) {
+          if (tree_tile) write_p1<true>(sv, vis, p.scale_log2, nbase, sbuf, ps);
+          else write_p1<false>(sv, vis, p.scale_log2, nbase, sbuf, ps);
         } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t* v = h == 0 ? v0 : v1;
-            uint32_t hi[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const float e0 = ex2_approx(fmaf(__uint_as_float(v[2 * q]), p.scale_log2, nbase));
-              const float e1 = ex2_approx(fmaf(__uint_as_float(v[2 * q + 1]), p.scale_log2, nbase));
-              ps[q & 3] += e0 + e1;
-              hi[q] = pack_bf16x2(e0, e1);
-            }
-            tmem_st16(sbuf + 32 * h, hi);
-          }
+          if (tree_tile) write_p2<true>(vis, p.scale_log2, nbase, Sh::head_of(r), sbuf, ps);
+          else write_p2<false>(vis, p.scale_log2, nbase, Sh::head_of(r), sbuf, ps);
         }
         tmem_st_wait();
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
@@ -649,17 +727,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // 0 * NaN is NaN, so zero them in the V tile before PV reads it
         const int keys = c.P + c.n;
         if (key0 + kBlockN > keys) {
-          const int vslot = k % kSlots;
-          if (!mbar_wait(&ctl->v_full[vslot], (k >> 2) & 1)) {  // the tile has landed
+          const int vslot = k % Sh::kVSlots;
+          if (!mbar_wait(&ctl->v_full[vslot], (k / Sh::kVSlots) & 1)) {  // the tile has landed
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
           }
-          const int first = keys - key0;
-          const int nvec = (kBlockN - first) * 8;
+          // keys first .. 63 are shared-memory rows HP * first .. 64 HP - 1 of each half
+          const int first = HP * (keys - key0);
+          const int nvec = (static_cast<int>(Sh::kHalfRows) - first) * 8;
           for (int h = 0; h < 2; ++h)
             for (int xv = r; xv < nvec; xv += kRowsTc)
-              reinterpret_cast<uint4*>(smem + L.v + v_half_off(vslot, h) + first * 128)[xv] = make_uint4(0, 0, 0, 0);
+              reinterpret_cast<uint4*>(smem + L.v + Sh::v_half_off(vslot, h) + first * 128)[xv] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         tc_fence_before();
@@ -668,7 +747,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
         // ---- this warpgroup's last tile of the segment
         if (last_owned) {
-          if (!mbar_wait(&ctl->pv_done[wg][bb], (k >> 2) & 1)) {
+          if (!mbar_wait(&ctl->pv_done[wg][bb], Sh::use(k) & 1)) {
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -701,9 +780,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             const float Ls = l * a_own + lo_ * a_oth;
             const float inv = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
             const float f_own = a_own * inv, f_oth = a_oth * inv;
-            const int kvh = c.uir;
             const bool complete = c.seg_complete(k, n_tiles);
-            const int i = r / p.group, h = kvh * p.group + r % p.group;
+            // packed row r: head HP * unit + head_of(r), query local_of(r) / G
+            const int loc = Sh::local_of(r);
+            const int i = loc / p.group, h = (HP * c.uir + Sh::head_of(r)) * p.group + loc % p.group;
             const int64_t unit = static_cast<int64_t>(c.b) * units_per_req + c.uir;
             const int64_t slot = static_cast<int64_t>(blockIdx.x) + unit;
             // Each 32-column chunk of this warp's 32 rows goes through shared
@@ -740,9 +820,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {  // 8 rows x 64 bytes per instruction
                   const int rr = it * 8 + (lane >> 2), c4 = lane & 3;
-                  const int row = row0 + rr;
-                  if (row >= p.rows) continue;
-                  const int ii = row / p.group, hh = kvh * p.group + row % p.group;
+                  const int row = row0 + rr, lrow = Sh::local_of(row);
+                  if (lrow >= p.rows) continue;
+                  const int ii = lrow / p.group, hh = (HP * c.uir + Sh::head_of(row)) * p.group + lrow % p.group;
                   const uint4 val = *reinterpret_cast<const uint4*>(stg + sw128(rr, c4));
                   reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(c.b) * p.n_query + ii) * p.hq + hh) * 128 +
                                            ch * 32)[c4] = val;
@@ -770,7 +850,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               if (other_in) mbar_arrive(&ctl->o_free[oth]);
             }
             const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
-            if (r < p.rows) {
+            if (loc < p.rows) {
               if (complete) {
                 if (p.lse != nullptr)
                   p.lse[(static_cast<int64_t>(c.b) * p.hq + h) * p.n_query + i] = lse2 * 0.69314718055994530942f;
@@ -812,9 +892,10 @@ int attn_tc_occupancy(int stages, int num_req) {
   int nb = 0;
   const size_t smem = attn_tc_smem_bytes(stages, num_req);
   if (smem > static_cast<size_t>(optin)) return 0;
-  if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+  if (cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_tc_kernel, kTcThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_tc_kernel<1>, kTcThreads, smem) != cudaSuccess) return 0;
   return nb;
 }
 
@@ -823,7 +904,9 @@ int attn_tc_occupancy(int stages, int num_req) {
 cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& pmap,
                            const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = attn_tc_smem_bytes(p.stages, p.num_req);
-  return launch_pdl(attn_tc_kernel, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, pmap, qmap, p);
+  if (p.hp == 2)
+    return launch_pdl(attn_tc_kernel<2>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, pmap, qmap, p);
+  return launch_pdl(attn_tc_kernel<1>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, pmap, qmap, p);
 }
 
 }  // namespace ts

@@ -40,6 +40,7 @@ constexpr size_t kWsHeader = 256;  // error word + padding at the start of every
 struct AttnParams {
   int num_req, hq, hkv, group, head_dim, n_query, n_tree_max;
   int rows;          // R = G * n_query packed rows per KV head
+  int hp;            // KV heads per unit: 2 when the tcgen05 kernel packs two heads (R <= 64), else 1
   int row_groups;    // ceil(R / 128)
   int rows_pad;      // rows per unit rounded up to 16 (<= 128)
   int max_kv_len;

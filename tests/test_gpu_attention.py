@@ -56,7 +56,8 @@ TC = [
 ]
 
 
-# R < 128: the tcgen05 kernel pads the packed rows to one 128-row tile
+# R < 128: the tcgen05 kernel pads the packed rows to one 128-row tile; with
+# R <= 64 and an even KV-head count two adjacent heads share the tile
 TC_SMALL_R = [
     dict(num_req=4, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(60, 700), chain=True),          # R = 40
     dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=40, n_query=8, prefix_range=(100, 400)),         # R = 32
@@ -64,6 +65,9 @@ TC_SMALL_R = [
     dict(num_req=2, hq=2, hkv=2, d=128, n_tree_max=6, n_query=1, prefix_range=(0, 260)),             # R = 1
     dict(num_req=2, hq=16, hkv=4, d=128, n_tree_max=30, n_query=25, prefix_range=(0, 200)),          # R = 100
     dict(num_req=1, hq=127, hkv=1, d=128, n_tree_max=9, n_query=1, prefix_range=(30, 90)),           # R = 127
+    dict(num_req=2, hq=3, hkv=3, d=128, n_tree_max=12, n_query=8, prefix_range=(0, 300)),            # R = 8, odd Hkv
+    dict(num_req=2, hq=32, hkv=16, d=128, n_tree_max=40, n_query=32, ragged_tree=True,
+         prefix_range=(0, 400)),                                                                   # R = 64
 ]
 
 
