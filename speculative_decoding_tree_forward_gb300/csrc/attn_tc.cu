@@ -73,11 +73,16 @@ __host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
 // pair.  HP = 2 (packed rows R <= 64, two adjacent KV heads share one CTA):
 // a tile is 64 keys of both heads, loaded as one TMA box per page-half (keys
 // interleaved by head: shared-memory row 2 key + head); each warpgroup has one
-// 128-column S/P buffer; K lives in three 32 KB slots and V in two.
+// 128-column S/P buffer; K lives in two 32 KB slots and V in three (a V slot
+// is then released by its own barrier rather than with its S/P buffer, and
+// the extra slot lets V loads run further ahead of the PVs that need them).
 template <int HP>
 struct TcShape {
-  static constexpr int kKSlots = HP == 1 ? 6 : 3;
-  static constexpr int kVSlots = HP == 1 ? 4 : 2;     // = S/P buffers in all: slot of tile k is k % kVSlots
+  static constexpr int kKSlots = HP == 1 ? 6 : 2;
+  static constexpr int kVSlots = HP == 1 ? 4 : 3;     // slot of tile k is k % kVSlots
+  static constexpr bool kVTied = HP == 1;             // V slot k % 4 = the S/P buffer of tile k
+  static constexpr int kSBufs = HP == 1 ? 4 : 2;      // S/P buffers in all: tile k reuses tile k - kSBufs's
+  static constexpr uint32_t kKBytes = HP == 1 ? 6u * 16384u : 2u * 32768u;
   static constexpr uint32_t kTileBytes = 64u * 128u * 2u * HP;  // one K or V tile (two 64-column halves)
   static constexpr uint32_t kHalfRows = 64u * HP;    // shared-memory rows of one half of a tile
   __device__ static uint32_t col_s(int w, int b) { return HP == 1 ? 128u * b + 64u * w : 128u * w; }
@@ -102,12 +107,11 @@ struct TcLayout {
   uint32_t q, k, v, ctrl, par, xch, cum, stg, total;
   static constexpr uint32_t kStgWarpBytes = 32 * 128;  // 32 rows x 128 bytes, 128-byte swizzle
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
-  static constexpr uint32_t kKBytes = 96 * 1024;       // K ring (same bytes for HP = 1 and 2)
-  static constexpr uint32_t kVBytes = 64 * 1024;       // V ring
+  static constexpr uint32_t kKVBytes = 160 * 1024;     // K ring + V ring (split per HP)
 };
 
 struct TcCtrl {
-  uint64_t k_full[kMaxKSlots], k_empty[kMaxKSlots], v_full[kMaxVSlots];
+  uint64_t k_full[kMaxKSlots], k_empty[kMaxKSlots], v_full[kMaxVSlots], v_empty[kMaxVSlots];
   uint64_t q_full[kQBufs], q_empty[kQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
   uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
@@ -116,12 +120,13 @@ struct TcCtrl {
   int abort;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int num_req) {
+// k_bytes: the K ring's share of the K/V region (TcShape<HP>::kKBytes)
+__host__ __device__ inline TcLayout tc_layout(int num_req, uint32_t k_bytes = 6u * 16384u) {
   TcLayout L;
   L.q = 0;
   L.k = L.q + kQBufs * TcLayout::kQBytes;
-  L.v = L.k + TcLayout::kKBytes;
-  L.ctrl = L.v + TcLayout::kVBytes;
+  L.v = L.k + k_bytes;
+  L.ctrl = L.k + TcLayout::kKVBytes;
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TcLayout L = tc_layout(p.num_req);
+  const TcLayout L = tc_layout(p.num_req, TcShape<HP>::kKBytes);
   TcCtrl* ctl = reinterpret_cast<TcCtrl*>(smem + L.ctrl);
   int64_t* cum = reinterpret_cast<int64_t*>(smem + L.cum);
   volatile int* abort_flag = &ctl->abort;
@@ -347,7 +352,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 1);
     }
-    for (int s = 0; s < Sh::kVSlots; ++s) mbar_init(&ctl->v_full[s], 1);
+    for (int s = 0; s < Sh::kVSlots; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
+    }
     for (int i = 0; i < kQBufs; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
@@ -439,10 +447,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       }
       const int sl = kside ? it % Sh::kKSlots : it % Sh::kVSlots, w = it & 1, bb = Sh::buf(it);
       // a K slot is free once the S that read it is computed, a V slot once
-      // the PV of the previous tile in the same S/P buffer is done
+      // the PV that read it is done (HP = 1: the PV of the previous tile in
+      // the same S/P buffer)
       if (lane == 0)
         ok = kside ? (it < Sh::kKSlots || mbar_wait(&ctl->k_empty[sl], ((it / Sh::kKSlots) - 1) & 1))
-                   : (it < Sh::kVSlots || mbar_wait(&ctl->pv_done[w][bb], (Sh::use(it) - 1) & 1));
+                   : (it < Sh::kVSlots || (Sh::kVTied ? mbar_wait(&ctl->pv_done[w][bb], (Sh::use(it) - 1) & 1)
+                                                      : mbar_wait(&ctl->v_empty[sl], ((it / Sh::kVSlots) - 1) & 1)));
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       uint64_t* full = kside ? &ctl->k_full[sl] : &ctl->v_full[sl];
@@ -492,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full[qb], (cq.unit / kQBufs) & 1)) { ok = false; break; }
         for (int t = k; t < k + cnt && ok; ++t)
           ok = mbar_wait(&ctl->k_full[t % Sh::kKSlots], (t / Sh::kKSlots) & 1) &&
-               (t < Sh::kVSlots || mbar_wait(&ctl->pv_done[t & 1][Sh::buf(t)], (Sh::use(t) - 1) & 1));
+               (t < Sh::kSBufs || mbar_wait(&ctl->pv_done[t & 1][Sh::buf(t)], (Sh::use(t) - 1) & 1));
         if (!ok) break;
         tc_fence_after();
         // the descriptors of the 8 K-slices differ only in the start address
@@ -558,6 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tc_mma_bf16_ts(dst, pa + 32 * (kk >> 1) + 16 + 8 * (kk & 1), vdesc + ((kk * 2048) >> 4), kIdescPV, 1u);
         }
         tc_commit(&ctl->pv_done[w][bb]);
+        if (!Sh::kVTied) tc_commit(&ctl->v_empty[k % Sh::kVSlots]);
         if (k == sl) {  // segment ends: both warpgroups' participation counts
           ++part[sl & 1];
           if (sl > sf) ++part[(sl & 1) ^ 1];
