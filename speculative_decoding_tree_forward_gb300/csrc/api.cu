@@ -325,6 +325,10 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.max_blocks = p.paged ? a->max_blocks_per_req : 0;
   p.num_blocks = p.paged ? a->num_blocks : 0;
   p.num_ctas = pl.num_ctas;
+  // a segment's epilogue (and the refill after it) costs about 4 tiles of
+  // time; a sweep of E = 1..8 on the verify and paged chain workloads
+  // measured the best totals at E = 4..6
+  p.seg_cost = pl.use_tc ? 4 : 0;
   p.stages = pl.stages;
   p.num_units = pl.units;
   p.prefix_len = a->prefix_len;

@@ -56,16 +56,28 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   attn_lengths(p, b, P, n, false);
   const int tiles = attn_tiles(P + n);
   const int64_t first = before + static_cast<int64_t>(uir) * tiles;
-  const int c_lo = sched_cta_of(first, T, p.num_ctas);
-  const int c_hi = sched_cta_of(first + tiles - 1, T, p.num_ctas);
+  // CTAs holding the unit's first and last tile (plain or cost-weighted split)
+  const int E = p.seg_cost;
+  const int64_t W = T + static_cast<int64_t>(E) * units_per_req * p.num_req;
+  const int64_t pf = before + static_cast<int64_t>(E) * units_per_req * b + static_cast<int64_t>(uir) * (tiles + E);
+  const int c_lo = E > 0 ? wsched_cta_of_pos(pf, W, p.num_ctas) : sched_cta_of(first, T, p.num_ctas);
+  const int c_hi = E > 0 ? wsched_cta_of_pos(pf + (tiles >= 2 ? E + tiles - 1 : 0), W, p.num_ctas)
+                         : sched_cta_of(first + tiles - 1, T, p.num_ctas);
   if (c_lo == c_hi) return;  // one CTA held the whole unit and wrote it
+  // does CTA c (c_lo <= c <= c_hi) hold a tile of this unit, i.e. a partial?
+  auto holds = [&](int c) -> bool {
+    if (E == 0) return slot_nonempty(c, T, p.num_ctas);
+    if (c == c_lo) return true;
+    const int j = wsched_tile_in_unit(wsched_x(c, W, p.num_ctas) - pf, E, tiles);
+    return j < tiles && wsched_cta_of_pos(pf + E + j, W, p.num_ctas) == c;
+  };
 
   // slot of CTA c: c + unit; its lse at part_lse[slot * rows_pad + row]
   const float* lse_col = p.part_lse + unit * p.rows_pad + rl;
   float mx = -INFINITY;
   for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
     const int c = c0 + lane;
-    if (c <= c_hi && slot_nonempty(c, T, p.num_ctas))
+    if (c <= c_hi && holds(c))
       mx = fmaxf(mx, __ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad));
   }
 #pragma unroll
@@ -78,7 +90,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   float wsum = 0.f;
   for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
     const int c = c0 + lane;
-    const bool valid = c <= c_hi && slot_nonempty(c, T, p.num_ctas);
+    const bool valid = c <= c_hi && holds(c);
     const float wl = valid ? exp2f(__ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad) - mbase) : 0.f;
     wsum += wl;
     unsigned mask = __ballot_sync(0xffffffffu, valid);

@@ -310,6 +310,30 @@ __device__ __forceinline__ void write_p2(uint64_t vis, float scale_log2, float n
   }
 }
 
+// First tile of CTA c under the cost-weighted split (common.cuh): cum[b] =
+// tiles before request b (every unit of request b has (cum[b + 1] - cum[b]) /
+// upr tiles), E = the weight a unit's first tile carries beyond 1.
+__device__ __forceinline__ int64_t wsched_begin(int c, const int64_t* cum, int num_req, int upr, int E, int64_t T,
+                                                int NC) {
+  const int64_t W = T + static_cast<int64_t>(E) * upr * num_req;
+  const int64_t x = wsched_x(c, W, NC);
+  if (x >= W) return T;
+  int lo = 0, hi = num_req - 1;  // the request whose weighted range holds x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (cum[mid] + static_cast<int64_t>(E) * upr * mid <= x) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int tiles = static_cast<int>((cum[b + 1] - cum[b]) / upr);
+  const int64_t span = tiles + E;
+  if (span <= 0) return cum[b + 1];
+  const int64_t off = x - (cum[b] + static_cast<int64_t>(E) * upr * b);
+  const int uir = static_cast<int>(off / span);
+  if (uir >= upr) return cum[b + 1];
+  const int j = wsched_tile_in_unit(off - uir * span, E, tiles);
+  return cum[b] + static_cast<int64_t>(uir) * tiles + j;
+}
+
 // Waits (bounded) for the last copy issued into each slot of a ring.
 __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued) {
   for (int st = 0; st < slots && st < issued; ++st) {
@@ -379,8 +403,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     for (int b = 0; b < p.num_req; ++b) cum[b + 1] += cum[b];
   __syncthreads();
   const int64_t T = cum[p.num_req];
-  const int64_t t_begin = sched_begin(blockIdx.x, T, p.num_ctas);
-  const int64_t t_end = sched_begin(blockIdx.x + 1, T, p.num_ctas);
+  const int64_t t_begin = wsched_begin(blockIdx.x, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
+  const int64_t t_end = wsched_begin(blockIdx.x + 1, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
   if (t_begin >= t_end) return;
   const int n_tiles = static_cast<int>(t_end - t_begin);
   int b0 = 0;

@@ -258,4 +258,24 @@ __host__ __device__ __forceinline__ int sched_cta_of(int64_t t, int64_t T, int N
   return static_cast<int>(((t + 1) * NC + T - 1) / T - 1);
 }
 
+// Cost-weighted split (the tcgen05 path).  The tile sequence is laid on a
+// weighted line: the first tile of every unit weighs 1 + E, the others 1 (a
+// unit segment ends in an epilogue that costs about E tiles of time, so a CTA
+// whose range crosses unit boundaries should take fewer tiles).  With
+// pos(t) = the weight before tile t and W = T + E * units, CTA c takes the
+// tiles whose pos lies in [ceil(c W / NC), ceil((c + 1) W / NC)), i.e. the
+// CTA of tile t is floor(pos(t) NC / W).  A unit of `tiles` tiles starting at
+// weighted position pf: tile 0 at pf, tile j >= 1 at pf + E + j.
+__host__ __device__ __forceinline__ int64_t wsched_x(int c, int64_t W, int NC) {
+  return (static_cast<int64_t>(c) * W + NC - 1) / NC;
+}
+// first tile (0 .. tiles, tiles meaning "past the unit") with pos >= pf + r
+__host__ __device__ __forceinline__ int wsched_tile_in_unit(int64_t r, int E, int tiles) {
+  const int j = r <= 0 ? 0 : (r <= E + 1 ? 1 : static_cast<int>(r - E));
+  return j < tiles ? j : tiles;
+}
+__host__ __device__ __forceinline__ int wsched_cta_of_pos(int64_t pos, int64_t W, int NC) {
+  return static_cast<int>((pos * NC) / W);
+}
+
 }  // namespace ts

@@ -46,6 +46,7 @@ struct AttnParams {
   int max_kv_len;
   int paged, page_size, max_blocks, num_blocks;
   int num_ctas;      // NC
+  int seg_cost;      // E of the cost-weighted split (tcgen05 path, > 0); 0 = plain split of the tiles
   int stages;
   int64_t num_units; // num_req * hkv * row_groups
   const int32_t* prefix_len;
