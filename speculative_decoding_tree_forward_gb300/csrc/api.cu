@@ -88,7 +88,7 @@ struct AttnPlan {
   bool use_tc;
   int rows, row_groups, rows_pad, group, stages, num_ctas, hp;
   int64_t units, slots;
-  size_t ws_bytes, off_o, off_lse;
+  size_t ws_bytes, off_cum, off_o, off_lse;
 };
 
 ts_status validate_attn(const ts_attn_args* a) {
@@ -168,7 +168,8 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
     pl->num_ctas = static_cast<int>(nc < 1 ? 1 : nc);
   }
   pl->slots = pl->num_ctas + pl->units;
-  pl->off_o = kWsHeader;
+  pl->off_cum = kWsHeader;
+  pl->off_o = pl->off_cum + align256(static_cast<size_t>(a->num_requests + 1) * sizeof(int64_t));
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
   pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
   return TS_OK;
@@ -234,7 +235,7 @@ bool encode_partial_map(CUtensorMap* map, float* part_o, int64_t rows) {
 size_t attn_zero_prefix_bytes(const ts_attn_args* a) {
   AttnPlan pl;
   if (plan_attn(a, &pl) != TS_OK) return 0;
-  return pl.off_o;
+  return kWsHeader;
 }
 
 }  // namespace ts
@@ -343,6 +344,7 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(static_cast<float>(a->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = reinterpret_cast<unsigned*>(ws);
+  p.cum_out = reinterpret_cast<int64_t*>(ws + pl.off_cum);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

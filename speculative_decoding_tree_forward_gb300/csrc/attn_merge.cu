@@ -7,22 +7,27 @@
 //   O = sum_s 2^(lse_s - lse) O_s,   lse = log2 sum_s 2^lse_s,
 // skipping CTAs whose tile range was empty, and writes the bf16 output and
 // the natural-log lse.  Units held by one CTA were written directly by the
-// attention kernel and are skipped here.  One warp per output row: the lanes
-// find the row's non-empty slots with a ballot and each lane owns four
-// columns, so a slot's partial row is one coalesced 512-byte read and up to
-// four slots are in flight per lane; no block-wide synchronisation.
+// attention kernel and are skipped here.  One warp per output row, eight rows
+// per CTA: the split comes from the tile prefix the attention kernel's CTA 0
+// left in the workspace (three loads), and each lane owns four columns.  The
+// lse of the row's first 32 shares (one per lane) and its first four partial
+// rows (coalesced 512-byte reads) are all requested before the weights are
+// known, so a typical row costs one dependent round trip to L2; shares of
+// CTAs that hold no tile of the unit get weight 0.
 #include "attn_common.cuh"
 
 namespace ts {
 namespace {
 
-constexpr int kMergeWarps = 4;  // rows per CTA
+constexpr int kMergeWarps = 8;  // rows per CTA
+constexpr int kPrefetchSlots = 4;  // partial rows loaded before the weights are known
 
 __device__ __forceinline__ bool slot_nonempty(int c, int64_t T, int nc) {
   return sched_begin(c, T, nc) < sched_begin(c + 1, T, nc);
 }
 
-__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
+// at most 64 registers: four CTAs (32 warps) per SM, so the grid lands in one wave
+__global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const AttnParams p) {
   pdl_wait();
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -30,31 +35,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   // a unit is (request, group of hp KV heads, row group); with hp = 2 the
   // unit's rows are two heads' R <= 64 rows at 0 and 64
   const int units_per_req = (p.hkv / p.hp) * p.row_groups;
-  const int b = static_cast<int>(unit / units_per_req);
-  const int uir = static_cast<int>(unit % units_per_req);
+  const int b = static_cast<int>(blockIdx.x) / units_per_req;
+  const int uir = static_cast<int>(blockIdx.x) % units_per_req;
   const int kvh = uir / p.row_groups;  // head group
   const int rg = uir % p.row_groups;
   const int rl = blockIdx.y * kMergeWarps + warp;
   const int hj = p.hp == 2 ? rl >> 6 : 0, loc = p.hp == 2 ? rl & 63 : rl;
   if (p.hp == 2 ? loc >= p.rows : rl >= min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit)) return;
-  // tiles before this unit and in total (same clamped lengths as the attention kernels)
-  long long before = 0, total = 0;
-  for (int bb = lane; bb < p.num_req; bb += 32) {
-    int P, n;
-    attn_lengths(p, bb, P, n, false);
-    const long long tl = static_cast<long long>(attn_tiles(P + n)) * units_per_req;
-    total += tl;
-    if (bb < b) before += tl;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    total += __shfl_xor_sync(0xffffffffu, total, o);
-  }
-  const int64_t T = total;
-  int P, n;
-  attn_lengths(p, b, P, n, false);
-  const int tiles = attn_tiles(P + n);
+  // the split as the attention kernel laid it out (its CTA 0 wrote the tile
+  // prefix over requests)
+  const int64_t before = __ldcg(p.cum_out + b);
+  const int64_t T = __ldcg(p.cum_out + p.num_req);
+  const int tiles = static_cast<int>(__ldcg(p.cum_out + b + 1) - before) / units_per_req;  // < 2^31 per request
   const int64_t first = before + static_cast<int64_t>(uir) * tiles;
   // CTAs holding the unit's first and last tile (plain or cost-weighted split)
   const int E = p.seg_cost;
@@ -74,50 +66,72 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
 
   // slot of CTA c: c + unit; its lse at part_lse[slot * rows_pad + row]
   const float* lse_col = p.part_lse + unit * p.rows_pad + rl;
-  float mx = -INFINITY;
-  for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
+  const int D = p.head_dim;
+  const bool active = lane * 4 < D;
+  const int ncs = c_hi - c_lo + 1;
+  auto part_row = [&](int c) {
+    return reinterpret_cast<const float4*>(p.part_o + ((static_cast<int64_t>(c) + unit) * p.rows_pad + rl) * D +
+                                           lane * 4);
+  };
+  // one round trip: the lse of the first 32 slots (one per lane) and the
+  // partial rows of the first kPrefetchSlots slots, all issued before the
+  // weights are known (slots of CTAs without a share get weight 0)
+  float lse_l = -INFINITY;
+  if (lane < ncs) lse_l = __ldcg(lse_col + static_cast<int64_t>(c_lo + lane) * p.rows_pad);
+  float4 x[kPrefetchSlots];
+#pragma unroll
+  for (int q = 0; q < kPrefetchSlots; ++q) {
+    x[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (q < ncs && active) x[q] = __ldcg(part_row(c_lo + q));
+  }
+  bool valid_l = lane < ncs && holds(c_lo + lane);
+  float mx = valid_l ? lse_l : -INFINITY;
+  for (int c0 = c_lo + 32; c0 <= c_hi; c0 += 32) {  // more than 32 shares: rare
     const int c = c0 + lane;
-    if (c <= c_hi && holds(c))
-      mx = fmaxf(mx, __ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad));
+    if (c <= c_hi && holds(c)) mx = fmaxf(mx, __ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   const float mbase = (mx == -INFINITY) ? 0.f : mx;
 
-  const int D = p.head_dim;
-  const bool active = lane * 4 < D;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
+  float wl = valid_l ? exp2f(lse_l - mbase) : 0.f;
+  float wsum = wl;
+#pragma unroll
+  for (int q = 0; q < kPrefetchSlots; ++q) {
+    const float wq = __shfl_sync(0xffffffffu, wl, q);
+    acc.x += wq * x[q].x;
+    acc.y += wq * x[q].y;
+    acc.z += wq * x[q].z;
+    acc.w += wq * x[q].w;
+  }
+  // slots kPrefetchSlots .. 31 of the first chunk, then further chunks of 32
   for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
-    const int c = c0 + lane;
-    const bool valid = c <= c_hi && holds(c);
-    const float wl = valid ? exp2f(__ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad) - mbase) : 0.f;
-    wsum += wl;
-    unsigned mask = __ballot_sync(0xffffffffu, valid);
-    while (mask != 0u) {  // warp-uniform
-      int j[4];
+    float wc = wl;
+    if (c0 != c_lo) {
+      const int c = c0 + lane;
+      const bool v = c <= c_hi && holds(c);
+      wc = v ? exp2f(__ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad) - mbase) : 0.f;
+      wsum += wc;
+    }
+    const int q0 = c0 == c_lo ? kPrefetchSlots : 0;
+    for (int q = q0; q < 32 && c0 + q <= c_hi; q += 4) {  // warp-uniform bounds
+      float w4[4];
+      float4 y[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        j[q] = mask != 0u ? __ffs(mask) - 1 : -1;
-        if (mask != 0u) mask &= mask - 1u;
-      }
-      float w[4];
-      float4 x[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        w[q] = __shfl_sync(0xffffffffu, wl, j[q] < 0 ? 0 : j[q]);
-        x[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j[q] >= 0 && active)
-          x[q] = __ldcg(reinterpret_cast<const float4*>(
-              p.part_o + ((static_cast<int64_t>(c0 + j[q]) + unit) * p.rows_pad + rl) * D + lane * 4));
+      for (int u = 0; u < 4; ++u) {
+        const bool in = q + u < 32 && c0 + q + u <= c_hi;
+        w4[u] = __shfl_sync(0xffffffffu, wc, in ? q + u : 0);
+        if (!in) w4[u] = 0.f;
+        y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in && w4[u] != 0.f && active) y[u] = __ldcg(part_row(c0 + q + u));
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float wq = j[q] >= 0 ? w[q] : 0.f;
-        acc.x += wq * x[q].x;
-        acc.y += wq * x[q].y;
-        acc.z += wq * x[q].z;
-        acc.w += wq * x[q].w;
+      for (int u = 0; u < 4; ++u) {
+        acc.x += w4[u] * y[u].x;
+        acc.y += w4[u] * y[u].y;
+        acc.z += w4[u] * y[u].z;
+        acc.w += w4[u] * y[u].w;
       }
     }
   }

@@ -206,13 +206,14 @@ __device__ __forceinline__ void tile_pages(const AttnParams& p, const Cursor& c,
 // the TMA unit.
 template <int HP>
 __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, const CUtensorMap* map, uint8_t* dst0,
-                                          uint8_t* dst1, uint64_t* bar, const int (&blk)[kMaxPagesPerTile]) {
+                                          uint8_t* dst1, uint64_t* bar, const int (&blk)[kMaxPagesPerTile],
+                                          uint64_t pol) {
   const int kvh = HP * c.uir;  // first KV head of the unit (the box covers HP heads)
   const int key0 = c.tile * kBlockN;
   if (!p.paged) {
     const int row = c.b * p.max_kv_len + key0;
-    tma_load_3d(dst0, map, 0, kvh, row, bar);
-    tma_load_3d(dst1, map, 64, kvh, row, bar);
+    tma_load_3d_hint(dst0, map, 0, kvh, row, bar, pol);
+    tma_load_3d_hint(dst1, map, 64, kvh, row, bar, pol);
     return;
   }
   const int pages = kBlockN / p.page_size;
@@ -227,8 +228,8 @@ __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, 
       else report_error(p.err, TS_DEVERR_BAD_BLOCK);
     }
     const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u * HP;
-    tma_load_3d(dst0 + off, map, 0, kvh, row, bar);
-    tma_load_3d(dst1 + off, map, 64, kvh, row, bar);
+    tma_load_3d_hint(dst0 + off, map, 0, kvh, row, bar, pol);
+    tma_load_3d_hint(dst1 + off, map, 64, kvh, row, bar, pol);
   }
 }
 
@@ -237,7 +238,7 @@ __device__ __forceinline__ void load_tile(const AttnParams& p, const Cursor& c, 
 template <int HP>
 __device__ __forceinline__ void load_tile_paged_lanes(const AttnParams& p, const Cursor& c, const CUtensorMap* map,
                                                       uint8_t* dst0, uint8_t* dst1, uint64_t* bar,
-                                                      const int (&blk)[kMaxPagesPerTile], int lane) {
+                                                      const int (&blk)[kMaxPagesPerTile], int lane, uint64_t pol) {
   const int pages = kBlockN / p.page_size;
   if (lane >= 2 * pages) return;
   const int pg = lane >> 1, h = lane & 1;
@@ -252,7 +253,7 @@ __device__ __forceinline__ void load_tile_paged_lanes(const AttnParams& p, const
     else report_error(p.err, TS_DEVERR_BAD_BLOCK);
   }
   const uint32_t off = static_cast<uint32_t>(pg * p.page_size) * 128u * HP;
-  tma_load_3d((h == 0 ? dst0 : dst1) + off, map, h * 64, kvh, row, bar);
+  tma_load_3d_hint((h == 0 ? dst0 : dst1) + off, map, h * 64, kvh, row, bar, pol);
 }
 
 // Pass 2 of the softmax for one row: P = 2^(s * scale_log2 + nbase) (keys
@@ -399,8 +400,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0)
+  if (tid == 0) {
     for (int b = 0; b < p.num_req; ++b) cum[b + 1] += cum[b];
+    if (blockIdx.x == 0)  // the merge kernel reads the split from here
+      for (int b = 0; b <= p.num_req; ++b) p.cum_out[b] = cum[b];
+  }
   __syncthreads();
   const int64_t T = cum[p.num_req];
   const int64_t t_begin = wsched_begin(blockIdx.x, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
@@ -449,6 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     c.start(p, b0, local0);
     int issued = 0, q_issued = 0;
     int blk[kMaxPagesPerTile];
+    const uint64_t kv_policy = l2_policy_evict_first();  // K/V rows are read once
     if (p.paged) tile_pages(p, c, blk);
     bool ok = true;
     for (int it = 0; it < n_tiles; ++it) {
@@ -484,10 +489,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       uint8_t* dst1 = smem + (kside ? L.k + Sh::k_half_off(sl, 1) : L.v + Sh::v_half_off(sl, 1));
       if (lane == 0) mbar_arrive_expect_tx(full, Sh::kTileBytes);
       if (!p.paged) {
-        if (lane == 0) load_tile<HP>(p, c, map, dst0, dst1, full, blk);
+        if (lane == 0) load_tile<HP>(p, c, map, dst0, dst1, full, blk, kv_policy);
       } else {
         __syncwarp();  // the transaction count is armed before any box lands
-        load_tile_paged_lanes<HP>(p, c, map, dst0, dst1, full, blk, lane);
+        load_tile_paged_lanes<HP>(p, c, map, dst0, dst1, full, blk, lane, kv_policy);
       }
       ++issued;
       c.advance(p, units_per_req);

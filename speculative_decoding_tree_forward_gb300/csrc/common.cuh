@@ -138,6 +138,22 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// L2 policy for data read exactly once (streamed K/V): evicted first, so it
+// does not push out data that is read again soon (the split partials).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -266,8 +282,12 @@ __host__ __device__ __forceinline__ int sched_cta_of(int64_t t, int64_t T, int N
 // tiles whose pos lies in [ceil(c W / NC), ceil((c + 1) W / NC)), i.e. the
 // CTA of tile t is floor(pos(t) NC / W).  A unit of `tiles` tiles starting at
 // weighted position pf: tile 0 at pf, tile j >= 1 at pf + E + j.
+// (32-bit division when the operands fit: 64-bit division is a long
+// software sequence on the GPU; the results are identical.)
 __host__ __device__ __forceinline__ int64_t wsched_x(int c, int64_t W, int NC) {
-  return (static_cast<int64_t>(c) * W + NC - 1) / NC;
+  const int64_t num = static_cast<int64_t>(c) * W + NC - 1;
+  if (num < (1ll << 31)) return static_cast<int64_t>(static_cast<uint32_t>(num) / static_cast<uint32_t>(NC));
+  return num / NC;
 }
 // first tile (0 .. tiles, tiles meaning "past the unit") with pos >= pf + r
 __host__ __device__ __forceinline__ int wsched_tile_in_unit(int64_t r, int E, int tiles) {
@@ -275,7 +295,10 @@ __host__ __device__ __forceinline__ int wsched_tile_in_unit(int64_t r, int E, in
   return j < tiles ? j : tiles;
 }
 __host__ __device__ __forceinline__ int wsched_cta_of_pos(int64_t pos, int64_t W, int NC) {
-  return static_cast<int>((pos * NC) / W);
+  const int64_t num = pos * NC;
+  if (num < (1ll << 31) && W < (1ll << 31))
+    return static_cast<int>(static_cast<uint32_t>(num) / static_cast<uint32_t>(W));
+  return static_cast<int>(num / W);
 }
 
 }  // namespace ts

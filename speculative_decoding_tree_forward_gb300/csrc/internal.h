@@ -60,6 +60,7 @@ struct AttnParams {
   float* lse;
   float scale_log2;  // softmax scale * log2(e)
   unsigned* err;     // workspace error word
+  int64_t* cum_out;  // [num_req + 1] tiles before each request, written by CTA 0 for the merge
   float* part_o;     // [slots][rows_pad][head_dim]
   float* part_lse;   // [slots][rows_pad] (log2 domain)
 };
