@@ -215,8 +215,14 @@ TS_API ts_status tree_accept_greedy(const ts_accept_args* args, void* workspace,
  *   new_prefix_len = P + |path|, new_n_tree = |survivors|,
  *   new_parent[j] = -1 if the survivor's parent is the last matched node,
  *   else that parent's new index; new_tokens[j] = tokens of survivor j.
- *   new_parent / new_tokens may alias parent / tokens (in-place update);
+ *   new_prefix_len / new_n_tree / new_parent / new_tokens may alias
+ *   prefix_len / n_tree / parent / tokens (in-place update);
  *   src_rows (optional) gets src (entries beyond |src| set to -1).
+ * One kernel launch: every CTA of a request derives the re-root from the
+ * request's tree and moves its share of the (layer, K|V) rows; the new
+ * metadata is written by the request's last CTA to have read the old, found
+ * with a per-request ticket counter in the workspace (zero before the first
+ * call, left at zero by every call).  num_requests <= 65535.
  * Layers: k_layers / v_layers are device arrays of num_layers device
  * pointers, each one layer's cache in the given layout; the paged block
  * table is shared by all layers.  A row is num_kv_heads * head_dim *

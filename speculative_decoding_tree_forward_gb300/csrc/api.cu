@@ -3,6 +3,7 @@
 // and launches its kernels asynchronously on the caller's stream.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -88,7 +89,7 @@ struct AttnPlan {
   bool use_tc;
   int rows, row_groups, rows_pad, group, stages, num_ctas, hp;
   int64_t units, slots;
-  size_t ws_bytes, off_cum, off_o, off_lse;
+  size_t ws_bytes, off_o, off_lse;
 };
 
 ts_status validate_attn(const ts_attn_args* a) {
@@ -168,8 +169,7 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
     pl->num_ctas = static_cast<int>(nc < 1 ? 1 : nc);
   }
   pl->slots = pl->num_ctas + pl->units;
-  pl->off_cum = kWsHeader;
-  pl->off_o = pl->off_cum + align256(static_cast<size_t>(a->num_requests + 1) * sizeof(int64_t));
+  pl->off_o = kWsHeader;
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
   pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
   return TS_OK;
@@ -344,7 +344,6 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt(static_cast<float>(a->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = reinterpret_cast<unsigned*>(ws);
-  p.cum_out = reinterpret_cast<int64_t*>(ws + pl.off_cum);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -414,14 +413,14 @@ ts_status tree_accept_greedy(const ts_accept_args* a, void* workspace, size_t wo
 // ------------------------------------------------------------------ compaction
 size_t tree_compact_workspace_size(const ts_compact_args* a) {
   if (a == nullptr || a->num_requests < 1) return 0;
-  return kWsHeader + align256(static_cast<size_t>(a->num_requests) * kPlanStride * sizeof(int32_t));
+  return kWsHeader + align256(static_cast<size_t>(a->num_requests) * sizeof(unsigned));
 }
 
 ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t workspace_bytes, void* stream) {
   if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->m_max < 0 || a->num_layers < 1 ||
       a->num_kv_heads < 1 || a->head_dim < 1 || a->elem_bytes < 1)
     return TS_ERR_INVALID_ARG;
-  if (a->n_tree_max > TS_MAX_TREE) return TS_ERR_UNSUPPORTED;
+  if (a->n_tree_max > TS_MAX_TREE || a->num_requests > 65535) return TS_ERR_UNSUPPORTED;
   const int64_t row_bytes = static_cast<int64_t>(a->num_kv_heads) * a->head_dim * a->elem_bytes;
   if (row_bytes % 16 != 0 || row_bytes > (1 << 20)) return TS_ERR_UNSUPPORTED;
   if (!a->k_layers || !a->v_layers || !a->prefix_len || !a->n_tree || !a->parent || !a->tokens || !a->m ||
@@ -451,12 +450,20 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   p.page_size = a->page_size;
   p.max_blocks = a->max_blocks_per_req;
   p.num_blocks = a->num_blocks;
-  int chunk = (32768 / a->n_tree_max) / 16 * 16;
-  if (chunk < 16) chunk = 16;
-  if (chunk > row_bytes) chunk = static_cast<int>(row_bytes);
-  p.chunk_bytes = chunk;
-  p.num_chunk_groups = static_cast<int>((row_bytes + chunk - 1) / chunk);
-  if (p.num_chunk_groups > 65535) return TS_ERR_UNSUPPORTED;
+  // about two CTAs per SM over all requests, each taking a run of
+  // (layer, K|V) items; a CTA's vector count stays below 2^31
+  const int items = 2 * a->num_layers;
+  const int sms = device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  int per_req = static_cast<int>(std::min<int64_t>(items, std::max<int64_t>(1, (2LL * sms + a->num_requests - 1) /
+                                                                                    a->num_requests)));
+  int ipc = (items + per_req - 1) / per_req;
+  const int64_t max_item_vecs = static_cast<int64_t>(a->n_tree_max) * (row_bytes / 16);
+  ipc = static_cast<int>(std::min<int64_t>(ipc, std::max<int64_t>(1, (INT32_MAX / 2) / max_item_vecs)));
+  p.items_per_cta = ipc;
+  // shared-memory staging: the CTA's largest possible move, at most 96 KB
+  const int64_t most = max_item_vecs * ipc;
+  p.batch_vecs = static_cast<int>(std::min<int64_t>(most, kCompactBatchBytes / 16));
   p.k_layers = a->k_layers;
   p.v_layers = a->v_layers;
   p.block_table = a->block_table;
@@ -472,7 +479,7 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   p.new_tokens = a->new_tokens;
   p.src_rows = a->src_rows;
   p.err = reinterpret_cast<unsigned*>(ws);
-  p.plan = reinterpret_cast<int32_t*>(ws + kWsHeader);
+  p.ticket = reinterpret_cast<unsigned*>(ws + kWsHeader);
   cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }

@@ -59,4 +59,33 @@ __device__ __forceinline__ uint64_t tile_visibility(const uint32_t a[4], int off
   return tree | pre;
 }
 
+// The CTAs holding tiles of one unit under the split of the tile sequence
+// (plain when E = 0, cost-weighted with a first-tile weight of 1 + E
+// otherwise): CTA c left a share of the unit iff c_lo <= c <= c_hi and
+// holds(c).  before = tiles of earlier requests, T = all tiles, tiles = tiles
+// of every unit of request b, upr = units per request, nc = CTAs.
+struct UnitSplit {
+  int64_t T, W, pf;
+  int E, tiles, nc, c_lo, c_hi;
+  __device__ __forceinline__ void init(int64_t before, int64_t T_, int tiles_, int b, int uir, int upr, int num_req,
+                                       int E_, int nc_) {
+    T = T_;
+    tiles = tiles_;
+    E = E_;
+    nc = nc_;
+    W = T + static_cast<int64_t>(E) * upr * num_req;
+    pf = before + static_cast<int64_t>(E) * upr * b + static_cast<int64_t>(uir) * (tiles + E);
+    const int64_t first = before + static_cast<int64_t>(uir) * tiles;
+    c_lo = E > 0 ? wsched_cta_of_pos(pf, W, nc) : sched_cta_of(first, T, nc);
+    c_hi = E > 0 ? wsched_cta_of_pos(pf + (tiles >= 2 ? E + tiles - 1 : 0), W, nc)
+                 : sched_cta_of(first + tiles - 1, T, nc);
+  }
+  __device__ __forceinline__ bool holds(int c) const {
+    if (E == 0) return sched_begin(c, T, nc) < sched_begin(c + 1, T, nc);
+    if (c == c_lo) return true;
+    const int j = wsched_tile_in_unit(wsched_x(c, W, nc) - pf, E, tiles);
+    return j < tiles && wsched_cta_of_pos(pf + E + j, W, nc) == c;
+  }
+};
+
 }  // namespace ts

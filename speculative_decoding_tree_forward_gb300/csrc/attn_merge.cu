@@ -8,28 +8,23 @@
 // skipping CTAs whose tile range was empty, and writes the bf16 output and
 // the natural-log lse.  Units held by one CTA were written directly by the
 // attention kernel and are skipped here.  One warp per output row, eight rows
-// per CTA: the split comes from the tile prefix the attention kernel's CTA 0
-// left in the workspace (three loads), and each lane owns four columns.  The
-// lse of the row's first 32 shares (one per lane) and its first four partial
-// rows (coalesced 512-byte reads) are all requested before the weights are
-// known, so a typical row costs one dependent round trip to L2; shares of
-// CTAs that hold no tile of the unit get weight 0.
+// per CTA, each lane owning four columns.  The split (which CTAs hold tiles
+// of the unit) follows from the request lengths alone, so it is worked out
+// before the kernel waits for the attention kernel's results.  After the wait
+// the lse of the row's first 32 shares (one per lane) and its first eight
+// partial rows (coalesced 512-byte reads) are all requested before the
+// weights are known, so a row with up to eight shares costs one round trip
+// to L2; shares of CTAs that hold no tile of the unit get weight 0.
 #include "attn_common.cuh"
 
 namespace ts {
 namespace {
 
 constexpr int kMergeWarps = 8;  // rows per CTA
-constexpr int kPrefetchSlots = 4;  // partial rows loaded before the weights are known
-
-__device__ __forceinline__ bool slot_nonempty(int c, int64_t T, int nc) {
-  return sched_begin(c, T, nc) < sched_begin(c + 1, T, nc);
-}
+constexpr int kPrefetchSlots = 8;  // partial rows loaded before the weights are known
 
 // at most 64 registers: four CTAs (32 warps) per SM, so the grid lands in one wave
 __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const AttnParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t unit = blockIdx.x;
   // a unit is (request, group of hp KV heads, row group); with hp = 2 the
@@ -41,34 +36,51 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
   const int rg = uir % p.row_groups;
   const int rl = blockIdx.y * kMergeWarps + warp;
   const int hj = p.hp == 2 ? rl >> 6 : 0, loc = p.hp == 2 ? rl & 63 : rl;
-  if (p.hp == 2 ? loc >= p.rows : rl >= min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit)) return;
-  // the split as the attention kernel laid it out (its CTA 0 wrote the tile
-  // prefix over requests)
-  const int64_t before = __ldcg(p.cum_out + b);
-  const int64_t T = __ldcg(p.cum_out + p.num_req);
-  const int tiles = static_cast<int>(__ldcg(p.cum_out + b + 1) - before) / units_per_req;  // < 2^31 per request
-  const int64_t first = before + static_cast<int64_t>(uir) * tiles;
-  // CTAs holding the unit's first and last tile (plain or cost-weighted split)
-  const int E = p.seg_cost;
-  const int64_t W = T + static_cast<int64_t>(E) * units_per_req * p.num_req;
-  const int64_t pf = before + static_cast<int64_t>(E) * units_per_req * b + static_cast<int64_t>(uir) * (tiles + E);
-  const int c_lo = E > 0 ? wsched_cta_of_pos(pf, W, p.num_ctas) : sched_cta_of(first, T, p.num_ctas);
-  const int c_hi = E > 0 ? wsched_cta_of_pos(pf + (tiles >= 2 ? E + tiles - 1 : 0), W, p.num_ctas)
-                         : sched_cta_of(first + tiles - 1, T, p.num_ctas);
-  if (c_lo == c_hi) return;  // one CTA held the whole unit and wrote it
-  // does CTA c (c_lo <= c <= c_hi) hold a tile of this unit, i.e. a partial?
-  auto holds = [&](int c) -> bool {
-    if (E == 0) return slot_nonempty(c, T, p.num_ctas);
-    if (c == c_lo) return true;
-    const int j = wsched_tile_in_unit(wsched_x(c, W, p.num_ctas) - pf, E, tiles);
-    return j < tiles && wsched_cta_of_pos(pf + E + j, W, p.num_ctas) == c;
-  };
+  const bool row_valid = p.hp == 2 ? loc < p.rows : rl < min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit);
+  // The split as the attention kernel laid it out, from the request lengths
+  // it read (clamped the same way).  They were final before the attention
+  // kernel passed its own wait, which precedes this grid's launch, so warp 0
+  // works the split out for the CTA's unit before the wait for the attention
+  // kernel's results: the CTAs holding tiles of the unit and, for the first
+  // 32 of them, which hold a share.
+  __shared__ UnitSplit s_sp;
+  __shared__ unsigned s_hold;
+  if (warp == 0) {
+    int64_t before = 0, total = 0;
+    int mine = 0;
+    for (int r = lane; r < p.num_req; r += 32) {
+      int P, n;
+      attn_lengths(p, r, P, n, false);
+      const int t = attn_tiles(P + n);
+      total += static_cast<int64_t>(t) * units_per_req;
+      if (r < b) before += static_cast<int64_t>(t) * units_per_req;
+      if (r == b) mine = t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+      mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, o));
+    }
+    if (lane == 0) s_sp.init(before, total, mine, b, uir, units_per_req, p.num_req, p.seg_cost, p.num_ctas);
+    __syncwarp();
+    const int c = s_sp.c_lo + lane;
+    const unsigned hold = __ballot_sync(0xffffffffu, c <= s_sp.c_hi && s_sp.c_lo != s_sp.c_hi && s_sp.holds(c));
+    if (lane == 0) s_hold = hold;
+  }
+  __syncthreads();
+  const int c_lo = s_sp.c_lo, c_hi = s_sp.c_hi;
+  const bool valid_l = (s_hold >> lane) & 1u;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (!row_valid || c_lo == c_hi) return;  // padding row, or one CTA held the whole unit and wrote it
+  auto holds = [&](int c) -> bool { return s_sp.holds(c); };
+  const int ncs = c_hi - c_lo + 1;
 
   // slot of CTA c: c + unit; its lse at part_lse[slot * rows_pad + row]
   const float* lse_col = p.part_lse + unit * p.rows_pad + rl;
   const int D = p.head_dim;
   const bool active = lane * 4 < D;
-  const int ncs = c_hi - c_lo + 1;
   auto part_row = [&](int c) {
     return reinterpret_cast<const float4*>(p.part_o + ((static_cast<int64_t>(c) + unit) * p.rows_pad + rl) * D +
                                            lane * 4);
@@ -76,15 +88,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
   // one round trip: the lse of the first 32 slots (one per lane) and the
   // partial rows of the first kPrefetchSlots slots, all issued before the
   // weights are known (slots of CTAs without a share get weight 0)
+  const unsigned hold = s_hold;
   float lse_l = -INFINITY;
-  if (lane < ncs) lse_l = __ldcg(lse_col + static_cast<int64_t>(c_lo + lane) * p.rows_pad);
+  if (valid_l) lse_l = __ldcg(lse_col + static_cast<int64_t>(c_lo + lane) * p.rows_pad);
   float4 x[kPrefetchSlots];
 #pragma unroll
   for (int q = 0; q < kPrefetchSlots; ++q) {
     x[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q < ncs && active) x[q] = __ldcg(part_row(c_lo + q));
+    if (((hold >> q) & 1u) && active) x[q] = __ldcg(part_row(c_lo + q));
   }
-  bool valid_l = lane < ncs && holds(c_lo + lane);
   float mx = valid_l ? lse_l : -INFINITY;
   for (int c0 = c_lo + 32; c0 <= c_hi; c0 += 32) {  // more than 32 shares: rare
     const int c = c0 + lane;

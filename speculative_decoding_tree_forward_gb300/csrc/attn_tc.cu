@@ -402,8 +402,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   __syncthreads();
   if (tid == 0) {
     for (int b = 0; b < p.num_req; ++b) cum[b + 1] += cum[b];
-    if (blockIdx.x == 0)  // the merge kernel reads the split from here
-      for (int b = 0; b <= p.num_req; ++b) p.cum_out[b] = cum[b];
   }
   __syncthreads();
   const int64_t T = cum[p.num_req];

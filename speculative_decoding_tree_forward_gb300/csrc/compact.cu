@@ -1,48 +1,65 @@
-// Evolving tree cache: re-root walk and in-place KV-row compaction.
+// Evolving tree cache: re-root walk and in-place KV-row compaction, one kernel.
 //
 // SwiftSpec summary, §3.2 (the prefix-cache / tree-cache invariant and its
 // update procedure), Figure 4 (t12, t15 promoted, t17, t18 moved to the front
 // of the tree cache, the rest dropped) and Figure 2 with its walkthrough
 // (re-rooting at t6 reuses its subtree; an out-of-tree token reuses nothing).
 //
-// Kernel 1 (one CTA per request) walks the verified tokens down the tree,
-// taking at each step the lowest-index child that carries the token, and
-// writes the source-row list src = path ++ survivors into the workspace plan,
-// plus the new prefix length, tree size, parents and tokens.
+// Grid (G, num_requests): the G CTAs of request b share its (layer, K|V)
+// row moves.  Every CTA derives the re-root itself from the request's tree,
+// held in shared memory (at most TS_MAX_TREE nodes):
+//   1. one warp walks the verified tokens down the tree, taking at each step
+//      the lowest-index child of the current node that carries the token
+//      (each lane holds four nodes in registers; a warp min-reduction per
+//      step, no block barriers);
+//   2. survivors = proper descendants of the last matched node (every node
+//      when no token was verified), found by walking each node's parent
+//      chain up to that node's index, ranked in index order;
+//   3. src = path ++ survivors; row j of the new tree cache takes old row
+//      src[j].  Only rows with src[j] != j move.
+// The new metadata (prefix length, tree size, parents, tokens, src) may
+// overwrite the old in place, so it is written by exactly one CTA per
+// request, the one that takes the last of the request's G tickets: every
+// CTA takes its ticket only after it has read the old metadata.  That CTA
+// resets the ticket for the next call.  No CTA waits for another.
 //
-// Kernel 2 moves the rows: one CTA per (chunk of the row bytes, K|V, layer,
-// request).  The source list is strictly increasing (parent[i] < i, and
-// survivors descend from the last matched node), so every destination row
-// P + j is at or below its source row P + src[j]; a CTA first loads its byte
-// chunk of every source row into shared memory and only then stores, so no
-// row is overwritten before it is read.  Rows whose source equals their
-// destination are skipped.  Transfers are 16-byte vectors.
+// Row moves: the CTA's items are (layer, K|V) pairs; their moved rows form a
+// sequence of 16-byte vectors (item, moved row in increasing destination
+// order, vector).  The sequence goes through shared memory in batches: load
+// the whole batch, then store it.  A source row is never below its
+// destination (src is strictly increasing and src[j] >= j), so within an
+// item a row is read, at the latest, in the batch that overwrites it, and
+// every read of a batch precedes its stores: no row is overwritten before it
+// is read.  Items of different CTAs are disjoint.
 #include "common.cuh"
 #include "internal.h"
 
 namespace ts {
 namespace {
 
-constexpr int kWalkThreads = TS_MAX_TREE;
-constexpr int kGatherThreads = 256;
+constexpr int kCompactThreads = 256;
+constexpr int kLoadsInFlight = 8;  // 16-byte loads per thread before the first store to shared memory
 
-__device__ __forceinline__ void block_sync() { __syncthreads(); }
-
-__global__ void __launch_bounds__(kWalkThreads) reroot_walk_kernel(const CompactParams p) {
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactParams p) {
   pdl_wait();
   pdl_launch_dependents();
-  const int b = blockIdx.x;
-  const int i = threadIdx.x;
+  extern __shared__ uint4 buf[];  // [batch_vecs]
   __shared__ int par_s[TS_MAX_TREE];
   __shared__ int tok_s[TS_MAX_TREE];
-  __shared__ uint32_t anc[TS_MAX_TREE][4];
-  __shared__ int jmp[TS_MAX_TREE];
-  __shared__ int path_s[TS_MAX_TREE + 1];
-  __shared__ int red[2 * (kWalkThreads / 32)];
-  __shared__ int cnt[kWalkThreads / 32];
   __shared__ int ver_s[TS_MAX_TREE + 1];
+  __shared__ int path_s[TS_MAX_TREE + 1];
+  __shared__ int surv_s[TS_MAX_TREE];     // survivors' old indices, by rank
+  __shared__ int newidx[TS_MAX_TREE];     // old index -> survivor rank, or -1
+  __shared__ int64_t mv_src[TS_MAX_TREE]; // moved row k: source / destination row within a layer's cache
+  __shared__ int64_t mv_dst[TS_MAX_TREE];
+  __shared__ int cnt[kCompactThreads / 32];
+  __shared__ int walk_cur, walk_plen, walk_all, last_ticket;
 
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t rowbase = static_cast<int64_t>(b) * p.n_tree_max;
+
+  // ---- the request's lengths and tree (clamped and reported as before)
   int n = p.n_tree[b];
   int m = p.m[b];
   int P = p.prefix_len[b];
@@ -51,170 +68,206 @@ __global__ void __launch_bounds__(kWalkThreads) reroot_walk_kernel(const Compact
   if (m < 0 || m > p.m_max) { m = min(max(m, 0), p.m_max); bad = true; }
   const int cap = p.paged ? p.max_blocks * p.page_size : p.max_kv_len;
   if (P < 0 || P + n > cap) { P = min(max(P, 0), max(cap - n, 0)); bad = true; }
-  if (bad && i == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
-
-  // the verified tokens, loaded once (the walk below reads one per step).
+  if (bad && tid == 0 && blockIdx.x == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
   // A walk step matches at most one node, so with n <= TS_MAX_TREE nodes the
   // walk has always ended by step TS_MAX_TREE + 1: later tokens are never read.
   const int mw = min(m, TS_MAX_TREE + 1);
-  for (int j = i; j < mw; j += kWalkThreads) ver_s[j] = p.verified[static_cast<int64_t>(b) * p.m_max + j];
+  for (int j = tid; j < mw; j += kCompactThreads) ver_s[j] = p.verified[static_cast<int64_t>(b) * p.m_max + j];
   int my_par = -1, my_tok = 0;
-  if (i < n) {
-    my_par = p.parent[rowbase + i];
-    if (my_par < -1 || my_par >= i) {
-      report_error(p.err, TS_DEVERR_BAD_PARENT);
+  if (tid < n) {
+    my_par = p.parent[rowbase + tid];
+    if (my_par < -1 || my_par >= tid) {
+      if (blockIdx.x == 0) report_error(p.err, TS_DEVERR_BAD_PARENT);
       my_par = -1;
     }
-    my_tok = p.tokens[rowbase + i];
-    par_s[i] = my_par;
-    tok_s[i] = my_tok;
+    my_tok = p.tokens[rowbase + tid];
+    par_s[tid] = my_par;
+    tok_s[tid] = my_tok;
   }
-  __syncthreads();  // every read of parent/tokens happens before any write (aliasing allowed)
+  __syncthreads();  // every read of the old metadata is done
 
-  // ---- walk the verified tokens from the prefix tail
-  int cur = -1, plen = 0;
-  bool matched_all = true;
-  for (int j = 0; j < mw; ++j) {
-    const int v = ver_s[j];
-    int cand = (i < n && my_par == cur && my_tok == v) ? i : INT32_MAX;
-    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-    // two slot sets: set j % 2 is rewritten at step j + 2, after every
-    // thread has passed the barrier of step j + 1 and so finished reading it
-    if ((i & 31) == 0) red[(j & 1) * (kWalkThreads / 32) + (i >> 5)] = cand;
-    __syncthreads();
-    int c = red[(j & 1) * (kWalkThreads / 32)];
-    for (int w = 1; w < kWalkThreads / 32; ++w) c = min(c, red[(j & 1) * (kWalkThreads / 32) + w]);
-    if (c == INT32_MAX) {
-      matched_all = false;
-      break;
-    }
-    if (i == 0) path_s[plen] = c;
-    ++plen;
-    cur = c;
+  // ---- ticket: the request's last CTA writes the new metadata
+  if (tid == 0) {
+    __threadfence();
+    const unsigned before = atomicAdd(p.ticket + b, 1u);
+    const int last = before + 1u == gridDim.x;
+    if (last) p.ticket[b] = 0u;
+    __threadfence();
+    last_ticket = last;
   }
-  // ---- survivors: proper descendants of cur (everything when cur = -1)
-  build_ancestor_masks(par_s, n, anc, jmp, i, kWalkThreads, nullptr, block_sync);
+
+  // ---- 1. walk (warp 0): lane l holds nodes l, l + 32, l + 64, l + 96
+  if (warp == 0) {
+    int wp[TS_MAX_TREE / 32], wt[TS_MAX_TREE / 32];
+#pragma unroll
+    for (int q = 0; q < TS_MAX_TREE / 32; ++q) {
+      const int i = lane + 32 * q;
+      wp[q] = i < n ? par_s[i] : -2;  // -2: never a child of anything
+      wt[q] = i < n ? tok_s[i] : 0;
+    }
+    int cur = -1, plen = 0, all = 1;
+    for (int j = 0; j < mw; ++j) {
+      const int v = ver_s[j];
+      int cand = INT32_MAX;
+#pragma unroll
+      for (int q = TS_MAX_TREE / 32 - 1; q >= 0; --q)  // the lane's lowest matching index wins
+        if (wp[q] == cur && wt[q] == v) cand = lane + 32 * q;
+      cand = __reduce_min_sync(0xffffffffu, cand);
+      if (cand == INT32_MAX) {
+        all = 0;
+        break;
+      }
+      if (lane == 0) path_s[plen] = cand;
+      ++plen;
+      cur = cand;
+    }
+    if (lane == 0) {
+      walk_cur = cur;
+      walk_plen = plen;
+      walk_all = all;
+    }
+  }
+  __syncthreads();
+  const int cur = walk_cur, plen = walk_plen;
+  const bool all = walk_all != 0;
+
+  // ---- 2. survivors: proper descendants of cur (every node when cur = -1)
   bool surv = false;
-  if (matched_all && i < n && i != cur) surv = (cur < 0) || ((anc[i][cur >> 5] >> (cur & 31)) & 1u);
+  if (all && tid < n && tid != cur) {
+    if (cur < 0) {
+      surv = true;
+    } else if (tid > cur) {
+      int u = my_par;  // parent indices strictly decrease: at most n steps
+      while (u > cur) u = par_s[u];
+      surv = u == cur;
+    }
+  }
   const unsigned bal = __ballot_sync(0xffffffffu, surv);
-  if ((i & 31) == 0) cnt[i >> 5] = __popc(bal);
+  if (lane == 0) cnt[warp] = __popc(bal);
   __syncthreads();
   int before = 0, total = 0;
-  for (int w = 0; w < kWalkThreads / 32; ++w) {
-    if (w < (i >> 5)) before += cnt[w];
+#pragma unroll
+  for (int w = 0; w < kCompactThreads / 32; ++w) {
+    if (w < warp) before += cnt[w];
     total += cnt[w];
   }
-  const int rank = before + __popc(bal & ((1u << (i & 31)) - 1u));  // new index if surv
-  // ranks of all nodes for the parent remap
-  __shared__ int newidx[TS_MAX_TREE];
-  if (i < n) newidx[i] = surv ? rank : -1;
-  __syncthreads();
+  const int rank = before + __popc(bal & ((1u << lane) - 1u));
+  if (tid < n) newidx[tid] = surv ? rank : -1;
+  if (surv) surv_s[rank] = tid;
+  __syncthreads();  // cnt is reused below; surv_s / newidx complete
 
-  int32_t* plan = p.plan + static_cast<int64_t>(b) * kPlanStride;
-  if (i == 0) {
-    plan[0] = P;
-    plan[1] = plen + total;
-    p.new_prefix_len[b] = P + plen;
-    p.new_n_tree[b] = total;
-  }
-  if (i < plen) plan[2 + i] = path_s[i];
-  if (surv) {
-    plan[2 + plen + rank] = i;
-    const int np = (my_par == cur) ? -1 : newidx[my_par];
-    p.new_parent[rowbase + rank] = np;
-    p.new_tokens[rowbase + rank] = my_tok;
-  }
-  if (p.src_rows != nullptr && i < p.n_tree_max) {
-    int v = -1;
-    if (i < plen) v = path_s[i];
-    p.src_rows[rowbase + i] = v;  // survivors overwrite their slots below
-  }
+  // ---- 3. moved rows: destination j < plen + total whose source differs
+  const int L = plen + total;
+  const int srcj = tid < L ? (tid < plen ? path_s[tid] : surv_s[tid - plen]) : tid;
+  const bool moves = tid < L && srcj != tid;
+  const unsigned mbal = __ballot_sync(0xffffffffu, moves);
+  if (lane == 0) cnt[warp] = __popc(mbal);
   __syncthreads();
-  if (p.src_rows != nullptr && surv) p.src_rows[rowbase + plen + rank] = i;
-  // entries of the new tree beyond its size
-  if (i >= total && i < p.n_tree_max) {
-    p.new_parent[rowbase + i] = -1;
-    p.new_tokens[rowbase + i] = 0;
-  }
-}
-
-__device__ __forceinline__ uint8_t* row_ptr(const CompactParams& p, void* layer, int b, int row) {
-  uint8_t* base = static_cast<uint8_t*>(layer);
-  if (!p.paged) return base + (static_cast<int64_t>(b) * p.max_kv_len + row) * p.row_bytes;
-  const int blk = p.block_table[static_cast<int64_t>(b) * p.max_blocks + row / p.page_size];
-  if (blk < 0 || blk >= p.num_blocks) return nullptr;
-  return base + (static_cast<int64_t>(blk) * p.page_size + row % p.page_size) * p.row_bytes;
-}
-
-__global__ void __launch_bounds__(kGatherThreads) compact_gather_kernel(const CompactParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
-  extern __shared__ uint4 buf[];  // [rows][chunk_bytes / 16]
-  __shared__ int plan_s[kPlanStride];
-  const int group = blockIdx.z;
-  const int kv = blockIdx.y;  // 0 = K, 1 = V
-  const int layer = blockIdx.x / p.num_req;
-  const int b = blockIdx.x % p.num_req;
-  const int32_t* plan = p.plan + static_cast<int64_t>(b) * kPlanStride;
-  for (int x = threadIdx.x; x < kPlanStride; x += blockDim.x) plan_s[x] = plan[x];
-  __syncthreads();
-  const int P = plan_s[0];
-  const int L = min(max(plan_s[1], 0), TS_MAX_TREE);
-  void* base = kv == 0 ? p.k_layers[layer] : p.v_layers[layer];
-  const int vecs = p.chunk_bytes / 16;
-  const int c0 = group * p.chunk_bytes;
-  const int nvec = min(vecs, (p.row_bytes - c0) / 16);
-  if (nvec <= 0) return;
-  const int total = L * nvec;
-  // load phase: four independent 16-byte loads in flight per thread
-  for (int x0 = threadIdx.x; x0 < total; x0 += 4 * kGatherThreads) {
-    uint4 v[4];
-    int slot[4];
+  int mbefore = 0, nmv = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int x = x0 + q * kGatherThreads;
-      slot[q] = -1;
-      if (x < total) {
-        const int j = x / nvec, e = x % nvec;
-        const int src = plan_s[2 + j];
-        if (src != j) {
-          const uint8_t* sp = row_ptr(p, base, b, P + src);
-          if (sp == nullptr) {
-            report_error(p.err, TS_DEVERR_BAD_BLOCK);
-          } else {
-            v[q] = *reinterpret_cast<const uint4*>(sp + c0 + 16 * e);
-            slot[q] = j * vecs + e;
-          }
-        }
+  for (int w = 0; w < kCompactThreads / 32; ++w) {
+    if (w < warp) mbefore += cnt[w];
+    nmv += cnt[w];
+  }
+  if (moves) {
+    const int k = mbefore + __popc(mbal & ((1u << lane) - 1u));
+    const int rs = P + srcj, rd = P + tid;
+    int64_t s = -1, d = -1;
+    if (!p.paged) {
+      s = static_cast<int64_t>(b) * p.max_kv_len + rs;
+      d = static_cast<int64_t>(b) * p.max_kv_len + rd;
+    } else {
+      const int bs = p.block_table[static_cast<int64_t>(b) * p.max_blocks + rs / p.page_size];
+      const int bd = p.block_table[static_cast<int64_t>(b) * p.max_blocks + rd / p.page_size];
+      if (bs < 0 || bs >= p.num_blocks || bd < 0 || bd >= p.num_blocks) {
+        report_error(p.err, TS_DEVERR_BAD_BLOCK);  // the row is not moved
+      } else {
+        s = static_cast<int64_t>(bs) * p.page_size + rs % p.page_size;
+        d = static_cast<int64_t>(bd) * p.page_size + rd % p.page_size;
       }
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (slot[q] >= 0) buf[slot[q]] = v[q];
+    mv_src[k] = s;
+    mv_dst[k] = d;
   }
-  __syncthreads();
-  // store phase
-  for (int x = threadIdx.x; x < total; x += kGatherThreads) {
-    const int j = x / nvec, e = x % nvec;
-    const int src = plan_s[2 + j];
-    if (src == j) continue;
-    uint8_t* d = row_ptr(p, base, b, P + j);
-    const uint8_t* sp = row_ptr(p, base, b, P + src);
-    if (d == nullptr || sp == nullptr) continue;
-    *reinterpret_cast<uint4*>(d + c0 + 16 * e) = buf[j * vecs + e];
+
+  // ---- new metadata (one CTA per request)
+  if (last_ticket) {
+    if (tid == 0) {
+      p.new_prefix_len[b] = P + plen;
+      p.new_n_tree[b] = total;
+    }
+    if (tid < p.n_tree_max) {
+      int np = -1, nt = 0;
+      if (tid < total) {
+        const int i = surv_s[tid];
+        const int q = par_s[i];
+        np = q == cur ? -1 : newidx[q];
+        nt = tok_s[i];
+      }
+      p.new_parent[rowbase + tid] = np;
+      p.new_tokens[rowbase + tid] = nt;
+      if (p.src_rows != nullptr) p.src_rows[rowbase + tid] = tid < L ? srcj : -1;
+    }
+  }
+  __syncthreads();  // mv_src / mv_dst complete
+
+  // ---- row moves: items it0 .. it1 - 1 of this CTA, as 16-byte vectors
+  const int items = 2 * p.num_layers;
+  const int it0 = blockIdx.x * p.items_per_cta;
+  const int it1 = min(items, it0 + p.items_per_cta);
+  if (nmv == 0 || it0 >= it1) return;
+  const int vr = p.row_bytes / 16;
+  const int64_t per_item = static_cast<int64_t>(nmv) * vr;
+  const int64_t nvec = per_item * (it1 - it0);
+  // nvec < 2^31 (the host bounds items_per_cta), so 32-bit divisions suffice
+  const uint32_t per_item32 = static_cast<uint32_t>(per_item), vr32 = static_cast<uint32_t>(vr);
+  auto address = [&](int64_t x, bool dst) -> uint4* {
+    const uint32_t x32 = static_cast<uint32_t>(x);
+    const int it = it0 + static_cast<int>(x32 / per_item32);
+    const uint32_t rem = x32 % per_item32;
+    const int k = static_cast<int>(rem / vr32), e = static_cast<int>(rem % vr32);
+    const int64_t row = dst ? mv_dst[k] : mv_src[k];  // both -1 when the row does not move
+    if (row < 0) return nullptr;
+    void* base = (it & 1) ? p.v_layers[it >> 1] : p.k_layers[it >> 1];
+    return reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + row * p.row_bytes) + e;
+  };
+  for (int64_t x0 = 0; x0 < nvec; x0 += p.batch_vecs) {
+    const int nb = static_cast<int>(min(static_cast<int64_t>(p.batch_vecs), nvec - x0));
+    for (int y0 = tid; y0 < nb; y0 += kLoadsInFlight * kCompactThreads) {
+      uint4 v[kLoadsInFlight];
+#pragma unroll
+      for (int q = 0; q < kLoadsInFlight; ++q) {
+        const int y = y0 + q * kCompactThreads;
+        v[q] = make_uint4(0, 0, 0, 0);
+        if (y < nb) {
+          const uint4* s = address(x0 + y, false);
+          if (s != nullptr) v[q] = *s;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kLoadsInFlight; ++q) {
+        const int y = y0 + q * kCompactThreads;
+        if (y < nb) buf[y] = v[q];
+      }
+    }
+    __syncthreads();
+    for (int y = tid; y < nb; y += kCompactThreads) {
+      uint4* d = address(x0 + y, true);
+      if (d != nullptr) *d = buf[y];
+    }
+    __syncthreads();  // the next batch rewrites buf
   }
 }
 
 }  // namespace
 
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream) {
-  cudaError_t e = launch_pdl(reroot_walk_kernel, dim3(p.num_req), dim3(kWalkThreads), 0, stream, p);
-  if (e != cudaSuccess) return e;
-  const size_t smem = static_cast<size_t>(p.n_tree_max) * p.chunk_bytes;
+  const size_t smem = static_cast<size_t>(p.batch_vecs) * 16;
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(compact_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  dim3 grid(p.num_layers * p.num_req, 2, p.num_chunk_groups);
-  return launch_pdl(compact_gather_kernel, grid, dim3(kGatherThreads), smem, stream, p);
+    cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const int items = 2 * p.num_layers;
+  const int ctas = (items + p.items_per_cta - 1) / p.items_per_cta;
+  return launch_pdl(compact_kernel, dim3(ctas, p.num_req), dim3(kCompactThreads), smem, stream, p);
 }
 
 }  // namespace ts

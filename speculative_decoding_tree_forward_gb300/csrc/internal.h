@@ -35,6 +35,7 @@ constexpr int kBlockN = 64;        // keys per K/V tile
 constexpr int kMaxRowsPerUnit = 128;  // packed query rows handled by one CTA
 constexpr int kMaxRequestsAttn = 1024;
 constexpr size_t kWsHeader = 256;  // error word + padding at the start of every workspace
+constexpr int64_t kCompactBatchBytes = 96 * 1024;  // row-move staging per CTA (two CTAs per SM)
 
 // Parameters of one tree_attn_forward call as the kernels see them.
 struct AttnParams {
@@ -60,7 +61,6 @@ struct AttnParams {
   float* lse;
   float scale_log2;  // softmax scale * log2(e)
   unsigned* err;     // workspace error word
-  int64_t* cum_out;  // [num_req + 1] tiles before each request, written by CTA 0 for the merge
   float* part_o;     // [slots][rows_pad][head_dim]
   float* part_lse;   // [slots][rows_pad] (log2 domain)
 };
@@ -101,7 +101,8 @@ cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 struct CompactParams {
   int num_req, n_tree_max, m_max, num_layers, row_bytes;
   int paged, max_kv_len, page_size, max_blocks, num_blocks;
-  int chunk_bytes, num_chunk_groups;
+  int items_per_cta;  // (layer, K|V) items per CTA; CTAs per request = ceil(2 * num_layers / items_per_cta)
+  int batch_vecs;     // 16-byte vectors staged in shared memory per batch
   void* const* k_layers;
   void* const* v_layers;
   const int32_t* block_table;
@@ -117,9 +118,8 @@ struct CompactParams {
   int32_t* new_tokens;
   int32_t* src_rows;
   unsigned* err;
-  int32_t* plan;     // per request: [0] = old P, [1] = rows in src list, [2..] = src list
+  unsigned* ticket;  // [num_req] CTAs of the request that have read its metadata; 0 between calls
 };
-constexpr int kPlanStride = TS_MAX_TREE + 4;
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream);
 
 }  // namespace ts

@@ -233,6 +233,33 @@ def _sampled(case, requests, heads, **kw):
     check_attention(case, out, lse, ref, heads=heads)
 
 
+def test_tcgen05_one_workspace_serves_repeated_calls():
+    """One workspace serves repeated calls, also of other shapes and CTA
+    counts, with identical results and a clean error word."""
+    cases = [
+        (W.random_attn_case(31, num_req=3, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(200, 1500))),  # R = 128
+        (W.random_attn_case(32, num_req=5, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(100, 2000),
+                            chain=True, paged=True)),                                                      # R = 40
+    ]
+    ws = ts.new_workspace(1 << 24)
+    for num_ctas in (40, 0, 96):
+        for case in cases:
+            d = attn_inputs(case)
+            outs = []
+            for _ in range(2):
+                out = torch.empty_like(d["q"])
+                lse = torch.empty((case.num_req, case.num_q_heads, case.n_query), dtype=torch.float32, device="cuda")
+                a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"], out,
+                                 lse, d.get("block_table"), case.softmax_scale, 2, num_ctas)
+                assert ts.tree_attn_workspace_size(a) <= ws.numel()
+                ts.tree_attn_forward_args(a, ws)
+                torch.cuda.synchronize()
+                assert int(ws[:4].view(torch.int32)[0]) == 0
+                outs.append((out.clone(), lse.clone()))
+            assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+            check_attention(case, outs[0][0], outs[0][1], A.attention_case(case))
+
+
 def test_workload_tree16_prefix128():
     w = W.tree16_prefix128()
     _sampled(w.attn[0], None, None)

@@ -113,7 +113,7 @@ def _logical(cache, b, nrows, table):
     return A.logical_rows(cache, b, nrows, table)
 
 
-def run_compact_case(case, layers=3, hkv=2, d=64, paged=False, seed=0, max_rows=None):
+def run_compact_case(case, layers=3, hkv=2, d=64, paged=False, seed=0, max_rows=None, workspace=None):
     """Random KV for `layers` layers; compaction on GPU vs oracle (metadata + bytes)."""
     rng = np.random.default_rng(seed)
     B = case.num_req
@@ -136,7 +136,7 @@ def run_compact_case(case, layers=3, hkv=2, d=64, paged=False, seed=0, max_rows=
     vd = [torch.from_numpy(x.view(np.int16)).cuda() for x in vs]
     res = ts.tree_cache_compact(kd, vd, i32_dev(case.prefix_len), i32_dev(case.n_tree), i32_dev(case.parent),
                                 i32_dev(case.tokens), i32_dev(case.verified), i32_dev(case.m),
-                                block_table=None if table is None else i32_dev(table))
+                                block_table=None if table is None else i32_dev(table), workspace=workspace)
     torch.cuda.synchronize()
     got = {k: v.cpu().numpy() for k, v in res.items() if not k.startswith("_")}
     for b in range(B):
@@ -161,6 +161,25 @@ def test_compact_random(seed, paged):
     case = W.random_compact_case(seed, num_req=5, n_tree_max=24 if seed else 128, forest=bool(seed % 2))
     run_compact_case(case, layers=2 + seed % 3, hkv=2 if seed % 2 else 8, d=64 if seed < 3 else 128,
                      paged=paged, seed=seed)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_compact_many_layers_and_requests(paged):
+    """Sixteen requests x 24 layers of 1 KB rows on 128-node trees: several
+    (layer, K|V) items per CTA and row moves staged in several batches."""
+    case = W.random_compact_case(40, num_req=16, n_tree_max=128, max_verified=129)
+    run_compact_case(case, layers=24, hkv=8, d=64, paged=paged, seed=40)
+
+
+def test_compact_one_workspace_serves_repeated_calls():
+    """The per-request tickets are left at zero: one workspace serves
+    successive calls of different shapes."""
+    ws = ts.new_workspace(1 << 16)
+    for seed, nreq, nmax in ((50, 6, 24), (51, 3, 128), (52, 9, 40), (53, 6, 24)):
+        case = W.random_compact_case(seed, num_req=nreq, n_tree_max=nmax)
+        run_compact_case(case, layers=3, hkv=4, d=64, paged=bool(seed % 2), seed=seed, workspace=ws)
+        assert int(ws[256:256 + 4 * nreq].view(torch.int32).abs().sum()) == 0
+        assert int(ws[:4].view(torch.int32)[0]) == 0
 
 
 def test_compact_fig4_on_gpu():
