@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_chunk_kernel(const Acce
   if ((p.vocab & 3) == 0) {
     const float4* lg4 = reinterpret_cast<const float4*>(lg);
     const int64_t a = v0 / 4, e = v1 / 4;
-#pragma unroll 4
+#pragma unroll 8
     for (int64_t x = a + threadIdx.x; x < e; x += kArgmaxThreads) {
       const float4 f = __ldcs(lg4 + x);
       const int base = static_cast<int>(x * 4);
@@ -80,8 +80,6 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_chunk_kernel(const Acce
 __device__ __forceinline__ void block_sync() { __syncthreads(); }
 
 __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int i = threadIdx.x;
   __shared__ uint32_t anc[TS_MAX_TREE][4];
@@ -90,12 +88,24 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
   __shared__ uint32_t ok_mask[4];
   __shared__ int best_key[TS_MAX_TREE / 32];
 
+  // The tree (sizes, parents, tokens) is an input of the call, final before
+  // the argmax kernel passed its own wait, which precedes this grid's launch:
+  // read it and build the ancestor masks before waiting for the argmax.
   int n = p.n_tree[b];
   if (n < 0 || n > p.n_tree_max) {
     if (i == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
     n = min(max(n, 0), p.n_tree_max);
   }
   const int64_t rowbase = static_cast<int64_t>(b) * p.n_tree_max;
+  int par = -1, tok = 0;
+  if (i < n) {
+    par = p.parent[rowbase + i];
+    if (par < -1 || par >= i) par = -1;  // reported by build_ancestor_masks
+    tok = p.tokens[rowbase + i];
+  }
+  if (n > 0) build_ancestor_masks(p.parent + rowbase, n, anc, jmp, i, blockDim.x, p.err, block_sync);
+  pdl_wait();
+  pdl_launch_dependents();
   // argmax per node from the chunk partials
   int am = -1;
   if (i < n) {
@@ -120,14 +130,10 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
       for (int x = i; x <= p.n_tree_max; x += blockDim.x) p.verified[static_cast<int64_t>(b) * (p.n_tree_max + 1) + x] = -1;
     return;
   }
-  build_ancestor_masks(p.parent + rowbase, n, anc, jmp, i, blockDim.x, p.err, block_sync);
+  __syncthreads();  // am_s complete
   // ok[i]: the root, or a child whose token is the target argmax at its parent
   bool ok = false;
-  if (i < n) {
-    int par = p.parent[rowbase + i];
-    if (par < -1 || par >= i) par = -1;
-    ok = (i == 0) || (par >= 0 && p.tokens[rowbase + i] == am_s[par]);
-  }
+  if (i < n) ok = (i == 0) || (par >= 0 && tok == am_s[par]);
   const unsigned bal = __ballot_sync(0xffffffffu, ok);
   if ((i & 31) == 0) ok_mask[i >> 5] = bal;
   __syncthreads();
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
         else if (w == (i >> 5)) pos += __popc(pm[w] & ((1u << (i & 31)) - 1u));
       }
       p.path[rowbase + pos] = i;
-      if (p.verified) p.verified[static_cast<int64_t>(b) * (p.n_tree_max + 1) + pos] = p.tokens[rowbase + i];
+      if (p.verified) p.verified[static_cast<int64_t>(b) * (p.n_tree_max + 1) + pos] = tok;
     }
     if (i >= al) p.path[rowbase + i] = -1;
   }

@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   __shared__ int64_t mv_src[TS_MAX_TREE]; // moved row k: source / destination row within a layer's cache
   __shared__ int64_t mv_dst[TS_MAX_TREE];
   __shared__ int cnt[kCompactThreads / 32];
+  __shared__ int blk_s[TS_MAX_TREE + 2];  // paged: block-table entries of the pages holding rows P .. P + n - 1
   __shared__ int walk_cur, walk_plen, walk_all, last_ticket;
 
   const int b = blockIdx.y;
@@ -86,8 +87,16 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   }
   __syncthreads();  // every read of the old metadata is done
 
-  // ---- ticket: the request's last CTA writes the new metadata
-  if (tid == 0) {
+  // ---- ticket: the request's last CTA writes the new metadata (taken by
+  //      warp 1 while warp 0 walks); paged: the tree rows' block-table
+  //      entries, read by warps 2.. while warp 0 walks
+  const int pg0 = p.paged ? P / p.page_size : 0;
+  if (p.paged && tid >= 64) {
+    const int npg = n > 0 ? (P + n - 1) / p.page_size - pg0 + 1 : 0;
+    for (int j = tid - 64; j < npg; j += kCompactThreads - 64)
+      blk_s[j] = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg0 + j];
+  }
+  if (tid == 32) {
     __threadfence();
     const unsigned before = atomicAdd(p.ticket + b, 1u);
     const int last = before + 1u == gridDim.x;
@@ -177,8 +186,8 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
       s = static_cast<int64_t>(b) * p.max_kv_len + rs;
       d = static_cast<int64_t>(b) * p.max_kv_len + rd;
     } else {
-      const int bs = p.block_table[static_cast<int64_t>(b) * p.max_blocks + rs / p.page_size];
-      const int bd = p.block_table[static_cast<int64_t>(b) * p.max_blocks + rd / p.page_size];
+      const int bs = blk_s[rs / p.page_size - pg0];
+      const int bd = blk_s[rd / p.page_size - pg0];
       if (bs < 0 || bs >= p.num_blocks || bd < 0 || bd >= p.num_blocks) {
         report_error(p.err, TS_DEVERR_BAD_BLOCK);  // the row is not moved
       } else {
