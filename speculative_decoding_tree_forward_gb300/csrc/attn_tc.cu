@@ -349,8 +349,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap pmap,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const AttnParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcLayout L = tc_layout(p.num_req, TcShape<HP>::kKBytes);
@@ -364,14 +362,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   using Sh = TcShape<HP>;
   const int units_per_req = p.hkv / HP;  // one row group: HP heads x R <= 128 rows
 
-  // ---- schedule (identical to the warp-MMA kernel) and barrier set-up
-  for (int b = tid; b < p.num_req; b += blockDim.x) {
-    int P, n;
-    attn_lengths(p, b, P, n, blockIdx.x == 0);
-    cum[b + 1] = static_cast<int64_t>(attn_tiles(P + n)) * units_per_req;
-  }
+  // ---- set-up that reads no input, done while the previous kernel in the
+  //      stream may still be finishing: barriers, TMEM, tensor maps, and the
+  //      Q padding rows (fewer than 128 packed rows: the Q loads fill rows
+  //      0 .. R-1 of each head's 128 / HP rows only, so the rest of the Q
+  //      buffer is zeroed once, before any copy into it)
   if (tid == 0) {
-    cum[0] = 0;
     ctl->abort = 0;
     for (int s = 0; s < Sh::kKSlots; ++s) {
       mbar_init(&ctl->k_full[s], 1);
@@ -399,15 +395,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     mbar_init(&ctl->fin_pv, 1);
     fence_mbar_init();
   }
+  if (p.rows < kRowsTc / HP) {
+    for (int x = tid; x < kQBufs * static_cast<int>(TcLayout::kQBytes / 16); x += kTcThreads)
+      reinterpret_cast<uint4*>(smem + L.q)[x] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (warp == kQkWarp) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (lane == 0 && warp == kProducerWarp) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&qmap);
+  }
+  if (lane == 0 && warp == kVProducerWarp) prefetch_tmap(&vmap);
+
+  // ---- the inputs: wait for the previous kernel in the stream
+  pdl_wait();
+  pdl_launch_dependents();
+  // schedule (identical to the warp-MMA kernel)
+  for (int b = tid; b < p.num_req; b += blockDim.x) {
+    int P, n;
+    attn_lengths(p, b, P, n, blockIdx.x == 0);
+    cum[b + 1] = static_cast<int64_t>(attn_tiles(P + n)) * units_per_req;
+  }
+  if (tid == 0) cum[0] = 0;
   __syncthreads();
   if (tid == 0) {
     for (int b = 0; b < p.num_req; ++b) cum[b + 1] += cum[b];
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = ctl->tmem_base;
   const int64_t T = cum[p.num_req];
   const int64_t t_begin = wsched_begin(blockIdx.x, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
   const int64_t t_end = wsched_begin(blockIdx.x + 1, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
-  if (t_begin >= t_end) return;
+  if (t_begin >= t_end) {  // no tiles: release TMEM and leave
+    if (warp == kQkWarp) tmem_dealloc(tbase, kTmemCols);
+    return;
+  }
   const int n_tiles = static_cast<int>(t_end - t_begin);
   int b0 = 0;
   {
@@ -420,33 +447,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
   const int64_t local0 = t_begin - cum[b0];
 
-  // fewer than 128 packed rows: the Q loads fill rows 0 .. R-1 of each head's
-  // 128 / HP rows only, so the rest of each Q buffer is zeroed once (before
-  // any copy into it)
-  if (p.rows < kRowsTc / HP) {
-    for (int x = tid; x < kQBufs * static_cast<int>(TcLayout::kQBytes / 16); x += kTcThreads)
-      reinterpret_cast<uint4*>(smem + L.q)[x] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-  }
-  if (warp == kQkWarp) {
-    tmem_alloc(&ctl->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = ctl->tmem_base;
-
   if (warp == kProducerWarp || warp == kVProducerWarp) {
     // ======================= K / V producers =======================
     // Lane 0 waits for slots and issues the TMA loads; a paged tile's page
     // boxes are issued by several lanes at once.
     const bool kside = warp == kProducerWarp;
     const CUtensorMap* map = kside ? &kmap : &vmap;
-    if (lane == 0) {
-      prefetch_tmap(map);
-      if (kside) prefetch_tmap(&qmap);
-    }
     Cursor c;
     c.start(p, b0, local0);
     int issued = 0, q_issued = 0;
@@ -838,16 +844,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               *abort_flag = 1;
               break;
             }
+            // chunk ch + 1 is read from TMEM while chunk ch is staged and stored
+            uint32_t v[32], u[32];
+            tmem_ld32(lane_addr + col_o(wg), v);
+            if (other_in) tmem_ld32(lane_addr + col_o(oth), u);
+            tmem_ld_wait();
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
-              uint32_t v[32], u[32];
-              tmem_ld32(lane_addr + col_o(wg) + ch * 32, v);
-              if (other_in) tmem_ld32(lane_addr + col_o(oth) + ch * 32, u);
-              tmem_ld_wait();
               float o[32];
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 o[e] = __uint_as_float(v[e]) * f_own + (other_in ? __uint_as_float(u[e]) * f_oth : 0.f);
+              if (ch < 3) {
+                tmem_ld32(lane_addr + col_o(wg) + (ch + 1) * 32, v);
+                if (other_in) tmem_ld32(lane_addr + col_o(oth) + (ch + 1) * 32, u);
+              }
               if (complete) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -880,6 +891,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 __syncwarp();
               }
+              if (ch < 3) tmem_ld_wait();
             }
             if (lane == 0) mbar_arrive(&ctl->stg_free);            tc_fence_before();
             __syncwarp();
