@@ -249,7 +249,7 @@ def build_step(args, torch, ts, W, device):
                                  outs["src_rows"], max_kv)
             cws = ts.new_workspace(ts.tree_compact_workspace_size(ca), device)
             comp_states.append((ca, cws, kl, vl, kp, vp, P, N, par, tok, outs, side))
-            launches += 2
+            launches += 1  # re-root and row moves are one kernel
 
     def step():
         for a, ws, *_ in attn_calls:
