@@ -5,8 +5,9 @@
 // first mismatch plus the target's own token, 1 <= AL <= 1 + D) and the
 // SwiftSpec summary, Figure 2 (the target picks one path of the tree).
 //
-// Kernel 1 streams the fp32 logits once (16-byte loads, a chunk of the vocab
-// per CTA) and keeps (max, lowest index) per chunk.  Kernel 2 runs one CTA
+// Kernel 1 streams the fp32 logits once (16-byte loads, a slice of the vocab
+// per CTA, sized on the host so that all CTAs are resident at once) and keeps
+// (max, lowest index) per slice.  Kernel 2 runs one CTA
 // per request: it reduces the chunk partials to argmax[i], builds the
 // ancestor bitmasks, marks node i "ok" when token[i] equals the argmax at its
 // parent, accepts i iff every node on its root path is ok, and picks the

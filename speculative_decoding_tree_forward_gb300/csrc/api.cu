@@ -362,16 +362,25 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
 }
 
 // ------------------------------------------------------------------ acceptance
-static int accept_chunk(int vocab) {
-  const int c = 8192;
-  return vocab <= c ? ((vocab + 3) / 4) * 4 : c;
+// Vocab slice per argmax CTA: the scored rows x slices fill one resident wave
+// of 256-thread CTAs (eight per SM), each streaming its slice in steps of
+// eight 16-byte loads per thread, so the logits stream without a second wave
+// of CTA launches.  Slices are multiples of 1024 floats (16-byte aligned).
+static int accept_chunk(int vocab, int64_t rows) {
+  const int sms = device_sm_count();
+  int64_t c = 8192;
+  if (sms > 0 && rows > 0) {
+    const int64_t slices = std::max<int64_t>(1, static_cast<int64_t>(sms) * 8 / rows);
+    c = ((vocab + slices - 1) / slices + 1023) / 1024 * 1024;
+  }
+  return vocab <= c ? ((vocab + 3) / 4) * 4 : static_cast<int>(c);
 }
 
 size_t tree_accept_workspace_size(const ts_accept_args* a) {
   if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1) return 0;
-  const int chunk = accept_chunk(a->vocab);
-  const int64_t chunks = (a->vocab + chunk - 1) / chunk;
   const int64_t rows = static_cast<int64_t>(a->num_requests) * a->n_tree_max;
+  const int chunk = accept_chunk(a->vocab, rows);
+  const int64_t chunks = (a->vocab + chunk - 1) / chunk;
   return kWsHeader + align256(rows * chunks * sizeof(float)) + align256(rows * chunks * sizeof(int32_t));
 }
 
@@ -389,7 +398,7 @@ ts_status tree_accept_greedy(const ts_accept_args* a, void* workspace, size_t wo
   p.num_req = a->num_requests;
   p.n_tree_max = a->n_tree_max;
   p.vocab = a->vocab;
-  p.chunk = accept_chunk(a->vocab);
+  p.chunk = accept_chunk(a->vocab, static_cast<int64_t>(a->num_requests) * a->n_tree_max);
   p.num_chunks = (a->vocab + p.chunk - 1) / p.chunk;
   p.logits = a->logits;
   p.tokens = a->tokens;
