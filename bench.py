@@ -141,13 +141,17 @@ def attn_algorithmic_bytes(case) -> int:
     return kv + qo + lse + meta
 
 
+# the sources that decide what the attention kernels read and write
+ATTN_SOURCES = ("api.cu", "attn_common.cuh", "attn_merge.cu", "attn_mma.cu", "attn_tc.cu", "common.cuh", "internal.h",
+                "tcgen05.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_tree_forward_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in ATTN_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
