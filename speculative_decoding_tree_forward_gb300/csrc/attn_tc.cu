@@ -21,8 +21,9 @@
 //              writes the bf16 output or an fp32 split-KV partial (merged
 //              afterwards by the combine kernel, attn_merge.cu).
 //   warps 8, 11  TMA producers: warp 8 loads Q once per unit (3-D box
-//              G x n_query rows) and the K tiles into a 6-slot ring (slots
-//              2i and 2i + 1 form one 128-row operand); warp 11 loads the V
+//              G x n_query rows, into one of two Q buffers) and the K tiles
+//              into a 4-slot ring (slots 2i and 2i + 1 form one 128-row
+//              operand); warp 11 loads the V
 //              tiles, tile k into V slot 2 b + w of its S/P buffer (b, w)
 //              below.  A K slot is refilled as soon as the S that read it is
 //              computed, without queueing behind a V slot.  Tile k uses S/P
@@ -53,8 +54,8 @@ namespace ts {
 namespace {
 
 constexpr int kMaxVSlots = 4;  // V slots (one per S/P buffer)
-constexpr int kMaxKSlots = 6;  // K slots
-constexpr int kQBufs = 1;      // Q buffers (unit u uses buffer u % kQBufs)
+constexpr int kMaxKSlots = 4;  // K slots
+constexpr int kMaxQBufs = 2;   // Q buffers (unit u uses buffer u % kQBufs)
 constexpr int kTcThreads = 384;
 constexpr int kRowsTc = 128;
 constexpr int kProducerWarp = 8;  // Q and K
@@ -69,8 +70,10 @@ __host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
 // Shape of the pipeline for HP KV heads per unit.  HP = 1: a tile is 64 keys
 // of one head; each warpgroup has two 64-column S/P buffers (tile k of
 // warpgroup w = k % 2 uses buffer (k / 2) % 2 and V slot k % 4); K lives in
-// six 16 KB slots, two adjacent slots forming the 128-row operand of a tile
-// pair.  HP = 2 (packed rows R <= 64, two adjacent KV heads share one CTA):
+// four 16 KB slots, two adjacent slots forming the 128-row operand of a tile
+// pair; two Q buffers, so the next unit's Q loads while the current unit's
+// last tiles are computed.  HP = 2 (packed rows R <= 64, two adjacent KV
+// heads share one CTA):
 // a tile is 64 keys of both heads, loaded as one TMA box per page-half (keys
 // interleaved by head: shared-memory row 2 key + head); each warpgroup has one
 // 128-column S/P buffer; K lives in two 32 KB slots and V in three (a V slot
@@ -78,11 +81,12 @@ __host__ __device__ constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
 // the extra slot lets V loads run further ahead of the PVs that need them).
 template <int HP>
 struct TcShape {
-  static constexpr int kKSlots = HP == 1 ? 6 : 2;
+  static constexpr int kQBufs = HP == 1 ? 2 : 1;
+  static constexpr int kKSlots = HP == 1 ? 4 : 2;
   static constexpr int kVSlots = HP == 1 ? 4 : 3;     // slot of tile k is k % kVSlots
   static constexpr bool kVTied = HP == 1;             // V slot k % 4 = the S/P buffer of tile k
   static constexpr int kSBufs = HP == 1 ? 4 : 2;      // S/P buffers in all: tile k reuses tile k - kSBufs's
-  static constexpr uint32_t kKBytes = HP == 1 ? 6u * 16384u : 2u * 32768u;
+  static constexpr uint32_t kKBytes = HP == 1 ? 4u * 16384u : 2u * 32768u;
   static constexpr uint32_t kTileBytes = 64u * 128u * 2u * HP;  // one K or V tile (two 64-column halves)
   static constexpr uint32_t kHalfRows = 64u * HP;    // shared-memory rows of one half of a tile
   __device__ static uint32_t col_s(int w, int b) { return HP == 1 ? 128u * b + 64u * w : 128u * w; }
@@ -107,12 +111,12 @@ struct TcLayout {
   uint32_t q, k, v, ctrl, par, xch, cum, stg, total;
   static constexpr uint32_t kStgWarpBytes = 32 * 128;  // 32 rows x 128 bytes, 128-byte swizzle
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
-  static constexpr uint32_t kKVBytes = 160 * 1024;     // K ring + V ring (split per HP)
+  static constexpr uint32_t kQKVBytes = 192 * 1024;    // Q buffers + K ring + V ring (split per HP)
 };
 
 struct TcCtrl {
   uint64_t k_full[kMaxKSlots], k_empty[kMaxKSlots], v_full[kMaxVSlots], v_empty[kMaxVSlots];
-  uint64_t q_full[kQBufs], q_empty[kQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
+  uint64_t q_full[kMaxQBufs], q_empty[kMaxQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
   uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
   uint64_t stg_free;  // one phase per segment epilogue: the staging rows are reused in segment order
@@ -120,13 +124,14 @@ struct TcCtrl {
   int abort;
 };
 
-// k_bytes: the K ring's share of the K/V region (TcShape<HP>::kKBytes)
-__host__ __device__ inline TcLayout tc_layout(int num_req, uint32_t k_bytes = 6u * 16384u) {
+// q_bufs, k_bytes: TcShape<HP>::kQBufs and kKBytes (the V ring takes the
+// rest of the Q/K/V region, whose size is the same for every HP)
+__host__ __device__ inline TcLayout tc_layout(int num_req, int q_bufs = 2, uint32_t k_bytes = 4u * 16384u) {
   TcLayout L;
   L.q = 0;
-  L.k = L.q + kQBufs * TcLayout::kQBytes;
+  L.k = L.q + q_bufs * TcLayout::kQBytes;
   L.v = L.k + k_bytes;
-  L.ctrl = L.k + TcLayout::kKVBytes;
+  L.ctrl = TcLayout::kQKVBytes;
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                                                                 const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TcLayout L = tc_layout(p.num_req, TcShape<HP>::kKBytes);
+  const TcLayout L = tc_layout(p.num_req, TcShape<HP>::kQBufs, TcShape<HP>::kKBytes);
   TcCtrl* ctl = reinterpret_cast<TcCtrl*>(smem + L.ctrl);
   int64_t* cum = reinterpret_cast<int64_t*>(smem + L.cum);
   volatile int* abort_flag = &ctl->abort;
@@ -377,7 +382,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->v_empty[s], 1);
     }
-    for (int i = 0; i < kQBufs; ++i) {
+    for (int i = 0; i < Sh::kQBufs; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
     }
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     fence_mbar_init();
   }
   if (p.rows < kRowsTc / HP) {
-    for (int x = tid; x < kQBufs * static_cast<int>(TcLayout::kQBytes / 16); x += kTcThreads)
+    for (int x = tid; x < Sh::kQBufs * static_cast<int>(TcLayout::kQBytes / 16); x += kTcThreads)
       reinterpret_cast<uint4*>(smem + L.q)[x] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
@@ -462,10 +467,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     bool ok = true;
     for (int it = 0; it < n_tiles; ++it) {
       if (kside && (it == 0 || c.tile == 0)) {
-        // buffer u % kQBufs is free once the QK^T of unit u - kQBufs are done
-        const int qb = c.unit % kQBufs;
+        // buffer u % Sh::kQBufs is free once the QK^T of unit u - Sh::kQBufs are done
+        const int qb = c.unit % Sh::kQBufs;
         if (lane == 0) {
-          ok = c.unit < kQBufs || mbar_wait(&ctl->q_empty[qb], ((c.unit / kQBufs) - 1) & 1);
+          ok = c.unit < Sh::kQBufs || mbar_wait(&ctl->q_empty[qb], ((c.unit / Sh::kQBufs) - 1) & 1);
           if (ok) {
             mbar_arrive_expect_tx(&ctl->q_full[qb], static_cast<uint32_t>(HP * p.rows) * 256u);
             for (int h = 0; h < 2; ++h)
@@ -512,8 +517,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // never leave with copies into this CTA's shared memory in flight
       if (lane == 0) {
         drain_ring(kside ? ctl->k_full : ctl->v_full, kside ? Sh::kKSlots : Sh::kVSlots, issued);
-        for (int u = max(q_issued - kQBufs, 0); u < q_issued; ++u)
-          mbar_wait(&ctl->q_full[u % kQBufs], static_cast<uint32_t>((u / kQBufs) & 1));
+        for (int u = max(q_issued - Sh::kQBufs, 0); u < q_issued; ++u)
+          mbar_wait(&ctl->q_full[u % Sh::kQBufs], static_cast<uint32_t>((u / Sh::kQBufs) & 1));
       }
     }
   } else if (warp == kQkWarp) {
@@ -531,8 +536,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // HP = 1: two consecutive tiles of one unit as one N = 128 product
         const bool pair = HP == 1 && (k & 1) == 0 && k + 1 < n_tiles && cq.tile != cq.tiles - 1;
         const int cnt = pair ? 2 : 1;
-        const int qb = cq.unit % kQBufs;
-        if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full[qb], (cq.unit / kQBufs) & 1)) { ok = false; break; }
+        const int qb = cq.unit % Sh::kQBufs;
+        if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full[qb], (cq.unit / Sh::kQBufs) & 1)) { ok = false; break; }
         for (int t = k; t < k + cnt && ok; ++t)
           ok = mbar_wait(&ctl->k_full[t % Sh::kKSlots], (t / Sh::kKSlots) & 1) &&
                (t < Sh::kSBufs || mbar_wait(&ctl->pv_done[t & 1][Sh::buf(t)], (Sh::use(t) - 1) & 1));
