@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--force-path", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
     return ap.parse_args()
 
 
@@ -489,6 +490,30 @@ def main():
     attn_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps / n_attn
     ms_max = max_over_ranks(ms, world)
 
+    # the same step captured once as a CUDA graph and replayed (launch
+    # latency off the host; the kernels and their dependencies are the same)
+    graph = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+                flush_r.max()
+            gev[i][0].record(stream)
+            g.replay()
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        g_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in gev) / args.steps, world)
+        graph = {"ms_per_step": g_ms, "value": replica_value(info["tokens_per_step"], world, g_ms), "unit": UNIT}
+        del g
+
     tokens = info["tokens_per_step"] * world
     value = replica_value(info["tokens_per_step"], world, ms_max)
     peak, peak_kind = peaks()
@@ -529,6 +554,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": info["launches"] * args.steps,
+        "graph": graph,
         "clocks": ck,
     }
     print(json.dumps(line))

@@ -31,6 +31,8 @@
 // item a row is read, at the latest, in the batch that overwrites it, and
 // every read of a batch precedes its stores: no row is overwritten before it
 // is read.  Items of different CTAs are disjoint.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -270,10 +272,26 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
 
 }  // namespace
 
+// The dynamic shared-memory limit is raised once per device (to the largest
+// staging batch), so a launch is a plain stream operation (graph capture).
+static bool compact_smem_ready() {
+  static std::mutex m;
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(m);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kCompactBatchBytes)) != cudaSuccess)
+      return false;
+    done[dev] = true;
+  }
+  return true;
+}
+
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(p.batch_vecs) * 16;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (smem > 48 * 1024 && !compact_smem_ready()) return cudaErrorInvalidValue;
   const int items = 2 * p.num_layers;
   const int ctas = (items + p.items_per_cta - 1) / p.items_per_cta;
   return launch_pdl(compact_kernel, dim3(ctas, p.num_req), dim3(kCompactThreads), smem, stream, p);
