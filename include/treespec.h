@@ -262,6 +262,90 @@ TS_API ts_status tree_cache_compact(const ts_compact_args* args, void* workspace
                              void* stream);
 
 /* ------------------------------------------------------------------------
+ * Draft-side tree growth: maximum-likelihood expansion (one step) and the
+ * selection of the most promising subtree.
+ *
+ * SwiftSpec summary, §3.1.1 (the draft worker's iteration: Expand the w most
+ * probable leaves d times while the target verifies, then Select a subtree
+ * of size bs) and §3.1.3 (a node's value is the log-softmax probability of
+ * its token under the draft model, its weight the sum of the values from
+ * the root; the leaves to expand come from a priority queue); Figure 2
+ * (w = 2 nodes per expansion, six in d = 3 steps).
+ *
+ * Per request b and node i < n_tree[b] (row stride n_tree_max): parent,
+ * token, weight (fp32), and the node's candidate children
+ * cand_tok[b][i][0..k), cand_lp[b][i][0..k) (token ids and log-softmax
+ * values in decreasing order, ties to the lower token id; token -1 with
+ * -inf past the vocabulary), of which the first cand_taken[b][i] have become
+ * children (k: none known).
+ *
+ * tree_expand, one step, per request:
+ *  1. each row r of `logits` with rows[b][r] in [0, n) gives that node its k
+ *     candidates (the row's k largest logits, value = logit - log-sum-exp of
+ *     the row) and cand_taken = 0;
+ *  2. w times: among the nodes with a candidate left, the one whose next
+ *     candidate has the largest weight[node] + cand_lp (ties: the lower node
+ *     index) gives it up: node n is appended with that parent, token and
+ *     weight, cand_taken = k, and the parent's cand_taken grows by one.
+ *     Growth stops at n_tree_max or when no candidate is left;
+ *  3. added[b][0..w) gets the new nodes in order (-1 past the last): the
+ *     next draft queries.  n_tree grows accordingly.
+ *  `added` may alias `rows`.  Workspace: tree_expand_workspace_size().
+ *  Errors: TS_ERR_UNSUPPORTED if n_tree_max > TS_MAX_TREE, w or k > 16.
+ *  Device: a row node outside [0, n) is ignored (TS_DEVERR_BAD_LENGTH).
+ *
+ * tree_select_subtree, per request: the min(bs, n) nodes of largest weight
+ *  (ties: lower index), in index order: keep[b][j] = old index,
+ *  new_parent[b][j] (remapped; -1 where the old parent is -1), new_tokens,
+ *  new_weight, n_sel[b]; entries past n_sel are -1 / 0 / -inf.  Weights built
+ *  by tree_expand never increase from a parent to a child, so the set holds
+ *  every selected node's parent; a selected node whose parent is not
+ *  selected (weights from elsewhere) gets new parent -1 and
+ *  TS_DEVERR_BAD_PARENT.  Workspace: tree_select_workspace_size().
+ * ------------------------------------------------------------------------ */
+#define TS_MAX_EXPAND 16
+
+typedef struct ts_expand_args {
+  int num_requests;
+  int n_tree_max;          /* capacity and row stride, <= TS_MAX_TREE */
+  int vocab;               /* >= 1 */
+  int w;                   /* rows of logits and nodes added per step, 1..TS_MAX_EXPAND */
+  int k;                   /* candidates per node, 1..TS_MAX_EXPAND */
+  const float* logits;     /* device [num_requests][w][vocab] */
+  const int32_t* rows;     /* device [num_requests][w]: node of each logits row, -1 = none */
+  int32_t* n_tree;         /* device [num_requests] (in/out) */
+  int32_t* parent;         /* device [num_requests][n_tree_max] (in/out) */
+  int32_t* tokens;         /* device [num_requests][n_tree_max] (in/out) */
+  float* weight;           /* device [num_requests][n_tree_max] (in/out) */
+  int32_t* cand_tok;       /* device [num_requests][n_tree_max][k] (in/out) */
+  float* cand_lp;          /* device [num_requests][n_tree_max][k] (in/out) */
+  int32_t* cand_taken;     /* device [num_requests][n_tree_max] (in/out) */
+  int32_t* added;          /* device [num_requests][w] (out; may alias rows) */
+} ts_expand_args;
+
+TS_API size_t tree_expand_workspace_size(const ts_expand_args* args);
+TS_API ts_status tree_expand(const ts_expand_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+typedef struct ts_select_args {
+  int num_requests;
+  int n_tree_max;          /* row stride of the inputs, <= TS_MAX_TREE */
+  int bs;                  /* nodes to keep, >= 1; row stride of the outputs */
+  const int32_t* n_tree;   /* device [num_requests] */
+  const int32_t* parent;   /* device [num_requests][n_tree_max] */
+  const int32_t* tokens;   /* device [num_requests][n_tree_max] */
+  const float* weight;     /* device [num_requests][n_tree_max] */
+  int32_t* keep;           /* device [num_requests][bs] (out) */
+  int32_t* new_parent;     /* device [num_requests][bs] (out) */
+  int32_t* new_tokens;     /* device [num_requests][bs] (out) */
+  float* new_weight;       /* device [num_requests][bs] (out) */
+  int32_t* n_sel;          /* device [num_requests] (out) */
+} ts_select_args;
+
+TS_API size_t tree_select_workspace_size(const ts_select_args* args);
+TS_API ts_status tree_select_subtree(const ts_select_args* args, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
  * Status and error reporting.
  * ------------------------------------------------------------------------ */
 TS_API const char* ts_status_string(ts_status status);

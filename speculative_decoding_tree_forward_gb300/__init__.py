@@ -58,6 +58,18 @@ class CompactArgs(ctypes.Structure):
                 ("src_rows", _vp)]
 
 
+class ExpandArgs(ctypes.Structure):
+    _fields_ = [("num_requests", _i32), ("n_tree_max", _i32), ("vocab", _i32), ("w", _i32), ("k", _i32),
+                ("logits", _vp), ("rows", _vp), ("n_tree", _vp), ("parent", _vp), ("tokens", _vp), ("weight", _vp),
+                ("cand_tok", _vp), ("cand_lp", _vp), ("cand_taken", _vp), ("added", _vp)]
+
+
+class SelectArgs(ctypes.Structure):
+    _fields_ = [("num_requests", _i32), ("n_tree_max", _i32), ("bs", _i32), ("n_tree", _vp), ("parent", _vp),
+                ("tokens", _vp), ("weight", _vp), ("keep", _vp), ("new_parent", _vp), ("new_tokens", _vp),
+                ("new_weight", _vp), ("n_sel", _vp)]
+
+
 def _sig(name, restype, argtypes):
     f = getattr(_lib, name)
     f.restype = restype
@@ -75,6 +87,10 @@ _acc_ws = _sig("tree_accept_workspace_size", ctypes.c_size_t, [ctypes.POINTER(Ac
 _acc = _sig("tree_accept_greedy", _i32, [ctypes.POINTER(AcceptArgs), _vp, ctypes.c_size_t, _vp])
 _cmp_ws = _sig("tree_compact_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CompactArgs)])
 _cmp = _sig("tree_cache_compact", _i32, [ctypes.POINTER(CompactArgs), _vp, ctypes.c_size_t, _vp])
+_exp_ws = _sig("tree_expand_workspace_size", ctypes.c_size_t, [ctypes.POINTER(ExpandArgs)])
+_exp = _sig("tree_expand", _i32, [ctypes.POINTER(ExpandArgs), _vp, ctypes.c_size_t, _vp])
+_sel_ws = _sig("tree_select_workspace_size", ctypes.c_size_t, [ctypes.POINTER(SelectArgs)])
+_sel = _sig("tree_select_subtree", _i32, [ctypes.POINTER(SelectArgs), _vp, ctypes.c_size_t, _vp])
 _status_string = _sig("ts_status_string", ctypes.c_char_p, [_i32])
 _read_err = _sig("ts_read_device_error", _i32, [_vp, ctypes.POINTER(_i32), _i32, _vp])
 _version = _sig("ts_version", _i32, [])
@@ -82,7 +98,8 @@ _version = _sig("ts_version", _i32, [])
 EXPORTED = ["tree_meta_workspace_size", "tree_build_mask", "tree_attn_workspace_size", "tree_attn_selected_path",
             "tree_attn_forward", "tree_attn_forward_noalloc",
             "tree_accept_workspace_size", "tree_accept_greedy", "tree_compact_workspace_size",
-            "tree_cache_compact", "ts_status_string", "ts_read_device_error", "ts_version"]
+            "tree_cache_compact", "tree_expand_workspace_size", "tree_expand", "tree_select_workspace_size",
+            "tree_select_subtree", "ts_status_string", "ts_read_device_error", "ts_version"]
 
 
 class TreeSpecError(RuntimeError):
@@ -325,3 +342,86 @@ def tree_cache_compact(k_layers: Sequence[torch.Tensor], v_layers: Sequence[torc
     tree_cache_compact_args(a, workspace, stream)
     out["_ptr_tables"] = (kp, vp)   # keep the pointer tables alive until the stream reaches the kernels
     return out
+
+
+# ------------------------------------------------------------------ draft-side expansion and selection
+TS_MAX_EXPAND = 16
+
+
+class DraftTree:
+    """Device state of a batch of draft trees for ``tree_expand`` (per node:
+    parent, token, weight, and k candidate children with their log-probs and
+    how many have been taken)."""
+
+    def __init__(self, num_requests: int, n_tree_max: int, k: int, device=None):
+        dev = device or "cuda"
+        B, N = num_requests, n_tree_max
+        self.k = k
+        self.n_tree = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.parent = torch.full((B, N), -1, dtype=torch.int32, device=dev)
+        self.tokens = torch.zeros((B, N), dtype=torch.int32, device=dev)
+        self.weight = torch.zeros((B, N), dtype=torch.float32, device=dev)
+        self.cand_tok = torch.full((B, N, k), -1, dtype=torch.int32, device=dev)
+        self.cand_lp = torch.full((B, N, k), float("-inf"), dtype=torch.float32, device=dev)
+        self.cand_taken = torch.full((B, N), k, dtype=torch.int32, device=dev)
+
+
+def expand_args(tree: DraftTree, logits: torch.Tensor, rows: torch.Tensor, added: torch.Tensor) -> ExpandArgs:
+    """logits fp32 [B][w][vocab] (16-byte aligned rows when vocab % 4 == 0), rows / added int32 [B][w]."""
+    B, w, V = logits.shape
+    a = ExpandArgs()
+    a.num_requests, a.n_tree_max, a.vocab, a.w, a.k = B, tree.parent.shape[1], V, w, tree.k
+    a.logits, a.rows = logits.data_ptr(), rows.data_ptr()
+    a.n_tree, a.parent, a.tokens, a.weight = (tree.n_tree.data_ptr(), tree.parent.data_ptr(),
+                                              tree.tokens.data_ptr(), tree.weight.data_ptr())
+    a.cand_tok, a.cand_lp, a.cand_taken = tree.cand_tok.data_ptr(), tree.cand_lp.data_ptr(), tree.cand_taken.data_ptr()
+    a.added = added.data_ptr()
+    return a
+
+
+def tree_expand_workspace_size(args: ExpandArgs) -> int:
+    n = _exp_ws(ctypes.byref(args))
+    if n == 0:
+        raise TreeSpecError(TS_ERR_INVALID_ARG, "tree_expand_workspace_size")
+    return n
+
+
+def tree_expand_args(args: ExpandArgs, workspace: torch.Tensor, stream=None) -> None:
+    _check(_exp(ctypes.byref(args), workspace.data_ptr(), workspace.numel(), _stream(stream)), "tree_expand")
+
+
+def tree_expand(tree: DraftTree, logits: torch.Tensor, rows: torch.Tensor, workspace=None, stream=None) -> torch.Tensor:
+    """One maximum-likelihood expansion step in place; returns the added nodes [B][w] (-1 past the last)."""
+    added = torch.empty_like(rows)
+    a = expand_args(tree, logits, rows, added)
+    if workspace is None:
+        workspace = new_workspace(tree_expand_workspace_size(a), logits.device)
+    tree_expand_args(a, workspace, stream)
+    return added
+
+
+def select_args(n_tree, parent, tokens, weight, bs: int, out: dict) -> SelectArgs:
+    B, N = parent.shape
+    a = SelectArgs()
+    a.num_requests, a.n_tree_max, a.bs = B, N, bs
+    a.n_tree, a.parent, a.tokens, a.weight = n_tree.data_ptr(), parent.data_ptr(), tokens.data_ptr(), weight.data_ptr()
+    a.keep, a.new_parent, a.new_tokens = out["keep"].data_ptr(), out["new_parent"].data_ptr(), out["new_tokens"].data_ptr()
+    a.new_weight, a.n_sel = out["new_weight"].data_ptr(), out["n_sel"].data_ptr()
+    return a
+
+
+def tree_select_subtree(n_tree, parent, tokens, weight, bs: int, workspace=None, stream=None) -> dict:
+    """The bs heaviest nodes of each tree, in index order, with remapped parents."""
+    B = parent.shape[0]
+    dev = parent.device
+    out = {"keep": torch.empty((B, bs), dtype=torch.int32, device=dev),
+           "new_parent": torch.empty((B, bs), dtype=torch.int32, device=dev),
+           "new_tokens": torch.empty((B, bs), dtype=torch.int32, device=dev),
+           "new_weight": torch.empty((B, bs), dtype=torch.float32, device=dev),
+           "n_sel": torch.empty(B, dtype=torch.int32, device=dev)}
+    a = select_args(n_tree, parent, tokens, weight, bs, out)
+    if workspace is None:
+        workspace = new_workspace(int(_sel_ws(ctypes.byref(a))), dev)
+    _check(_sel(ctypes.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "tree_select_subtree")
+    return out
+

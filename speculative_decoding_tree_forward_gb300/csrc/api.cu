@@ -493,4 +493,87 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ draft-side expansion and selection
+// Vocab slice per candidate CTA (a multiple of 1024 floats): the queried rows
+// x slices fill about one resident wave (eight 256-thread CTAs per SM), with
+// at most 16 slices per row for the merge.
+static int expand_slice(int vocab, int64_t rows) {
+  const int sms = device_sm_count();
+  int64_t slices = 16;
+  if (sms > 0 && rows > 0) slices = std::min<int64_t>(16, std::max<int64_t>(1, static_cast<int64_t>(sms) * 8 / rows));
+  return static_cast<int>(((vocab + slices - 1) / slices + 1023) / 1024 * 1024);
+}
+
+size_t tree_expand_workspace_size(const ts_expand_args* a) {
+  if (a == nullptr || a->num_requests < 1 || a->w < 1 || a->w > TS_MAX_EXPAND || a->vocab < 1) return 0;
+  const int64_t rows = static_cast<int64_t>(a->num_requests) * a->w;
+  const int slice = expand_slice(a->vocab, rows);
+  const int64_t slices = (a->vocab + slice - 1) / slice;
+  return kWsHeader + align256(static_cast<size_t>(rows * slices) * sizeof(CandPartial));
+}
+
+ts_status tree_expand(const ts_expand_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1 || a->w < 1 || a->k < 1)
+    return TS_ERR_INVALID_ARG;
+  if (a->n_tree_max > TS_MAX_TREE || a->w > TS_MAX_EXPAND || a->k > TS_MAX_EXPAND) return TS_ERR_UNSUPPORTED;
+  if (!a->logits || !a->rows || !a->n_tree || !a->parent || !a->tokens || !a->weight || !a->cand_tok ||
+      !a->cand_lp || !a->cand_taken || !a->added)
+    return TS_ERR_INVALID_ARG;
+  if (!aligned(a->logits, (a->vocab % 4 == 0) ? 16 : 4)) return TS_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(a->num_requests) * a->w;
+  if (rows > INT32_MAX) return TS_ERR_UNSUPPORTED;
+  const size_t need = tree_expand_workspace_size(a);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ExpandParams p;
+  p.num_req = a->num_requests;
+  p.n_tree_max = a->n_tree_max;
+  p.vocab = a->vocab;
+  p.w = a->w;
+  p.k = a->k;
+  p.slice = expand_slice(a->vocab, rows);
+  p.num_slices = (a->vocab + p.slice - 1) / p.slice;
+  p.logits = a->logits;
+  p.rows = a->rows;
+  p.n_tree = a->n_tree;
+  p.parent = a->parent;
+  p.tokens = a->tokens;
+  p.weight = a->weight;
+  p.cand_tok = a->cand_tok;
+  p.cand_lp = a->cand_lp;
+  p.cand_taken = a->cand_taken;
+  p.added = a->added;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.part = reinterpret_cast<CandPartial*>(ws + kWsHeader);
+  cudaError_t e = launch_expand(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+size_t tree_select_workspace_size(const ts_select_args* a) { return a == nullptr ? 0 : kWsHeader; }
+
+ts_status tree_select_subtree(const ts_select_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->bs < 1) return TS_ERR_INVALID_ARG;
+  if (a->n_tree_max > TS_MAX_TREE) return TS_ERR_UNSUPPORTED;
+  if (!a->n_tree || !a->parent || !a->tokens || !a->weight || !a->keep || !a->new_parent || !a->new_tokens ||
+      !a->new_weight || !a->n_sel)
+    return TS_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWsHeader || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  SelectParams p;
+  p.num_req = a->num_requests;
+  p.n_tree_max = a->n_tree_max;
+  p.bs = a->bs;
+  p.n_tree = a->n_tree;
+  p.parent = a->parent;
+  p.tokens = a->tokens;
+  p.weight = a->weight;
+  p.keep = a->keep;
+  p.new_parent = a->new_parent;
+  p.new_tokens = a->new_tokens;
+  p.new_weight = a->new_weight;
+  p.n_sel = a->n_sel;
+  p.err = reinterpret_cast<unsigned*>(workspace);
+  cudaError_t e = launch_select(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -122,4 +122,45 @@ struct CompactParams {
 };
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream);
 
+// One (row, vocab slice) partial of the draft-candidate pass: running max m,
+// sum of exp(logit - m), and the slice's TS_MAX_EXPAND largest logits.
+struct CandPartial {
+  float m, s;
+  float val[TS_MAX_EXPAND];
+  int idx[TS_MAX_EXPAND];
+};
+
+struct ExpandParams {
+  int num_req, n_tree_max, vocab, w, k;
+  int slice, num_slices;   // vocab floats per candidate CTA (multiple of 1024), slices per row (<= 32)
+  const float* logits;
+  const int32_t* rows;
+  int32_t* n_tree;
+  int32_t* parent;
+  int32_t* tokens;
+  float* weight;
+  int32_t* cand_tok;
+  float* cand_lp;
+  int32_t* cand_taken;
+  int32_t* added;
+  unsigned* err;
+  CandPartial* part;       // [num_req * w][num_slices]
+};
+cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
+
+struct SelectParams {
+  int num_req, n_tree_max, bs;
+  const int32_t* n_tree;
+  const int32_t* parent;
+  const int32_t* tokens;
+  const float* weight;
+  int32_t* keep;
+  int32_t* new_parent;
+  int32_t* new_tokens;
+  float* new_weight;
+  int32_t* n_sel;
+  unsigned* err;
+};
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+
 }  // namespace ts
