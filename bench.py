@@ -205,6 +205,38 @@ def build_step(args, torch, ts, W, device):
     info["attn_inputs"] = attn_calls
     launches = 2 * len(attn_calls)
 
+    # draft-side iteration (config 2): each attention call queries the w nodes
+    # an expansion step just added to the tree it reads; a subtree is
+    # selected at the end; the tree is reset to its initial state first
+    draft = None
+    if w.draft is not None:
+        D = w.draft
+        tree = ts.DraftTree(D.num_req, D.parent.shape[1], D.k, device)
+        for name in ("parent", "tokens", "weight", "cand_tok", "cand_lp", "cand_taken"):
+            getattr(tree, name).copy_(torch.from_numpy(getattr(D, name)).to(device))
+        n0 = torch.full((D.num_req,), D.n0, dtype=torch.int32, device=device)
+        taken0 = tree.cand_taken.clone()
+        tree.n_tree.copy_(n0)
+        dlogits = [torch.from_numpy(x).to(device) for x in D.logits]
+        added = [torch.full((D.num_req, D.w), -1, dtype=torch.int32, device=device) for _ in attn_calls]
+        rows0 = torch.full((D.num_req, D.w), -1, dtype=torch.int32, device=device)
+        exp_args = [ts.expand_args(tree, dlogits[max(e - 1, 0)], added[e - 1] if e > 0 else rows0, added[e])
+                    for e in range(len(attn_calls))]   # expansion 1 queries no row: its logits are not read
+        ews = ts.new_workspace(max(ts.tree_expand_workspace_size(x) for x in exp_args), device)
+        sel_out = {"keep": torch.empty((D.num_req, D.bs), dtype=torch.int32, device=device),
+                   "new_parent": torch.empty((D.num_req, D.bs), dtype=torch.int32, device=device),
+                   "new_tokens": torch.empty((D.num_req, D.bs), dtype=torch.int32, device=device),
+                   "new_weight": torch.empty((D.num_req, D.bs), dtype=torch.float32, device=device),
+                   "n_sel": torch.empty(D.num_req, dtype=torch.int32, device=device)}
+        sel = ts.select_args(tree.n_tree, tree.parent, tree.tokens, tree.weight, D.bs, sel_out)
+        sws = ts.new_workspace(256, device)
+        for a, *_ in attn_calls:   # the attention calls read the tree the expansions grow
+            a.parent, a.n_tree = tree.parent.data_ptr(), tree.n_tree.data_ptr()
+        draft = dict(tree=tree, n0=n0, taken0=taken0, exp_args=exp_args, ews=ews, sel=sel, sws=sws,
+                     sel_out=sel_out, logits=dlogits, added=added)
+        launches += 2 * len(attn_calls) + 1
+        info["expand_logit_bytes"] = sum(x.nbytes for x in D.logits)
+
     acc_state = None
     if w.accept is not None:
         A = w.accept
@@ -256,16 +288,30 @@ def build_step(args, torch, ts, W, device):
             comp_states.append((ca, cws, kl, vl, kp, vp, P, N, par, tok, outs, side))
             launches += 1  # re-root and row moves are one kernel
 
+    # the step as phases: ("attn" | "accept" | "other", [calls]); attention
+    # phases are the ones the roofline times
+    phases = []
+    if draft is not None:
+        dt = draft
+        phases.append(("other", [lambda: (dt["tree"].n_tree.copy_(dt["n0"]), dt["tree"].cand_taken.copy_(dt["taken0"]))]))
+        for e, (a, ws, *_) in enumerate(attn_calls):
+            phases.append(("other", [lambda x=dt["exp_args"][e]: ts.tree_expand_args(x, dt["ews"])]))
+            phases.append(("attn", [lambda a=a, ws=ws: ts.tree_attn_forward_args(a, ws)]))
+        phases.append(("other", [lambda: ts.tree_select_subtree_args(dt["sel"], dt["sws"])]))
+    else:
+        phases.append(("attn", [lambda a=a, ws=ws: ts.tree_attn_forward_args(a, ws) for a, ws, *_ in attn_calls]))
+    if acc_state is not None:
+        phases.append(("accept", [lambda: ts.tree_accept_greedy_args(acc_state[0], acc_state[1])]))
+    if comp_states:
+        phases.append(("other", [lambda st=st: ts.tree_cache_compact_args(st[0], st[1]) for st in comp_states]))
+
     def step():
-        for a, ws, *_ in attn_calls:
-            ts.tree_attn_forward_args(a, ws)
-        if acc_state is not None:
-            ts.tree_accept_greedy_args(acc_state[0], acc_state[1])
-        for st in comp_states:
-            ts.tree_cache_compact_args(st[0], st[1])
+        for _, calls in phases:
+            for f in calls:
+                f()
 
     info.update(tokens_per_step=tokens_per_step, launches=launches, acc_state=acc_state, comp_states=comp_states,
-                workload_obj=w)
+                workload_obj=w, phases=phases, draft=draft)
     return step, info
 
 
@@ -280,6 +326,8 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     main_in, main_host = [], []
     for a, ws, d, out, lse in info["attn_inputs"]:
         main_in.append(d["q"])
+    if info["draft"] is not None:
+        main_in += info["draft"]["logits"]   # draft logits of the nodes the expansions query
     acc = info["acc_state"]
     side_in = [acc[2], acc[3]] if acc is not None else []
     for st in info["comp_states"]:
@@ -292,6 +340,8 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
         outs += list(acc[4].values())
     for st in info["comp_states"]:
         outs += list(st[10].values())
+    if info["draft"] is not None:
+        outs += list(info["draft"]["sel_out"].values())
     host_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in main_host + side_host)
     d2h = sum(t.numel() * t.element_size() for t in host_outs)
@@ -309,14 +359,16 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
         copied.record(side)
         for h, dv in zip(main_host, main_in):
             dv.copy_(h, non_blocking=True)
-        for a, ws, *_ in info["attn_inputs"]:
-            ts.tree_attn_forward_args(a, ws)
-        main.wait_event(copied)
-        if acc is not None:
-            ts.tree_accept_greedy_args(acc[0], acc[1])
-        consumed.record(main)
-        for st in info["comp_states"]:
-            ts.tree_cache_compact_args(st[0], st[1])
+        for kind, calls in info["phases"]:
+            if kind == "accept":
+                main.wait_event(copied)
+            for f in calls:
+                f()
+            if kind == "accept":
+                consumed.record(main)
+        if acc is None:
+            main.wait_event(copied)
+            consumed.record(main)
         for dv, h in zip(outs, host_outs):
             h.copy_(dv, non_blocking=True)
 
@@ -449,7 +501,9 @@ def main():
 
     # attention launches timed on the launching stream inside the timed region
     n_attn = len(info["attn_inputs"])
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    n_phases = sum(1 for kind, _ in info["phases"] if kind == "attn")
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_phases)]
+          for _ in range(args.steps)]
     clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3)
     barrier(world)
@@ -470,14 +524,15 @@ def main():
             flush.zero_()
             flush_r.max()
         step_ev[i][0].record(stream)
-        ev[i][0].record(stream)
-        for a, ws, *_ in info["attn_inputs"]:
-            ts.tree_attn_forward_args(a, ws)
-        ev[i][1].record(stream)
-        if info["acc_state"] is not None:
-            ts.tree_accept_greedy_args(info["acc_state"][0], info["acc_state"][1])
-        for st in info["comp_states"]:
-            ts.tree_cache_compact_args(st[0], st[1])
+        j = 0
+        for kind, calls in info["phases"]:
+            if kind == "attn":
+                ev[i][j][0].record(stream)
+            for f in calls:
+                f()
+            if kind == "attn":
+                ev[i][j][1].record(stream)
+                j += 1
         step_ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -487,7 +542,7 @@ def main():
         ms = t_start.elapsed_time(t_end) / args.steps
     else:
         ms = sum(a.elapsed_time(b) for a, b in step_ev) / args.steps
-    attn_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps / n_attn
+    attn_ms = sum(a.elapsed_time(b) for evs in ev for a, b in evs) / args.steps / n_attn
     ms_max = max_over_ranks(ms, world)
 
     # the same step captured once as a CUDA graph and replayed (launch
@@ -541,7 +596,7 @@ def main():
         "config": {"workload": info["workload"], "requests": info["attn_cases"][0].num_req,
                    "q_heads": info["attn_cases"][0].num_q_heads, "kv_heads": info["attn_cases"][0].num_kv_heads,
                    "head_dim": info["attn_cases"][0].head_dim, "tree_nodes": info["attn_cases"][0].n_tree_max,
-                   "layers_compacted": args.layers if info["comp_states"] else 0, "attention_path": path,
+                   "layers_compacted": args.layers if info["comp_states"] else 0, "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
                    "l2": ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2" % (attn_bytes / 1e6)
                           if flush is None else
                           "L2 flushed (258 MB write, then 258 MB read) before every timed step, outside the step times: "

@@ -410,6 +410,10 @@ def select_args(n_tree, parent, tokens, weight, bs: int, out: dict) -> SelectArg
     return a
 
 
+def tree_select_subtree_args(args: SelectArgs, workspace: torch.Tensor, stream=None) -> None:
+    _check(_sel(ctypes.byref(args), workspace.data_ptr(), workspace.numel(), _stream(stream)), "tree_select_subtree")
+
+
 def tree_select_subtree(n_tree, parent, tokens, weight, bs: int, workspace=None, stream=None) -> dict:
     """The bs heaviest nodes of each tree, in index order, with remapped parents."""
     B = parent.shape[0]

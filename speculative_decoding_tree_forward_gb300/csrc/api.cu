@@ -494,13 +494,14 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
 }
 
 // ------------------------------------------------------------------ draft-side expansion and selection
-// Vocab slice per candidate CTA (a multiple of 1024 floats): the queried rows
-// x slices fill about one resident wave (eight 256-thread CTAs per SM), with
-// at most 16 slices per row for the merge.
+// Vocab slice per candidate CTA (a multiple of 1024 floats): as many slices
+// as keep the SMs busy (about one resident wave of 256-thread CTAs), at most
+// 16 per row for the merge.
 static int expand_slice(int vocab, int64_t rows) {
   const int sms = device_sm_count();
-  int64_t slices = 16;
-  if (sms > 0 && rows > 0) slices = std::min<int64_t>(16, std::max<int64_t>(1, static_cast<int64_t>(sms) * 8 / rows));
+  int64_t slices = std::min<int64_t>(16, (vocab + 1023) / 1024);
+  if (sms > 0 && rows > 0) slices = std::min<int64_t>(slices, std::max<int64_t>(1, static_cast<int64_t>(sms) * 8 / rows));
+  slices = std::max<int64_t>(slices, 1);
   return static_cast<int>(((vocab + slices - 1) / slices + 1023) / 1024 * 1024);
 }
 

@@ -9,10 +9,11 @@
 //
 // Kernel 1 (candidates) streams the draft logits of the queried nodes once:
 // each CTA takes a vocab slice of one row with 16-byte loads and keeps, per
-// thread, an online log-sum-exp and its K largest logits (ties: lower token);
-// the block merges them (K rounds of a warp arg-max over list heads) and
-// writes one partial per (row, slice).  The slices are sized so that all
-// CTAs are resident at once.
+// thread, an online log-sum-exp and a sorted list of its largest logits
+// (ties: lower token; 8 or 16 long, the smallest that holds k); the block
+// merges the lists (one warp arg-max over list heads per entry) and writes
+// one partial per (row, slice).  Per batch of eight 16-byte loads the
+// log-sum-exp takes the batch max first, so its exponentials are independent.
 // Kernel 2 (step) runs one CTA per request: it merges a row's partials into
 // the node's k candidates (value = logit - log-sum-exp), then makes the w
 // picks of the step, each a block-wide arg-max over the nodes' next
@@ -25,7 +26,7 @@ namespace ts {
 namespace {
 
 constexpr int kCandThreads = 256;
-constexpr int K = TS_MAX_EXPAND;
+constexpr int K = TS_MAX_EXPAND;  // candidate slots stored per (row, slice) and per node
 
 // (value, index) order of the candidate lists: larger value first, then the
 // lower index
@@ -33,12 +34,13 @@ __device__ __forceinline__ bool ahead(float v, int i, float bv, int bi) { return
 
 // Inserts (x, i) into a list sorted by `ahead`; x arrives with the largest
 // index seen so far, so an equal value stays behind the entries present.
-__device__ __forceinline__ void list_insert(float (&val)[K], int (&idx)[K], float x, int i) {
-  if (!(x > val[K - 1])) return;
+template <int KL>
+__device__ __forceinline__ void list_insert(float (&val)[KL], int (&idx)[KL], float x, int i) {
+  if (!(x > val[KL - 1])) return;
   float cv = x;
   int ci = i;
 #pragma unroll
-  for (int j = 0; j < K; ++j) {
+  for (int j = 0; j < KL; ++j) {
     if (cv > val[j]) {
       const float tv = val[j];
       const int ti = idx[j];
@@ -51,22 +53,24 @@ __device__ __forceinline__ void list_insert(float (&val)[K], int (&idx)[K], floa
 }
 
 // Drops the head of a sorted list (the next entry becomes the head).
-__device__ __forceinline__ void list_pop(float (&val)[K], int (&idx)[K]) {
+template <int KL>
+__device__ __forceinline__ void list_pop(float (&val)[KL], int (&idx)[KL]) {
 #pragma unroll
-  for (int j = 0; j < K - 1; ++j) {
+  for (int j = 0; j < KL - 1; ++j) {
     val[j] = val[j + 1];
     idx[j] = idx[j + 1];
   }
-  val[K - 1] = -INFINITY;
-  idx[K - 1] = INT32_MAX;
+  val[KL - 1] = -INFINITY;
+  idx[KL - 1] = INT32_MAX;
 }
 
 // Merges the lanes' sorted lists: round j's winner (the best head over the
 // warp) goes to (out_v[j], out_i[j]) on every lane, and its lane pops it.
-__device__ __forceinline__ void warp_merge(float (&val)[K], int (&idx)[K], float (&out_v)[K], int (&out_i)[K]) {
+template <int KL>
+__device__ __forceinline__ void warp_merge(float (&val)[KL], int (&idx)[KL], float (&out_v)[KL], int (&out_i)[KL]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int j = 0; j < K; ++j) {
+  for (int j = 0; j < KL; ++j) {
     float bv = val[0];
     int bi = idx[0], bl = lane;
 #pragma unroll
@@ -86,12 +90,14 @@ __device__ __forceinline__ void warp_merge(float (&val)[K], int (&idx)[K], float
   }
 }
 
+// (max, sum of exp(x - max)) pairs; __expf's error is a few ulp here (its
+// argument is <= 0 and above -100 for finite logits of one distribution)
 __device__ __forceinline__ void lse_combine(float& m, float& s, float om, float os) {
   if (om > m) {
-    s = s * expf(m - om) + os;
+    s = s * __expf(m - om) + os;
     m = om;
   } else if (om != -INFINITY) {
-    s += os * expf(om - m);
+    s += os * __expf(om - m);
   }
 }
 
@@ -99,6 +105,7 @@ __device__ __forceinline__ int clamp_n(const ExpandParams& p, int b) {
   return min(max(p.n_tree[b], 0), p.n_tree_max);
 }
 
+template <int KL>  // list length: the smallest of 8, 16 that holds k
 __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const ExpandParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -110,51 +117,79 @@ __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const Expand
   const int64_t v1 = min(static_cast<int64_t>(p.vocab), v0 + p.slice);
   const float* lg = p.logits + static_cast<int64_t>(row) * p.vocab;
   float m = -INFINITY, s = 0.f;
-  float val[K];
-  int idx[K];
+  float val[KL];
+  int idx[KL];
 #pragma unroll
-  for (int j = 0; j < K; ++j) {
+  for (int j = 0; j < KL; ++j) {
     val[j] = -INFINITY;
     idx[j] = INT32_MAX;
   }
   auto push = [&](float x, int i) {
     if (x > m) {
-      s = s * expf(m - x) + 1.f;
+      s = s * __expf(m - x) + 1.f;
       m = x;
     } else {
-      s += expf(x - m);
+      s += __expf(x - m);
     }
-    list_insert(val, idx, x, i);
+    list_insert<KL>(val, idx, x, i);
   };
   if ((p.vocab & 3) == 0) {  // 16-byte rows: slices are multiples of 1024 floats
+    // eight 16-byte loads in flight per thread, issued before any of them is
+    // consumed (the insertions branch)
+    constexpr int kLoads = 8;
     const float4* lg4 = reinterpret_cast<const float4*>(lg);
-#pragma unroll 4
-    for (int64_t x = v0 / 4 + threadIdx.x; x < v1 / 4; x += kCandThreads) {
-      const float4 f = __ldcs(lg4 + x);
-      const int i = static_cast<int>(x * 4);
-      push(f.x, i);
-      push(f.y, i + 1);
-      push(f.z, i + 2);
-      push(f.w, i + 3);
+    const int64_t e4 = v1 / 4;
+    for (int64_t x0 = v0 / 4 + threadIdx.x; x0 < e4; x0 += kLoads * kCandThreads) {
+      float4 f[kLoads];
+#pragma unroll
+      for (int q = 0; q < kLoads; ++q)
+        f[q] = x0 + q * kCandThreads < e4 ? __ldcs(lg4 + x0 + q * kCandThreads)
+                                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      // log-sum-exp of the batch: its max first, then independent exponentials
+      float bm = m;
+#pragma unroll
+      for (int q = 0; q < kLoads; ++q) bm = fmaxf(bm, fmaxf(fmaxf(f[q].x, f[q].y), fmaxf(f[q].z, f[q].w)));
+      if (bm > m) {
+        s *= __expf(m - bm);
+        m = bm;
+      }
+      float es[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < kLoads; ++q) {
+        es[0] += __expf(f[q].x - m);   // -inf (past the slice) gives 0
+        es[1] += __expf(f[q].y - m);
+        es[2] += __expf(f[q].z - m);
+        es[3] += __expf(f[q].w - m);
+      }
+      s += (es[0] + es[1]) + (es[2] + es[3]);
+#pragma unroll
+      for (int q = 0; q < kLoads; ++q) {
+        if (x0 + q * kCandThreads >= e4) break;
+        const int i = static_cast<int>((x0 + q * kCandThreads) * 4);
+        list_insert<KL>(val, idx, f[q].x, i);
+        list_insert<KL>(val, idx, f[q].y, i + 1);
+        list_insert<KL>(val, idx, f[q].z, i + 2);
+        list_insert<KL>(val, idx, f[q].w, i + 3);
+      }
     }
   } else {
     for (int64_t x = v0 + threadIdx.x; x < v1; x += kCandThreads) push(__ldcs(lg + x), static_cast<int>(x));
   }
   // block: (m, s) by shuffles + shared memory; lists warp by warp, then warp 0
   __shared__ float wm[kCandThreads / 32], wsum[kCandThreads / 32];
-  __shared__ float wv[kCandThreads / 32][K];
-  __shared__ int wi[kCandThreads / 32][K];
+  __shared__ float wv[kCandThreads / 32][KL];
+  __shared__ int wi[kCandThreads / 32][KL];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-  float tv[K];
-  int ti[K];
-  warp_merge(val, idx, tv, ti);
+  float tv[KL];
+  int ti[KL];
+  warp_merge<KL>(val, idx, tv, ti);
   if (lane == 0) {
     wm[warp] = m;
     wsum[warp] = s;
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
+    for (int j = 0; j < KL; ++j) {
       wv[warp][j] = tv[j];
       wi[warp][j] = ti[j];
     }
@@ -163,7 +198,7 @@ __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const Expand
   if (warp == 0) {
     float bm = -INFINITY, bs = 0.f;
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
+    for (int j = 0; j < KL; ++j) {
       val[j] = -INFINITY;
       idx[j] = INT32_MAX;
     }
@@ -171,7 +206,7 @@ __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const Expand
       bm = wm[lane];
       bs = wsum[lane];
 #pragma unroll
-      for (int j = 0; j < K; ++j) {
+      for (int j = 0; j < KL; ++j) {
         val[j] = wv[lane][j];
         idx[j] = wi[lane][j];
       }
@@ -179,13 +214,13 @@ __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const Expand
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
       lse_combine(bm, bs, __shfl_xor_sync(0xffffffffu, bm, o), __shfl_xor_sync(0xffffffffu, bs, o));
-    warp_merge(val, idx, tv, ti);
+    warp_merge<KL>(val, idx, tv, ti);
     if (lane == 0) {
       CandPartial* out = p.part + static_cast<int64_t>(row) * p.num_slices + blockIdx.y;
       out->m = bm;
       out->s = bs;
 #pragma unroll
-      for (int j = 0; j < K; ++j) {
+      for (int j = 0; j < KL; ++j) {
         out->val[j] = tv[j];
         out->idx[j] = ti[j];
       }
@@ -193,17 +228,20 @@ __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const Expand
   }
 }
 
-__global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandParams p) {
+constexpr int kStepThreads = 2 * TS_MAX_TREE;  // thread i < n owns node i; warp r merges row r
+
+template <int KL>
+__global__ void __launch_bounds__(kStepThreads) expand_step_kernel(const ExpandParams p) {
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t nb = static_cast<int64_t>(b) * p.n_tree_max;
-  __shared__ float c_lp[TS_MAX_TREE][K];
-  __shared__ int c_tok[TS_MAX_TREE][K];
+  __shared__ float c_lp[TS_MAX_TREE][KL];
+  __shared__ int c_tok[TS_MAX_TREE][KL];
   __shared__ int rows_s[K];
-  __shared__ float red_v[TS_MAX_TREE / 32];
-  __shared__ int red_i[TS_MAX_TREE / 32];
+  __shared__ float red_v[kStepThreads / 32];
+  __shared__ int red_i[kStepThreads / 32];
   int n = p.n_tree[b];
   if (n < 0 || n > p.n_tree_max) {
     if (tid == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
@@ -212,16 +250,25 @@ __global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandPa
   if (tid < p.w) rows_s[tid] = p.rows[static_cast<int64_t>(b) * p.w + tid];
   // each node's candidates as they stand (rows queried now are replaced below)
   int taken = p.k;
+  const float my_w = tid < n ? p.weight[nb + tid] : 0.f;
   if (tid < n) {
     taken = min(max(p.cand_taken[nb + tid], 0), p.k);
-    for (int j = 0; j < p.k; ++j) {
-      c_lp[tid][j] = p.cand_lp[(nb + tid) * p.k + j];
-      c_tok[tid][j] = p.cand_tok[(nb + tid) * p.k + j];
+    float lp[KL];
+    int tk[KL];
+#pragma unroll
+    for (int j = 0; j < KL; ++j) {  // issued together
+      lp[j] = j < p.k ? p.cand_lp[(nb + tid) * p.k + j] : -INFINITY;
+      tk[j] = j < p.k ? p.cand_tok[(nb + tid) * p.k + j] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < KL; ++j) {
+      c_lp[tid][j] = lp[j];
+      c_tok[tid][j] = tk[j];
     }
   }
   __syncthreads();
   // ---- 1. the queried rows: merge the slices into k candidates (warp per row)
-  for (int r = warp; r < p.w; r += TS_MAX_TREE / 32) {
+  for (int r = warp; r < p.w; r += kStepThreads / 32) {
     const int u = rows_s[r];
     if (u < 0) continue;
     if (u >= n) {
@@ -229,11 +276,11 @@ __global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandPa
       continue;
     }
     const CandPartial* part = p.part + (static_cast<int64_t>(b) * p.w + r) * p.num_slices;
-    float val[K];
-    int idx[K];
+    float val[KL];
+    int idx[KL];
     float m = -INFINITY, s = 0.f;
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
+    for (int j = 0; j < KL; ++j) {
       val[j] = -INFINITY;
       idx[j] = INT32_MAX;
     }
@@ -241,7 +288,7 @@ __global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandPa
       m = part[lane].m;
       s = part[lane].s;
 #pragma unroll
-      for (int j = 0; j < K; ++j) {
+      for (int j = 0; j < KL; ++j) {
         val[j] = part[lane].val[j];
         idx[j] = part[lane].idx[j];
       }
@@ -249,14 +296,14 @@ __global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandPa
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
     const float lse = m + logf(s);
-    float tv[K];
-    int ti[K];
-    warp_merge(val, idx, tv, ti);
+    float tv[KL];
+    int ti[KL];
+    warp_merge<KL>(val, idx, tv, ti);
     if (lane < p.k) {
       float v = -INFINITY;
       int t = -1;
 #pragma unroll
-      for (int j = 0; j < K; ++j)
+      for (int j = 0; j < KL; ++j)
         if (j == lane) {
           v = tv[j];
           t = ti[j];
@@ -270,7 +317,6 @@ __global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandPa
   for (int r = 0; r < p.w; ++r)
     if (rows_s[r] == tid && tid < n) taken = 0;
   // ---- 2. the picks: each node offers its next candidate
-  const float my_w = tid < n ? p.weight[nb + tid] : 0.f;
   float key = (tid < n && taken < p.k && c_tok[tid][taken] >= 0) ? my_w + c_lp[tid][taken] : -INFINITY;
   int added = 0;
   for (int j = 0; j < p.w; ++j) {
@@ -294,7 +340,7 @@ __global__ void __launch_bounds__(TS_MAX_TREE) expand_step_kernel(const ExpandPa
     bv = red_v[0];
     bi = red_i[0];
 #pragma unroll
-    for (int q = 1; q < TS_MAX_TREE / 32; ++q)
+    for (int q = 1; q < kStepThreads / 32; ++q)
       if (ahead(red_v[q], red_i[q], bv, bi)) {
         bv = red_v[q];
         bi = red_i[q];
@@ -391,10 +437,12 @@ __global__ void __launch_bounds__(TS_MAX_TREE) select_subtree_kernel(const Selec
 }  // namespace
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream) {
-  cudaError_t e = launch_pdl(cand_partial_kernel, dim3(p.num_req * p.w, p.num_slices), dim3(kCandThreads), 0,
-                             stream, p);
+  const dim3 grid(p.num_req * p.w, p.num_slices);
+  cudaError_t e = p.k <= 8 ? launch_pdl(cand_partial_kernel<8>, grid, dim3(kCandThreads), 0, stream, p)
+                           : launch_pdl(cand_partial_kernel<16>, grid, dim3(kCandThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(expand_step_kernel, dim3(p.num_req), dim3(TS_MAX_TREE), 0, stream, p);
+  return p.k <= 8 ? launch_pdl(expand_step_kernel<8>, dim3(p.num_req), dim3(kStepThreads), 0, stream, p)
+                  : launch_pdl(expand_step_kernel<16>, dim3(p.num_req), dim3(kStepThreads), 0, stream, p);
 }
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {

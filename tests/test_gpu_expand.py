@@ -178,3 +178,47 @@ def test_select_reports_a_parent_that_is_not_kept():
     torch.cuda.synchronize()
     assert out["keep"][0].tolist() == [0, 2] and out["new_parent"][0].tolist() == [-1, -1]
     assert ts.read_device_error(ws) & ts.TS_DEVERR_BAD_PARENT
+
+
+def test_expansion_then_attention_on_the_grown_tree():
+    """The draft loop on one stream: each expansion appends w nodes, then the
+    tree attention queries exactly those nodes, reading the parents and tree
+    size the expansion wrote (SwiftSpec summary §3.1.1 and Figure 3: the new
+    leaves attend to their ancestors and the prefix)."""
+    import dataclasses
+
+    import workloads as W
+    from oracle import attention as A
+    from gpu_util import attn_inputs, check_attention
+
+    B, w, k, n_max, steps, vocab = 2, 4, 4, 40, 3, 3000
+    case = W.random_attn_case(90, num_req=B, hq=16, hkv=4, d=128, n_tree_max=n_max, n_query=w,
+                              prefix_range=(100, 400))
+    d = attn_inputs(case)
+    rng = np.random.default_rng(91)
+    tree = ts.DraftTree(B, n_max, k)
+    n0 = 12
+    for b in range(B):   # a chain of n0 nodes whose last node has candidates
+        tree.parent[b, :n0] = torch.arange(-1, n0 - 1, dtype=torch.int32)
+        tree.weight[b, :n0] = -torch.arange(n0, dtype=torch.float32) * 0.3
+        tree.cand_tok[b, n0 - 1] = torch.from_numpy(rng.choice(vocab, size=k, replace=False).astype(np.int32))
+        tree.cand_lp[b, n0 - 1] = torch.tensor([-0.1, -0.5, -1.2, -2.0])
+        tree.cand_taken[b, n0 - 1] = 0
+    tree.n_tree.fill_(n0)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((B, case.num_q_heads, w), dtype=torch.float32, device="cuda")
+    a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], tree.n_tree, tree.parent, out, lse,
+                     None, case.softmax_scale, 2)
+    aws = ts.new_workspace(ts.tree_attn_workspace_size(a))
+    rows = torch.full((B, w), -1, dtype=torch.int32, device="cuda")
+    for step in range(steps):
+        logits = torch.randn((B, w, vocab), device="cuda")
+        added = ts.tree_expand(tree, logits, rows)
+        ts.tree_attn_forward_args(a, aws)
+        torch.cuda.synchronize()
+        assert (added >= 0).all()
+        n = tree.n_tree.cpu().numpy()
+        assert (n == n0 + w * (step + 1)).all()
+        grown = dataclasses.replace(case, n_tree=n.astype(np.int32), parent=tree.parent.cpu().numpy())
+        check_attention(grown, out, lse, A.attention_case(grown, heads=[0, 5, 11]), heads=[0, 5, 11])
+        rows = added

@@ -69,7 +69,7 @@ def normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
 
 def _streams(seed: int):
     ss = np.random.SeedSequence(seed)
-    names = ["lengths", "shape", "logits", "tokens", "q", "k", "v", "blocks"]
+    names = ["lengths", "shape", "logits", "tokens", "q", "k", "v", "blocks", "draft"]
     return {nm: np.random.default_rng(s) for nm, s in zip(names, ss.spawn(len(names)))}
 
 
@@ -196,6 +196,27 @@ class CompactCase:
 
 
 @dataclasses.dataclass
+class DraftState:
+    """Draft-side expansion inputs: a tree whose nodes already carry their
+    candidate children (tokens and decreasing log-probabilities, as a draft
+    model would have produced them), and the draft logits of the nodes that
+    expansions 2..d query (expansion 1 draws on the existing candidates)."""
+    num_req: int
+    w: int                   # nodes added per expansion (= attention queries)
+    k: int                   # candidates per node
+    bs: int                  # nodes of the subtree selected at the end
+    vocab: int
+    n0: int                  # nodes before the first expansion
+    parent: np.ndarray       # [num_req][n_tree_max] int32
+    tokens: np.ndarray       # [num_req][n_tree_max] int32
+    weight: np.ndarray       # [num_req][n_tree_max] float32, non-increasing from parent to child
+    cand_tok: np.ndarray     # [num_req][n_tree_max][k] int32 (distinct per node)
+    cand_lp: np.ndarray      # [num_req][n_tree_max][k] float32, decreasing, < 0
+    cand_taken: np.ndarray   # [num_req][n_tree_max] int32 (children already in the tree, capped at k)
+    logits: list             # per expansion 2..d: float32 [num_req][w][vocab]
+
+
+@dataclasses.dataclass
 class Workload:
     name: str
     description: str
@@ -204,6 +225,7 @@ class Workload:
     compact: Optional[CompactCase] = None          # target side: same tree as acceptance
     compact_draft: Optional[CompactCase] = None    # draft side (long-context workload)
     num_layers: int = 1
+    draft: Optional[DraftState] = None             # draft-side expansion loop (config 2)
 
 
 # --------------------------------------------------------------------------
@@ -288,8 +310,25 @@ def expand_w8_prefix2048(seed: int = 0) -> Workload:
         q = normal_bf16(rs["q"], (num_req, w, hq, d))
         cases.append(AttnCase(num_req, hq, hkv, d, n_max, w, P + n_max, False, prefix,
                               np.full(num_req, n, np.int32), parent, q, k, v))
+    # the draft side of the same iteration: the 64-node tree with candidate
+    # children on every node, draft logits (vocab 128256, a 32/8/128-head
+    # model's) for the nodes expansions 2..4 query, a 32-node subtree at the end
+    k, bs, vocab = 8, 32, 128256
+    g = rs["draft"]
+    weight = np.zeros((num_req, n_max), np.float32)
+    for i in range(1, n0):
+        weight[0, i] = weight[0, base[i]] - np.float32(g.exponential(1.0))
+    cand_tok = np.stack([[g.choice(vocab, size=k, replace=False) for _ in range(n_max)]]).astype(np.int32)
+    cand_lp = (-np.cumsum(g.exponential(0.7, size=(num_req, n_max, k)), axis=2)).astype(np.float32)
+    children = np.bincount(base[1:], minlength=n_max)[:n_max]
+    taken = np.minimum(children, k).astype(np.int32)[None, :]
+    tokens = g.integers(0, vocab, size=(num_req, n_max)).astype(np.int32)
+    dparent = np.full((num_req, n_max), -1, np.int32)
+    dparent[0, :n0] = base
+    logits = [(g.normal(size=(num_req, w, vocab)) * 2.0).astype(np.float32) for _ in range(steps - 1)]
+    draft = DraftState(num_req, w, k, bs, vocab, n0, dparent, tokens, weight, cand_tok, cand_lp, taken, logits)
     return Workload("expand_w8_prefix2048", "1 req, Hq 32 / Hkv 8, d 128, prefix 2048, "
-                    "tree 64 (depth<=8) + 4 expansions of w=8 new leaves (8x2120..8x2144)", cases)
+                    "tree 64 (depth<=8) + 4 expansions of w=8 new leaves (8x2120..8x2144)", cases, draft=draft)
 
 
 def verify_b8_tree16(seed: int = 0) -> Workload:
