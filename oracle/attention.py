@@ -75,6 +75,32 @@ def tree_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, prefix_len: int,
     return out, lse
 
 
+def tree_positions(parent, n: int, prefix_len: int) -> np.ndarray:
+    """Position id of each tree node: the prefix length plus the node's depth
+    (the root, parent -1, sits at position prefix_len).  Nodes on one root
+    path get consecutive positions, siblings share one: the tree positions
+    that RoPE inside the verify attention uses (SwiftSpec summary §3.3)."""
+    pos = np.zeros(n, dtype=np.int64)
+    for i in range(n):
+        p = int(parent[i])
+        pos[i] = prefix_len if p < 0 else pos[p] + 1
+    return pos
+
+
+def rope(x: np.ndarray, positions, theta: float) -> np.ndarray:
+    """Rotary position embedding, rotate-half convention, fp64: for j < d/2,
+    angle = position * theta^(-2j/d), and the pair (x_j, x_{j+d/2}) turns by
+    that angle.  x: [rows][heads][d], positions: [rows]."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    inv = theta ** (-2.0 * np.arange(half) / d)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * inv[None, :]      # [rows][half]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
+
+
 def default_scale(head_dim: int, softmax_scale: float = 0.0) -> float:
     return softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(head_dim)
 
@@ -94,5 +120,9 @@ def attention_case(case, requests=None, heads=None):
         kb = bf16_bits_to_f64(logical_rows(case.k, b, keys, table))
         vb = bf16_bits_to_f64(logical_rows(case.v, b, keys, table))
         qb = bf16_bits_to_f64(case.q[b])
+        theta = getattr(case, "rope_theta", 0.0)
+        if theta > 0:   # queries at their tree positions; K rows are stored rotated
+            pos = tree_positions(case.parent[b], n, P)[n - case.n_query:]
+            qb = rope(qb, pos, theta)
         res[b] = tree_attention(qb, kb, vb, P, n, case.parent[b][:n], case.n_query, scale, heads)
     return res

@@ -164,6 +164,7 @@ class AttnCase:
     v: np.ndarray
     block_table: Optional[np.ndarray] = None   # [num_req][max_blocks] int32 (paged only)
     softmax_scale: float = 0.0                  # 0 -> 1/sqrt(head_dim)
+    rope_theta: float = 0.0                     # > 0: queries rotated at their tree positions
 
     @property
     def scale(self) -> float:
