@@ -100,6 +100,13 @@ TS_API ts_status tree_build_mask(const int32_t* parent, const int32_t* n_tree, i
  *   out[b][r][h] = sum_j softmax_j(scale * q.k_j) v_j   (bf16, fp32 accumulation)
  *   lse[b][h][r] = log sum_j exp(scale * q.k_j)         (fp32, natural log)
  * The caller has already written the tree's K/V rows at P .. P + n - 1.
+ * With rope_theta > 0 the queries are first rotated at their tree positions
+ * (SwiftSpec summary §3.3, RoPE inside the verify attention; position of
+ * node u = prefix_len[b] + depth(u), the root at depth 0): rotate-half
+ * rotary embedding, pair (x_j, x_{j+d/2}) turned by position *
+ * rope_theta^(-2j/d) (angles in fp64, rotation in fp32, bf16 result), into
+ * workspace scratch; `q` itself is not written.  The K rows are read as
+ * stored (rotated by the writer, as in any KV cache).
  * ------------------------------------------------------------------------ */
 typedef struct ts_attn_args {
   int num_requests;
@@ -126,6 +133,7 @@ typedef struct ts_attn_args {
   float softmax_scale;        /* <= 0 selects 1 / sqrt(head_dim) */
   int force_path;             /* 0 automatic; 1 warp-mma kernel; 2 tcgen05 kernel (G*n_query == 128 only) */
   int num_ctas;               /* 0 automatic; else the number of split-KV CTAs (testing) */
+  float rope_theta;           /* 0: no rotation; > 0: RoPE base of the queries at tree positions */
 } ts_attn_args;
 
 TS_API size_t tree_attn_workspace_size(const ts_attn_args* args);

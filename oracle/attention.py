@@ -101,6 +101,14 @@ def rope(x: np.ndarray, positions, theta: float) -> np.ndarray:
     return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to bfloat16 (through float32, round to nearest even on the 16
+    dropped bits); the attention's operands are bf16."""
+    bits = np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    rounded = ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16) << 16
+    return rounded.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def default_scale(head_dim: int, softmax_scale: float = 0.0) -> float:
     return softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(head_dim)
 
@@ -121,8 +129,8 @@ def attention_case(case, requests=None, heads=None):
         vb = bf16_bits_to_f64(logical_rows(case.v, b, keys, table))
         qb = bf16_bits_to_f64(case.q[b])
         theta = getattr(case, "rope_theta", 0.0)
-        if theta > 0:   # queries at their tree positions; K rows are stored rotated
+        if theta > 0:   # queries at their tree positions, as bf16 operands; K rows are stored rotated
             pos = tree_positions(case.parent[b], n, P)[n - case.n_query:]
-            qb = rope(qb, pos, theta)
+            qb = round_bf16(rope(qb, pos, theta))
         res[b] = tree_attention(qb, kb, vb, P, n, case.parent[b][:n], case.n_query, scale, heads)
     return res

@@ -89,7 +89,7 @@ struct AttnPlan {
   bool use_tc;
   int rows, row_groups, rows_pad, group, stages, num_ctas, hp;
   int64_t units, slots;
-  size_t ws_bytes, off_o, off_lse;
+  size_t ws_bytes, off_o, off_lse, off_q;  // off_q: rotated queries (rope_theta > 0), else 0
 };
 
 ts_status validate_attn(const ts_attn_args* a) {
@@ -118,6 +118,8 @@ ts_status validate_attn(const ts_attn_args* a) {
       !aligned(a->lse, 4))
     return TS_ERR_INVALID_ARG;
   if (a->force_path < 0 || a->force_path > 2 || a->num_ctas < 0) return TS_ERR_INVALID_ARG;
+  if (!(a->rope_theta >= 0.f) || std::isinf(a->rope_theta) || (a->rope_theta > 0.f && a->rope_theta <= 1.f))
+    return TS_ERR_INVALID_ARG;  // NaN, infinite, or a base that does not decay
   return TS_OK;
 }
 
@@ -172,6 +174,11 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   pl->off_o = kWsHeader;
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
   pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
+  pl->off_q = 0;
+  if (a->rope_theta > 0.f) {
+    pl->off_q = pl->ws_bytes;
+    pl->ws_bytes += align256(static_cast<size_t>(a->num_requests) * a->n_query * a->num_q_heads * a->head_dim * 2);
+  }
   return TS_OK;
 }
 
@@ -198,7 +205,7 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const ts_attn_args* a, in
 // Q as a 3-D tensor (head_dim, Hq, num_requests * n_query); one box of
 // (64, G, n_query) is the 128 packed rows (node-major, head within the group)
 // of one KV head, in two 64-column halves.
-bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, int group) {
+bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, const void* q, int group) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->head_dim), static_cast<cuuint64_t>(a->num_q_heads),
@@ -207,7 +214,7 @@ bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, int group) {
                            static_cast<cuuint64_t>(a->head_dim) * 2 * a->num_q_heads};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(a->n_query)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims, strides, box, estr,
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -348,9 +355,14 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (a->rope_theta > 0.f) {  // the kernels read the queries rotated at their tree positions
+    void* qr = ws + pl.off_q;
+    if (launch_rope_q(p, a->q, qr, a->rope_theta, s) != cudaSuccess) return TS_ERR_CUDA;
+    p.q = static_cast<const __nv_bfloat16*>(qr);
+  }
   if (pl.use_tc) {
     CUtensorMap qmap, pmap;
-    if (!encode_q_map(&qmap, a, pl.group)) return TS_ERR_CUDA;
+    if (!encode_q_map(&qmap, a, p.q, pl.group)) return TS_ERR_CUDA;
     if (!encode_partial_map(&pmap, p.part_o, pl.slots * pl.rows_pad)) return TS_ERR_CUDA;
     e = launch_attn_tc(p, kmap, vmap, pmap, qmap, s);
   } else {

@@ -260,6 +260,45 @@ def test_tcgen05_one_workspace_serves_repeated_calls():
             check_attention(case, outs[0][0], outs[0][1], A.attention_case(case))
 
 
+ROPE = [  # (case, forced path)
+    (dict(num_req=2, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(0, 3000)), 2),                  # R = 128
+    (dict(num_req=3, hq=64, hkv=8, d=128, n_tree_max=5, prefix_range=(60, 900), chain=True, paged=True), 2),  # R = 40
+    (dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=40, n_query=8, prefix_range=(100, 400)), 2),      # expansion
+    (dict(num_req=2, hq=8, hkv=2, d=64, n_tree_max=24, prefix_range=(0, 300), ragged_tree=True), 1),   # warp MMA
+    (dict(num_req=1, hq=32, hkv=8, d=128, n_tree_max=32, prefix_range=(32000, 32768)), 2),             # far positions
+]
+
+
+@pytest.mark.parametrize("theta", [10000.0, 500000.0])
+@pytest.mark.parametrize("cfg", range(len(ROPE)))
+def test_rope_at_tree_positions_matches_oracle(cfg, theta):
+    """Queries rotated at position prefix_len + depth inside the attention call."""
+    import dataclasses
+    kw, path = ROPE[cfg]
+    case = dataclasses.replace(W.random_attn_case(300 + cfg, **kw), rope_theta=theta)
+    d = attn_inputs(case)
+    q_before = d["q"].clone()
+    out, lse = ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
+                                    block_table=d.get("block_table"), force_path=path, rope_theta=theta)
+    torch.cuda.synchronize()
+    assert torch.equal(d["q"], q_before)   # the rotation goes to workspace scratch
+    heads = list(range(0, case.num_q_heads, max(1, case.num_q_heads // 6)))
+    check_attention(case, out, lse, A.attention_case(case, heads=heads), heads=heads)
+
+
+def test_rope_changes_the_result_and_rejects_bad_bases():
+    import dataclasses
+    case = W.random_attn_case(320, num_req=1, hq=32, hkv=8, d=128, n_tree_max=32, prefix_range=(500, 600))
+    plain, _ = run(case, force_path=2)
+    rotated, _ = run(case, force_path=2, rope_theta=10000.0)
+    assert not torch.equal(plain, rotated)
+    d = attn_inputs(case)
+    for bad in (float("nan"), 0.5, float("inf"), -1.0):
+        with pytest.raises(ts.TreeSpecError):
+            ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
+                                 rope_theta=bad)
+
+
 def test_workload_tree16_prefix128():
     w = W.tree16_prefix128()
     _sampled(w.attn[0], None, None)

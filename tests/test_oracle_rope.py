@@ -46,3 +46,15 @@ def test_tree_positions_are_prefix_plus_depth():
     assert pos.tolist() == [100 + T.depth(parent, i) for i in range(7)] == [100, 101, 102, 101, 102, 102, 100]
     # a chain's positions are sequential, as in ordinary decoding
     assert A.tree_positions(list(range(-1, 9)), 10, 37).tolist() == list(range(37, 47))
+
+
+def test_bf16_rounding_is_nearest_even():
+    assert A.round_bf16(np.array([1.0, -2.5, 0.0]) ).tolist() == [1.0, -2.5, 0.0]
+    one_ulp = 2.0 ** -7                                  # bf16 spacing just above 1
+    assert A.round_bf16(np.array([1.0 + one_ulp * 0.5]))[0] == 1.0            # tie: to even (1.0)
+    assert A.round_bf16(np.array([1.0 + one_ulp * 1.5]))[0] == 1.0 + 2 * one_ulp   # tie: to even (1 + 2 ulp)
+    assert A.round_bf16(np.array([1.0 + one_ulp * 0.51]))[0] == 1.0 + one_ulp
+    x = np.random.default_rng(3).normal(size=1000) * 100
+    r = A.round_bf16(x)
+    assert np.all(r.astype(np.float32).view(np.uint32) & 0xFFFF == 0)
+    assert np.all(np.abs(r - x) <= 2.0 ** -8 * np.abs(x) + 1e-30)   # half a unit of the 8-bit significand
