@@ -46,6 +46,8 @@ def parse():
                              "expand_w8_prefix2048", "tree16_prefix128"])
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--rope-theta", type=float, default=0.0,
+                    help="rotate the queries at their tree positions with this RoPE base (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
@@ -196,7 +198,7 @@ def build_step(args, torch, ts, W, device):
         out = torch.empty_like(d["q"])
         lse = torch.empty((case.num_req, case.num_q_heads, case.n_query), dtype=torch.float32, device=device)
         a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"], out, lse,
-                         d.get("block_table"), case.softmax_scale, args.force_path)
+                         d.get("block_table"), case.softmax_scale, args.force_path, 0, args.rope_theta)
         ws = ts.new_workspace(ts.tree_attn_workspace_size(a), device)
         attn_calls.append((a, ws, d, out, lse))
         tokens_per_step += case.num_req * case.n_query
@@ -596,7 +598,7 @@ def main():
         "config": {"workload": info["workload"], "requests": info["attn_cases"][0].num_req,
                    "q_heads": info["attn_cases"][0].num_q_heads, "kv_heads": info["attn_cases"][0].num_kv_heads,
                    "head_dim": info["attn_cases"][0].head_dim, "tree_nodes": info["attn_cases"][0].n_tree_max,
-                   "layers_compacted": args.layers if info["comp_states"] else 0, "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
+                   "layers_compacted": args.layers if info["comp_states"] else 0, "rope_theta": args.rope_theta, "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
                    "l2": ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2" % (attn_bytes / 1e6)
                           if flush is None else
                           "L2 flushed (258 MB write, then 258 MB read) before every timed step, outside the step times: "

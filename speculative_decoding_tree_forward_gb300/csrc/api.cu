@@ -357,7 +357,10 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   cudaError_t e;
   if (a->rope_theta > 0.f) {  // the kernels read the queries rotated at their tree positions
     void* qr = ws + pl.off_q;
-    if (launch_rope_q(p, a->q, qr, a->rope_theta, s) != cudaSuccess) return TS_ERR_CUDA;
+    RopeFreqs f;
+    for (int j = 0; j < 64; ++j)
+      f.inv_freq[j] = j < a->head_dim / 2 ? std::pow(static_cast<double>(a->rope_theta), -2.0 * j / a->head_dim) : 0.0;
+    if (launch_rope_q(p, f, a->q, qr, s) != cudaSuccess) return TS_ERR_CUDA;
     p.q = static_cast<const __nv_bfloat16*>(qr);
   }
   if (pl.use_tc) {

@@ -72,8 +72,12 @@ cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const C
                            const CUtensorMap& qmap, cudaStream_t stream);
 size_t attn_zero_prefix_bytes(const ts_attn_args* a);
 cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream);
+// RoPE inverse frequencies theta^(-2j/d), j < d/2, computed on the host in fp64.
+struct RopeFreqs {
+  double inv_freq[64];
+};
 // Queries rotated at their tree positions into q_out (same layout as q_in).
-cudaError_t launch_rope_q(const AttnParams& p, const void* q_in, void* q_out, float theta, cudaStream_t stream);
+cudaError_t launch_rope_q(const AttnParams& p, const RopeFreqs& f, const void* q_in, void* q_out, cudaStream_t stream);
 size_t attn_mma_smem_bytes(int head_dim, int stages, int num_req, int rows_pad);
 size_t attn_tc_smem_bytes(int stages, int num_req);
 int attn_mma_threads(int rows_pad);
