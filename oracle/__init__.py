@@ -5,6 +5,8 @@ Plain, slow, obviously-correct definitions in fp64 (numpy) and Python lists:
 * ``oracle.tree``       -- ancestor sets, the tree mask, greedy acceptance,
                            re-root + KV-row compaction.
 * ``oracle.attention``  -- tree-masked GQA attention with an explicit mask.
+* ``oracle.stochastic`` -- stochastic tree acceptance (speculative sampling
+                           with the residual norm(max(0, p - q)), per child).
 * ``oracle.expand``     -- draft-side maximum-likelihood expansion (candidate
                            children from log-softmax, priority picks) and the
                            selection of the most promising subtree.
@@ -25,4 +27,4 @@ check it against the pages' worked figures (Figures 2, 3, 4 of the SwiftSpec
 summary), closed forms and brute force.  Absolute attention values on a real
 model are not available anywhere and are not claimed.
 """
-from . import attention, expand, tree  # noqa: F401
+from . import attention, expand, stochastic, tree  # noqa: F401
