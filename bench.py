@@ -46,6 +46,8 @@ def parse():
                              "expand_w8_prefix2048", "tree16_prefix128"])
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="> 0: stochastic acceptance at this temperature instead of greedy")
     ap.add_argument("--rope-theta", type=float, default=0.0,
                     help="rotate the queries at their tree positions with this RoPE base (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -250,11 +252,24 @@ def build_step(args, torch, ts, W, device):
             ("verified_len", (A.num_req,))]}
         par = attn_calls[0][2]["parent"] if attn_calls else i32_dev(A.parent)
         ntree = attn_calls[0][2]["n_tree"] if attn_calls else i32_dev(A.n_tree)
-        aa = ts.accept_args(logits, tok, par, ntree, **res)
-        aws = ts.new_workspace(ts.tree_accept_workspace_size(aa), device)
-        acc_state = (aa, aws, logits, tok, res)
+        if args.temperature > 0:
+            # stochastic acceptance: a draft that differs from the target by
+            # N(0, 0.5^2) per logit, and the walk's uniforms (seeded inputs)
+            g = torch.Generator(device=device)
+            g.manual_seed(7)
+            dlog = logits + 0.5 * torch.randn(logits.shape, generator=g, device=device)
+            u_acc = torch.rand(tok.shape, generator=g, device=device)
+            u_bon = torch.rand(tok.shape, generator=g, device=device)
+            aa = ts.sample_args(logits, dlog, tok, par, ntree, u_acc, u_bon, args.temperature, res)
+            aws = ts.new_workspace(ts.tree_accept_sample_workspace_size(aa), device)
+            acc_state = (aa, aws, logits, tok, res, "sample", [dlog, u_acc, u_bon])
+            info["accept_bytes"] = 2 * A.logits.nbytes
+        else:
+            aa = ts.accept_args(logits, tok, par, ntree, **res)
+            aws = ts.new_workspace(ts.tree_accept_workspace_size(aa), device)
+            acc_state = (aa, aws, logits, tok, res, "greedy", [])
         launches += 2
-        info["accept_bytes"] = A.logits.nbytes
+        info.setdefault("accept_bytes", A.logits.nbytes)
 
     comp_states = []
     if w.compact is not None and acc_state is not None:
@@ -303,7 +318,8 @@ def build_step(args, torch, ts, W, device):
     else:
         phases.append(("attn", [lambda a=a, ws=ws: ts.tree_attn_forward_args(a, ws) for a, ws, *_ in attn_calls]))
     if acc_state is not None:
-        phases.append(("accept", [lambda: ts.tree_accept_greedy_args(acc_state[0], acc_state[1])]))
+        accept_call = ts.tree_accept_sample_args if acc_state[5] == "sample" else ts.tree_accept_greedy_args
+        phases.append(("accept", [lambda: accept_call(acc_state[0], acc_state[1])]))
     if comp_states:
         phases.append(("other", [lambda st=st: ts.tree_cache_compact_args(st[0], st[1]) for st in comp_states]))
 
@@ -331,7 +347,7 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     if info["draft"] is not None:
         main_in += info["draft"]["logits"]   # draft logits of the nodes the expansions query
     acc = info["acc_state"]
-    side_in = [acc[2], acc[3]] if acc is not None else []
+    side_in = [acc[2], acc[3]] + acc[6] if acc is not None else []   # logits, tokens (+ draft logits, uniforms)
     for st in info["comp_states"]:
         main_in += [st[8], st[9]]          # parent, tokens (tree metadata)
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
@@ -598,7 +614,8 @@ def main():
         "config": {"workload": info["workload"], "requests": info["attn_cases"][0].num_req,
                    "q_heads": info["attn_cases"][0].num_q_heads, "kv_heads": info["attn_cases"][0].num_kv_heads,
                    "head_dim": info["attn_cases"][0].head_dim, "tree_nodes": info["attn_cases"][0].n_tree_max,
-                   "layers_compacted": args.layers if info["comp_states"] else 0, "rope_theta": args.rope_theta, "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
+                   "layers_compacted": args.layers if info["comp_states"] else 0, "rope_theta": args.rope_theta,
+                   "acceptance": "stochastic, T = %g" % args.temperature if args.temperature > 0 else "greedy", "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
                    "l2": ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2" % (attn_bytes / 1e6)
                           if flush is None else
                           "L2 flushed (258 MB write, then 258 MB read) before every timed step, outside the step times: "

@@ -63,6 +63,7 @@ typedef enum ts_kv_layout {
 #define TS_DEVERR_BAD_LENGTH 0x2u   /* prefix_len / n_tree / m outside its stated bound: clamped */
 #define TS_DEVERR_BAD_BLOCK 0x4u    /* block_table entry outside [0, num_blocks): rows read as zero / not moved */
 #define TS_DEVERR_TIMEOUT 0x8u      /* a bounded wait inside a kernel expired; outputs are invalid */
+#define TS_DEVERR_BAD_TOKEN 0x10u   /* a draft token outside [0, vocab): never accepted */
 
 /* Largest tree the kernels accept (ancestor sets are 128-bit masks). */
 #define TS_MAX_TREE 128
@@ -268,6 +269,54 @@ typedef struct ts_compact_args {
 TS_API size_t tree_compact_workspace_size(const ts_compact_args* args);
 TS_API ts_status tree_cache_compact(const ts_compact_args* args, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * Stochastic tree acceptance (speculative sampling at temperature > 0).
+ *
+ * MineDraft summary (on a rejection one token is resampled from
+ * norm(max(0, p - q)); the default temperature is 1.0), generalised to the
+ * draft tree of the SwiftSpec summary, Figure 2.  p_u = softmax(
+ * target_logits[u] / T) is the target's distribution after node u, q_u =
+ * softmax(draft_logits[u] / T) the draft's (u's children were drawn from
+ * it).  From the root (node 0, always accepted), at the current node u the
+ * children are tried in index order with a running target r = p_u: child c
+ * (token t) is accepted iff u_accept[c] < r(t) / q_u(t) (if q_u(t) is 0 in
+ * fp32: iff r(t) > 0); on a rejection r becomes norm(max(0, r - q_u)) (kept
+ * if that is all zero).  An accepted child becomes the current node.  When
+ * every child was rejected, or u has none, the bonus is the smallest token v
+ * with r(0) + ... + r(v) > u_bonus[u] * sum(r).  Children drawn
+ * independently from q_u make the emitted tokens follow the target's law.
+ *   path[b][0..AL) = accepted nodes (root first, -1 after), accept_len[b] =
+ *   AL in [1, 1 + depth], bonus[b]; verified[b] = tokens(path) ++ bonus
+ *   (-1 after, optional), verified_len[b] = AL + 1 (optional).
+ * The uniforms are inputs in [0, 1).  Arithmetic: fp32 (exp of scaled
+ * logits minus the row's log-sum-exp); a decision within fp32 rounding of
+ * its threshold may go either way.  Workspace: tree_accept_sample_workspace_size().
+ * Errors: TS_ERR_INVALID_ARG unless temperature > 0 and finite;
+ * TS_ERR_UNSUPPORTED if vocab > 262144 or n_tree_max > TS_MAX_TREE.
+ * ------------------------------------------------------------------------ */
+typedef struct ts_sample_args {
+  int num_requests;
+  int n_tree_max;              /* <= TS_MAX_TREE */
+  int vocab;                   /* >= 1 */
+  float temperature;           /* > 0 */
+  const float* target_logits;  /* device [num_requests][n_tree_max][vocab] */
+  const float* draft_logits;   /* device [num_requests][n_tree_max][vocab] */
+  const int32_t* tokens;       /* device [num_requests][n_tree_max] */
+  const int32_t* parent;       /* device [num_requests][n_tree_max] */
+  const int32_t* n_tree;       /* device [num_requests] */
+  const float* u_accept;       /* device [num_requests][n_tree_max] */
+  const float* u_bonus;        /* device [num_requests][n_tree_max] */
+  int32_t* path;               /* device [num_requests][n_tree_max] (out) */
+  int32_t* accept_len;         /* device [num_requests] (out) */
+  int32_t* bonus;              /* device [num_requests] (out) */
+  int32_t* verified;           /* device [num_requests][n_tree_max + 1] (out) or NULL */
+  int32_t* verified_len;       /* device [num_requests] (out) or NULL */
+} ts_sample_args;
+
+TS_API size_t tree_accept_sample_workspace_size(const ts_sample_args* args);
+TS_API ts_status tree_accept_sample(const ts_sample_args* args, void* workspace, size_t workspace_bytes,
+                                    void* stream);
 
 /* ------------------------------------------------------------------------
  * Draft-side tree growth: maximum-likelihood expansion (one step) and the

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libtreespec.so")
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_WORKSPACE = range(5)
 TS_KV_CONTIGUOUS, TS_KV_PAGED = 0, 1
 TS_DEVERR_BAD_PARENT, TS_DEVERR_BAD_LENGTH, TS_DEVERR_BAD_BLOCK, TS_DEVERR_TIMEOUT = 1, 2, 4, 8
+TS_DEVERR_BAD_TOKEN = 16
 TS_MAX_TREE = 128
 
 if not os.path.exists(LIB_PATH):
@@ -59,6 +60,13 @@ class CompactArgs(ctypes.Structure):
                 ("src_rows", _vp)]
 
 
+class SampleArgs(ctypes.Structure):
+    _fields_ = [("num_requests", _i32), ("n_tree_max", _i32), ("vocab", _i32), ("temperature", ctypes.c_float),
+                ("target_logits", _vp), ("draft_logits", _vp), ("tokens", _vp), ("parent", _vp), ("n_tree", _vp),
+                ("u_accept", _vp), ("u_bonus", _vp), ("path", _vp), ("accept_len", _vp), ("bonus", _vp),
+                ("verified", _vp), ("verified_len", _vp)]
+
+
 class ExpandArgs(ctypes.Structure):
     _fields_ = [("num_requests", _i32), ("n_tree_max", _i32), ("vocab", _i32), ("w", _i32), ("k", _i32),
                 ("logits", _vp), ("rows", _vp), ("n_tree", _vp), ("parent", _vp), ("tokens", _vp), ("weight", _vp),
@@ -88,6 +96,8 @@ _acc_ws = _sig("tree_accept_workspace_size", ctypes.c_size_t, [ctypes.POINTER(Ac
 _acc = _sig("tree_accept_greedy", _i32, [ctypes.POINTER(AcceptArgs), _vp, ctypes.c_size_t, _vp])
 _cmp_ws = _sig("tree_compact_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CompactArgs)])
 _cmp = _sig("tree_cache_compact", _i32, [ctypes.POINTER(CompactArgs), _vp, ctypes.c_size_t, _vp])
+_smp_ws = _sig("tree_accept_sample_workspace_size", ctypes.c_size_t, [ctypes.POINTER(SampleArgs)])
+_smp = _sig("tree_accept_sample", _i32, [ctypes.POINTER(SampleArgs), _vp, ctypes.c_size_t, _vp])
 _exp_ws = _sig("tree_expand_workspace_size", ctypes.c_size_t, [ctypes.POINTER(ExpandArgs)])
 _exp = _sig("tree_expand", _i32, [ctypes.POINTER(ExpandArgs), _vp, ctypes.c_size_t, _vp])
 _sel_ws = _sig("tree_select_workspace_size", ctypes.c_size_t, [ctypes.POINTER(SelectArgs)])
@@ -99,7 +109,8 @@ _version = _sig("ts_version", _i32, [])
 EXPORTED = ["tree_meta_workspace_size", "tree_build_mask", "tree_attn_workspace_size", "tree_attn_selected_path",
             "tree_attn_forward", "tree_attn_forward_noalloc",
             "tree_accept_workspace_size", "tree_accept_greedy", "tree_compact_workspace_size",
-            "tree_cache_compact", "tree_expand_workspace_size", "tree_expand", "tree_select_workspace_size",
+            "tree_cache_compact", "tree_accept_sample_workspace_size", "tree_accept_sample",
+            "tree_expand_workspace_size", "tree_expand", "tree_select_workspace_size",
             "tree_select_subtree", "ts_status_string", "ts_read_device_error", "ts_version"]
 
 
@@ -430,5 +441,48 @@ def tree_select_subtree(n_tree, parent, tokens, weight, bs: int, workspace=None,
     if workspace is None:
         workspace = new_workspace(int(_sel_ws(ctypes.byref(a))), dev)
     _check(_sel(ctypes.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "tree_select_subtree")
+    return out
+
+
+# ------------------------------------------------------------------ stochastic acceptance
+def sample_args(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature: float,
+                out: dict) -> SampleArgs:
+    """target_logits / draft_logits fp32 [B][n_max][V]; u_accept / u_bonus fp32 [B][n_max] in [0, 1)."""
+    B, n_max, V = target_logits.shape
+    a = SampleArgs()
+    a.num_requests, a.n_tree_max, a.vocab, a.temperature = B, n_max, V, temperature
+    a.target_logits, a.draft_logits = target_logits.data_ptr(), draft_logits.data_ptr()
+    a.tokens, a.parent, a.n_tree = tokens.data_ptr(), parent.data_ptr(), n_tree.data_ptr()
+    a.u_accept, a.u_bonus = u_accept.data_ptr(), u_bonus.data_ptr()
+    a.path, a.accept_len, a.bonus = out["path"].data_ptr(), out["accept_len"].data_ptr(), out["bonus"].data_ptr()
+    a.verified, a.verified_len = out["verified"].data_ptr(), out["verified_len"].data_ptr()
+    return a
+
+
+def tree_accept_sample_workspace_size(args: SampleArgs) -> int:
+    n = _smp_ws(ctypes.byref(args))
+    if n == 0:
+        raise TreeSpecError(TS_ERR_INVALID_ARG, "tree_accept_sample_workspace_size")
+    return n
+
+
+def tree_accept_sample_args(args: SampleArgs, workspace: torch.Tensor, stream=None) -> None:
+    _check(_smp(ctypes.byref(args), workspace.data_ptr(), workspace.numel(), _stream(stream)), "tree_accept_sample")
+
+
+def tree_accept_sample(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature: float,
+                       workspace=None, stream=None) -> dict:
+    """Stochastic tree acceptance; returns dict of path, accept_len, bonus, verified, verified_len."""
+    B, n_max, _ = target_logits.shape
+    dev = target_logits.device
+    out = {"path": torch.empty((B, n_max), dtype=torch.int32, device=dev),
+           "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "bonus": torch.empty(B, dtype=torch.int32, device=dev),
+           "verified": torch.empty((B, n_max + 1), dtype=torch.int32, device=dev),
+           "verified_len": torch.empty(B, dtype=torch.int32, device=dev)}
+    a = sample_args(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature, out)
+    if workspace is None:
+        workspace = new_workspace(tree_accept_sample_workspace_size(a), dev)
+    tree_accept_sample_args(a, workspace, stream)
     return out
 

@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreespec.so")
 
-SOURCES = ["api.cu", "meta.cu", "accept.cu", "compact.cu", "expand.cu", "rope.cu", "attn_mma.cu", "attn_tc.cu",
-           "attn_merge.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "meta.cu", "accept.cu", "compact.cu", "expand.cu", "sample.cu", "rope.cu", "attn_mma.cu",
+           "attn_tc.cu", "attn_merge.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden"]

@@ -508,6 +508,67 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ stochastic acceptance
+// Vocab slice per row-statistics CTA (a multiple of 1024 floats): the
+// target and draft rows x slices fill about one resident wave, at most 32
+// slices per row for the walk's merge.
+static int sample_slice(int vocab, int64_t rows) {
+  const int sms = device_sm_count();
+  int64_t slices = std::min<int64_t>(32, (vocab + 1023) / 1024);
+  if (sms > 0 && rows > 0) slices = std::min<int64_t>(slices, std::max<int64_t>(1, static_cast<int64_t>(sms) * 8 / rows));
+  slices = std::max<int64_t>(slices, 1);
+  return static_cast<int>(((vocab + slices - 1) / slices + 1023) / 1024 * 1024);
+}
+
+size_t tree_accept_sample_workspace_size(const ts_sample_args* a) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1) return 0;
+  const int64_t rows = 2LL * a->num_requests * a->n_tree_max;
+  const int slice = sample_slice(a->vocab, rows);
+  const int64_t slices = (a->vocab + slice - 1) / slice;
+  return kWsHeader + align256(static_cast<size_t>(rows * slices) * sizeof(float2)) +
+         align256(static_cast<size_t>(a->num_requests) * 2 * a->vocab * sizeof(float));
+}
+
+ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1) return TS_ERR_INVALID_ARG;
+  if (!(a->temperature > 0.f) || std::isinf(a->temperature)) return TS_ERR_INVALID_ARG;
+  if (a->n_tree_max > TS_MAX_TREE || a->vocab > 262144) return TS_ERR_UNSUPPORTED;
+  if (!a->target_logits || !a->draft_logits || !a->tokens || !a->parent || !a->n_tree || !a->u_accept ||
+      !a->u_bonus || !a->path || !a->accept_len || !a->bonus)
+    return TS_ERR_INVALID_ARG;
+  const size_t al = (a->vocab % 4 == 0) ? 16 : 4;
+  if (!aligned(a->target_logits, al) || !aligned(a->draft_logits, al)) return TS_ERR_INVALID_ARG;
+  const int64_t rows = 2LL * a->num_requests * a->n_tree_max;
+  if (rows > INT32_MAX) return TS_ERR_UNSUPPORTED;
+  const size_t need = tree_accept_sample_workspace_size(a);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SampleParams p;
+  p.num_req = a->num_requests;
+  p.n_tree_max = a->n_tree_max;
+  p.vocab = a->vocab;
+  p.slice = sample_slice(a->vocab, rows);
+  p.num_slices = (a->vocab + p.slice - 1) / p.slice;
+  p.inv_t = 1.0f / a->temperature;
+  p.tl = a->target_logits;
+  p.dl = a->draft_logits;
+  p.tokens = a->tokens;
+  p.parent = a->parent;
+  p.n_tree = a->n_tree;
+  p.u_acc = a->u_accept;
+  p.u_bonus = a->u_bonus;
+  p.path = a->path;
+  p.accept_len = a->accept_len;
+  p.bonus = a->bonus;
+  p.verified = a->verified;
+  p.verified_len = a->verified_len;
+  p.err = reinterpret_cast<unsigned*>(ws);
+  p.part = reinterpret_cast<float2*>(ws + kWsHeader);
+  p.resid = reinterpret_cast<float*>(ws + kWsHeader + align256(static_cast<size_t>(rows * p.num_slices) * sizeof(float2)));
+  cudaError_t e = launch_sample(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ draft-side expansion and selection
 // Vocab slice per candidate CTA (a multiple of 1024 floats): as many slices
 // as keep the SMs busy (about one resident wave of 256-thread CTAs), at most

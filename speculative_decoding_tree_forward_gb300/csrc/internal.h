@@ -169,4 +169,26 @@ struct SelectParams {
 };
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
+struct SampleParams {
+  int num_req, n_tree_max, vocab;
+  int slice, num_slices;  // vocab floats per statistics CTA (multiple of 1024), slices per row (<= 32)
+  float inv_t;            // 1 / temperature
+  const float* tl;
+  const float* dl;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* n_tree;
+  const float* u_acc;
+  const float* u_bonus;
+  int32_t* path;
+  int32_t* accept_len;
+  int32_t* bonus;
+  int32_t* verified;
+  int32_t* verified_len;
+  unsigned* err;
+  float2* part;           // [2][num_req * n_tree_max][num_slices]: (max, sum of exp) of logit / T
+  float* resid;           // [num_req][2][vocab]: residual rows
+};
+cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream);
+
 }  // namespace ts
