@@ -343,8 +343,6 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.n_tree = a->n_tree;
   p.parent = a->parent;
   p.q = static_cast<const __nv_bfloat16*>(a->q);
-  p.k_cache = a->k_cache;
-  p.v_cache = a->v_cache;
   p.block_table = a->block_table;
   p.out = static_cast<__nv_bfloat16*>(a->out);
   p.lse = a->lse;

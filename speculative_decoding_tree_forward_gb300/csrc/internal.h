@@ -54,8 +54,6 @@ struct AttnParams {
   const int32_t* n_tree;
   const int32_t* parent;
   const __nv_bfloat16* q;
-  const void* k_cache;   // K / V base (the paged tcgen05 path gathers rows with cp.async)
-  const void* v_cache;
   const int32_t* block_table;
   __nv_bfloat16* out;
   float* lse;
