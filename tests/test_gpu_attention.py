@@ -110,6 +110,24 @@ def test_tcgen05_first_call_many_short_splits(num_ctas):
     check_attention(case, out, lse, A.attention_case(case))
 
 
+@pytest.mark.parametrize("which", ["tc_r128", "tc_two_heads", "mma_r16"])
+def test_merge_of_many_split_units(which):
+    """More split units than one resident wave of merge CTAs holds: 80 units
+    of 128 rows, 160 two-head units, and 624 units of 16 rows."""
+    if which == "tc_r128":
+        case = W.random_attn_case(32, num_req=10, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(100, 700))
+        path = 2
+    elif which == "tc_two_heads":
+        case = W.random_attn_case(33, num_req=40, hq=32, hkv=8, d=128, n_tree_max=16, n_query=8,
+                                  prefix_range=(100, 500), ragged_tree=True)
+        path = 2
+    else:
+        case = W.random_attn_case(31, num_req=78, hq=16, hkv=8, d=64, n_tree_max=8, prefix_range=(10, 150))
+        path = 1
+    out, lse = run(case, force_path=path)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
 @pytest.mark.parametrize("path", [1, 2])
 def test_large_scores_rescale_running_max(path):
     """Scale 2.0 makes scores grow by far more than 2^8 across tiles: the running max is raised many times."""
