@@ -110,7 +110,7 @@ TS_API ts_status tree_build_mask(const int32_t* parent, const int32_t* n_tree, i
  * stored (rotated by the writer, as in any KV cache).
  * ------------------------------------------------------------------------ */
 typedef struct ts_attn_args {
-  int num_requests;
+  int num_requests;           /* >= 1 (an empty batch is TS_ERR_INVALID_ARG) */
   int num_q_heads;            /* Hq */
   int num_kv_heads;           /* Hkv; Hq % Hkv == 0, G = Hq / Hkv */
   int head_dim;               /* 64 or 128 */
@@ -187,7 +187,7 @@ TS_API ts_status tree_attn_forward_noalloc(const ts_attn_args* args, void* strea
  *   verified_len device int32 [num_requests] (out) or NULL
  * ------------------------------------------------------------------------ */
 typedef struct ts_accept_args {
-  int num_requests;
+  int num_requests;           /* >= 1 */
   int n_tree_max;             /* <= TS_MAX_TREE */
   int vocab;                  /* >= 1 */
   const float* logits;
@@ -238,7 +238,7 @@ TS_API ts_status tree_accept_greedy(const ts_accept_args* args, void* workspace,
  * elem_bytes bytes, a multiple of 16.
  * ------------------------------------------------------------------------ */
 typedef struct ts_compact_args {
-  int num_requests;
+  int num_requests;           /* >= 1 */
   int n_tree_max;             /* <= TS_MAX_TREE */
   int m_max;                  /* row stride of `verified` */
   int num_layers;
@@ -296,7 +296,7 @@ TS_API ts_status tree_cache_compact(const ts_compact_args* args, void* workspace
  * TS_ERR_UNSUPPORTED if vocab > 262144 or n_tree_max > TS_MAX_TREE.
  * ------------------------------------------------------------------------ */
 typedef struct ts_sample_args {
-  int num_requests;
+  int num_requests;           /* >= 1 */
   int n_tree_max;              /* <= TS_MAX_TREE */
   int vocab;                   /* >= 1 */
   float temperature;           /* > 0 */
@@ -363,7 +363,7 @@ TS_API ts_status tree_accept_sample(const ts_sample_args* args, void* workspace,
 #define TS_MAX_EXPAND 16
 
 typedef struct ts_expand_args {
-  int num_requests;
+  int num_requests;           /* >= 1 */
   int n_tree_max;          /* capacity and row stride, <= TS_MAX_TREE */
   int vocab;               /* >= 1 */
   int w;                   /* rows of logits and nodes added per step, 1..TS_MAX_EXPAND */
@@ -384,7 +384,7 @@ TS_API size_t tree_expand_workspace_size(const ts_expand_args* args);
 TS_API ts_status tree_expand(const ts_expand_args* args, void* workspace, size_t workspace_bytes, void* stream);
 
 typedef struct ts_select_args {
-  int num_requests;
+  int num_requests;           /* >= 1 */
   int n_tree_max;          /* row stride of the inputs, <= TS_MAX_TREE */
   int bs;                  /* nodes to keep, >= 1; row stride of the outputs */
   const int32_t* n_tree;   /* device [num_requests] */

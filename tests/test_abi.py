@@ -75,20 +75,23 @@ def test_host_validation_without_gpu(lib):
 
 
 def test_struct_layouts_match_header():
-    """Field order/size of the ctypes mirrors equals the C declarations (checked by compiling the header)."""
+    """Every field of every ctypes mirror sits at the offset the C declaration
+    gives it, and every struct has the C size (checked by compiling the header)."""
     import subprocess
     import tempfile
-    src = r'''
-#include <stdio.h>
-#include <stddef.h>
-#include "treespec.h"
-int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(ts_attn_args), offsetof(ts_attn_args, num_ctas),
-         sizeof(ts_accept_args), offsetof(ts_accept_args, verified_len),
-         sizeof(ts_compact_args), offsetof(ts_compact_args, src_rows));
-  return 0;
-}
-'''
+    import torch  # noqa: F401
+    import speculative_decoding_tree_forward_gb300 as ts
+    mirrors = {"ts_attn_args": ts.AttnArgs, "ts_accept_args": ts.AcceptArgs, "ts_compact_args": ts.CompactArgs,
+               "ts_sample_args": ts.SampleArgs, "ts_expand_args": ts.ExpandArgs, "ts_select_args": ts.SelectArgs}
+    lines, expect = [], []
+    for cname, py in mirrors.items():
+        lines.append(f'  printf("%zu\\n", sizeof({cname}));')
+        expect.append(ctypes.sizeof(py))
+        for field, _ in py._fields_:
+            lines.append(f'  printf("%zu\\n", offsetof({cname}, {field}));')
+            expect.append(getattr(py, field).offset)
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"treespec.h\"\nint main(void) {\n" + "\n".join(lines) + \
+          "\n  return 0;\n}\n"
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "t.c")
         exe = os.path.join(d, "t")
@@ -99,7 +102,30 @@ int main(void) {
         if r.returncode != 0:
             pytest.skip("no C compiler: " + r.stderr[:200])
         got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
+    assert got == expect
+
+
+def test_empty_batches_and_null_arguments_are_rejected_on_the_host(lib):
+    """Validation happens before any CUDA call: an empty batch or a null
+    pointer returns TS_ERR_INVALID_ARG with no GPU present."""
     import torch  # noqa: F401
     import speculative_decoding_tree_forward_gb300 as ts
-    assert got == [ctypes.sizeof(ts.AttnArgs), ts.AttnArgs.num_ctas.offset, ctypes.sizeof(ts.AcceptArgs),
-                   ts.AcceptArgs.verified_len.offset, ctypes.sizeof(ts.CompactArgs), ts.CompactArgs.src_rows.offset]
+    for name in ("tree_accept_sample", "tree_expand", "tree_select_subtree"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        assert f(None, None, 0, None) == 1, name
+    for name in ("tree_accept_sample_workspace_size", "tree_expand_workspace_size", "tree_select_workspace_size",
+                 "tree_accept_workspace_size", "tree_compact_workspace_size"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_size_t
+        assert f(None) == 0, name
+    lib.tree_build_mask.restype = ctypes.c_int
+    assert lib.tree_build_mask(None, None, 1, 16, None, None, None, 0, None) == 1
+    a = ts.AttnArgs(num_requests=0, num_q_heads=8, num_kv_heads=2, head_dim=64, n_tree_max=16, n_query=16,
+                    max_kv_len=256)
+    assert lib.tree_attn_forward(ctypes.byref(a), None, 0, None) == 1
+    assert lib.tree_attn_workspace_size(ctypes.byref(a)) == 0
+    acc = ts.AcceptArgs(num_requests=0, n_tree_max=16, vocab=100)
+    assert lib.tree_accept_greedy(ctypes.byref(acc), None, 0, None) == 1
+    cmp_ = ts.CompactArgs(num_requests=0, n_tree_max=16, num_layers=1, num_kv_heads=2, head_dim=64, elem_bytes=2)
+    assert lib.tree_cache_compact(ctypes.byref(cmp_), None, 0, None) == 1
