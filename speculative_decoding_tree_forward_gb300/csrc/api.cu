@@ -87,7 +87,7 @@ int cached_occupancy(bool tc, int head_dim, int stages, int rows_pad, int num_re
 // ------------------------------------------------------------------ attention plan
 struct AttnPlan {
   bool use_tc;
-  int rows, row_groups, rows_pad, group, stages, num_ctas, hp;
+  int rows, row_groups, rows_pad, group, stages, num_ctas, hp, merge_half_warp;
   int64_t units, slots;
   size_t ws_bytes, off_o, off_lse, off_q;  // off_q: rotated queries (rope_theta > 0), else 0
 };
@@ -170,6 +170,11 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
     if (nc > t_max) nc = t_max;
     pl->num_ctas = static_cast<int>(nc < 1 ? 1 : nc);
   }
+  // The merge runs eight warps per CTA, four CTAs per SM.  One warp per row
+  // (eight shares prefetched) while that grid fits one resident wave; past
+  // that, one half-warp per row (four prefetched), which keeps twice the rows
+  // in flight: a second wave would cost every row of it another round trip.
+  pl->merge_half_warp = pl->units * ((pl->rows_pad + 7) / 8) > 4LL * device_sm_count() ? 1 : 0;
   pl->slots = pl->num_ctas + pl->units;
   pl->off_o = kWsHeader;
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
@@ -338,6 +343,7 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   // measured the best totals at E = 4..6
   p.seg_cost = pl.use_tc ? 4 : 0;
   p.stages = pl.stages;
+  p.merge_half_warp = pl.merge_half_warp;
   p.num_units = pl.units;
   p.prefix_len = a->prefix_len;
   p.n_tree = a->n_tree;

@@ -7,24 +7,65 @@
 //   O = sum_s 2^(lse_s - lse) O_s,   lse = log2 sum_s 2^lse_s,
 // skipping CTAs whose tile range was empty, and writes the bf16 output and
 // the natural-log lse.  Units held by one CTA were written directly by the
-// attention kernel and are skipped here.  One warp per output row, eight rows
-// per CTA, each lane owning four columns.  The split (which CTAs hold tiles
+// attention kernel and are skipped here.  The split (which CTAs hold tiles
 // of the unit) follows from the request lengths alone, so it is worked out
-// before the kernel waits for the attention kernel's results.  After the wait
-// the lse of the row's first 32 shares (one per lane) and its first eight
-// partial rows (coalesced 512-byte reads) are all requested before the
-// weights are known, so a row with up to eight shares costs one round trip
-// to L2; shares of CTAs that hold no tile of the unit get weight 0.
+// before the kernel waits for the attention kernel's results.  After the
+// wait the lse of a row's first shares (one per lane) and its first few
+// partial rows (coalesced reads) are all requested before the weights are
+// known, so a row with up to that many shares costs one round trip to L2;
+// shares of CTAs that hold no tile of the unit get weight 0.
+//
+// Two shapes, picked by the host: one warp per row with eight shares
+// prefetched (when that grid fits one resident wave of CTAs: many shares per
+// row, few rows), or one half-warp per row with four prefetched (twice the
+// rows in flight for the same registers, so a grid of many rows lands in
+// one wave instead of two).
 #include "attn_common.cuh"
 
 namespace ts {
 namespace {
 
-constexpr int kMergeWarps = 8;  // rows per CTA
-constexpr int kPrefetchSlots = 8;  // partial rows loaded before the weights are known
+constexpr int kMergeWarps = 8;
+constexpr int kPrefetchWarp = 8;              // warp per row: partial rows loaded before the weights are known
+constexpr int kRowsPerCtaHalf = 2 * kMergeWarps;  // half-warp per row
+constexpr int kPrefetchHalf = 4;              // half-warp per row: partial rows loaded before the weights are known
+constexpr int kMaxVec = 2;                    // half-warp per row: float4 per lane of one partial row (head_dim 128)
 
-// at most 64 registers: four CTAs (32 warps) per SM, so the grid lands in one wave
-__global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const AttnParams p) {
+// The split as the attention kernel laid it out, from the request lengths it
+// read (clamped the same way).  They were final before the attention kernel
+// passed its own wait, which precedes the merge grid's launch, so warp 0 of a
+// merge CTA works the split out for the CTA's unit before the wait for the
+// attention kernel's results: the CTAs holding tiles of the unit and, for the
+// first 32 of them, which hold a share (bit i of *hold: CTA c_lo + i).
+__device__ __forceinline__ void merge_split(const AttnParams& p, int b, int uir, int units_per_req, int lane,
+                                            UnitSplit* sp, unsigned* hold) {
+  int64_t before = 0, total = 0;
+  int mine = 0;
+  for (int r = lane; r < p.num_req; r += 32) {
+    int P, n;
+    attn_lengths(p, r, P, n, false);
+    const int t = attn_tiles(P + n);
+    total += static_cast<int64_t>(t) * units_per_req;
+    if (r < b) before += static_cast<int64_t>(t) * units_per_req;
+    if (r == b) mine = t;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+    mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, o));
+  }
+  if (lane == 0) sp->init(before, total, mine, b, uir, units_per_req, p.num_req, p.seg_cost, p.num_ctas);
+  __syncwarp();
+  const int c = sp->c_lo + lane;
+  const unsigned h = __ballot_sync(0xffffffffu, c <= sp->c_hi && sp->c_lo != sp->c_hi && sp->holds(c));
+  if (lane == 0) *hold = h;
+}
+
+// One warp per output row, eight rows per CTA, each lane owning four
+// columns; the first kPrefetchWarp shares of a row are prefetched.  At most
+// 64 registers: four CTAs (32 warps) per SM.
+__global__ void __launch_bounds__(kMergeWarps * 32, 4) merge_row_per_warp_kernel(const AttnParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t unit = blockIdx.x;
   // a unit is (request, group of hp KV heads, row group); with hp = 2 the
@@ -37,37 +78,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
   const int rl = blockIdx.y * kMergeWarps + warp;
   const int hj = p.hp == 2 ? rl >> 6 : 0, loc = p.hp == 2 ? rl & 63 : rl;
   const bool row_valid = p.hp == 2 ? loc < p.rows : rl < min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit);
-  // The split as the attention kernel laid it out, from the request lengths
-  // it read (clamped the same way).  They were final before the attention
-  // kernel passed its own wait, which precedes this grid's launch, so warp 0
-  // works the split out for the CTA's unit before the wait for the attention
-  // kernel's results: the CTAs holding tiles of the unit and, for the first
-  // 32 of them, which hold a share.
   __shared__ UnitSplit s_sp;
   __shared__ unsigned s_hold;
-  if (warp == 0) {
-    int64_t before = 0, total = 0;
-    int mine = 0;
-    for (int r = lane; r < p.num_req; r += 32) {
-      int P, n;
-      attn_lengths(p, r, P, n, false);
-      const int t = attn_tiles(P + n);
-      total += static_cast<int64_t>(t) * units_per_req;
-      if (r < b) before += static_cast<int64_t>(t) * units_per_req;
-      if (r == b) mine = t;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-      total += __shfl_xor_sync(0xffffffffu, total, o);
-      mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, o));
-    }
-    if (lane == 0) s_sp.init(before, total, mine, b, uir, units_per_req, p.num_req, p.seg_cost, p.num_ctas);
-    __syncwarp();
-    const int c = s_sp.c_lo + lane;
-    const unsigned hold = __ballot_sync(0xffffffffu, c <= s_sp.c_hi && s_sp.c_lo != s_sp.c_hi && s_sp.holds(c));
-    if (lane == 0) s_hold = hold;
-  }
+  if (warp == 0) merge_split(p, b, uir, units_per_req, lane, &s_sp, &s_hold);
   __syncthreads();
   const int c_lo = s_sp.c_lo, c_hi = s_sp.c_hi;
   const bool valid_l = (s_hold >> lane) & 1u;
@@ -75,7 +88,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
   pdl_launch_dependents();
   if (!row_valid || c_lo == c_hi) return;  // padding row, or one CTA held the whole unit and wrote it
   auto holds = [&](int c) -> bool { return s_sp.holds(c); };
-  const int ncs = c_hi - c_lo + 1;
 
   // slot of CTA c: c + unit; its lse at part_lse[slot * rows_pad + row]
   const float* lse_col = p.part_lse + unit * p.rows_pad + rl;
@@ -86,14 +98,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
                                            lane * 4);
   };
   // one round trip: the lse of the first 32 slots (one per lane) and the
-  // partial rows of the first kPrefetchSlots slots, all issued before the
+  // partial rows of the first kPrefetchWarp slots, all issued before the
   // weights are known (slots of CTAs without a share get weight 0)
   const unsigned hold = s_hold;
   float lse_l = -INFINITY;
   if (valid_l) lse_l = __ldcg(lse_col + static_cast<int64_t>(c_lo + lane) * p.rows_pad);
-  float4 x[kPrefetchSlots];
+  float4 x[kPrefetchWarp];
 #pragma unroll
-  for (int q = 0; q < kPrefetchSlots; ++q) {
+  for (int q = 0; q < kPrefetchWarp; ++q) {
     x[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (((hold >> q) & 1u) && active) x[q] = __ldcg(part_row(c_lo + q));
   }
@@ -110,14 +122,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
   float wl = valid_l ? exp2f(lse_l - mbase) : 0.f;
   float wsum = wl;
 #pragma unroll
-  for (int q = 0; q < kPrefetchSlots; ++q) {
+  for (int q = 0; q < kPrefetchWarp; ++q) {
     const float wq = __shfl_sync(0xffffffffu, wl, q);
     acc.x += wq * x[q].x;
     acc.y += wq * x[q].y;
     acc.z += wq * x[q].z;
     acc.w += wq * x[q].w;
   }
-  // slots kPrefetchSlots .. 31 of the first chunk, then further chunks of 32
+  // slots kPrefetchWarp .. 31 of the first chunk, then further chunks of 32
   for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
     float wc = wl;
     if (c0 != c_lo) {
@@ -126,7 +138,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
       wc = v ? exp2f(__ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad) - mbase) : 0.f;
       wsum += wc;
     }
-    const int q0 = c0 == c_lo ? kPrefetchSlots : 0;
+    const int q0 = c0 == c_lo ? kPrefetchWarp : 0;
     for (int q = q0; q < 32 && c0 + q <= c_hi; q += 4) {  // warp-uniform bounds
       float w4[4];
       float4 y[4];
@@ -160,12 +172,149 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) attn_merge_kernel(const A
     p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (mbase + log2f(wsum)) * 0.69314718055994530942f;
 }
 
+// One half-warp per output row, 16 rows per CTA, each of its 16 lanes
+// owning head_dim / 16 columns; the first kPrefetchHalf shares of a row are
+// prefetched.  At most 64 registers: four CTAs (32 warps, 64 rows) per SM.
+__global__ void __launch_bounds__(kMergeWarps * 32, 4) merge_row_per_half_warp_kernel(const AttnParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;  // the row of this half-warp, the lane within it
+  const int64_t unit = blockIdx.x;
+  // a unit is (request, group of hp KV heads, row group); with hp = 2 the
+  // unit's rows are two heads' R <= 64 rows at 0 and 64
+  const int units_per_req = (p.hkv / p.hp) * p.row_groups;
+  const int b = static_cast<int>(blockIdx.x) / units_per_req;
+  const int uir = static_cast<int>(blockIdx.x) % units_per_req;
+  const int kvh = uir / p.row_groups;  // head group
+  const int rg = uir % p.row_groups;
+  const int rl = blockIdx.y * kRowsPerCtaHalf + warp * 2 + half;
+  const int hj = p.hp == 2 ? rl >> 6 : 0, loc = p.hp == 2 ? rl & 63 : rl;
+  const bool row_valid = p.hp == 2 ? loc < p.rows : rl < min(kMaxRowsPerUnit, p.rows - rg * kMaxRowsPerUnit);
+  __shared__ UnitSplit s_sp;
+  __shared__ unsigned s_hold;
+  if (warp == 0) merge_split(p, b, uir, units_per_req, lane, &s_sp, &s_hold);
+  __syncthreads();
+  const int c_lo = s_sp.c_lo, c_hi = s_sp.c_hi;
+  const unsigned hold = s_hold;
+  const bool valid_l = row_valid && ((hold >> hl) & 1u);  // this lane's share of the first 16
+  pdl_wait();
+  pdl_launch_dependents();
+  // padding rows (both halves), or one CTA held the whole unit and wrote it
+  if (!__any_sync(0xffffffffu, row_valid) || c_lo == c_hi) return;
+  auto holds = [&](int c) -> bool { return s_sp.holds(c); };
+  const int D = p.head_dim;
+  const int nv = D >> 6;  // float4 per lane: 1 (head_dim 64) or 2 (128)
+  const int col = hl * (D >> 4);
+  // slot of CTA c: c + unit; its lse at part_lse[slot * rows_pad + row]
+  const float* lse_col = p.part_lse + unit * p.rows_pad + rl;
+  auto part_row = [&](int c) {
+    return reinterpret_cast<const float4*>(p.part_o + ((static_cast<int64_t>(c) + unit) * p.rows_pad + rl) * D + col);
+  };
+  const int hbase = half * 16;
+
+  // one round trip: the lse of the first 16 slots (one per lane of the half)
+  // and the partial rows of the first kPrefetchHalf slots, all issued before the
+  // weights are known (slots of CTAs without a share get weight 0)
+  float lse_l = -INFINITY;
+  if (valid_l) lse_l = __ldcg(lse_col + static_cast<int64_t>(c_lo + hl) * p.rows_pad);
+  float4 x[kPrefetchHalf][kMaxVec];
+#pragma unroll
+  for (int q = 0; q < kPrefetchHalf; ++q)
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v) {
+      x[q][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row_valid && ((hold >> q) & 1u) && v < nv) x[q][v] = __ldcg(part_row(c_lo + q) + v);
+    }
+  float mx = lse_l;
+  for (int c0 = c_lo + 16; c0 <= c_hi; c0 += 16) {  // more than 16 shares: rare
+    const int c = c0 + hl;
+    if (row_valid && c <= c_hi && holds(c)) mx = fmaxf(mx, __ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad));
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));  // within the half
+  const float mbase = (mx == -INFINITY) ? 0.f : mx;
+
+  float4 acc[kMaxVec];
+#pragma unroll
+  for (int v = 0; v < kMaxVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float wl = valid_l ? exp2f(lse_l - mbase) : 0.f;
+  float wsum = wl;
+#pragma unroll
+  for (int q = 0; q < kPrefetchHalf; ++q) {
+    const float wq = __shfl_sync(0xffffffffu, wl, hbase + q);
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v) {
+      acc[v].x += wq * x[q][v].x;
+      acc[v].y += wq * x[q][v].y;
+      acc[v].z += wq * x[q][v].z;
+      acc[v].w += wq * x[q][v].w;
+    }
+  }
+  // slots kPrefetchHalf .. 15 of the first chunk, then further chunks of 16
+  // (the unit, hence every bound, is the same for both halves)
+  for (int c0 = c_lo; c0 <= c_hi; c0 += 16) {
+    float wc = wl;
+    if (c0 != c_lo) {
+      const int c = c0 + hl;
+      const bool v = row_valid && c <= c_hi && holds(c);
+      wc = v ? exp2f(__ldcg(lse_col + static_cast<int64_t>(c) * p.rows_pad) - mbase) : 0.f;
+      wsum += wc;
+    }
+    const int q0 = c0 == c_lo ? kPrefetchHalf : 0;
+    for (int q = q0; q < 16 && c0 + q <= c_hi; q += 2) {  // warp-uniform bounds
+      float w2[2];
+      float4 y[2][kMaxVec];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const bool in = q + u < 16 && c0 + q + u <= c_hi;
+        w2[u] = __shfl_sync(0xffffffffu, wc, hbase + (in ? q + u : 0));
+        if (!in) w2[u] = 0.f;
+#pragma unroll
+        for (int v = 0; v < kMaxVec; ++v) {
+          y[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (in && w2[u] != 0.f && v < nv) y[u][v] = __ldcg(part_row(c0 + q + u) + v);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int v = 0; v < kMaxVec; ++v) {
+          acc[v].x += w2[u] * y[u][v].x;
+          acc[v].y += w2[u] * y[u][v].y;
+          acc[v].z += w2[u] * y[u][v].z;
+          acc[v].w += w2[u] * y[u][v].w;
+        }
+    }
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);  // within the half
+  if (!row_valid) return;
+  const float inv = wsum > 0.f ? __frcp_rn(wsum) : 0.f;
+  const int r = rg * kMaxRowsPerUnit + loc;
+  const int i = r / p.group, h = (p.hp * kvh + hj) * p.group + r % p.group;
+  __nv_bfloat16* orow = p.out + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * D + col;
+  if (nv == 2) {
+    *reinterpret_cast<uint4*>(orow) =
+        make_uint4(pack_bf16x2(acc[0].x * inv, acc[0].y * inv), pack_bf16x2(acc[0].z * inv, acc[0].w * inv),
+                   pack_bf16x2(acc[1].x * inv, acc[1].y * inv), pack_bf16x2(acc[1].z * inv, acc[1].w * inv));
+  } else {
+    *reinterpret_cast<uint2*>(orow) =
+        make_uint2(pack_bf16x2(acc[0].x * inv, acc[0].y * inv), pack_bf16x2(acc[0].z * inv, acc[0].w * inv));
+  }
+  if (p.lse != nullptr && hl == 0)
+    p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (mbase + log2f(wsum)) * 0.69314718055994530942f;
+}
+
 }  // namespace
 
 cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream) {
+  if (p.merge_half_warp) {
+    const int row_blocks = (p.rows_pad + kRowsPerCtaHalf - 1) / kRowsPerCtaHalf;
+    return launch_pdl(merge_row_per_half_warp_kernel, dim3(static_cast<unsigned>(p.num_units), row_blocks),
+                      dim3(kMergeWarps * 32), 0, stream, p);
+  }
   const int row_blocks = (p.rows_pad + kMergeWarps - 1) / kMergeWarps;
-  return launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(p.num_units), row_blocks), dim3(kMergeWarps * 32), 0,
-                    stream, p);
+  return launch_pdl(merge_row_per_warp_kernel, dim3(static_cast<unsigned>(p.num_units), row_blocks),
+                    dim3(kMergeWarps * 32), 0, stream, p);
 }
 
 }  // namespace ts

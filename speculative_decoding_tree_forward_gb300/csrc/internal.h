@@ -49,6 +49,7 @@ struct AttnParams {
   int num_ctas;      // NC
   int seg_cost;      // E of the cost-weighted split (tcgen05 path, > 0); 0 = plain split of the tiles
   int stages;
+  int merge_half_warp;  // the merge takes one row per half-warp (else one per warp)
   int64_t num_units; // num_req * hkv * row_groups
   const int32_t* prefix_len;
   const int32_t* n_tree;

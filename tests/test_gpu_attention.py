@@ -112,8 +112,10 @@ def test_tcgen05_first_call_many_short_splits(num_ctas):
 
 @pytest.mark.parametrize("which", ["tc_r128", "tc_two_heads", "mma_r16"])
 def test_merge_of_many_split_units(which):
-    """More split units than one resident wave of merge CTAs holds: 80 units
-    of 128 rows, 160 two-head units, and 624 units of 16 rows."""
+    """More split rows than one resident wave of warp-per-row merge CTAs
+    holds, so the merge takes one row per half-warp: 80 units of 128 rows,
+    160 two-head units, and 624 units of 16 rows at head_dim 64 (one float4
+    per lane)."""
     if which == "tc_r128":
         case = W.random_attn_case(32, num_req=10, hq=64, hkv=8, d=128, n_tree_max=16, prefix_range=(100, 700))
         path = 2
