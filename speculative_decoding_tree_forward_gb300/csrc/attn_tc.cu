@@ -840,11 +840,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             // fp32 partials leave as one TMA store per chunk, so the warp waits
             // only until the tile has been read; bf16 outputs leave as whole
             // 64-byte row segments.
-            uint8_t* stg = smem + L.stg + (warp & 3) * TcLayout::kStgWarpBytes;
+            // The CTA's last segment stages in the V ring, idle by now (every
+            // tile has been loaded and its PV is done): 16 KB per warp, one
+            // 4 KB tile per chunk, so the chunks' stores need not wait for
+            // one another.  Other segments share 4 KB per warp.
+            const bool last_seg = sl == n_tiles - 1;
+            const uint32_t stg_step = last_seg ? TcLayout::kStgWarpBytes : 0u;  // between chunks
+            const uint32_t stg = last_seg ? L.v + (warp & 3) * 4 * TcLayout::kStgWarpBytes
+                                          : L.stg + (warp & 3) * TcLayout::kStgWarpBytes;
             const int row0 = (warp & 3) * 32;
             // finishers of consecutive short segments may be different
             // warpgroups with no O in common: take the staging rows in turn
-            if (seg_idx > 0 && !mbar_wait(&ctl->stg_free, (seg_idx - 1) & 1)) {
+            if (!last_seg && seg_idx > 0 && !mbar_wait(&ctl->stg_free, (seg_idx - 1) & 1)) {
               report_error(p.err, TS_DEVERR_TIMEOUT);
               *abort_flag = 1;
               break;
@@ -856,6 +863,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             tmem_ld_wait();
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
+              uint8_t* const cs = smem + stg + ch * stg_step;
               float o[32];
 #pragma unroll
               for (int e = 0; e < 32; ++e)
@@ -867,7 +875,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               if (complete) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                  *reinterpret_cast<uint4*>(stg + sw128(lane, q)) =
+                  *reinterpret_cast<uint4*>(cs + sw128(lane, q)) =
                       make_uint4(pack_bf16x2(o[8 * q + 0], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
                                  pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
                 __syncwarp();
@@ -877,7 +885,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                   const int row = row0 + rr, lrow = Sh::local_of(row);
                   if (lrow >= p.rows) continue;
                   const int ii = lrow / p.group, hh = (HP * c.uir + Sh::head_of(row)) * p.group + lrow % p.group;
-                  const uint4 val = *reinterpret_cast<const uint4*>(stg + sw128(rr, c4));
+                  const uint4 val = *reinterpret_cast<const uint4*>(cs + sw128(rr, c4));
                   reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(c.b) * p.n_query + ii) * p.hq + hh) * 128 +
                                            ch * 32)[c4] = val;
                 }
@@ -885,20 +893,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               } else {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                  *reinterpret_cast<float4*>(stg + sw128(lane, q)) =
+                  *reinterpret_cast<float4*>(cs + sw128(lane, q)) =
                       make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                  tma_store_2d(&pmap, stg, ch * 32, static_cast<int>(slot * 128 + row0));
+                  tma_store_2d(&pmap, cs, ch * 32, static_cast<int>(slot * 128 + row0));
                   bulk_commit();
-                  bulk_wait_read_all();  // the staging rows may be rewritten
+                  if (stg_step == 0u) bulk_wait_read_all();  // the staging rows may be rewritten
                 }
                 __syncwarp();
               }
               if (ch < 3) tmem_ld_wait();
             }
-            if (lane == 0) mbar_arrive(&ctl->stg_free);            tc_fence_before();
+            if (lane == 0) mbar_arrive(&ctl->stg_free);
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(&ctl->o_free[wg]);  // both O accumulators have been read
