@@ -8,8 +8,8 @@ trees, vocab 152064, 64 layers):
   2. greedy acceptance over the vocab logits (tree_accept_greedy),
   3. target-side re-root + KV compaction over 64 layers (tree_cache_compact),
   4. draft-side re-root + KV compaction of the 64-node draft trees over the
-     draft cache's 64 layers (tree_cache_compact), on a second stream beside 3
-     (the two caches are disjoint; --serial-compaction runs them in order).
+     draft cache's 64 layers, in the same launch as 3 (tree_cache_compact_batch:
+     the two caches are disjoint; --serial-compaction makes two calls).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
 bounded sample of the same workload instead.  With torchrun and N > 1 every
@@ -55,7 +55,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
     ap.add_argument("--serial-compaction", action="store_true",
-                    help="run the target- and draft-side compactions one after the other on one stream")
+                    help="compact the target- and draft-side caches with two calls instead of one batched launch")
     return ap.parse_args()
 
 
@@ -324,23 +324,11 @@ def build_step(args, torch, ts, W, device):
         accept_call = ts.tree_accept_sample_args if acc_state[5] == "sample" else ts.tree_accept_greedy_args
         phases.append(("accept", [lambda: accept_call(acc_state[0], acc_state[1])]))
     if len(comp_states) == 2 and not args.serial_compaction:
-        # the target- and draft-side caches and their metadata are disjoint,
-        # so the two compactions run side by side: the draft side on a second
-        # stream forked after the acceptance and joined before the step ends
-        side = torch.cuda.Stream(device)
-        fork, join = torch.cuda.Event(), torch.cuda.Event()
-        tgt, drf = comp_states
-
-        def both_compactions():
-            main = torch.cuda.current_stream(device)
-            fork.record(main)
-            side.wait_event(fork)
-            ts.tree_cache_compact_args(drf[0], drf[1], stream=side)
-            ts.tree_cache_compact_args(tgt[0], tgt[1], stream=main)
-            join.record(side)
-            main.wait_event(join)
-
-        phases.append(("other", [both_compactions]))
+        # the target- and draft-side caches and their metadata are disjoint:
+        # both compactions run as one launch (tree_cache_compact_batch)
+        batch_args, batch_ws = [st[0] for st in comp_states], [st[1] for st in comp_states]
+        launches -= 1   # one kernel for both
+        phases.append(("other", [lambda: ts.tree_cache_compact_batch_args(batch_args, batch_ws)]))
     elif comp_states:
         phases.append(("other", [lambda st=st: ts.tree_cache_compact_args(st[0], st[1]) for st in comp_states]))
 
@@ -636,7 +624,8 @@ def main():
                    "q_heads": info["attn_cases"][0].num_q_heads, "kv_heads": info["attn_cases"][0].num_kv_heads,
                    "head_dim": info["attn_cases"][0].head_dim, "tree_nodes": info["attn_cases"][0].n_tree_max,
                    "layers_compacted": args.layers if info["comp_states"] else 0,
-                   "compaction_streams": 2 if len(info["comp_states"]) == 2 and not args.serial_compaction else 1,
+                   "compaction": ("one launch for both caches" if len(info["comp_states"]) == 2
+                                  and not args.serial_compaction else "one launch per cache"),
                    "rope_theta": args.rope_theta,
                    "acceptance": "stochastic, T = %g" % args.temperature if args.temperature > 0 else "greedy", "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
                    "l2": ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2" % (attn_bytes / 1e6)

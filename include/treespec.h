@@ -270,6 +270,21 @@ TS_API size_t tree_compact_workspace_size(const ts_compact_args* args);
 TS_API ts_status tree_cache_compact(const ts_compact_args* args, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* Several independent compactions in one kernel launch, e.g. the target-side
+ * and the draft-side cache of one verify step (SwiftSpec summary, §3.2: both
+ * the target and the draft keep a prefix cache and a tree cache).  args[i],
+ * workspaces[i] and workspace_bytes[i] are exactly what tree_cache_compact
+ * would take for call i (each call keeps its own workspace, error word and
+ * ticket counters, so the workspaces must be distinct); the calls must not
+ * share any written buffer (caches, new metadata), and the result equals
+ * `count` tree_cache_compact calls.
+ * count in [1, TS_MAX_COMPACT_BATCH]; the requests of all calls together
+ * <= 65535.  Every call is validated before anything is launched: the
+ * first failing status is returned and nothing runs. */
+#define TS_MAX_COMPACT_BATCH 4
+TS_API ts_status tree_cache_compact_batch(const ts_compact_args* args, int count, void* const* workspaces,
+                                          const size_t* workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------
  * Stochastic tree acceptance (speculative sampling at temperature > 0).
  *

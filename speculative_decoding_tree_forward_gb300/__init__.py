@@ -96,6 +96,8 @@ _acc_ws = _sig("tree_accept_workspace_size", ctypes.c_size_t, [ctypes.POINTER(Ac
 _acc = _sig("tree_accept_greedy", _i32, [ctypes.POINTER(AcceptArgs), _vp, ctypes.c_size_t, _vp])
 _cmp_ws = _sig("tree_compact_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CompactArgs)])
 _cmp = _sig("tree_cache_compact", _i32, [ctypes.POINTER(CompactArgs), _vp, ctypes.c_size_t, _vp])
+_cmp_batch = _sig("tree_cache_compact_batch", _i32, [ctypes.POINTER(CompactArgs), _i32, ctypes.POINTER(_vp),
+                                                  ctypes.POINTER(ctypes.c_size_t), _vp])
 _smp_ws = _sig("tree_accept_sample_workspace_size", ctypes.c_size_t, [ctypes.POINTER(SampleArgs)])
 _smp = _sig("tree_accept_sample", _i32, [ctypes.POINTER(SampleArgs), _vp, ctypes.c_size_t, _vp])
 _exp_ws = _sig("tree_expand_workspace_size", ctypes.c_size_t, [ctypes.POINTER(ExpandArgs)])
@@ -109,7 +111,8 @@ _version = _sig("ts_version", _i32, [])
 EXPORTED = ["tree_meta_workspace_size", "tree_build_mask", "tree_attn_workspace_size", "tree_attn_selected_path",
             "tree_attn_forward", "tree_attn_forward_noalloc",
             "tree_accept_workspace_size", "tree_accept_greedy", "tree_compact_workspace_size",
-            "tree_cache_compact", "tree_accept_sample_workspace_size", "tree_accept_sample",
+            "tree_cache_compact", "tree_cache_compact_batch", "tree_accept_sample_workspace_size",
+            "tree_accept_sample",
             "tree_expand_workspace_size", "tree_expand", "tree_select_workspace_size",
             "tree_select_subtree", "ts_status_string", "ts_read_device_error", "ts_version"]
 
@@ -324,6 +327,18 @@ def tree_compact_workspace_size(args: CompactArgs) -> int:
 
 def tree_cache_compact_args(args: CompactArgs, workspace: torch.Tensor, stream=None) -> None:
     _check(_cmp(ctypes.byref(args), workspace.data_ptr(), workspace.numel(), _stream(stream)), "tree_cache_compact")
+
+
+def tree_cache_compact_batch_args(args: Sequence[CompactArgs], workspaces: Sequence[torch.Tensor], stream=None) -> None:
+    """Several independent compactions (e.g. the target- and draft-side caches) in one launch; each call keeps
+    the workspace it would take alone."""
+    n = len(args)
+    if n != len(workspaces):
+        raise ValueError("one workspace per compaction")
+    arr = (CompactArgs * n)(*args)
+    ptrs = (_vp * n)(*[w.data_ptr() for w in workspaces])
+    sizes = (ctypes.c_size_t * n)(*[w.numel() for w in workspaces])
+    _check(_cmp_batch(arr, n, ptrs, sizes, _stream(stream)), "tree_cache_compact_batch")
 
 
 def tree_cache_compact(k_layers: Sequence[torch.Tensor], v_layers: Sequence[torch.Tensor], prefix_len, n_tree,

@@ -444,7 +444,12 @@ size_t tree_compact_workspace_size(const ts_compact_args* a) {
   return kWsHeader + align256(static_cast<size_t>(a->num_requests) * sizeof(unsigned));
 }
 
-ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// Validates one compaction call and fills its kernel parameters; the CTA
+// count per request is sized for `total_requests` requests in the launch.
+static ts_status compact_params(const ts_compact_args* a, void* workspace, size_t workspace_bytes, int64_t total_requests,
+                                CompactParams& p) {
   if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->m_max < 0 || a->num_layers < 1 ||
       a->num_kv_heads < 1 || a->head_dim < 1 || a->elem_bytes < 1)
     return TS_ERR_INVALID_ARG;
@@ -467,7 +472,6 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   const size_t need = tree_compact_workspace_size(a);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TS_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  CompactParams p;
   p.num_req = a->num_requests;
   p.n_tree_max = a->n_tree_max;
   p.m_max = a->m_max;
@@ -483,12 +487,13 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   const int items = 2 * a->num_layers;
   const int sms = device_sm_count();
   if (sms <= 0) return TS_ERR_CUDA;
-  int per_req = static_cast<int>(std::min<int64_t>(items, std::max<int64_t>(1, (2LL * sms + a->num_requests - 1) /
-                                                                                    a->num_requests)));
+  int per_req = static_cast<int>(std::min<int64_t>(items, std::max<int64_t>(1, (2LL * sms + total_requests - 1) /
+                                                                                    total_requests)));
   int ipc = (items + per_req - 1) / per_req;
   const int64_t max_item_vecs = static_cast<int64_t>(a->n_tree_max) * (row_bytes / 16);
   ipc = static_cast<int>(std::min<int64_t>(ipc, std::max<int64_t>(1, (INT32_MAX / 2) / max_item_vecs)));
   p.items_per_cta = ipc;
+  p.ctas = (items + ipc - 1) / ipc;
   // shared-memory staging: the CTA's largest possible move, at most 96 KB
   const int64_t most = max_item_vecs * ipc;
   p.batch_vecs = static_cast<int>(std::min<int64_t>(most, kCompactBatchBytes / 16));
@@ -508,9 +513,43 @@ ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t w
   p.src_rows = a->src_rows;
   p.err = reinterpret_cast<unsigned*>(ws);
   p.ticket = reinterpret_cast<unsigned*>(ws + kWsHeader);
+  return TS_OK;
+}
+
+extern "C" {
+
+ts_status tree_cache_compact(const ts_compact_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a == nullptr) return TS_ERR_INVALID_ARG;
+  CompactParams p;
+  const ts_status st = compact_params(a, workspace, workspace_bytes, a->num_requests, p);
+  if (st != TS_OK) return st;
   cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
+
+ts_status tree_cache_compact_batch(const ts_compact_args* args, int count, void* const* workspaces,
+                                   const size_t* workspace_bytes, void* stream) {
+  if (args == nullptr || workspaces == nullptr || workspace_bytes == nullptr || count < 1) return TS_ERR_INVALID_ARG;
+  if (count > TS_MAX_COMPACT_BATCH) return TS_ERR_UNSUPPORTED;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (args[i].num_requests < 1) return TS_ERR_INVALID_ARG;
+    total += args[i].num_requests;
+  }
+  if (total > 65535) return TS_ERR_UNSUPPORTED;
+  CompactBatch bt;
+  bt.count = count;
+  int64_t end = 0;
+  for (int i = 0; i < count; ++i) {
+    const ts_status st = compact_params(&args[i], workspaces[i], workspace_bytes[i], total, bt.p[i]);
+    if (st != TS_OK) return st;
+    end += args[i].num_requests;
+    bt.req_end[i] = static_cast<int>(end);
+  }
+  cudaError_t e = launch_compact_batch(bt, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 
 // ------------------------------------------------------------------ stochastic acceptance
 // Vocab slice per row-statistics CTA (a multiple of 1024 floats): the

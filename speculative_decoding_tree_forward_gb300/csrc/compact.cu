@@ -6,7 +6,9 @@
 // (re-rooting at t6 reuses its subtree; an out-of-tree token reuses nothing).
 //
 // Grid (G, num_requests): the G CTAs of request b share its (layer, K|V)
-// row moves.  Every CTA derives the re-root itself from the request's tree,
+// row moves.  A batch of independent calls (e.g. the target-side and the
+// draft-side cache of one verify step) runs as one launch whose grid rows
+// are the requests of all calls.  Every CTA derives the re-root itself from the request's tree,
 // held in shared memory (at most TS_MAX_TREE nodes):
 //   1. one warp walks the verified tokens down the tree, taking at each step
 //      the lowest-index child of the current node that carries the token
@@ -31,6 +33,7 @@
 // item a row is read, at the latest, in the batch that overwrites it, and
 // every read of a batch precedes its stores: no row is overwritten before it
 // is read.  Items of different CTAs are disjoint.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -42,9 +45,9 @@ namespace {
 constexpr int kCompactThreads = 256;
 constexpr int kLoadsInFlight = 8;  // 16-byte loads per thread before the first store to shared memory
 
-__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
+// One CTA's share of one request's compaction: request b of the call whose
+// parameters are p, CTA `cta` of its p.ctas.
+__device__ __forceinline__ void compact_body(const CompactParams& p, const int b, const int cta) {
   extern __shared__ uint4 buf[];  // [batch_vecs]
   __shared__ int par_s[TS_MAX_TREE];
   __shared__ int tok_s[TS_MAX_TREE];
@@ -58,7 +61,6 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   __shared__ int blk_s[TS_MAX_TREE + 2];  // paged: block-table entries of the pages holding rows P .. P + n - 1
   __shared__ int walk_cur, walk_plen, walk_all, last_ticket;
 
-  const int b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t rowbase = static_cast<int64_t>(b) * p.n_tree_max;
 
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   if (m < 0 || m > p.m_max) { m = min(max(m, 0), p.m_max); bad = true; }
   const int cap = p.paged ? p.max_blocks * p.page_size : p.max_kv_len;
   if (P < 0 || P + n > cap) { P = min(max(P, 0), max(cap - n, 0)); bad = true; }
-  if (bad && tid == 0 && blockIdx.x == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
+  if (bad && tid == 0 && cta == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
   // A walk step matches at most one node, so with n <= TS_MAX_TREE nodes the
   // walk has always ended by step TS_MAX_TREE + 1: later tokens are never read.
   const int mw = min(m, TS_MAX_TREE + 1);
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   if (tid < n) {
     my_par = p.parent[rowbase + tid];
     if (my_par < -1 || my_par >= tid) {
-      if (blockIdx.x == 0) report_error(p.err, TS_DEVERR_BAD_PARENT);
+      if (cta == 0) report_error(p.err, TS_DEVERR_BAD_PARENT);
       my_par = -1;
     }
     my_tok = p.tokens[rowbase + tid];
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   if (tid == 32) {
     __threadfence();
     const unsigned before = atomicAdd(p.ticket + b, 1u);
-    const int last = before + 1u == gridDim.x;
+    const int last = before + 1u == static_cast<unsigned>(p.ctas);
     if (last) p.ticket[b] = 0u;
     __threadfence();
     last_ticket = last;
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
 
   // ---- row moves: items it0 .. it1 - 1 of this CTA, as 16-byte vectors
   const int items = 2 * p.num_layers;
-  const int it0 = blockIdx.x * p.items_per_cta;
+  const int it0 = cta * p.items_per_cta;
   const int it1 = min(items, it0 + p.items_per_cta);
   if (nmv == 0 || it0 >= it1) return;
   const int vr = p.row_bytes / 16;
@@ -270,6 +272,31 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   }
 }
 
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  compact_body(p, blockIdx.y, blockIdx.x);
+}
+
+// Several independent compactions in one launch: row y of the grid is
+// request y - req_end[i - 1] of call i; call i uses the first p[i].ctas CTAs
+// of the row.  Each branch passes a fixed element, so the parameters are
+// read from the constant bank as in the single kernel.
+__global__ void __launch_bounds__(kCompactThreads) compact_batch_kernel(const CompactBatch bt) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int y = blockIdx.y, x = blockIdx.x;
+  if (y < bt.req_end[0]) {
+    if (x < bt.p[0].ctas) compact_body(bt.p[0], y, x);
+  } else if (bt.count > 1 && y < bt.req_end[1]) {
+    if (x < bt.p[1].ctas) compact_body(bt.p[1], y - bt.req_end[0], x);
+  } else if (bt.count > 2 && y < bt.req_end[2]) {
+    if (x < bt.p[2].ctas) compact_body(bt.p[2], y - bt.req_end[1], x);
+  } else if (bt.count > 3 && y < bt.req_end[3]) {
+    if (x < bt.p[3].ctas) compact_body(bt.p[3], y - bt.req_end[2], x);
+  }
+}
+
 }  // namespace
 
 // The dynamic shared-memory limit is raised once per device (to the largest
@@ -282,6 +309,8 @@ static bool compact_smem_ready() {
   std::lock_guard<std::mutex> lock(m);
   if (!done[dev]) {
     if (cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kCompactBatchBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(compact_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kCompactBatchBytes)) != cudaSuccess)
       return false;
     done[dev] = true;
@@ -292,9 +321,19 @@ static bool compact_smem_ready() {
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(p.batch_vecs) * 16;
   if (smem > 48 * 1024 && !compact_smem_ready()) return cudaErrorInvalidValue;
-  const int items = 2 * p.num_layers;
-  const int ctas = (items + p.items_per_cta - 1) / p.items_per_cta;
-  return launch_pdl(compact_kernel, dim3(ctas, p.num_req), dim3(kCompactThreads), smem, stream, p);
+  return launch_pdl(compact_kernel, dim3(p.ctas, p.num_req), dim3(kCompactThreads), smem, stream, p);
+}
+
+cudaError_t launch_compact_batch(const CompactBatch& bt, cudaStream_t stream) {
+  int vecs = 0, ctas = 0;
+  for (int i = 0; i < bt.count; ++i) {
+    vecs = std::max(vecs, bt.p[i].batch_vecs);
+    ctas = std::max(ctas, bt.p[i].ctas);
+  }
+  const size_t smem = static_cast<size_t>(vecs) * 16;
+  if (smem > 48 * 1024 && !compact_smem_ready()) return cudaErrorInvalidValue;
+  return launch_pdl(compact_batch_kernel, dim3(ctas, bt.req_end[bt.count - 1]), dim3(kCompactThreads), smem, stream,
+                    bt);
 }
 
 }  // namespace ts

@@ -106,7 +106,8 @@ cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 struct CompactParams {
   int num_req, n_tree_max, m_max, num_layers, row_bytes;
   int paged, max_kv_len, page_size, max_blocks, num_blocks;
-  int items_per_cta;  // (layer, K|V) items per CTA; CTAs per request = ceil(2 * num_layers / items_per_cta)
+  int items_per_cta;  // (layer, K|V) items per CTA
+  int ctas;           // CTAs per request: ceil(2 * num_layers / items_per_cta)
   int batch_vecs;     // 16-byte vectors staged in shared memory per batch
   void* const* k_layers;
   void* const* v_layers;
@@ -126,6 +127,14 @@ struct CompactParams {
   unsigned* ticket;  // [num_req] CTAs of the request that have read its metadata; 0 between calls
 };
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream);
+// Up to TS_MAX_COMPACT_BATCH independent compactions in one launch; call i
+// owns grid rows req_end[i - 1] .. req_end[i] - 1 (req_end[-1] = 0).
+struct CompactBatch {
+  CompactParams p[TS_MAX_COMPACT_BATCH];
+  int req_end[TS_MAX_COMPACT_BATCH];
+  int count;
+};
+cudaError_t launch_compact_batch(const CompactBatch& bt, cudaStream_t stream);
 
 // One (row, vocab slice) partial of the draft-candidate pass: running max m,
 // sum of exp(logit - m), and the slice's TS_MAX_EXPAND largest logits.

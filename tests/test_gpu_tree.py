@@ -182,6 +182,94 @@ def test_compact_one_workspace_serves_repeated_calls():
         assert int(ws[:4].view(torch.int32)[0]) == 0
 
 
+def _compact_inputs(case, layers, hkv, d, paged, seed):
+    """Random KV of `layers` layers for a compaction case, the C arguments of
+    its call and their device buffers (kept alive by the returned dict)."""
+    rng = np.random.default_rng(seed)
+    B = case.num_req
+    rows = case.prefix_len + case.n_tree
+    if paged:
+        nblk = [(int(r) + 15) // 16 for r in rows]
+        perm = rng.permutation(sum(nblk) + 2)
+        table = np.full((B, max(max(nblk), 1)), -1, np.int32)
+        off = 0
+        for b in range(B):
+            table[b, :nblk[b]] = perm[off:off + nblk[b]]
+            off += nblk[b]
+        shape = (len(perm), 16, hkv, d)
+    else:
+        table = None
+        shape = (B, int(rows.max()) + 3, hkv, d)
+    ks = [rng.integers(0, 65535, size=shape, dtype=np.uint16) for _ in range(layers)]
+    vs = [rng.integers(0, 65535, size=shape, dtype=np.uint16) for _ in range(layers)]
+    dev = {"kd": [torch.from_numpy(x.view(np.int16)).cuda() for x in ks],
+           "vd": [torch.from_numpy(x.view(np.int16)).cuda() for x in vs]}
+    dev["kp"], dev["vp"] = ts.layer_pointer_table(dev["kd"]), ts.layer_pointer_table(dev["vd"])
+    meta = {k: i32_dev(getattr(case, k)) for k in ("prefix_len", "n_tree", "parent", "tokens", "verified", "m")}
+    out = {"new_prefix_len": torch.empty(B, dtype=torch.int32, device="cuda"),
+           "new_n_tree": torch.empty(B, dtype=torch.int32, device="cuda"),
+           "new_parent": torch.empty_like(meta["parent"]), "new_tokens": torch.empty_like(meta["tokens"]),
+           "src_rows": torch.empty_like(meta["parent"])}
+    bt = None if table is None else i32_dev(table)
+    args = ts.compact_args(dev["kp"], dev["vp"], layers, hkv, d, meta["prefix_len"], meta["n_tree"], meta["parent"],
+                           meta["tokens"], meta["verified"], meta["m"], out["new_prefix_len"], out["new_n_tree"],
+                           out["new_parent"], out["new_tokens"], out["src_rows"],
+                           shape[1] if table is None else 0, bt, 16 if paged else 0, shape[0] if paged else 0)
+    return {"args": args, "ks": ks, "vs": vs, "table": table, "dev": dev, "meta": meta, "out": out, "bt": bt,
+            "layers": layers}
+
+
+def _check_compact(case, x):
+    got = {k: v.cpu().numpy() for k, v in x["out"].items()}
+    table = x["table"]
+    for b in range(case.num_req):
+        n, P = int(case.n_tree[b]), int(case.prefix_len[b])
+        r = T.reroot(case.parent[b][:n], case.tokens[b][:n], n, P, case.verified[b][: int(case.m[b])])
+        assert got["new_prefix_len"][b] == r.new_prefix_len and got["new_n_tree"][b] == r.new_n_tree
+        assert list(got["new_parent"][b][: r.new_n_tree]) == r.new_parent
+        assert list(got["new_tokens"][b][: r.new_n_tree]) == r.new_tokens
+        assert list(got["src_rows"][b][: len(r.src)]) == r.src
+        keep = P + len(r.src)
+        for li in range(x["layers"]):
+            for host, dv in ((x["ks"][li], x["dev"]["kd"][li]), (x["vs"][li], x["dev"]["vd"][li])):
+                expect = T.compact_rows(_logical(host, b, P + n, table), P, r.src)[:keep]
+                after = _logical(dv.cpu().numpy().view(np.uint16), b, keep, table)
+                assert np.array_equal(after, expect), f"request {b} layer {li}"
+
+
+@pytest.mark.parametrize("count", [1, 2, 4])
+def test_compact_batch_matches_oracle(count):
+    """tree_cache_compact_batch: up to four independent caches of different
+    shapes and layouts (a target-side and a draft-side cache, say) in one
+    launch, each compared with the oracle as if compacted alone."""
+    shapes = [(61, 4, 32, 3, 8, 128, False), (62, 6, 64, 2, 2, 64, True), (63, 3, 128, 5, 4, 64, False),
+              (64, 7, 24, 1, 8, 128, True)]
+    cases, xs = [], []
+    for seed, nreq, nmax, layers, hkv, d, paged in shapes[:count]:
+        case = W.random_compact_case(seed, num_req=nreq, n_tree_max=nmax, forest=bool(seed % 2))
+        cases.append(case)
+        xs.append(_compact_inputs(case, layers, hkv, d, paged, seed))
+    wss = [ts.new_workspace(ts.tree_compact_workspace_size(x["args"])) for x in xs]
+    ts.tree_cache_compact_batch_args([x["args"] for x in xs], wss)
+    torch.cuda.synchronize()
+    for case, x, ws in zip(cases, xs, wss):
+        _check_compact(case, x)
+        assert ts.read_device_error(ws) == 0
+        assert int(ws[256:256 + 4 * case.num_req].view(torch.int32).abs().sum()) == 0   # tickets left at zero
+
+
+def test_compact_batch_rejects_bad_calls():
+    case = W.random_compact_case(65, num_req=2, n_tree_max=16)
+    x = _compact_inputs(case, 1, 2, 64, False, 65)
+    ws = ts.new_workspace(ts.tree_compact_workspace_size(x["args"]))
+    for bad in ([], [x["args"]] * 5):
+        with pytest.raises(ts.TreeSpecError):
+            ts.tree_cache_compact_batch_args(bad, [ws] * len(bad))
+    small = ts.new_workspace(256)
+    with pytest.raises(ts.TreeSpecError):   # the second call's workspace is too small: nothing runs
+        ts.tree_cache_compact_batch_args([x["args"], x["args"]], [ws, small])
+
+
 def test_compact_fig4_on_gpu():
     with open(os.path.join(GOLDEN, "fig4_compaction.json")) as f:
         g = json.load(f)
