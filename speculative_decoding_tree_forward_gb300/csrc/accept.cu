@@ -29,7 +29,9 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
   }
 }
 
-__global__ void __launch_bounds__(kArgmaxThreads) argmax_chunk_kernel(const AcceptParams p) {
+// At most 32 registers: eight CTAs per SM, the residency the host's slice
+// sizing assumes (rows x slices = about eight CTAs per SM, one wave).
+__global__ void __launch_bounds__(kArgmaxThreads, 8) argmax_chunk_kernel(const AcceptParams p) {
   pdl_wait();
   pdl_launch_dependents();
   const int row = blockIdx.x;  // b * n_tree_max + i
@@ -45,11 +47,11 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_chunk_kernel(const Acce
   // vector body when the row start is 16-byte aligned (vocab % 4 == 0)
   if ((p.vocab & 3) == 0) {
     const float4* lg4 = reinterpret_cast<const float4*>(lg);
-    const int64_t a = v0 / 4, e = v1 / 4;
+    const int a = static_cast<int>(v0 / 4), e = static_cast<int>(v1 / 4);  // vocab < 2^31
 #pragma unroll 8
-    for (int64_t x = a + threadIdx.x; x < e; x += kArgmaxThreads) {
+    for (int x = a + static_cast<int>(threadIdx.x); x < e; x += kArgmaxThreads) {
       const float4 f = __ldcs(lg4 + x);
-      const int base = static_cast<int>(x * 4);
+      const int base = x * 4;
       better(bv, bi, f.x, base);
       better(bv, bi, f.y, base + 1);
       better(bv, bi, f.z, base + 2);
