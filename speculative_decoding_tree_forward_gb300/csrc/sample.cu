@@ -44,7 +44,9 @@ __device__ __forceinline__ int tree_size(const SampleParams& p, int b) {
   return min(max(p.n_tree[b], 0), p.n_tree_max);
 }
 
-__global__ void __launch_bounds__(kLseThreads) sample_lse_kernel(const SampleParams p) {
+// At most 32 registers: eight CTAs per SM, the residency the host's slice
+// sizing assumes (target and draft rows x slices = about one wave).
+__global__ void __launch_bounds__(kLseThreads, 8) sample_lse_kernel(const SampleParams p) {
   pdl_wait();
   pdl_launch_dependents();
   const int rows = p.num_req * p.n_tree_max;
@@ -56,10 +58,10 @@ __global__ void __launch_bounds__(kLseThreads) sample_lse_kernel(const SamplePar
   const int64_t v1 = min(static_cast<int64_t>(p.vocab), v0 + p.slice);
   float m = -INFINITY, s = 0.f;
   if ((p.vocab & 3) == 0) {
-    constexpr int kLoads = 8;
+    constexpr int kLoads = 4;  // 16-byte loads in flight per thread (eight CTAs per SM)
     const float4* lg4 = reinterpret_cast<const float4*>(lg);
-    const int64_t e4 = v1 / 4;
-    for (int64_t x0 = v0 / 4 + threadIdx.x; x0 < e4; x0 += kLoads * kLseThreads) {
+    const int e4 = static_cast<int>(v1 / 4);  // vocab < 2^31
+    for (int x0 = static_cast<int>(v0 / 4) + static_cast<int>(threadIdx.x); x0 < e4; x0 += kLoads * kLseThreads) {
       float4 f[kLoads];
 #pragma unroll
       for (int q = 0; q < kLoads; ++q)
