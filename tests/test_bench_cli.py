@@ -36,3 +36,25 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_without_an_oracle_sample_says_so():
     d = _run("--workload", "verify_b8_tree16", "--steps", "1", "--warmup", "0")
     assert d["impl"] == "reference" and "unavailable" in d
+
+
+def test_clock_sampler_parses_and_cleans_up(tmp_path, monkeypatch):
+    """The nvidia-smi sampler of the timed region, against a stand-in
+    nvidia-smi that prints two samples (one with sw_power_cap active)."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '0, 2070 MHz, 2070 MHz, 900.00 W, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '0, 1980 MHz, 2070 MHz, 1400.00 W, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ['PATH']}")
+    sys.path.insert(0, ROOT)
+    import time
+
+    import bench
+    c = bench.Clocks(0)
+    time.sleep(1.0)
+    path = c.path
+    got = c.stop()
+    assert got == {"sm_mhz": 2025.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
+    assert not os.path.exists(path)
