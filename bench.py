@@ -618,6 +618,12 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(args)
     traffic = measured_traffic(info["workload"], path)
+    # mean acceptance length of the last step (the inputs are the same every step)
+    acceptance = None
+    if info["acc_state"] is not None:
+        al = info["acc_state"][4]["accept_len"].float()
+        acceptance = {"mean_accept_len": float(al.mean()),
+                      "emitted_tokens_per_s": float(al.sum()) * world / (ms_max / 1e3)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -644,6 +650,7 @@ def main():
         "gpu_launches": info["launches"] * args.steps,
         "graph": graph,
         "clocks": ck,
+        "acceptance": acceptance,
     }
     print(json.dumps(line))
 
