@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the flushed attention calls of the verify-b8 and paged chain workloads")
+    ap.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--serial-compaction", action="store_true",
                     help="compact the target- and draft-side caches with two calls instead of one batched launch")
     return ap.parse_args()
@@ -193,7 +196,7 @@ def build_step(args, torch, ts, W, device):
     wl = getattr(W, args.workload)
     kw = {"num_layers": args.layers} if args.workload.startswith("longctx") else {}
     w = wl(**kw)
-    from tests.gpu_util import attn_inputs, i32_dev  # noqa: E402
+    attn_inputs, i32_dev = W.attn_inputs, W.i32_dev
     stream = torch.cuda.current_stream()
     calls = []        # (name, fn) run in order each step
     info = {"workload": w.name, "attn_cases": w.attn}
@@ -415,8 +418,69 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
 
 
 # ---------------------------------------------------------------------------
+SIDE_WORKLOADS = ("verify_b8_tree16", "chain_verify_b16_paged")
+
+
+def side_workloads(args, torch, ts, W, device, calls: int):
+    """The attention call of the verify-b8 (64 q / 8 kv heads, 8 requests, 16-node trees, R = 128) and
+    paged chain verify (16 requests, chains of 5, paged K/V) workloads, in the bench's own process: each
+    call after an L2 flush (258 MB write, then 258 MB read), event-timed on the launching stream."""
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=device)
+    peak, peak_kind = peaks()
+    out = {}
+    for name in SIDE_WORKLOADS:
+        case = getattr(W, name)().attn[0]
+        d = W.attn_inputs(case)
+        o = torch.empty_like(d["q"])
+        lse = torch.empty((case.num_req, case.num_q_heads, case.n_query), dtype=torch.float32, device=device)
+        a = ts.attn_args(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"], o, lse,
+                         d.get("block_table"), case.softmax_scale, args.force_path, 0, args.rope_theta)
+        ws = ts.new_workspace(ts.tree_attn_workspace_size(a), device)
+        for _ in range(max(args.warmup, 3)):
+            ts.tree_attn_forward_args(a, ws)
+        torch.cuda.synchronize()
+        assert ts.read_device_error(ws) == 0
+        clocks = Clocks(torch.cuda.current_device())
+        time.sleep(0.2)
+        evs = []
+        for _ in range(calls):
+            flush.zero_()
+            flush_r.max()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ts.tree_attn_forward_args(a, ws)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ck = clocks.stop()
+        ms = [x.elapsed_time(y) for x, y in evs]
+        mean_ms = sum(ms) / len(ms)
+        nbytes = attn_algorithmic_bytes(case)
+        path = ts.tree_attn_selected_path(a)
+        achieved = nbytes / (mean_ms / 1e3) / 1e9
+        out[name] = {"launch_ms": mean_ms, "launch_ms_median": statistics.median(ms), "calls": calls,
+                     "algorithmic_bytes_per_launch": nbytes, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": measured_traffic(name, path), "attention_path": path,
+                     "tree_tokens_per_s": case.num_req * case.n_query / (mean_ms / 1e3),
+                     "l2": "flushed before every call (258 MB write, then 258 MB read), outside the call times",
+                     "clocks": ck}
+        del d, o, lse, ws
+    return out
+
+
+# ---------------------------------------------------------------------------
 class OracleSample:
-    """Inputs of one request of the long-context workload for timing the CPU oracle."""
+    """One request of the long-context workload, processed completely by the CPU oracle.
+
+    The work of one request of a step: fp64 attention of all 32 query heads x
+    32 tree queries against 32800 keys, greedy acceptance of its 32-node tree
+    over 152064 logits, the target-side re-root (32-node tree) and the
+    draft-side re-root (the 64-node tree grown from it), and the out-of-place
+    row compaction of K and V over every layer for both sides.  The inputs are
+    drawn with the workload's shapes and recipe (seeded)."""
 
     def __init__(self, layers: int):
         import numpy as np
@@ -432,44 +496,64 @@ class OracleSample:
         self.k = OA.bf16_bits_to_f64(case.k[0, :keys])
         self.v = OA.bf16_bits_to_f64(case.v[0, :keys])
         self.acc = W.random_accept_case(0, num_req=1, n_tree_max=32, vocab=152064, p_accept=0.8, ragged_tree=False)
-        self.rows = np.zeros((keys + 32, 8, 128), np.uint16)
+        rs = np.random.default_rng(1)
+        self.dparent = W.grow_parents(rs, self.acc.parent[0], 32)
+        grown = W.draft_tokens(rs, self.dparent, self.acc.planted[0], 152064, 0.8, peak_rows=32)
+        self.dtokens = np.concatenate([self.acc.tokens[0], grown[32:]]).astype(np.int32)
+        self.rows_t = np.zeros((keys, 8, 128), np.uint16)
+        self.rows_d = np.zeros((32768 + 64, 8, 128), np.uint16)
 
-    def run(self, heads, one_query: bool = False):
-        """Times the oracle on `heads` q heads of attention (all 32 queries, or only the last
-        node's query), one acceptance, one re-root and one row compaction.
-
-        Returns the time of the full step (4 requests x 32 heads x 32 queries, 4
-        acceptances, 2 sides x 4 requests re-roots, 2 sides x 4 requests x layers
-        x {K, V} compactions) extrapolated linearly from the sample, and the
-        sample's wall time."""
+    def run(self) -> float:
+        """Wall time (s) of the oracle on the sample."""
         from oracle import attention as OA
         from oracle import tree as OT
-        nq = 1 if one_query else 32
-        q = self.q[32 - nq:]
         t0 = time.perf_counter()
-        OA.tree_attention(q, self.k, self.v, 32768, 32, self.case.parent[0], nq, self.case.scale, heads)
-        t1 = time.perf_counter()
+        OA.tree_attention(self.q, self.k, self.v, 32768, 32, self.case.parent[0], 32, self.case.scale)
         r = OT.greedy_accept(self.acc.logits[0], self.acc.tokens[0], self.acc.parent[0], 32)
-        t2 = time.perf_counter()
-        rr = OT.reroot(self.acc.parent[0], self.acc.tokens[0], 32, 32768, r.verified)
-        t3 = time.perf_counter()
-        OT.compact_rows(self.rows, 32768, rr.src)
-        t4 = time.perf_counter()
-        attn_scale = (4 * 32 / len(heads)) * (32 / nq)
-        full = attn_scale * (t1 - t0) + 4 * (t2 - t1) + 8 * (t3 - t2) + 8 * self.layers * 2 * (t4 - t3)
-        return full, t4 - t0
+        rt = OT.reroot(self.acc.parent[0], self.acc.tokens[0], 32, 32768, r.verified)
+        rd = OT.reroot(self.dparent, self.dtokens, 64, 32768, r.verified)
+        for _ in range(self.layers):
+            for _kv in range(2):
+                OT.compact_rows(self.rows_t, 32768, rt.src)
+                OT.compact_rows(self.rows_d, 32768, rd.src)
+        return time.perf_counter() - t0
+
+
+SAMPLE_TEXT = ("one request of the workload processed completely (32 tree tokens): fp64 attention of 32 q heads x 32 "
+               "queries x 32800 keys, greedy acceptance over 152064 logits, target- and draft-side re-roots, and the "
+               "out-of-place compaction of K and V over %d layers for both sides; tree tokens/s = 32 / sample time")
+
+
+def oracle_sample_child(threads: int, repeats: int, layers: int):
+    """Runs in a fresh process whose BLAS thread count was fixed by the environment: prints the sample times."""
+    s = OracleSample(layers)
+    times = [s.run() for _ in range(repeats)]
+    print(json.dumps({"times": times, "threads": threads}))
+
+
+def oracle_sample_times(threads: int, repeats: int, layers: int):
+    """Times the oracle sample `repeats` times in a child process with `threads` BLAS threads."""
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", str(threads), "--layers",
+                        str(layers), "--steps", str(repeats)], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])["times"]
 
 
 def cpu_oracle_sample(args):
+    """The oracle on the sample, single-threaded and on all host cores, median of 3 wall-clock runs each."""
     if not args.workload.startswith("longctx"):
         return None
-    s = OracleSample(args.layers)
-    full, _ = s.run(list(range(4)))
-    return {"value": 128.0 / full, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": ("request 0 of the workload: fp64 attention of one KV-head group (4 q heads x 32 queries x "
-                       "32800 keys), greedy acceptance of its 32-node tree over 152064 logits, one re-root and one "
-                       "row compaction of one layer; extrapolated to the full step (4 requests x 32 heads, "
-                       "4 acceptances, 8 re-roots, 2 x 4 x %d layers x {K,V} compactions)" % args.layers)}
+    cores = os.cpu_count() or 1
+    one = statistics.median(oracle_sample_times(1, 3, args.layers))
+    allc = statistics.median(oracle_sample_times(cores, 3, args.layers))
+    return {"value": 32.0 / allc, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": SAMPLE_TEXT % args.layers + "; median of 3 runs, all cores (BLAS threads = cores)",
+            "single_thread": {"value": 32.0 / one, "median_s": one, "cores": 1},
+            "all_cores": {"value": 32.0 / allc, "median_s": allc, "cores": cores}}
 
 
 def reference_arm(args):
@@ -481,22 +565,19 @@ def reference_arm(args):
                           "long-context workload only"}))
         return
     s = OracleSample(args.layers)
-    fulls = []
-    for i in range(args.warmup + args.steps):
-        full, _ = s.run([i % 32])   # one q head per step, all 32 queries; heads cycle
-        if i >= args.warmup:
-            fulls.append(full)
-    t = statistics.mean(fulls)
-    v = 128.0 / t
-    sample = ("per step: fp64 oracle attention of one q head of request 0 (32 queries x 32800 keys), greedy "
-              "acceptance of its 32-node tree over 152064 logits, one re-root and one row compaction of one "
-              "layer; extrapolated to the full step (4 requests x 32 heads x 32 queries, 4 acceptances, 8 re-roots, "
-              "2 x 4 x %d layers x {K,V} compactions)" % args.layers)
+    for _ in range(args.warmup):
+        s.run()
+    times = [s.run() for _ in range(args.steps)]
+    total = sum(times)
+    v = 32.0 * args.steps / total
+    cores = os.cpu_count() or 1
+    sample = ("per step: " + SAMPLE_TEXT % args.layers + "; BLAS on the default thread count of the host (%d cores)"
+              % cores)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "tree_tokens_per_step": 32},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -504,6 +585,9 @@ def reference_arm(args):
 # ---------------------------------------------------------------------------
 def main():
     args = parse()
+    if args.oracle_child:
+        oracle_sample_child(args.oracle_child, args.steps, args.layers)
+        return
     if args.impl == "reference":
         reference_arm(args)
         return
@@ -605,6 +689,10 @@ def main():
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
     path = ts.tree_attn_selected_path(info["attn_inputs"][0][0])
 
+    side = None
+    if not args.no_workloads and args.workload.startswith("longctx"):
+        side = side_workloads(args, torch, ts, W, device, max(20, min(args.steps * 5, 200)))
+
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(10, min(args.steps, 200))
@@ -651,6 +739,7 @@ def main():
         "graph": graph,
         "clocks": ck,
         "acceptance": acceptance,
+        "workloads": side,
     }
     print(json.dumps(line))
 

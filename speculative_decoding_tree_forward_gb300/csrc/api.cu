@@ -225,21 +225,6 @@ bool encode_q_map(CUtensorMap* map, const ts_attn_args* a, const void* q, int gr
   return r == CUDA_SUCCESS;
 }
 
-// fp32 split-KV partial O as a 2-D tensor (head_dim 128, slots * 128 rows);
-// the tcgen05 kernel stores one box of 32 columns x 32 rows per warp.
-bool encode_partial_map(CUtensorMap* map, float* part_o, int64_t rows) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {128 * sizeof(float)};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 // Leading workspace bytes that must be zero when a call starts (the error
@@ -368,15 +353,14 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
     p.q = static_cast<const __nv_bfloat16*>(qr);
   }
   if (pl.use_tc) {
-    CUtensorMap qmap, pmap;
+    CUtensorMap qmap;
     if (!encode_q_map(&qmap, a, p.q, pl.group)) return TS_ERR_CUDA;
-    if (!encode_partial_map(&pmap, p.part_o, pl.slots * pl.rows_pad)) return TS_ERR_CUDA;
-    e = launch_attn_tc(p, kmap, vmap, pmap, qmap, s);
+    e = launch_attn_tc(p, kmap, vmap, qmap, s);
   } else {
     e = launch_attn_mma(p, kmap, vmap, s);
   }
   if (e != cudaSuccess) return TS_ERR_CUDA;
-  e = launch_attn_merge(p, s);
+  e = launch_attn_merge(p, pl.use_tc, s);
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 

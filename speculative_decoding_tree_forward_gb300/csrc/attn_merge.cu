@@ -15,11 +15,14 @@
 // known, so a row with up to that many shares costs one round trip to L2;
 // shares of CTAs that hold no tile of the unit get weight 0.
 //
-// Two shapes, picked by the host: one warp per row with eight shares
+// The warp-MMA kernel's partials are row-major ([slot][row][head_dim]); two
+// shapes, picked by the host, merge them: one warp per row with eight shares
 // prefetched (when that grid fits one resident wave of CTAs: many shares per
 // row, few rows), or one half-warp per row with four prefetched (twice the
 // rows in flight for the same registers, so a grid of many rows lands in
-// one wave instead of two).
+// one wave instead of two).  The tcgen05 kernel's partials are column-blocked
+// (float4 j of row r at (slot * 32 + j) * 128 + r) and merged with one thread
+// per (row, 16 columns).
 #include "attn_common.cuh"
 
 namespace ts {
@@ -304,9 +307,105 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) merge_row_per_half_warp_k
     p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (mbase + log2f(wsum)) * 0.69314718055994530942f;
 }
 
+
+// tcgen05 layout: float4 j of row r of slot s at (s * 32 + j) * 128 + r, so
+// a warp's 32 consecutive rows read 512 contiguous bytes.  Grid (units, 4),
+// 256 threads: thread t merges row t % 128 of the unit over 16 columns
+// (column block 2 * blockIdx.y + t / 128).  The lse and the partial columns
+// of a row's first kPrefetchTc shares are all requested before the weights
+// are known, so a row with that many shares costs one round trip to L2.
+constexpr int kPrefetchTc = 4;
+
+__global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int64_t unit = blockIdx.x;
+  const int units_per_req = p.hkv / p.hp;  // one row group per unit on this path
+  const int b = static_cast<int>(blockIdx.x) / units_per_req;
+  const int uir = static_cast<int>(blockIdx.x) % units_per_req;
+  const int r = t & (kMaxRowsPerUnit - 1);
+  const int cb = 2 * static_cast<int>(blockIdx.y) + (t >> 7);  // 16 columns: float4 4 cb .. 4 cb + 3
+  const int hj = p.hp == 2 ? r >> 6 : 0, loc = p.hp == 2 ? r & 63 : r;
+  __shared__ UnitSplit s_sp;
+  __shared__ unsigned s_hold;
+  if (warp == 0) merge_split(p, b, uir, units_per_req, lane, &s_sp, &s_hold);
+  __syncthreads();
+  const int c_lo = s_sp.c_lo, c_hi = s_sp.c_hi;
+  const unsigned hold = s_hold;
+  pdl_wait();
+  pdl_launch_dependents();
+  // padding row, or one CTA held the whole unit and wrote it
+  if (loc >= p.rows || c_lo == c_hi) return;
+  auto held = [&](int c) -> bool { return c - c_lo < 32 ? ((hold >> (c - c_lo)) & 1u) != 0 : s_sp.holds(c); };
+  const float* lse_col = p.part_lse + unit * kMaxRowsPerUnit + r;
+  const float4* o_col = reinterpret_cast<const float4*>(p.part_o) + unit * (32 * kMaxRowsPerUnit) +
+                        (4 * cb) * kMaxRowsPerUnit + r;
+  auto lse_of = [&](int c) { return __ldcg(lse_col + static_cast<int64_t>(c) * kMaxRowsPerUnit); };
+  auto o_of = [&](int c, int j) { return __ldcg(o_col + (static_cast<int64_t>(c) * 32 + j) * kMaxRowsPerUnit); };
+
+  float lx[kPrefetchTc];
+  float4 x[kPrefetchTc][4];
+#pragma unroll
+  for (int q = 0; q < kPrefetchTc; ++q) {
+    lx[q] = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c_lo + q <= c_hi && ((hold >> q) & 1u)) {
+      lx[q] = lse_of(c_lo + q);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[q][j] = o_of(c_lo + q, j);
+    }
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kPrefetchTc; ++q) mx = fmaxf(mx, lx[q]);
+  for (int c = c_lo + kPrefetchTc; c <= c_hi; ++c)
+    if (held(c)) mx = fmaxf(mx, lse_of(c));
+  const float mb = (mx == -INFINITY) ? 0.f : mx;
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ws = 0.f;
+#pragma unroll
+  for (int q = 0; q < kPrefetchTc; ++q) {
+    const float w = exp2f(lx[q] - mb);  // 0 for shares that are not held (lse -inf)
+    ws += w;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j].x += w * x[q][j].x;
+      acc[j].y += w * x[q][j].y;
+      acc[j].z += w * x[q][j].z;
+      acc[j].w += w * x[q][j].w;
+    }
+  }
+  for (int c = c_lo + kPrefetchTc; c <= c_hi; ++c) {  // more shares: one round trip each
+    if (!held(c)) continue;
+    const float w = exp2f(lse_of(c) - mb);
+    ws += w;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 y = o_of(c, j);
+      acc[j].x += w * y.x;
+      acc[j].y += w * y.y;
+      acc[j].z += w * y.z;
+      acc[j].w += w * y.w;
+    }
+  }
+  const float inv = ws > 0.f ? __frcp_rn(ws) : 0.f;
+  const int i = loc / p.group, h = (p.hp * uir + hj) * p.group + loc % p.group;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * 128 + 16 * cb);
+  dst[0] = make_uint4(pack_bf16x2(acc[0].x * inv, acc[0].y * inv), pack_bf16x2(acc[0].z * inv, acc[0].w * inv),
+                      pack_bf16x2(acc[1].x * inv, acc[1].y * inv), pack_bf16x2(acc[1].z * inv, acc[1].w * inv));
+  dst[1] = make_uint4(pack_bf16x2(acc[2].x * inv, acc[2].y * inv), pack_bf16x2(acc[2].z * inv, acc[2].w * inv),
+                      pack_bf16x2(acc[3].x * inv, acc[3].y * inv), pack_bf16x2(acc[3].z * inv, acc[3].w * inv));
+  if (p.lse != nullptr && cb == 0)
+    p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (mb + log2f(ws)) * 0.69314718055994530942f;
+}
+
 }  // namespace
 
-cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_attn_merge(const AttnParams& p, bool tc_layout, cudaStream_t stream) {
+  if (tc_layout)
+    return launch_pdl(merge_tc_kernel, dim3(static_cast<unsigned>(p.num_units), 4), dim3(256), 0, stream, p);
   if (p.merge_half_warp) {
     const int row_blocks = (p.rows_pad + kRowsPerCtaHalf - 1) / kRowsPerCtaHalf;
     return launch_pdl(merge_row_per_half_warp_kernel, dim3(static_cast<unsigned>(p.num_units), row_blocks),

@@ -119,7 +119,7 @@ struct TcCtrl {
   uint64_t q_full[kMaxQBufs], q_empty[kMaxQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
   uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
-  uint64_t stg_free;  // one phase per segment epilogue: the staging rows are reused in segment order
+  uint64_t stg_free;  // one phase per complete mid-range segment: its finisher's staging tiles are free again
   uint32_t tmem_base;
   int abort;
 };
@@ -351,7 +351,6 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued
 template <int HP>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
-                                                                const __grid_constant__ CUtensorMap pmap,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -630,7 +629,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     Cursor c;
     c.start(p, b0, local0);
     int nonfin[2] = {0, 0};  // segments in which each warpgroup handed its state to the other
-    int seg_idx = 0;         // CTA-local index of the segment tile k belongs to
+    int stg_idx = 0;         // earlier segments whose epilogue used the shared staging tiles
     int anc_req = -1;
     uint32_t anc[4] = {0, 0, 0, 0};
     float m_used = -INFINITY, l = 0.f;
@@ -835,44 +834,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             const int i = loc / p.group, h = (HP * c.uir + Sh::head_of(r)) * p.group + loc % p.group;
             const int64_t unit = static_cast<int64_t>(c.b) * units_per_req + c.uir;
             const int64_t slot = static_cast<int64_t>(blockIdx.x) + unit;
-            // Each 32-column chunk of this warp's 32 rows goes through shared
-            // memory (128-byte rows, 16-byte chunk c of row r at c ^ (r % 8)):
-            // fp32 partials leave as one TMA store per chunk, so the warp waits
-            // only until the tile has been read; bf16 outputs leave as whole
-            // 64-byte row segments.
-            // The CTA's last segment stages in the V ring, idle by now (every
-            // tile has been loaded and its PV is done): 16 KB per warp, one
-            // 4 KB tile per chunk, so the chunks' stores need not wait for
-            // one another.  Other segments share 4 KB per warp.
             const bool last_seg = sl == n_tiles - 1;
-            const uint32_t stg_step = last_seg ? TcLayout::kStgWarpBytes : 0u;  // between chunks
-            const uint32_t stg = last_seg ? L.v + (warp & 3) * 4 * TcLayout::kStgWarpBytes
-                                          : L.stg + (warp & 3) * TcLayout::kStgWarpBytes;
-            const int row0 = (warp & 3) * 32;
-            // finishers of consecutive short segments may be different
-            // warpgroups with no O in common: take the staging rows in turn
-            if (!last_seg && seg_idx > 0 && !mbar_wait(&ctl->stg_free, (seg_idx - 1) & 1)) {
-              report_error(p.err, TS_DEVERR_TIMEOUT);
-              *abort_flag = 1;
-              break;
-            }
-            // chunk ch + 1 is read from TMEM while chunk ch is staged and stored
             uint32_t v[32], u[32];
             tmem_ld32(lane_addr + col_o(wg), v);
             if (other_in) tmem_ld32(lane_addr + col_o(oth), u);
             tmem_ld_wait();
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-              uint8_t* const cs = smem + stg + ch * stg_step;
-              float o[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                o[e] = __uint_as_float(v[e]) * f_own + (other_in ? __uint_as_float(u[e]) * f_oth : 0.f);
-              if (ch < 3) {
-                tmem_ld32(lane_addr + col_o(wg) + (ch + 1) * 32, v);
-                if (other_in) tmem_ld32(lane_addr + col_o(oth) + (ch + 1) * 32, u);
+            if (complete) {
+              // bf16 output: each 32-column chunk of this warp's 32 rows goes
+              // through shared memory (128-byte rows, 16-byte chunk c of row r
+              // at c ^ (r % 8)) and leaves as whole 64-byte row segments.  The
+              // CTA's last segment stages in the V ring, idle by now (every
+              // tile has been loaded and its PV is done); other segments share
+              // one 4 KB tile per warp, taken in turn by the finishers of
+              // consecutive complete segments, which may be different
+              // warpgroups.
+              const uint32_t stg_step = last_seg ? TcLayout::kStgWarpBytes : 0u;  // between chunks
+              const uint32_t stg = last_seg ? L.v + (warp & 3) * 4 * TcLayout::kStgWarpBytes
+                                            : L.stg + (warp & 3) * TcLayout::kStgWarpBytes;
+              const int row0 = (warp & 3) * 32;
+              if (!last_seg && stg_idx > 0 && !mbar_wait(&ctl->stg_free, (stg_idx - 1) & 1)) {
+                report_error(p.err, TS_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
               }
-              if (complete) {
+              // chunk ch + 1 is read from TMEM while chunk ch is staged and stored
+#pragma unroll 1
+              for (int ch = 0; ch < 4; ++ch) {
+                uint8_t* const cs = smem + stg + ch * stg_step;
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  o[e] = __uint_as_float(v[e]) * f_own + (other_in ? __uint_as_float(u[e]) * f_oth : 0.f);
+                if (ch < 3) {
+                  tmem_ld32(lane_addr + col_o(wg) + (ch + 1) * 32, v);
+                  if (other_in) tmem_ld32(lane_addr + col_o(oth) + (ch + 1) * 32, u);
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                   *reinterpret_cast<uint4*>(cs + sw128(lane, q)) =
@@ -890,23 +886,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                                            ch * 32)[c4] = val;
                 }
                 __syncwarp();  // the next chunk rewrites the staging rows
-              } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  *reinterpret_cast<float4*>(cs + sw128(lane, q)) =
-                      make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                  tma_store_2d(&pmap, cs, ch * 32, static_cast<int>(slot * 128 + row0));
-                  bulk_commit();
-                  if (stg_step == 0u) bulk_wait_read_all();  // the staging rows may be rewritten
-                }
-                __syncwarp();
+                if (ch < 3) tmem_ld_wait();
               }
-              if (ch < 3) tmem_ld_wait();
+              if (!last_seg && lane == 0) mbar_arrive(&ctl->stg_free);
+            } else {
+              // fp32 partial, written straight from registers: float4 j of
+              // row r at ((slot * 32 + j) * 128 + r), so a warp's 32 rows
+              // store 512 contiguous bytes per instruction.  No staging and
+              // no wait for the stores: both O accumulators are free as soon
+              // as the last chunk has been read from TMEM.
+              float4* prow = reinterpret_cast<float4*>(p.part_o) + slot * (kRowsTc * 32) + r;
+              const bool write_row = loc < p.rows;
+#pragma unroll 1
+              for (int ch = 0; ch < 4; ++ch) {
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  o[e] = __uint_as_float(v[e]) * f_own + (other_in ? __uint_as_float(u[e]) * f_oth : 0.f);
+                if (ch < 3) {
+                  tmem_ld32(lane_addr + col_o(wg) + (ch + 1) * 32, v);
+                  if (other_in) tmem_ld32(lane_addr + col_o(oth) + (ch + 1) * 32, u);
+                }
+                if (write_row) {
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+                    __stcg(prow + (ch * 8 + q) * kRowsTc, make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+                }
+                if (ch < 3) tmem_ld_wait();
+              }
             }
-            if (lane == 0) mbar_arrive(&ctl->stg_free);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -926,7 +934,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
       }
       if (k == sl && sl > sf) ++nonfin[(sl & 1) ^ 1];  // the non-finishing warpgroup handed over
-      if (k == sl) ++seg_idx;
+      if (k == sl && sl != n_tiles - 1 && c.seg_complete(k, n_tiles)) ++stg_idx;
       c.advance(p, units_per_req);
     }
   }
@@ -965,12 +973,12 @@ int attn_tc_occupancy(int stages, int num_req) {
 
 // The dynamic shared-memory attribute was raised by attn_tc_occupancy, which
 // the host plan runs (once per device) before any launch.
-cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& pmap,
-                           const CUtensorMap& qmap, cudaStream_t stream) {
+cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                           cudaStream_t stream) {
   const size_t smem = attn_tc_smem_bytes(p.stages, p.num_req);
   if (p.hp == 2)
-    return launch_pdl(attn_tc_kernel<2>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, pmap, qmap, p);
-  return launch_pdl(attn_tc_kernel<1>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, pmap, qmap, p);
+    return launch_pdl(attn_tc_kernel<2>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, qmap, p);
+  return launch_pdl(attn_tc_kernel<1>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, qmap, p);
 }
 
 }  // namespace ts

@@ -60,17 +60,18 @@ struct AttnParams {
   float* lse;
   float scale_log2;  // softmax scale * log2(e)
   unsigned* err;     // workspace error word
-  float* part_o;     // [slots][rows_pad][head_dim]
+  float* part_o;     // warp-MMA path: [slots][rows_pad][head_dim]; tcgen05 path: [slots][32][128] float4
+                     // (float4 j of row r at (slot * 32 + j) * 128 + r)
   float* part_lse;   // [slots][rows_pad] (log2 domain)
 };
 
 // Launchers (one per kernel family); return cudaGetLastError().
 cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream);
-cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& pmap,
-                           const CUtensorMap& qmap, cudaStream_t stream);
+cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                           cudaStream_t stream);
 size_t attn_zero_prefix_bytes(const ts_attn_args* a);
-cudaError_t launch_attn_merge(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attn_merge(const AttnParams& p, bool tc_layout, cudaStream_t stream);
 // RoPE inverse frequencies theta^(-2j/d), j < d/2, computed on the host in fp64.
 struct RopeFreqs {
   double inv_freq[64];

@@ -2,6 +2,8 @@
 import numpy as np
 import torch
 
+from workloads import attn_inputs, bf16_dev, i32_dev  # noqa: F401  (device copies of the seeded inputs)
+
 # Attention tolerance (bf16 inputs, fp32 accumulation, bf16 output):
 # |gpu - oracle| <= ATOL + RTOL * |oracle| elementwise.
 ATOL, RTOL = 2e-3, 1e-2
@@ -10,27 +12,9 @@ ATOL, RTOL = 2e-3, 1e-2
 LSE_ATOL, LSE_RTOL = 1e-4, 1e-4
 
 
-def bf16_dev(a: np.ndarray) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-
-
-def i32_dev(a) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).cuda()
-
-
 def bf16_host_f64(t: torch.Tensor) -> np.ndarray:
     bits = t.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32) << 16
     return bits.view(np.float32).astype(np.float64)
-
-
-def attn_inputs(case):
-    d = {
-        "q": bf16_dev(case.q), "k_cache": bf16_dev(case.k), "v_cache": bf16_dev(case.v),
-        "prefix_len": i32_dev(case.prefix_len), "n_tree": i32_dev(case.n_tree), "parent": i32_dev(case.parent),
-    }
-    if case.paged:
-        d["block_table"] = i32_dev(case.block_table)
-    return d
 
 
 def check_attention(case, out, lse, ref, requests=None, heads=None):

@@ -29,8 +29,16 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    # the value is the workload's 128 tree tokens per step over the extrapolated step time
-    assert abs(d["value"] * d["ms_per_step"] / 1e3 - 128.0) < 1e-6 * 128.0
+    # each step is one request of the workload processed completely: 32 tree tokens per step
+    assert d["config"]["tree_tokens_per_step"] == 32
+    assert abs(d["value"] * d["ms_per_step"] / 1e3 - 32.0) < 1e-6 * 32.0
+
+
+def test_oracle_sample_runs_in_a_child_with_the_stated_threads():
+    sys.path.insert(0, ROOT)
+    import bench
+    times = bench.oracle_sample_times(1, 2, 1)
+    assert len(times) == 2 and all(t > 0 for t in times)
 
 
 def test_reference_arm_without_an_oracle_sample_says_so():

@@ -498,3 +498,30 @@ def random_compact_case(seed: int, num_req=3, n_tree_max=24, vocab=50, p_follow=
         verified[b, :len(seq)] = seq
         m[b] = len(seq)
     return CompactCase(num_req, n_tree_max, prefix, n_tree, parent, tokens, verified, m)
+
+
+# --------------------------------------------------------------------------
+# device copies (torch is imported only when one of these is called)
+# --------------------------------------------------------------------------
+def bf16_dev(a: np.ndarray):
+    """bfloat16 bit patterns (uint16) -> a bfloat16 tensor on the current CUDA device."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def i32_dev(a):
+    """Integers -> an int32 tensor on the current CUDA device."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).cuda()
+
+
+def attn_inputs(case: AttnCase) -> dict:
+    """The device tensors of one attention case: q, k_cache, v_cache, prefix_len, n_tree, parent
+    (and block_table for paged K/V)."""
+    d = {
+        "q": bf16_dev(case.q), "k_cache": bf16_dev(case.k), "v_cache": bf16_dev(case.v),
+        "prefix_len": i32_dev(case.prefix_len), "n_tree": i32_dev(case.n_tree), "parent": i32_dev(case.parent),
+    }
+    if case.paged:
+        d["block_table"] = i32_dev(case.block_table)
+    return d
