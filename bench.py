@@ -253,6 +253,11 @@ def build_step(args, torch, ts, W, device):
     if w.accept is not None:
         A = w.accept
         logits = torch.from_numpy(A.logits).to(device)
+        # When the step's inputs are not flushed from L2 between steps (K/V
+        # larger than L2), the acceptance reads one of several copies of the
+        # logits in turn, so that every step streams them from DRAM.
+        n_rep = 1 if attn_bytes < 2 * L2_BYTES else min(8, -(-3 * L2_BYTES // A.logits.nbytes))
+        reps = [logits] + [logits.clone() for _ in range(n_rep - 1)]
         tok = i32_dev(A.tokens)
         res = {k: torch.empty(s, dtype=torch.int32, device=device) for k, s in [
             ("argmax", (A.num_req, A.n_tree_max)), ("path", (A.num_req, A.n_tree_max)),
@@ -268,14 +273,19 @@ def build_step(args, torch, ts, W, device):
             dlog = logits + 0.5 * torch.randn(logits.shape, generator=g, device=device)
             u_acc = torch.rand(tok.shape, generator=g, device=device)
             u_bon = torch.rand(tok.shape, generator=g, device=device)
-            aa = ts.sample_args(logits, dlog, tok, par, ntree, u_acc, u_bon, args.temperature, res)
-            aws = ts.new_workspace(ts.tree_accept_sample_workspace_size(aa), device)
-            acc_state = (aa, aws, logits, tok, res, "sample", [dlog, u_acc, u_bon])
+            dreps = [dlog] + [dlog.clone() for _ in range(n_rep - 1)]
+            aas = [ts.sample_args(x, y, tok, par, ntree, u_acc, u_bon, args.temperature, res)
+                   for x, y in zip(reps, dreps)]
+            aws = ts.new_workspace(ts.tree_accept_sample_workspace_size(aas[0]), device)
+            acc_state = (aas, aws, logits, tok, res, "sample", [dlog, u_acc, u_bon])
+            info["logits_keep"] = reps + dreps   # the copies the argument structs point at stay alive
             info["accept_bytes"] = 2 * A.logits.nbytes
         else:
-            aa = ts.accept_args(logits, tok, par, ntree, **res)
-            aws = ts.new_workspace(ts.tree_accept_workspace_size(aa), device)
-            acc_state = (aa, aws, logits, tok, res, "greedy", [])
+            aas = [ts.accept_args(x, tok, par, ntree, **res) for x in reps]
+            aws = ts.new_workspace(ts.tree_accept_workspace_size(aas[0]), device)
+            acc_state = (aas, aws, logits, tok, res, "greedy", [])
+            info["logits_keep"] = reps   # the copies the argument structs point at stay alive
+        info["logits_copies"] = n_rep
         launches += 2
         info.setdefault("accept_bytes", A.logits.nbytes)
 
@@ -327,7 +337,14 @@ def build_step(args, torch, ts, W, device):
         phases.append(("attn", [lambda a=a, ws=ws: ts.tree_attn_forward_args(a, ws) for a, ws, *_ in attn_calls]))
     if acc_state is not None:
         accept_call = ts.tree_accept_sample_args if acc_state[5] == "sample" else ts.tree_accept_greedy_args
-        phases.append(("accept", [lambda: accept_call(acc_state[0], acc_state[1])]))
+        turn = [0]
+
+        def accept_next():   # the next copy of the logits, in turn
+            a = acc_state[0][turn[0] % len(acc_state[0])]
+            turn[0] += 1
+            accept_call(a, acc_state[1])
+        phases.append(("accept", [accept_next]))
+        info["accept_first"] = lambda: accept_call(acc_state[0][0], acc_state[1])
     if len(comp_states) == 2 and not args.serial_compaction:
         # the target- and draft-side caches and their metadata are disjoint:
         # both compactions run as one launch (tree_cache_compact_batch)
@@ -394,6 +411,7 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
         for kind, calls in info["phases"]:
             if kind == "accept":
                 main.wait_event(copied)
+                calls = [info["accept_first"]]   # the copy the host writes into
             for f in calls:
                 f()
             if kind == "accept":
@@ -662,15 +680,18 @@ def main():
     # latency off the host; the kernels and their dependencies are the same)
     graph = None
     if not args.no_graph:
+        per_graph = info.get("logits_copies", 1)   # one captured step per copy of the logits
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            step()
+            for _ in range(per_graph):
+                step()
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        replays = max(1, -(-args.steps // per_graph))
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
         barrier(world)
-        for i in range(args.steps):
+        for i in range(replays):
             if flush is not None:
                 flush.zero_()
                 flush_r.max()
@@ -678,7 +699,7 @@ def main():
             g.replay()
             gev[i][1].record(stream)
         torch.cuda.synchronize()
-        g_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in gev) / args.steps, world)
+        g_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in gev) / (replays * per_graph), world)
         graph = {"ms_per_step": g_ms, "value": replica_value(info["tokens_per_step"], world, g_ms), "unit": UNIT}
         del g
 
@@ -724,7 +745,9 @@ def main():
                                   and not args.serial_compaction else "one launch per cache"),
                    "rope_theta": args.rope_theta,
                    "acceptance": "stochastic, T = %g" % args.temperature if args.temperature > 0 else "greedy", "draft_expansions": len(info["draft"]["exp_args"]) if info["draft"] else 0, "attention_path": path,
-                   "l2": ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2" % (attn_bytes / 1e6)
+                   "logits_copies": info.get("logits_copies", 1),
+                   "l2": ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2; the acceptance "
+                          "reads %d copies of the logits in turn" % (attn_bytes / 1e6, info.get("logits_copies", 1))
                           if flush is None else
                           "L2 flushed (258 MB write, then 258 MB read) before every timed step, outside the step times: "
                           "%.0f MB of K/V per step" % (attn_bytes / 1e6)),

@@ -132,15 +132,19 @@ typedef struct ts_attn_args {
   void* out;                  /* device bf16 [num_requests][n_query][Hq][head_dim] (out, 16-byte aligned) */
   float* lse;                 /* device fp32 [num_requests][Hq][n_query] (out) or NULL */
   float softmax_scale;        /* <= 0 selects 1 / sqrt(head_dim) */
-  int force_path;             /* 0 automatic; 1 warp-mma kernel; 2 tcgen05 kernel (G*n_query == 128 only) */
+  int force_path;             /* 0 automatic; 1 warp-mma kernel; 2 tcgen05 kernel (G*n_query <= 128, d 128) */
   int num_ctas;               /* 0 automatic; else the number of split-KV CTAs (testing) */
   float rope_theta;           /* 0: no rotation; > 0: RoPE base of the queries at tree positions */
+  unsigned wait_limit_ns;     /* testing: bound of each pipeline wait inside the attention kernels, in ns
+                                 (0 = the default, 2 s).  A wait that runs out sets TS_DEVERR_TIMEOUT; the
+                                 kernel then waits for its own copies in flight (with the default bound),
+                                 frees its tensor memory and returns, and the call's outputs are void. */
 } ts_attn_args;
 
 TS_API size_t tree_attn_workspace_size(const ts_attn_args* args);
 /* The kernel tree_attn_forward runs for these arguments: 1 = warp-level MMA,
- * 2 = tcgen05/TMEM (G * n_query == 128, head_dim 128); -(ts_status) when the
- * arguments are rejected. */
+ * 2 = tcgen05/TMEM (R = G * n_query <= 128 and head_dim 128; rows padded to the
+ * 128-row tile); -(ts_status) when the arguments are rejected. */
 TS_API int tree_attn_selected_path(const ts_attn_args* args);
 TS_API ts_status tree_attn_forward(const ts_attn_args* args, void* workspace, size_t workspace_bytes,
                             void* stream);
@@ -153,7 +157,10 @@ TS_API ts_status tree_attn_forward(const ts_attn_args* args, void* workspace, si
  * split-KV scratch is a 16 MiB array in device memory that the library
  * reserves on every GPU that loads it, until the process exits.  The first
  * call on each device (with that device current) looks up the array's device
- * address; make that first call before any stream capture.  Same arguments,
+ * address; make that first call before any stream capture.  The address is kept
+ * for the life of the process: it does not survive cudaDeviceReset (after a
+ * reset the array may sit elsewhere), so do not call this variant after
+ * resetting a device.  Same arguments,
  * results and tolerance as tree_attn_forward; when the partials of the
  * requested split would not fit, fewer split-KV CTAs are used; arguments whose
  * partials exceed 16 MiB even unsplit return TS_ERR_UNSUPPORTED.  No

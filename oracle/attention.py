@@ -113,10 +113,13 @@ def default_scale(head_dim: int, softmax_scale: float = 0.0) -> float:
     return softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(head_dim)
 
 
-def attention_case(case, requests=None, heads=None):
+def attention_case(case, requests=None, heads=None, round_rotated_q=True):
     """Oracle outputs for an ``AttnCase``-shaped object (tests only).
 
     Returns {b: (out [nq][Hq][d], lse [Hq][nq])} for the chosen requests.
+    With RoPE, the rotated queries enter the attention as bf16 (the
+    attention's operand precision); ``round_rotated_q=False`` keeps the fp64
+    rotation instead, to show how much that reading changes the result.
     """
     res = {}
     scale = default_scale(case.head_dim, case.softmax_scale)
@@ -131,6 +134,8 @@ def attention_case(case, requests=None, heads=None):
         theta = getattr(case, "rope_theta", 0.0)
         if theta > 0:   # queries at their tree positions, as bf16 operands; K rows are stored rotated
             pos = tree_positions(case.parent[b], n, P)[n - case.n_query:]
-            qb = round_bf16(rope(qb, pos, theta))
+            qb = rope(qb, pos, theta)
+            if round_rotated_q:
+                qb = round_bf16(qb)
         res[b] = tree_attention(qb, kb, vb, P, n, case.parent[b][:n], case.n_query, scale, heads)
     return res

@@ -41,7 +41,7 @@ class AttnArgs(ctypes.Structure):
                 ("prefix_len", _vp), ("n_tree", _vp), ("parent", _vp), ("q", _vp), ("k_cache", _vp),
                 ("v_cache", _vp), ("block_table", _vp), ("out", _vp), ("lse", _vp),
                 ("softmax_scale", ctypes.c_float), ("force_path", _i32), ("num_ctas", _i32),
-                ("rope_theta", ctypes.c_float)]
+                ("rope_theta", ctypes.c_float), ("wait_limit_ns", ctypes.c_uint)]
 
 
 class AcceptArgs(ctypes.Structure):
@@ -176,7 +176,7 @@ class AttnPlan:
 def attn_args(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_len: torch.Tensor,
               n_tree: torch.Tensor, parent: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
               block_table: Optional[torch.Tensor] = None, softmax_scale: float = 0.0, force_path: int = 0,
-              num_ctas: int = 0, rope_theta: float = 0.0) -> AttnArgs:
+              num_ctas: int = 0, rope_theta: float = 0.0, wait_limit_ns: int = 0) -> AttnArgs:
     """Fill ``ts_attn_args`` from tensors.
 
     q, out: bf16 [B][n_query][Hq][d].  Contiguous KV: bf16 [B][max_kv_len][Hkv][d];
@@ -200,6 +200,7 @@ def attn_args(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pre
     a.lse = _ptr(lse)
     a.softmax_scale, a.force_path, a.num_ctas = softmax_scale, force_path, num_ctas
     a.rope_theta = rope_theta
+    a.wait_limit_ns = wait_limit_ns
     return a
 
 
@@ -224,15 +225,16 @@ def tree_attn_forward_args(args: AttnArgs, workspace: torch.Tensor, stream=None)
 
 def tree_attn_forward(q, k_cache, v_cache, prefix_len, n_tree, parent, out=None, lse=None, block_table=None,
                       softmax_scale: float = 0.0, workspace=None, stream=None, force_path: int = 0,
-                      num_ctas: int = 0, want_lse: bool = True, rope_theta: float = 0.0):
+                      num_ctas: int = 0, want_lse: bool = True, rope_theta: float = 0.0, wait_limit_ns: int = 0):
     """Tree-masked GQA attention; returns (out, lse).  rope_theta > 0 rotates
-    the queries at their tree positions (prefix length + depth) first."""
+    the queries at their tree positions (prefix length + depth) first;
+    wait_limit_ns > 0 bounds each pipeline wait in the kernels (testing)."""
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
     a = attn_args(q, k_cache, v_cache, prefix_len, n_tree, parent, out, lse, block_table, softmax_scale,
-                  force_path, num_ctas, rope_theta)
+                  force_path, num_ctas, rope_theta, wait_limit_ns)
     if workspace is None:
         workspace = new_workspace(tree_attn_workspace_size(a), q.device)
     tree_attn_forward_args(a, workspace, stream)
@@ -240,7 +242,8 @@ def tree_attn_forward(q, k_cache, v_cache, prefix_len, n_tree, parent, out=None,
 
 
 def tree_attn_forward_noalloc(q, k_cache, v_cache, prefix_len, n_tree, parent, out, lse=None, block_table=None,
-                              softmax_scale: float = 0.0, stream=None, force_path: int = 0, num_ctas: int = 0):
+                              softmax_scale: float = 0.0, stream=None, force_path: int = 0, num_ctas: int = 0,
+                              rope_theta: float = 0.0):
     """tree_attn_forward for callers that cannot allocate device memory.
 
     The library keeps the split-KV scratch in its own 16 MiB device array, so
@@ -248,7 +251,7 @@ def tree_attn_forward_noalloc(q, k_cache, v_cache, prefix_len, n_tree, parent, o
     optionally ``lse``).  Calls that overlap on the GPU race on that array.
     """
     a = attn_args(q, k_cache, v_cache, prefix_len, n_tree, parent, out, lse, block_table, softmax_scale,
-                  force_path, num_ctas)
+                  force_path, num_ctas, rope_theta)
     _check(_attn_noalloc(ctypes.byref(a), _stream(stream)), "tree_attn_forward_noalloc")
     return out, lse
 

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreespec.so")
 
-SOURCES = ["api.cu", "meta.cu", "accept.cu", "compact.cu", "expand.cu", "sample.cu", "rope.cu", "attn_mma.cu",
+SOURCES = ["api.cu", "meta.cu", "accept.cu", "compact.cu", "expand.cu", "sample.cu", "attn_mma.cu",
            "attn_tc.cu", "attn_merge.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",

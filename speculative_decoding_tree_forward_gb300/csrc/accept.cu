@@ -105,6 +105,9 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
     par = p.parent[rowbase + i];
     if (par < -1 || par >= i) par = -1;  // reported by build_ancestor_masks
     tok = p.tokens[rowbase + i];
+    // a draft token outside the vocab never equals an argmax: never accepted
+    // (the root's own token is not tested)
+    if (i > 0 && (tok < 0 || tok >= p.vocab)) report_error(p.err, TS_DEVERR_BAD_TOKEN);
   }
   if (n > 0) build_ancestor_masks(p.parent + rowbase, n, anc, jmp, i, blockDim.x, p.err, block_sync);
   pdl_wait();

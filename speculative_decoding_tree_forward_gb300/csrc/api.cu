@@ -21,6 +21,8 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+constexpr uint64_t kWaitLimitNsHost = 2000000000ull;  // the kernels' default bound of a wait (2 s)
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -89,7 +91,7 @@ struct AttnPlan {
   bool use_tc;
   int rows, row_groups, rows_pad, group, stages, num_ctas, hp, merge_half_warp;
   int64_t units, slots;
-  size_t ws_bytes, off_o, off_lse, off_q;  // off_q: rotated queries (rope_theta > 0), else 0
+  size_t ws_bytes, off_o, off_lse;
 };
 
 ts_status validate_attn(const ts_attn_args* a) {
@@ -176,14 +178,10 @@ ts_status plan_attn(const ts_attn_args* a, AttnPlan* pl) {
   // in flight: a second wave would cost every row of it another round trip.
   pl->merge_half_warp = pl->units * ((pl->rows_pad + 7) / 8) > 4LL * device_sm_count() ? 1 : 0;
   pl->slots = pl->num_ctas + pl->units;
+  // [error word][partial O][partial lse]
   pl->off_o = kWsHeader;
   pl->off_lse = pl->off_o + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * a->head_dim * sizeof(float));
   pl->ws_bytes = pl->off_lse + align256(static_cast<size_t>(pl->slots) * pl->rows_pad * sizeof(float));
-  pl->off_q = 0;
-  if (a->rope_theta > 0.f) {
-    pl->off_q = pl->ws_bytes;
-    pl->ws_bytes += align256(static_cast<size_t>(a->num_requests) * a->n_query * a->num_q_heads * a->head_dim * 2);
-  }
   return TS_OK;
 }
 
@@ -342,15 +340,18 @@ ts_status tree_attn_forward(const ts_attn_args* a, void* workspace, size_t works
   p.err = reinterpret_cast<unsigned*>(ws);
   p.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
+  p.wait_ns = a->wait_limit_ns > 0 ? static_cast<uint64_t>(a->wait_limit_ns) : kWaitLimitNsHost;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (a->rope_theta > 0.f) {  // the kernels read the queries rotated at their tree positions
-    void* qr = ws + pl.off_q;
-    RopeFreqs f;
-    for (int j = 0; j < 64; ++j)
-      f.inv_freq[j] = j < a->head_dim / 2 ? std::pow(static_cast<double>(a->rope_theta), -2.0 * j / a->head_dim) : 0.0;
-    if (launch_rope_q(p, f, a->q, qr, s) != cudaSuccess) return TS_ERR_CUDA;
-    p.q = static_cast<const __nv_bfloat16*>(qr);
+  if (a->rope_theta > 0.f) {
+    // the kernels rotate the queries at their tree positions as they stage
+    // them; each frequency theta^(-2j/d) goes as a 64-bit fraction of a turn
+    p.rope = 1;
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    for (int j = 0; j < 64; ++j) {
+      const double f = j < a->head_dim / 2 ? std::pow(static_cast<double>(a->rope_theta), -2.0 * j / a->head_dim) : 0.0;
+      p.rope_turn[j] = static_cast<uint64_t>(std::ldexp(f / kTwoPi, 64));
+    }
   }
   if (pl.use_tc) {
     CUtensorMap qmap;

@@ -6,6 +6,15 @@
 
 namespace ts {
 
+// A pipeline wait: the default bound, or (the bounded-wait variant, when the
+// call gives its own bound) that bound; waits that drain copies in flight
+// after an abort always take the default bound.
+template <bool kBounded>
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if constexpr (kBounded) return mbar_wait_bounded(bar, parity, limit_ns);
+  else return mbar_wait(bar, parity);
+}
+
 // Per-request lengths, clamped to the stated bounds (violations reported).
 // Every kernel of one call clamps the same way, so they agree on the schedule.
 __device__ __forceinline__ void attn_lengths(const AttnParams& p, int b, int& P, int& n, bool report) {
@@ -40,6 +49,37 @@ __device__ __forceinline__ void ancestor_walk(const int* par, int u, uint32_t a[
 }
 
 __device__ __forceinline__ int attn_tiles(int keys) { return (keys + kBlockN - 1) / kBlockN; }
+
+// RoPE at a tree position (SwiftSpec summary §3.3: RoPE inside the verify
+// attention, position = prefix length + depth).  Pair j of a query at
+// position pos turns by pos * theta^(-2j/d) rad.  The host gives each
+// frequency as a 64-bit fraction of a turn (theta^(-2j/d) / 2 pi * 2^64), so
+// pos times it modulo 2^64 is the angle's fractional turn, exact up to that
+// fraction's rounding (far below 1e-9 rad at any int32 position).  Its top 32
+// bits read as a signed fraction give the angle in [-pi, pi), where the fast
+// sine and cosine are accurate to about 2^-21, well below the bf16 rounding
+// of the rotated query.
+__device__ __forceinline__ void rope_cos_sin(int pos, uint64_t turn_frac, float& c, float& s) {
+  const uint64_t t = static_cast<uint64_t>(static_cast<uint32_t>(pos)) * turn_frac;  // modulo 2^64
+  const float a = static_cast<float>(static_cast<int32_t>(t >> 32)) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+  __sincosf(a, &s, &c);
+}
+
+// Rotate-half RoPE of 8 pairs held as two 16-byte chunks of bf16: x_j (chunk
+// a, column j of the first half) and x_{j + d/2} (chunk b); pair e of the
+// chunks is frequency j0 + e (turn_frac in shared or parameter memory).
+__device__ __forceinline__ void rope_rotate8(uint4& a, uint4& b, int pos, const uint64_t* turn_frac, int j0) {
+  __nv_bfloat16* a8 = reinterpret_cast<__nv_bfloat16*>(&a);
+  __nv_bfloat16* b8 = reinterpret_cast<__nv_bfloat16*>(&b);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float c, s;
+    rope_cos_sin(pos, turn_frac[j0 + e], c, s);
+    const float x0 = __bfloat162float(a8[e]), x1 = __bfloat162float(b8[e]);
+    a8[e] = __float2bfloat16_rn(x0 * c - x1 * s);
+    b8[e] = __float2bfloat16_rn(x0 * s + x1 * c);
+  }
+}
 
 // Visibility of the 64 keys [P + off, P + off + 64) for a query whose
 // ancestor-or-self set is `a` (bit j = tree node j): prefix keys (negative

@@ -45,7 +45,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <int D>
+template <int D, bool kBounded>
 __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                                                        const __grid_constant__ CUtensorMap vmap,
                                                        const AttnParams p) {
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
       int issued = 0;
       for (int it = 0; it < n_tiles; ++it) {
         if (it >= p.stages) {
-          if (!mbar_wait(&empty_bar[s], (phase - 1) & 1)) {
+          if (!pipe_wait<kBounded>(&empty_bar[s], (phase - 1) & 1, p.wait_ns)) {
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -255,19 +255,36 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
       const int r1 = r0 + 8;
       ancestor_walk(par_w, n - p.n_query + min(r0, p.rows - 1) / p.group, anc0);
       ancestor_walk(par_w, n - p.n_query + min(r1, p.rows - 1) / p.group, anc1);
-      // this warp's 16 query rows -> shared memory, 128-byte swizzled rows
+      // this warp's 16 query rows -> shared memory, 128-byte swizzled rows;
+      // with RoPE each (row, 8 pairs) item is rotated on the way, at position
+      // P + depth of the row's node (SwiftSpec summary §3.3): chunk c16 of the
+      // first half pairs with chunk c16 + D / 16 of the second
       {
         uint8_t* qw = smem + L.qs + static_cast<uint32_t>(rb) * 16 * D * 2;
-        for (int x = lane; x < 16 * (D / 8); x += kThreadsPerWarp) {
-          const int rr = x / (D / 8), c16 = x % (D / 8);
+        const int per_row = p.rope ? D / 16 : D / 8;  // items per row
+        for (int x = lane; x < 16 * per_row; x += kThreadsPerWarp) {
+          const int rr = x / per_row, c16 = x % per_row;
           const int r = rg * kMaxRowsPerUnit + rb * 16 + rr;
-          uint4 v = make_uint4(0, 0, 0, 0);
+          uint4 v = make_uint4(0, 0, 0, 0), w = make_uint4(0, 0, 0, 0);
           if (r < p.rows) {
             const int i = r / p.group, h = kvh * p.group + r % p.group;
-            v = __ldg(reinterpret_cast<const uint4*>(
-                p.q + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * D + c16 * 8));
+            const __nv_bfloat16* qrow = p.q + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * D;
+            v = __ldg(reinterpret_cast<const uint4*>(qrow + c16 * 8));
+            if (p.rope) {
+              w = __ldg(reinterpret_cast<const uint4*>(qrow + D / 2 + c16 * 8));
+              int u = n - p.n_query + i, depth = 0;
+              while (par_w[u] >= 0) {  // parent[u] < u: at most n steps
+                u = par_w[u];
+                ++depth;
+              }
+              rope_rotate8(v, w, P + depth, p.rope_turn, 8 * c16);
+            }
           }
           *reinterpret_cast<uint4*>(qw + (c16 >> 3) * (16 * 128) + sw128(rr, c16 & 7)) = v;
+          if (p.rope) {
+            const int c2 = c16 + D / 16;
+            *reinterpret_cast<uint4*>(qw + (c2 >> 3) * (16 * 128) + sw128(rr, c2 & 7)) = w;
+          }
         }
         __syncwarp();
       }
@@ -276,7 +293,7 @@ __global__ void __launch_bounds__(288) attn_mma_kernel(const __grid_constant__ C
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
     }
-    if (*abort_flag || !mbar_wait(&full_bar[s], phase & 1)) {
+    if (*abort_flag || !pipe_wait<kBounded>(&full_bar[s], phase & 1, p.wait_ns)) {
       report_error(p.err, TS_DEVERR_TIMEOUT);
       *abort_flag = 1;
       break;
@@ -510,9 +527,12 @@ cudaError_t launch_attn_mma(const AttnParams& p, const CUtensorMap& kmap, const 
                             cudaStream_t stream) {
   const size_t smem = attn_mma_smem_bytes(p.head_dim, p.stages, p.num_req, p.rows_pad);
   const int threads = attn_mma_threads(p.rows_pad);
+  const bool bounded = p.wait_ns < kWaitLimitNs;  // a caller-given bound: the bounded-wait variant
   if (p.head_dim == 128)
-    return launch_pdl(attn_mma_kernel<128>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p);
-  return launch_pdl(attn_mma_kernel<64>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p);
+    return bounded ? launch_pdl(attn_mma_kernel<128, true>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p)
+                   : launch_pdl(attn_mma_kernel<128, false>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p);
+  return bounded ? launch_pdl(attn_mma_kernel<64, true>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p)
+                 : launch_pdl(attn_mma_kernel<64, false>, dim3(p.num_ctas), dim3(threads), smem, stream, kmap, vmap, p);
 }
 
 int attn_mma_occupancy(int head_dim, int stages, int num_req, int rows_pad) {
@@ -527,13 +547,19 @@ int attn_mma_occupancy(int head_dim, int stages, int num_req, int rows_pad) {
   if (smem > static_cast<size_t>(optin)) return 0;
   const int threads = attn_mma_threads(rows_pad);
   if (head_dim == 128) {
-    if (cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_mma_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_mma_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess)
       return 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_mma_kernel<128>, threads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_mma_kernel<128, false>, threads, smem);
   } else {
-    if (cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_mma_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_mma_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess)
       return 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_mma_kernel<64>, threads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_mma_kernel<64, false>, threads, smem);
   }
   return nb;
 }

@@ -108,7 +108,7 @@ struct TcShape {
 };
 
 struct TcLayout {
-  uint32_t q, k, v, ctrl, par, xch, cum, stg, total;
+  uint32_t q, k, v, ctrl, par, xch, cum, lenp, lenn, rope, stg, total;
   static constexpr uint32_t kStgWarpBytes = 32 * 128;  // 32 rows x 128 bytes, 128-byte swizzle
   static constexpr uint32_t kQBytes = 128 * 128 * 2;   // two 64-column halves of 128 rows
   static constexpr uint32_t kQKVBytes = 192 * 1024;    // Q buffers + K ring + V ring (split per HP)
@@ -117,9 +117,12 @@ struct TcLayout {
 struct TcCtrl {
   uint64_t k_full[kMaxKSlots], k_empty[kMaxKSlots], v_full[kMaxVSlots], v_empty[kMaxVSlots];
   uint64_t q_full[kMaxQBufs], q_empty[kMaxQBufs];  // Q buffer u % kQBufs holds the CTA's u-th unit
+  uint64_t q_rot[kMaxQBufs];  // with RoPE: the buffer's queries have been rotated at their tree positions
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // per (warpgroup, S/P buffer)
   uint64_t o_free[2], xch_full[2], fin_qk, fin_pv;
   uint64_t stg_free;  // one phase per complete mid-range segment: its finisher's staging tiles are free again
+  int64_t t_begin, t_end, local0;  // the CTA's tile range and its offset in request b0
+  int b0;
   uint32_t tmem_base;
   int abort;
 };
@@ -135,9 +138,12 @@ __host__ __device__ inline TcLayout tc_layout(int num_req, int q_bufs = 2, uint3
   L.par = L.ctrl + ((sizeof(TcCtrl) + 15) & ~size_t(15));
   L.xch = L.par + 2 * TS_MAX_TREE * 4;
   L.cum = L.xch + 2 * kRowsTc * 8;
-  // epilogue staging: 32 rows x 32 fp32 columns per warp of the finishing
-  // warpgroup, 1024-byte aligned for the swizzled TMA store
-  L.stg = (L.cum + 8 * (kMaxRequestsAttn + 1) + 1023) & ~1023u;
+  L.lenp = L.cum + 8 * (kMaxRequestsAttn + 1);  // clamped prefix length of every request
+  L.lenn = L.lenp + 4 * kMaxRequestsAttn;       // clamped tree size of every request (<= 128)
+  L.rope = L.lenn + kMaxRequestsAttn;           // RoPE frequencies as turn fractions (64 x 8 bytes)
+  // epilogue staging: 32 rows x 64 bytes of bf16 output per warp of the
+  // finishing warpgroup, 128-byte swizzled, 1024-byte aligned
+  L.stg = (L.rope + 64 * 8 + 1023) & ~1023u;
   L.total = L.stg + 4 * TcLayout::kStgWarpBytes;  // fixed: launch shape independent of the batch
   (void)num_req;
   return L;
@@ -154,12 +160,17 @@ __device__ __forceinline__ void wg_sync(int w) {
 struct Cursor {
   int b, uir, tile, P, n, tiles, unit;  // unit: CTA-local unit index
   int tile0;                            // unit tile at which the CTA's range starts
-  __device__ void start(const AttnParams& p, int b0, int64_t local) {
+  const int* lp;                        // clamped lengths of every request (shared memory)
+  const uint8_t* ln;
+  __device__ void start(const int* lp_, const uint8_t* ln_, int b0, int64_t local) {
+    lp = lp_;
+    ln = ln_;
     b = b0;
-    attn_lengths(p, b, P, n, false);
+    P = lp[b];
+    n = ln[b];
     tiles = attn_tiles(P + n);
     uir = static_cast<int>(local / tiles);
-    tile = static_cast<int>(local % tiles);
+    tile = static_cast<int>(local - static_cast<int64_t>(uir) * tiles);
     tile0 = tile;
     unit = 0;
   }
@@ -171,7 +182,8 @@ struct Cursor {
         uir = 0;
         ++b;
         if (b < p.num_req) {
-          attn_lengths(p, b, P, n, false);
+          P = lp[b];
+          n = ln[b];
           tiles = attn_tiles(P + n);
         }
       }
@@ -317,10 +329,11 @@ __device__ __forceinline__ void write_p2(uint64_t vis, float scale_log2, float n
 }
 
 // First tile of CTA c under the cost-weighted split (common.cuh): cum[b] =
-// tiles before request b (every unit of request b has (cum[b + 1] - cum[b]) /
-// upr tiles), E = the weight a unit's first tile carries beyond 1.
-__device__ __forceinline__ int64_t wsched_begin(int c, const int64_t* cum, int num_req, int upr, int E, int64_t T,
-                                                int NC) {
+// tiles before request b, every unit of request b has `tiles` = attn_tiles(P +
+// n) tiles (lengths from the shared-memory table), E = the weight a unit's
+// first tile carries beyond 1.
+__device__ __forceinline__ int64_t wsched_begin(int c, const int64_t* cum, const int* lp, const uint8_t* ln,
+                                                int num_req, int upr, int E, int64_t T, int NC) {
   const int64_t W = T + static_cast<int64_t>(E) * upr * num_req;
   const int64_t x = wsched_x(c, W, NC);
   if (x >= W) return T;
@@ -330,14 +343,54 @@ __device__ __forceinline__ int64_t wsched_begin(int c, const int64_t* cum, int n
     if (cum[mid] + static_cast<int64_t>(E) * upr * mid <= x) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
-  const int tiles = static_cast<int>((cum[b + 1] - cum[b]) / upr);
+  const int tiles = attn_tiles(lp[b] + ln[b]);
   const int64_t span = tiles + E;
   if (span <= 0) return cum[b + 1];
   const int64_t off = x - (cum[b] + static_cast<int64_t>(E) * upr * b);
-  const int uir = static_cast<int>(off / span);
+  const int uir = (off < (1ll << 31)) ? static_cast<int>(static_cast<uint32_t>(off) / static_cast<uint32_t>(span))
+                                      : static_cast<int>(off / span);
   if (uir >= upr) return cum[b + 1];
   const int j = wsched_tile_in_unit(off - uir * span, E, tiles);
   return cum[b] + static_cast<int64_t>(uir) * tiles + j;
+}
+
+// RoPE of one packed row of a 128-row Q tile in shared memory (two 64-column
+// halves of 128-byte swizzled rows: 16-byte chunk cc of the first half holds
+// pairs 8 cc .. 8 cc + 7, their partners sit in the same chunk of the second
+// half).  The G consecutive lanes that hold one query node's G heads (G
+// divides 32, so they never straddle a warp) share the node's angles: lane g
+// of the group computes frequencies g, g + G, ... and the others take them by
+// shuffles, which cuts the sine/cosine work by G.  All 32 lanes take part;
+// only rows with `write` set are stored.
+template <int G>
+__device__ __forceinline__ void rope_row_shared(uint8_t* q0, int r, int lane, int pos, const uint64_t* turn,
+                                                bool write) {
+  constexpr int kPer = 64 / G;
+  const int g = lane % G, base = lane - g;
+  float cs[kPer], sn[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) rope_cos_sin(pos, turn[g + k * G], cs[k], sn[k]);
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    uint4* pa = reinterpret_cast<uint4*>(q0 + sw128(r, cc));
+    uint4* pb = reinterpret_cast<uint4*>(q0 + TcLayout::kQBytes / 2 + sw128(r, cc));
+    uint4 va = *pa, vb = *pb;
+    __nv_bfloat16* a8 = reinterpret_cast<__nv_bfloat16*>(&va);
+    __nv_bfloat16* b8 = reinterpret_cast<__nv_bfloat16*>(&vb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j = 8 * cc + e;
+      const float c = __shfl_sync(0xffffffffu, cs[j / G], base + j % G);
+      const float sv = __shfl_sync(0xffffffffu, sn[j / G], base + j % G);
+      const float x0 = __bfloat162float(a8[e]), x1 = __bfloat162float(b8[e]);
+      a8[e] = __float2bfloat16_rn(x0 * c - x1 * sv);
+      b8[e] = __float2bfloat16_rn(x0 * sv + x1 * c);
+    }
+    if (write) {
+      *pa = va;
+      *pb = vb;
+    }
+  }
 }
 
 // Waits (bounded) for the last copy issued into each slot of a ring.
@@ -348,7 +401,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued
   }
 }
 
-template <int HP>
+template <int HP, bool kBounded>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const __grid_constant__ CUtensorMap qmap,
@@ -384,6 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     for (int i = 0; i < Sh::kQBufs; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
+      mbar_init(&ctl->q_rot[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       for (int j = 0; j < 2; ++j) {
@@ -413,43 +467,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     prefetch_tmap(&qmap);
   }
   if (lane == 0 && warp == kVProducerWarp) prefetch_tmap(&vmap);
+  uint64_t* rope_turn = reinterpret_cast<uint64_t*>(smem + L.rope);
+  if (p.rope && tid < 64) rope_turn[tid] = p.rope_turn[tid];
 
   // ---- the inputs: wait for the previous kernel in the stream
   pdl_wait();
   pdl_launch_dependents();
-  // schedule (identical to the warp-MMA kernel)
-  for (int b = tid; b < p.num_req; b += blockDim.x) {
-    int P, n;
-    attn_lengths(p, b, P, n, blockIdx.x == 0);
-    cum[b + 1] = static_cast<int64_t>(attn_tiles(P + n)) * units_per_req;
-  }
-  if (tid == 0) cum[0] = 0;
-  __syncthreads();
-  if (tid == 0) {
-    for (int b = 0; b < p.num_req; ++b) cum[b + 1] += cum[b];
+  // ---- schedule (warp 0): every request's lengths, clamped as every kernel
+  //      of the call clamps them, into the shared-memory table; the prefix
+  //      sums of the tile counts by warp scans; then the CTA's tile range
+  //      (lane 0 its start, lane 1 its end) and the request it starts in.
+  int* lenp = reinterpret_cast<int*>(smem + L.lenp);
+  uint8_t* lenn = smem + L.lenn;
+  if (warp == 0) {
+    int64_t run = 0;
+    for (int base = 0; base < p.num_req; base += 32) {
+      const int b = base + lane;
+      int64_t t = 0;
+      if (b < p.num_req) {
+        int P, n;
+        attn_lengths(p, b, P, n, blockIdx.x == 0);
+        lenp[b] = P;
+        lenn[b] = static_cast<uint8_t>(n);
+        t = static_cast<int64_t>(attn_tiles(P + n)) * units_per_req;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += v;
+      }
+      if (b < p.num_req) cum[b + 1] = run + t;
+      run += __shfl_sync(0xffffffffu, t, 31);
+    }
+    if (lane == 0) cum[0] = 0;
+    __syncwarp();
+    if (lane < 2) {
+      const int64_t x = wsched_begin(blockIdx.x + lane, cum, lenp, lenn, p.num_req, units_per_req, p.seg_cost, run,
+                                     p.num_ctas);
+      if (lane == 0) {
+        int lo = 0, hi = p.num_req - 1;  // the request holding the CTA's first tile
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) / 2;
+          if (cum[mid] <= x) lo = mid; else hi = mid - 1;
+        }
+        ctl->t_begin = x;
+        ctl->b0 = lo;
+        ctl->local0 = x - cum[lo];
+      } else {
+        ctl->t_end = x;
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
-  const int64_t T = cum[p.num_req];
-  const int64_t t_begin = wsched_begin(blockIdx.x, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
-  const int64_t t_end = wsched_begin(blockIdx.x + 1, cum, p.num_req, units_per_req, p.seg_cost, T, p.num_ctas);
+  const int64_t t_begin = ctl->t_begin, t_end = ctl->t_end;
   if (t_begin >= t_end) {  // no tiles: release TMEM and leave
     if (warp == kQkWarp) tmem_dealloc(tbase, kTmemCols);
     return;
   }
   const int n_tiles = static_cast<int>(t_end - t_begin);
-  int b0 = 0;
-  {
-    int lo = 0, hi = p.num_req - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) / 2;
-      if (cum[mid] <= t_begin) lo = mid; else hi = mid - 1;
-    }
-    b0 = lo;
-  }
-  const int64_t local0 = t_begin - cum[b0];
+  const int b0 = ctl->b0;
+  const int64_t local0 = ctl->local0;
 
   if (warp == kProducerWarp || warp == kVProducerWarp) {
     // ======================= K / V producers =======================
@@ -458,7 +538,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const bool kside = warp == kProducerWarp;
     const CUtensorMap* map = kside ? &kmap : &vmap;
     Cursor c;
-    c.start(p, b0, local0);
+    c.start(lenp, lenn, b0, local0);
     int issued = 0, q_issued = 0;
     int blk[kMaxPagesPerTile];
     const uint64_t kv_policy = l2_policy_evict_first();  // K/V rows are read once
@@ -469,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // buffer u % Sh::kQBufs is free once the QK^T of unit u - Sh::kQBufs are done
         const int qb = c.unit % Sh::kQBufs;
         if (lane == 0) {
-          ok = c.unit < Sh::kQBufs || mbar_wait(&ctl->q_empty[qb], ((c.unit / Sh::kQBufs) - 1) & 1);
+          ok = c.unit < Sh::kQBufs || pipe_wait<kBounded>(&ctl->q_empty[qb], ((c.unit / Sh::kQBufs) - 1) & 1, p.wait_ns);
           if (ok) {
             mbar_arrive_expect_tx(&ctl->q_full[qb], static_cast<uint32_t>(HP * p.rows) * 256u);
             for (int h = 0; h < 2; ++h)
@@ -487,9 +567,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // the PV that read it is done (HP = 1: the PV of the previous tile in
       // the same S/P buffer)
       if (lane == 0)
-        ok = kside ? (it < Sh::kKSlots || mbar_wait(&ctl->k_empty[sl], ((it / Sh::kKSlots) - 1) & 1))
-                   : (it < Sh::kVSlots || (Sh::kVTied ? mbar_wait(&ctl->pv_done[w][bb], (Sh::use(it) - 1) & 1)
-                                                      : mbar_wait(&ctl->v_empty[sl], ((it / Sh::kVSlots) - 1) & 1)));
+        ok = kside ? (it < Sh::kKSlots || pipe_wait<kBounded>(&ctl->k_empty[sl], ((it / Sh::kKSlots) - 1) & 1, p.wait_ns))
+                   : (it < Sh::kVSlots || (Sh::kVTied ? pipe_wait<kBounded>(&ctl->pv_done[w][bb], (Sh::use(it) - 1) & 1, p.wait_ns)
+                                                      : pipe_wait<kBounded>(&ctl->v_empty[sl], ((it / Sh::kVSlots) - 1) & 1, p.wait_ns)));
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       uint64_t* full = kside ? &ctl->k_full[sl] : &ctl->v_full[sl];
@@ -528,7 +608,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem + L.q), 16, 1024);
       const uint32_t sk = smem_u32(smem + L.k);
       Cursor cq;
-      cq.start(p, b0, local0);
+      cq.start(lenp, lenn, b0, local0);
       bool ok = true;
       for (int k = 0; k < n_tiles;) {
         if (*abort_flag) { ok = false; break; }
@@ -536,10 +616,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const bool pair = HP == 1 && (k & 1) == 0 && k + 1 < n_tiles && cq.tile != cq.tiles - 1;
         const int cnt = pair ? 2 : 1;
         const int qb = cq.unit % Sh::kQBufs;
-        if ((k == 0 || cq.tile == 0) && !mbar_wait(&ctl->q_full[qb], (cq.unit / Sh::kQBufs) & 1)) { ok = false; break; }
+        // the unit's queries: landed (and, with RoPE, rotated by the softmax
+        // warpgroup that owns the unit's first tile)
+        if ((k == 0 || cq.tile == 0) &&
+            !pipe_wait<kBounded>(p.rope ? &ctl->q_rot[qb] : &ctl->q_full[qb], (cq.unit / Sh::kQBufs) & 1, p.wait_ns)) {
+          ok = false;
+          break;
+        }
         for (int t = k; t < k + cnt && ok; ++t)
-          ok = mbar_wait(&ctl->k_full[t % Sh::kKSlots], (t / Sh::kKSlots) & 1) &&
-               (t < Sh::kSBufs || mbar_wait(&ctl->pv_done[t & 1][Sh::buf(t)], (Sh::use(t) - 1) & 1));
+          ok = pipe_wait<kBounded>(&ctl->k_full[t % Sh::kKSlots], (t / Sh::kKSlots) & 1, p.wait_ns) &&
+               (t < Sh::kSBufs || pipe_wait<kBounded>(&ctl->pv_done[t & 1][Sh::buf(t)], (Sh::use(t) - 1) & 1, p.wait_ns));
         if (!ok) break;
         tc_fence_after();
         // the descriptors of the 8 K-slices differ only in the start address
@@ -575,7 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
       const uint32_t sv = smem_u32(smem + L.v);
       Cursor cp;
-      cp.start(p, b0, local0);
+      cp.start(lenp, lenn, b0, local0);
       int part[2] = {0, 0};  // segments each warpgroup has finished taking part in (o_free phases)
       bool ok = true;
       for (int k = 0; k < n_tiles; ++k) {
@@ -583,9 +669,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const int w = k & 1, bb = Sh::buf(k);
         const int sf = cp.seg_first(k), sl = cp.seg_last(k, n_tiles);
         const bool first_owned = (k - sf) < 2;
-        if (!mbar_wait(&ctl->p_full[w][bb], Sh::use(k) & 1) ||
-            (first_owned && part[w] > 0 && !mbar_wait(&ctl->o_free[w], (part[w] - 1) & 1)) ||
-            !mbar_wait(&ctl->v_full[k % Sh::kVSlots], (k / Sh::kVSlots) & 1)) {
+        if (!pipe_wait<kBounded>(&ctl->p_full[w][bb], Sh::use(k) & 1, p.wait_ns) ||
+            (first_owned && part[w] > 0 && !pipe_wait<kBounded>(&ctl->o_free[w], (part[w] - 1) & 1, p.wait_ns)) ||
+            !pipe_wait<kBounded>(&ctl->v_full[k % Sh::kVSlots], (k / Sh::kVSlots) & 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -627,7 +713,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     int* par = reinterpret_cast<int*>(smem + L.par) + wg * TS_MAX_TREE;
     float2* xch = reinterpret_cast<float2*>(smem + L.xch);
     Cursor c;
-    c.start(p, b0, local0);
+    c.start(lenp, lenn, b0, local0);
     int nonfin[2] = {0, 0};  // segments in which each warpgroup handed its state to the other
     int stg_idx = 0;         // earlier segments whose epilogue used the shared staging tiles
     int anc_req = -1;
@@ -658,12 +744,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
             for (int w = 0; w < 4; ++w) anc[w] = 0u;
           }
+          if (p.rope && k == sf) {
+            // RoPE: the owner of the unit's first tile rotates the unit's
+            // queries in shared memory once they land, each thread its own
+            // packed row at position P + depth (16-byte chunk cc of the two
+            // 64-column halves holds pairs 8 cc .. 8 cc + 7); the QK^T issuer
+            // waits for q_rot before the unit's first product
+            // Rotations run in unit order: first the previous unit's (whose
+            // owner may be the other warpgroup).  That keeps each parity wait
+            // below within one phase of its barrier even when this warpgroup
+            // owns no tile of the previous unit: once unit u - 1 is rotated,
+            // its queries have landed, so q_full[qb] has completed every phase
+            // before this unit's, and q_rot[qb] cannot run ahead of this
+            // warpgroup, which rotates this unit.
+            const int qb = c.unit % Sh::kQBufs;
+            if (c.unit > 0 && !pipe_wait<kBounded>(&ctl->q_rot[(c.unit - 1) % Sh::kQBufs],
+                                         ((c.unit - 1) / Sh::kQBufs) & 1, p.wait_ns)) {
+              report_error(p.err, TS_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
+            if (!pipe_wait<kBounded>(&ctl->q_full[qb], (c.unit / Sh::kQBufs) & 1, p.wait_ns)) {
+              report_error(p.err, TS_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
+            {
+              const bool real = Sh::local_of(r) < p.rows;  // padding rows take part in the shuffles only
+              const int pos = c.P + __popc(anc[0]) + __popc(anc[1]) + __popc(anc[2]) + __popc(anc[3]) - 1;
+              uint8_t* q0 = smem + L.q + qb * TcLayout::kQBytes;
+              switch (p.group) {  // the G rows of one query node share its angles
+                case 4: rope_row_shared<4>(q0, r, lane, pos, rope_turn, real); break;
+                case 8: rope_row_shared<8>(q0, r, lane, pos, rope_turn, real); break;
+                case 16: rope_row_shared<16>(q0, r, lane, pos, rope_turn, real); break;
+                case 32: rope_row_shared<32>(q0, r, lane, pos, rope_turn, real); break;
+                default:
+                  if (real) {
+#pragma unroll 1
+                    for (int cc = 0; cc < 8; ++cc) {
+                      uint4* pa = reinterpret_cast<uint4*>(q0 + sw128(r, cc));
+                      uint4* pb = reinterpret_cast<uint4*>(q0 + TcLayout::kQBytes / 2 + sw128(r, cc));
+                      uint4 va = *pa, vb = *pb;
+                      rope_rotate8(va, vb, pos, rope_turn, 8 * cc);
+                      *pa = va;
+                      *pb = vb;
+                    }
+                  }
+              }
+            }
+            fence_proxy_async_smem();  // the tensor cores read the rotated rows
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->q_rot[qb]);
+          }
           m_used = -INFINITY;
           l = 0.f;
         }
         const int bb = Sh::buf(k);
         const uint32_t sbuf = lane_addr + Sh::col_s(wg, bb);
-        if (*abort_flag || !mbar_wait(&ctl->s_full[wg][bb], Sh::use(k) & 1)) {
+        if (*abort_flag || !pipe_wait<kBounded>(&ctl->s_full[wg][bb], Sh::use(k) & 1, p.wait_ns)) {
           report_error(p.err, TS_DEVERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -736,7 +874,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         // implies a previous tile in this segment)
         const bool need_rescale = __any_sync(0xffffffffu, rescale);
         if (need_rescale) {
-          if (!mbar_wait(&ctl->pv_done[wg][Sh::buf(k - 2)], Sh::use(k - 2) & 1)) {
+          if (!pipe_wait<kBounded>(&ctl->pv_done[wg][Sh::buf(k - 2)], Sh::use(k - 2) & 1, p.wait_ns)) {
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -776,7 +914,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const int keys = c.P + c.n;
         if (key0 + kBlockN > keys) {
           const int vslot = k % Sh::kVSlots;
-          if (!mbar_wait(&ctl->v_full[vslot], (k / Sh::kVSlots) & 1)) {  // the tile has landed
+          if (!pipe_wait<kBounded>(&ctl->v_full[vslot], (k / Sh::kVSlots) & 1, p.wait_ns)) {  // the tile has landed
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -795,7 +933,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
         // ---- this warpgroup's last tile of the segment
         if (last_owned) {
-          if (!mbar_wait(&ctl->pv_done[wg][bb], Sh::use(k) & 1)) {
+          if (!pipe_wait<kBounded>(&ctl->pv_done[wg][bb], Sh::use(k) & 1, p.wait_ns)) {
             report_error(p.err, TS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -812,7 +950,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           } else {
             float mo = -INFINITY, lo_ = 0.f;
             if (other_in) {
-              if (!mbar_wait(&ctl->xch_full[oth], nonfin[oth] & 1)) {
+              if (!pipe_wait<kBounded>(&ctl->xch_full[oth], nonfin[oth] & 1, p.wait_ns)) {
                 report_error(p.err, TS_DEVERR_TIMEOUT);
                 *abort_flag = 1;
                 break;
@@ -852,7 +990,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               const uint32_t stg = last_seg ? L.v + (warp & 3) * 4 * TcLayout::kStgWarpBytes
                                             : L.stg + (warp & 3) * TcLayout::kStgWarpBytes;
               const int row0 = (warp & 3) * 32;
-              if (!last_seg && stg_idx > 0 && !mbar_wait(&ctl->stg_free, (stg_idx - 1) & 1)) {
+              if (!last_seg && stg_idx > 0 && !pipe_wait<kBounded>(&ctl->stg_free, (stg_idx - 1) & 1, p.wait_ns)) {
                 report_error(p.err, TS_DEVERR_TIMEOUT);
                 *abort_flag = 1;
                 break;
@@ -927,7 +1065,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 if (p.lse != nullptr)
                   p.lse[(static_cast<int64_t>(c.b) * p.hq + h) * p.n_query + i] = lse2 * 0.69314718055994530942f;
               } else {
-                p.part_lse[slot * 128 + r] = lse2;
+                __stcg(p.part_lse + slot * 128 + r, lse2);
               }
             }
           }
@@ -939,7 +1077,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
   }
 
-  bulk_wait_all();  // partial stores issued by this thread have completed
+  bulk_wait_all();  // bulk copies issued by this thread have completed
   tc_fence_before();
   __syncthreads();
   if (warp == kQkWarp) {
@@ -964,10 +1102,13 @@ int attn_tc_occupancy(int stages, int num_req) {
   int nb = 0;
   const size_t smem = attn_tc_smem_bytes(stages, num_req);
   if (smem > static_cast<size_t>(optin)) return 0;
-  if (cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+  if (cudaFuncSetAttribute(attn_tc_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_tc_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_tc_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_tc_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_tc_kernel<1>, kTcThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, attn_tc_kernel<1, false>, kTcThreads, smem) != cudaSuccess)
+    return 0;
   return nb;
 }
 
@@ -976,9 +1117,13 @@ int attn_tc_occupancy(int stages, int num_req) {
 cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
                            cudaStream_t stream) {
   const size_t smem = attn_tc_smem_bytes(p.stages, p.num_req);
+  const bool bounded = p.wait_ns < kWaitLimitNs;  // a caller-given bound: the bounded-wait variant
+  const dim3 grid(p.num_ctas), block(kTcThreads);
   if (p.hp == 2)
-    return launch_pdl(attn_tc_kernel<2>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, qmap, p);
-  return launch_pdl(attn_tc_kernel<1>, dim3(p.num_ctas), dim3(kTcThreads), smem, stream, kmap, vmap, qmap, p);
+    return bounded ? launch_pdl(attn_tc_kernel<2, true>, grid, block, smem, stream, kmap, vmap, qmap, p)
+                   : launch_pdl(attn_tc_kernel<2, false>, grid, block, smem, stream, kmap, vmap, qmap, p);
+  return bounded ? launch_pdl(attn_tc_kernel<1, true>, grid, block, smem, stream, kmap, vmap, qmap, p)
+                 : launch_pdl(attn_tc_kernel<1, false>, grid, block, smem, stream, kmap, vmap, qmap, p);
 }
 
 }  // namespace ts

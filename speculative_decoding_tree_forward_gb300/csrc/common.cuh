@@ -82,8 +82,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete, for at most
-// kWaitLimitNs of %globaltimer; returns false when the limit expires.  One
-// PTX block, so the wait adds no register pressure to the loop around it.
+// kWaitLimitNs of %globaltimer; returns false when the limit expires.  The
+// loop spins on try_wait, which may suspend the thread in hardware until the
+// phase completes.  One PTX block, so the wait adds no register pressure to
+// the loop around it.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -100,6 +102,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, P1;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity), "l"(kWaitLimitNs)
+      : "memory");
+  return ok != 0;
+}
+
+// The same wait with a caller-given bound, for the kernels' bounded-wait
+// variant (a test that makes a wait run out): it spins on the non-blocking
+// test_wait, so the bound holds to the nanosecond.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t.reg .u64 t0, t1;\n\t"
+      "mov.u64 t0, %%globaltimer;\n"
+      "LAB_TEST:\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+      "@P1 bra.uni DONE_TEST;\n\t"
+      "mov.u64 t1, %%globaltimer;\n\t"
+      "sub.u64 t1, t1, t0;\n\t"
+      "setp.lt.u64 P1, t1, %3;\n\t"
+      "@P1 bra.uni LAB_TEST;\n"
+      "DONE_TEST:\n\t"
+      "selp.u32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "l"(limit_ns)
       : "memory");
   return ok != 0;
 }

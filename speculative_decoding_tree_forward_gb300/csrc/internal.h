@@ -63,6 +63,9 @@ struct AttnParams {
   float* part_o;     // warp-MMA path: [slots][rows_pad][head_dim]; tcgen05 path: [slots][32][128] float4
                      // (float4 j of row r at (slot * 32 + j) * 128 + r)
   float* part_lse;   // [slots][rows_pad] (log2 domain)
+  uint64_t wait_ns;    // bound of each pipeline wait (the drain waits after an abort keep kWaitLimitNs)
+  int rope;            // 1: rotate the queries at their tree positions (rope_turn holds the frequencies)
+  uint64_t rope_turn[64];  // theta^(-2j/d) / 2 pi as a 64-bit fraction of a turn, j < d/2
 };
 
 // Launchers (one per kernel family); return cudaGetLastError().
@@ -72,12 +75,6 @@ cudaError_t launch_attn_tc(const AttnParams& p, const CUtensorMap& kmap, const C
                            cudaStream_t stream);
 size_t attn_zero_prefix_bytes(const ts_attn_args* a);
 cudaError_t launch_attn_merge(const AttnParams& p, bool tc_layout, cudaStream_t stream);
-// RoPE inverse frequencies theta^(-2j/d), j < d/2, computed on the host in fp64.
-struct RopeFreqs {
-  double inv_freq[64];
-};
-// Queries rotated at their tree positions into q_out (same layout as q_in).
-cudaError_t launch_rope_q(const AttnParams& p, const RopeFreqs& f, const void* q_in, void* q_out, cudaStream_t stream);
 size_t attn_mma_smem_bytes(int head_dim, int stages, int num_req, int rows_pad);
 size_t attn_tc_smem_bytes(int stages, int num_req);
 int attn_mma_threads(int rows_pad);

@@ -14,9 +14,12 @@
 // code cannot use the array's name as a device address, so on the first call
 // on each device (with that device current) the entry point looks the address
 // up with cudaGetSymbolAddress and caches it; that first call should come
-// before any stream capture.  The call then runs the ordinary
-// tree_attn_forward path with the array as its workspace, choosing a
-// split-KV CTA count small enough for the partials to fit.
+// before any stream capture.  The cache is not refreshed: after a
+// cudaDeviceReset the module (and the array) may be loaded elsewhere, so this
+// entry point must not be used on a device that has been reset.  The call
+// then runs the ordinary tree_attn_forward path with the array as its
+// workspace, choosing a split-KV CTA count small enough for the partials to
+// fit.
 #include <cuda_runtime.h>
 
 #include <mutex>

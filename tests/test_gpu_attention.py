@@ -12,7 +12,7 @@ if torch.cuda.is_available():   # on a GPU machine a missing library is an error
     import speculative_decoding_tree_forward_gb300 as ts
 else:
     ts = None
-from gpu_util import attn_inputs, bf16_dev, bf16_host_f64, check_attention  # noqa: E402
+from gpu_util import ATOL, RTOL, attn_inputs, bf16_dev, bf16_host_f64, check_attention  # noqa: E402
 
 
 def run(case, **kw):
@@ -286,6 +286,9 @@ ROPE = [  # (case, forced path)
     (dict(num_req=2, hq=32, hkv=8, d=128, n_tree_max=40, n_query=8, prefix_range=(100, 400)), 2),      # expansion
     (dict(num_req=2, hq=8, hkv=2, d=64, n_tree_max=24, prefix_range=(0, 300), ragged_tree=True), 1),   # warp MMA
     (dict(num_req=1, hq=32, hkv=8, d=128, n_tree_max=32, prefix_range=(32000, 32768)), 2),             # far positions
+    (dict(num_req=2, hq=32, hkv=2, d=128, n_tree_max=8, prefix_range=(100, 900)), 2),                  # G = 16
+    (dict(num_req=2, hq=32, hkv=1, d=128, n_tree_max=4, prefix_range=(10, 700)), 2),                   # G = 32
+    (dict(num_req=2, hq=16, hkv=8, d=128, n_tree_max=20, prefix_range=(50, 500), ragged_tree=True), 2),  # G = 2
 ]
 
 
@@ -304,6 +307,37 @@ def test_rope_at_tree_positions_matches_oracle(cfg, theta):
     assert torch.equal(d["q"], q_before)   # the rotation goes to workspace scratch
     heads = list(range(0, case.num_q_heads, max(1, case.num_q_heads // 6)))
     check_attention(case, out, lse, A.attention_case(case, heads=heads), heads=heads)
+
+
+@pytest.mark.parametrize("cfg", [0, 4])
+def test_rope_error_against_the_unrounded_rotation(cfg, record_property):
+    """The effect of reading the rotated queries as bf16 operands: the GPU
+    output against the oracle with bf16-rounded rotated queries (the stated
+    reading) and against the oracle that keeps the fp64 rotation.  Both errors
+    are reported (as multiples of the tolerance) and both stay within it."""
+    import dataclasses
+    kw, path = ROPE[cfg]
+    case = dataclasses.replace(W.random_attn_case(300 + cfg, **kw), rope_theta=500000.0)
+    d = attn_inputs(case)
+    out, _ = ts.tree_attn_forward(d["q"], d["k_cache"], d["v_cache"], d["prefix_len"], d["n_tree"], d["parent"],
+                                  block_table=d.get("block_table"), force_path=path, rope_theta=500000.0)
+    torch.cuda.synchronize()
+    got = bf16_host_f64(out)
+    heads = list(range(0, case.num_q_heads, max(1, case.num_q_heads // 6)))
+    worst = {}
+    for name, rnd in (("rounded", True), ("unrounded", False)):
+        ref = A.attention_case(case, heads=heads, round_rotated_q=rnd)
+        w = 0.0
+        for b, (ro, _) in ref.items():
+            for h in heads:
+                e = np.abs(got[b][:, h, :] - ro[:, h, :]) / (ATOL + RTOL * np.abs(ro[:, h, :]))
+                w = max(w, float(e.max()))
+        worst[name] = w
+    record_property("tolerance_used_rounded", worst["rounded"])
+    record_property("tolerance_used_unrounded", worst["unrounded"])
+    print(f"rope cfg {cfg}: max error / tolerance = {worst['rounded']:.3f} (bf16-rounded rotated queries), "
+          f"{worst['unrounded']:.3f} (fp64 rotation)")
+    assert worst["rounded"] <= 1.0 and worst["unrounded"] <= 1.0
 
 
 def test_rope_changes_the_result_and_rejects_bad_bases():

@@ -17,6 +17,7 @@ import torch
 
 import workloads as W
 from oracle import stochastic as S
+from oracle import tree as T
 
 pytestmark = pytest.mark.gpu
 
@@ -61,9 +62,17 @@ def _walk(tl, dl, tokens, parent, n, temp, u_acc, u_bonus):
 BONUS_EPS = 1e-5   # fp32 prefix sums over up to ~1.5e5 probabilities
 
 
-def _case(seed, B, n_max, vocab, noise):
+def _case(seed, B, n_max, vocab, noise, plain=False):
     acc = W.random_accept_case(seed, num_req=B, n_tree_max=n_max, vocab=vocab, p_accept=0.8)
     rng = np.random.default_rng(seed + 1000)
+    if plain:   # N(0, 1) logits with no planted peak; draft tokens follow the oracle's argmax at rate 0.8
+        acc.logits[:] = rng.standard_normal(acc.logits.shape, dtype=np.float32)
+        for b in range(B):
+            n = int(acc.n_tree[b])
+            if n == 0:
+                continue
+            am = T.greedy_accept(acc.logits[b][:n], np.zeros(n, np.int32), acc.parent[b][:n], n).argmax
+            acc.tokens[b, :n] = W.draft_tokens(rng, acc.parent[b][:n], np.array(am, np.int32), vocab, 0.8)
     tl = acc.logits.astype(np.float32)
     dl = (tl + rng.normal(size=tl.shape) * noise).astype(np.float32)
     u_acc = rng.random((B, n_max)).astype(np.float32)
@@ -80,15 +89,17 @@ def _run_gpu(acc, tl, dl, u_acc, u_bonus, temp):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-@pytest.mark.parametrize("seed,B,n_max,vocab,noise,temp", [
-    (0, 6, 16, 1000, 0.3, 1.0),
-    (1, 4, 32, 152064, 0.5, 1.0),      # several vocab slices, 16-byte rows
-    (2, 5, 24, 1001, 0.2, 0.7),        # odd vocab (4-byte loads)
-    (3, 3, 64, 50000, 1.0, 1.5),       # a draft far from the target: many rejections
-    (4, 8, 8, 300, 0.05, 1.0),         # a draft close to the target: long paths
+@pytest.mark.parametrize("seed,B,n_max,vocab,noise,temp,plain", [
+    (0, 6, 16, 1000, 0.3, 1.0, False),
+    (1, 4, 32, 152064, 0.5, 1.0, False),      # several vocab slices, 16-byte rows
+    (2, 5, 24, 1001, 0.2, 0.7, False),        # odd vocab (4-byte loads)
+    (3, 3, 64, 50000, 1.0, 1.5, False),       # a draft far from the target: many rejections
+    (4, 8, 8, 300, 0.05, 1.0, False),         # a draft close to the target: long paths
+    (5, 4, 16, 128256, 0.3, 1.0, True),       # plain N(0, 1) logits, no planted peak
+    (6, 2, 32, 152064, 0.5, 0.8, True),
 ])
-def test_stochastic_acceptance_matches_oracle(seed, B, n_max, vocab, noise, temp):
-    acc, tl, dl, u_acc, u_bonus = _case(seed, B, n_max, vocab, noise)
+def test_stochastic_acceptance_matches_oracle(seed, B, n_max, vocab, noise, temp, plain):
+    acc, tl, dl, u_acc, u_bonus = _case(seed, B, n_max, vocab, noise, plain)
     got = _run_gpu(acc, tl, dl, u_acc, u_bonus, temp)
     compared = 0
     for b in range(B):

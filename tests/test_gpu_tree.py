@@ -82,6 +82,21 @@ def test_accept_argmax_ties_take_lowest_index():
     check_accept(case, run_accept(case))
 
 
+@pytest.mark.parametrize("vocab,B,n,p_acc", [(128256, 8, 16, 0.7), (152064, 4, 32, 0.8)])
+def test_accept_plain_normal_logits(vocab, B, n, p_acc):
+    """Logits drawn plainly from N(0, 1) at the workloads' vocab sizes, with no
+    planted peak: each row's maximum stands only a few tenths above the
+    runner-up.  Draft tokens follow the oracle's own argmax at rate p_acc."""
+    rng = np.random.default_rng(vocab + n)
+    logits = rng.standard_normal((B, n, vocab), dtype=np.float32)
+    parent = np.stack([W.random_parents(rng, n) for _ in range(B)]).astype(np.int32)
+    am = np.array([T.greedy_accept(logits[b], np.zeros(n, np.int32), parent[b], n).argmax for b in range(B)],
+                  np.int32)
+    tokens = np.stack([W.draft_tokens(rng, parent[b], am[b], vocab, p_acc) for b in range(B)]).astype(np.int32)
+    case = W.AcceptCase(B, n, vocab, np.full(B, n, np.int32), parent, tokens, logits, am)
+    check_accept(case, run_accept(case))
+
+
 def test_accept_fig2_target_verify():
     with open(os.path.join(GOLDEN, "fig2_walkthrough.json")) as f:
         g = json.load(f)["target_verify"]
