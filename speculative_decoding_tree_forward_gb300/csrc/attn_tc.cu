@@ -354,45 +354,6 @@ __device__ __forceinline__ int64_t wsched_begin(int c, const int64_t* cum, const
   return cum[b] + static_cast<int64_t>(uir) * tiles + j;
 }
 
-// RoPE of one packed row of a 128-row Q tile in shared memory (two 64-column
-// halves of 128-byte swizzled rows: 16-byte chunk cc of the first half holds
-// pairs 8 cc .. 8 cc + 7, their partners sit in the same chunk of the second
-// half).  The G consecutive lanes that hold one query node's G heads (G
-// divides 32, so they never straddle a warp) share the node's angles: lane g
-// of the group computes frequencies g, g + G, ... and the others take them by
-// shuffles, which cuts the sine/cosine work by G.  All 32 lanes take part;
-// only rows with `write` set are stored.
-template <int G>
-__device__ __forceinline__ void rope_row_shared(uint8_t* q0, int r, int lane, int pos, const uint64_t* turn,
-                                                bool write) {
-  constexpr int kPer = 64 / G;
-  const int g = lane % G, base = lane - g;
-  float cs[kPer], sn[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) rope_cos_sin(pos, turn[g + k * G], cs[k], sn[k]);
-#pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    uint4* pa = reinterpret_cast<uint4*>(q0 + sw128(r, cc));
-    uint4* pb = reinterpret_cast<uint4*>(q0 + TcLayout::kQBytes / 2 + sw128(r, cc));
-    uint4 va = *pa, vb = *pb;
-    __nv_bfloat16* a8 = reinterpret_cast<__nv_bfloat16*>(&va);
-    __nv_bfloat16* b8 = reinterpret_cast<__nv_bfloat16*>(&vb);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int j = 8 * cc + e;
-      const float c = __shfl_sync(0xffffffffu, cs[j / G], base + j % G);
-      const float sv = __shfl_sync(0xffffffffu, sn[j / G], base + j % G);
-      const float x0 = __bfloat162float(a8[e]), x1 = __bfloat162float(b8[e]);
-      a8[e] = __float2bfloat16_rn(x0 * c - x1 * sv);
-      b8[e] = __float2bfloat16_rn(x0 * sv + x1 * c);
-    }
-    if (write) {
-      *pa = va;
-      *pb = vb;
-    }
-  }
-}
-
 // Waits (bounded) for the last copy issued into each slot of a ring.
 __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued) {
   for (int st = 0; st < slots && st < issued; ++st) {
@@ -437,7 +398,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     for (int i = 0; i < Sh::kQBufs; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
-      mbar_init(&ctl->q_rot[i], 4);
+      mbar_init(&ctl->q_rot[i], 8);  // 8 warp arrivals: both warpgroups (first unit) or one, twice
     }
     for (int i = 0; i < 2; ++i) {
       for (int j = 0; j < 2; ++j) {
@@ -719,6 +680,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     int anc_req = -1;
     uint32_t anc[4] = {0, 0, 0, 0};
     float m_used = -INFINITY, l = 0.f;
+    if (p.rope) {
+      // RoPE of the CTA's first unit by both warpgroups (idle until the
+      // first S): each rotates half of the pairs of every packed row,
+      // thread r row r at position P + depth, once the queries land
+      for (int i = r; i < c.n; i += kRowsTc) {
+        int q = p.parent[static_cast<int64_t>(c.b) * p.n_tree_max + i];
+        if (q < -1 || q >= i) {
+          if (blockIdx.x == 0) report_error(p.err, TS_DEVERR_BAD_PARENT);
+          q = -1;
+        }
+        par[i] = q;
+      }
+      wg_sync(wg);
+      anc_req = c.b;
+      if (pipe_wait<kBounded>(&ctl->q_full[0], 0, p.wait_ns)) {
+        if (Sh::local_of(r) < p.rows) {
+          ancestor_walk(par, c.n - p.n_query + Sh::local_of(r) / p.group, anc);
+          const int pos = c.P + __popc(anc[0]) + __popc(anc[1]) + __popc(anc[2]) + __popc(anc[3]) - 1;
+#pragma unroll 1
+          for (int cc = 4 * wg; cc < 4 * wg + 4; ++cc) {
+            uint4* pa = reinterpret_cast<uint4*>(smem + L.q + sw128(r, cc));
+            uint4* pb = reinterpret_cast<uint4*>(smem + L.q + TcLayout::kQBytes / 2 + sw128(r, cc));
+            uint4 va = *pa, vb = *pb;
+            rope_rotate8(va, vb, pos, rope_turn, 8 * cc);
+            *pa = va;
+            *pb = vb;
+          }
+        }
+        fence_proxy_async_smem();  // the tensor cores read the rotated rows
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->q_rot[0]);
+      } else {
+        report_error(p.err, TS_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
     for (int k = 0; k < n_tiles; ++k) {
       const int sf = c.seg_first(k), sl = c.seg_last(k, n_tiles);
       if ((k & 1) == wg) {
@@ -744,12 +741,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
             for (int w = 0; w < 4; ++w) anc[w] = 0u;
           }
-          if (p.rope && k == sf) {
-            // RoPE: the owner of the unit's first tile rotates the unit's
-            // queries in shared memory once they land, each thread its own
-            // packed row at position P + depth (16-byte chunk cc of the two
-            // 64-column halves holds pairs 8 cc .. 8 cc + 7); the QK^T issuer
-            // waits for q_rot before the unit's first product
+          if (p.rope && k == sf && c.unit > 0) {
+            // RoPE of a later unit: the owner of the unit's first tile rotates
+            // the unit's queries in shared memory once they land, each thread
+            // its own packed row at position P + depth (16-byte chunk cc of the
+            // two 64-column halves holds pairs 8 cc .. 8 cc + 7); the QK^T
+            // issuer waits for q_rot before the unit's first product
             // Rotations run in unit order: first the previous unit's (whose
             // owner may be the other warpgroup).  That keeps each parity wait
             // below within one phase of its barrier even when this warpgroup
@@ -758,7 +755,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
             // before this unit's, and q_rot[qb] cannot run ahead of this
             // warpgroup, which rotates this unit.
             const int qb = c.unit % Sh::kQBufs;
-            if (c.unit > 0 && !pipe_wait<kBounded>(&ctl->q_rot[(c.unit - 1) % Sh::kQBufs],
+            if (!pipe_wait<kBounded>(&ctl->q_rot[(c.unit - 1) % Sh::kQBufs],
                                          ((c.unit - 1) / Sh::kQBufs) & 1, p.wait_ns)) {
               report_error(p.err, TS_DEVERR_TIMEOUT);
               *abort_flag = 1;
@@ -769,32 +766,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               *abort_flag = 1;
               break;
             }
-            {
-              const bool real = Sh::local_of(r) < p.rows;  // padding rows take part in the shuffles only
+            if (Sh::local_of(r) < p.rows) {
               const int pos = c.P + __popc(anc[0]) + __popc(anc[1]) + __popc(anc[2]) + __popc(anc[3]) - 1;
               uint8_t* q0 = smem + L.q + qb * TcLayout::kQBytes;
-              switch (p.group) {  // the G rows of one query node share its angles
-                case 4: rope_row_shared<4>(q0, r, lane, pos, rope_turn, real); break;
-                case 8: rope_row_shared<8>(q0, r, lane, pos, rope_turn, real); break;
-                case 16: rope_row_shared<16>(q0, r, lane, pos, rope_turn, real); break;
-                case 32: rope_row_shared<32>(q0, r, lane, pos, rope_turn, real); break;
-                default:
-                  if (real) {
 #pragma unroll 1
-                    for (int cc = 0; cc < 8; ++cc) {
-                      uint4* pa = reinterpret_cast<uint4*>(q0 + sw128(r, cc));
-                      uint4* pb = reinterpret_cast<uint4*>(q0 + TcLayout::kQBytes / 2 + sw128(r, cc));
-                      uint4 va = *pa, vb = *pb;
-                      rope_rotate8(va, vb, pos, rope_turn, 8 * cc);
-                      *pa = va;
-                      *pb = vb;
-                    }
-                  }
+              for (int cc = 0; cc < 8; ++cc) {
+                uint4* pa = reinterpret_cast<uint4*>(q0 + sw128(r, cc));
+                uint4* pb = reinterpret_cast<uint4*>(q0 + TcLayout::kQBytes / 2 + sw128(r, cc));
+                uint4 va = *pa, vb = *pb;
+                rope_rotate8(va, vb, pos, rope_turn, 8 * cc);
+                *pa = va;
+                *pb = vb;
               }
             }
             fence_proxy_async_smem();  // the tensor cores read the rotated rows
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->q_rot[qb]);
+            if (lane == 0) mbar_arrive_cnt(&ctl->q_rot[qb], 2);  // one warpgroup stands for both
           }
           m_used = -INFINITY;
           l = 0.f;
