@@ -22,7 +22,7 @@
 // rows in flight for the same registers, so a grid of many rows lands in
 // one wave instead of two).  The tcgen05 kernel's partials are column-blocked
 // (float4 j of row r at (slot * 32 + j) * 128 + r) and merged with one thread
-// per (row, 16 columns).
+// per (row, 16 columns, group of shares).
 #include "attn_common.cuh"
 
 namespace ts {
@@ -309,32 +309,41 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) merge_row_per_half_warp_k
 
 
 // tcgen05 layout: float4 j of row r of slot s at (s * 32 + j) * 128 + r, so
-// a warp's 32 consecutive rows read 512 contiguous bytes.  Grid (units, 4),
-// 256 threads: thread t merges row t % 128 of the unit over 16 columns
-// (column block 2 * blockIdx.y + t / 128).  The lse and the partial columns
-// of a row's first kPrefetchTc shares are all requested before the weights
-// are known, so a row with that many shares costs one round trip to L2.
+// a warp's 32 consecutive rows read 512 contiguous bytes.  A warp takes a
+// block of 32 rows x 16 columns of a unit and one of S share groups (the
+// unit's shares g, g + S, g + 2 S, ...): it requests the lse and partial
+// columns of kPrefetchTc of its shares at a time, before their weights are
+// known, and folds each batch in with a running max.  With S > 1 the S warps
+// of a block combine their sums through shared memory.  S grows with the
+// shares a unit has on average, so a unit split across many CTAs costs about
+// as many round trips to L2 as one split across a few.  Grid (units, 4 S),
+// 256 threads: 8 / S blocks per CTA.
 constexpr int kPrefetchTc = 4;
+constexpr int kMaxShareGroups = 8;
 
 __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int S = static_cast<int>(gridDim.y) / 4;  // share groups: 1, 2, 4 or 8
   const int64_t unit = blockIdx.x;
   const int units_per_req = p.hkv / p.hp;  // one row group per unit on this path
   const int b = static_cast<int>(blockIdx.x) / units_per_req;
   const int uir = static_cast<int>(blockIdx.x) % units_per_req;
-  const int r = t & (kMaxRowsPerUnit - 1);
-  const int cb = 2 * static_cast<int>(blockIdx.y) + (t >> 7);  // 16 columns: float4 4 cb .. 4 cb + 3
+  const int blk = static_cast<int>(blockIdx.y) * (8 / S) + warp / S;  // 0..31
+  const int g = warp % S;
+  const int cb = blk >> 2;                 // 16 columns: float4 4 cb .. 4 cb + 3
+  const int r = (blk & 3) * 32 + lane;     // row of the 128-row tile
   const int hj = p.hp == 2 ? r >> 6 : 0, loc = p.hp == 2 ? r & 63 : r;
   __shared__ UnitSplit s_sp;
   __shared__ unsigned s_hold;
+  __shared__ float xch[8][18][32];  // per warp: max, sum, 16 columns; lane-minor
   if (warp == 0) merge_split(p, b, uir, units_per_req, lane, &s_sp, &s_hold);
   __syncthreads();
   const int c_lo = s_sp.c_lo, c_hi = s_sp.c_hi;
   const unsigned hold = s_hold;
   pdl_wait();
   pdl_launch_dependents();
-  // padding row, or one CTA held the whole unit and wrote it
-  if (loc >= p.rows || c_lo == c_hi) return;
+  if (c_lo == c_hi) return;  // one CTA held the whole unit and wrote it
+  const bool row_ok = loc < p.rows;  // else a padding row of the tile
   auto held = [&](int c) -> bool { return c - c_lo < 32 ? ((hold >> (c - c_lo)) & 1u) != 0 : s_sp.holds(c); };
   const float* lse_col = p.part_lse + unit * kMaxRowsPerUnit + r;
   const float4* o_col = reinterpret_cast<const float4*>(p.part_o) + unit * (32 * kMaxRowsPerUnit) +
@@ -342,54 +351,92 @@ __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   auto lse_of = [&](int c) { return __ldcg(lse_col + static_cast<int64_t>(c) * kMaxRowsPerUnit); };
   auto o_of = [&](int c, int j) { return __ldcg(o_col + (static_cast<int64_t>(c) * 32 + j) * kMaxRowsPerUnit); };
 
-  float lx[kPrefetchTc];
-  float4 x[kPrefetchTc][4];
-#pragma unroll
-  for (int q = 0; q < kPrefetchTc; ++q) {
-    lx[q] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c_lo + q <= c_hi && ((hold >> q) & 1u)) {
-      lx[q] = lse_of(c_lo + q);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) x[q][j] = o_of(c_lo + q, j);
-    }
-  }
-  float mx = -INFINITY;
-#pragma unroll
-  for (int q = 0; q < kPrefetchTc; ++q) mx = fmaxf(mx, lx[q]);
-  for (int c = c_lo + kPrefetchTc; c <= c_hi; ++c)
-    if (held(c)) mx = fmaxf(mx, lse_of(c));
-  const float mb = (mx == -INFINITY) ? 0.f : mx;
+  float m = -INFINITY, ws = 0.f;
   float4 acc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float ws = 0.f;
+  if (row_ok) {
+    for (int c0 = c_lo + g; c0 <= c_hi; c0 += kPrefetchTc * S) {
+      float lx[kPrefetchTc];
+      float4 x[kPrefetchTc][4];
 #pragma unroll
-  for (int q = 0; q < kPrefetchTc; ++q) {
-    const float w = exp2f(lx[q] - mb);  // 0 for shares that are not held (lse -inf)
-    ws += w;
+      for (int q = 0; q < kPrefetchTc; ++q) {
+        const int c = c0 + q * S;
+        lx[q] = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j].x += w * x[q][j].x;
-      acc[j].y += w * x[q][j].y;
-      acc[j].z += w * x[q][j].z;
-      acc[j].w += w * x[q][j].w;
+        for (int j = 0; j < 4; ++j) x[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c <= c_hi && held(c)) {
+          lx[q] = lse_of(c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) x[q][j] = o_of(c, j);
+        }
+      }
+      float rm = lx[0];
+#pragma unroll
+      for (int q = 1; q < kPrefetchTc; ++q) rm = fmaxf(rm, lx[q]);
+      if (rm > m) {  // rescale what is summed so far (nothing yet: m = -inf gives 0)
+        const float sc = exp2f(m - rm);
+        ws *= sc;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[j].x *= sc;
+          acc[j].y *= sc;
+          acc[j].z *= sc;
+          acc[j].w *= sc;
+        }
+        m = rm;
+      }
+      const float mb = m == -INFINITY ? 0.f : m;
+#pragma unroll
+      for (int q = 0; q < kPrefetchTc; ++q) {
+        const float w = exp2f(lx[q] - mb);  // 0 for shares that are not held (lse -inf)
+        ws += w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[j].x += w * x[q][j].x;
+          acc[j].y += w * x[q][j].y;
+          acc[j].z += w * x[q][j].z;
+          acc[j].w += w * x[q][j].w;
+        }
+      }
     }
   }
-  for (int c = c_lo + kPrefetchTc; c <= c_hi; ++c) {  // more shares: one round trip each
-    if (!held(c)) continue;
-    const float w = exp2f(lse_of(c) - mb);
-    ws += w;
+  if (S > 1) {  // CTA-uniform
+    xch[warp][0][lane] = m;
+    xch[warp][1][lane] = ws;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float4 y = o_of(c, j);
-      acc[j].x += w * y.x;
-      acc[j].y += w * y.y;
-      acc[j].z += w * y.z;
-      acc[j].w += w * y.w;
+      xch[warp][2 + 4 * j][lane] = acc[j].x;
+      xch[warp][3 + 4 * j][lane] = acc[j].y;
+      xch[warp][4 + 4 * j][lane] = acc[j].z;
+      xch[warp][5 + 4 * j][lane] = acc[j].w;
+    }
+    __syncthreads();
+    if (g != 0) return;
+    for (int o = 1; o < S; ++o) {
+      const float om = xch[warp + o][0][lane], ow = xch[warp + o][1][lane];
+      float sa, sb;  // scales of this warp's sums and of the other's
+      if (om > m) {
+        sa = exp2f(m - om);
+        sb = 1.f;
+        m = om;
+      } else if (om != -INFINITY) {
+        sa = 1.f;
+        sb = exp2f(om - m);
+      } else {
+        continue;
+      }
+      ws = ws * sa + ow * sb;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j].x = acc[j].x * sa + xch[warp + o][2 + 4 * j][lane] * sb;
+        acc[j].y = acc[j].y * sa + xch[warp + o][3 + 4 * j][lane] * sb;
+        acc[j].z = acc[j].z * sa + xch[warp + o][4 + 4 * j][lane] * sb;
+        acc[j].w = acc[j].w * sa + xch[warp + o][5 + 4 * j][lane] * sb;
+      }
     }
   }
+  if (!row_ok) return;
   const float inv = ws > 0.f ? __frcp_rn(ws) : 0.f;
   const int i = loc / p.group, h = (p.hp * uir + hj) * p.group + loc % p.group;
   uint4* dst = reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(b) * p.n_query + i) * p.hq + h) * 128 + 16 * cb);
@@ -398,14 +445,21 @@ __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   dst[1] = make_uint4(pack_bf16x2(acc[2].x * inv, acc[2].y * inv), pack_bf16x2(acc[2].z * inv, acc[2].w * inv),
                       pack_bf16x2(acc[3].x * inv, acc[3].y * inv), pack_bf16x2(acc[3].z * inv, acc[3].w * inv));
   if (p.lse != nullptr && cb == 0)
-    p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (mb + log2f(ws)) * 0.69314718055994530942f;
+    p.lse[(static_cast<int64_t>(b) * p.hq + h) * p.n_query + i] = (m + log2f(ws)) * 0.69314718055994530942f;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_merge(const AttnParams& p, bool tc_layout, cudaStream_t stream) {
-  if (tc_layout)
-    return launch_pdl(merge_tc_kernel, dim3(static_cast<unsigned>(p.num_units), 4), dim3(256), 0, stream, p);
+  if (tc_layout) {
+    // share groups: enough that kPrefetchTc shares per warp cover a unit's
+    // average share count (its CTAs plus one at a boundary)
+    const int64_t shares = (p.num_ctas + p.num_units - 1) / p.num_units + 1;
+    int groups = 1;
+    while (groups < kMaxShareGroups && static_cast<int64_t>(groups) * kPrefetchTc < shares) groups *= 2;
+    return launch_pdl(merge_tc_kernel, dim3(static_cast<unsigned>(p.num_units), 4 * groups), dim3(256), 0, stream,
+                      p);
+  }
   if (p.merge_half_warp) {
     const int row_blocks = (p.rows_pad + kRowsPerCtaHalf - 1) / kRowsPerCtaHalf;
     return launch_pdl(merge_row_per_half_warp_kernel, dim3(static_cast<unsigned>(p.num_units), row_blocks),

@@ -8,17 +8,22 @@
 // queue); Figure 2 (w nodes per expansion).
 //
 // Kernel 1 (candidates) streams the draft logits of the queried nodes once:
-// each CTA takes a vocab slice of one row with 16-byte loads and keeps, per
-// thread, an online log-sum-exp and a sorted list of its largest logits
-// (ties: lower token; 8 or 16 long, the smallest that holds k); the block
-// merges the lists (one warp arg-max over list heads per entry) and writes
-// one partial per (row, slice).  Per batch of eight 16-byte loads the
-// log-sum-exp takes the batch max first, so its exponentials are independent.
-// Kernel 2 (step) runs one CTA per request: it merges a row's partials into
-// the node's k candidates (value = logit - log-sum-exp), then makes the w
-// picks of the step, each a block-wide arg-max over the nodes' next
-// candidates.  Kernel 3 (select) ranks the nodes by weight and keeps the top
-// bs in index order.
+// each CTA takes a vocab slice of one row in batches of 32 values per thread
+// (eight 16-byte loads issued together), keeps an online log-sum-exp, and
+// selects the slice's k largest logits (ties: lower token) without sorted
+// lists: per batch, the k-th largest of a warp's 32 per-thread maxima bounds
+// the warp's k-th largest value from below, so only values at or above that
+// running bound (a few dozen per CTA on random logits) go to a shared-memory
+// list; the CTA's k best are those whose rank among the listed entries (the
+// count of entries ahead of them) is below k.  A CTA whose list overflows
+// (heavy ties) takes its k best in k rounds of block arg-max instead.
+// Kernel 2 (step) runs one CTA per request.  It loads the tree state before
+// waiting for kernel 1, then each warp merges one queried row: the k-th entry
+// of any slice bounds the row's k-th largest, so only the entries at or above
+// the largest such bound are ranked (the row's log-sum-exp from the slices'
+// pairs).  Warp 0 then makes the w picks of the step, each a warp arg-max
+// over the nodes' next candidates (four nodes per lane).  Kernel 3 (select)
+// ranks the nodes by weight and keeps the top bs in index order.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,67 +31,48 @@ namespace ts {
 namespace {
 
 constexpr int kCandThreads = 256;
+constexpr int kCandWarps = kCandThreads / 32;
+constexpr int kBatch = 32;        // values per thread per batch
+constexpr int kCandCap = 512;     // listed candidates per CTA
 constexpr int K = TS_MAX_EXPAND;  // candidate slots stored per (row, slice) and per node
 
 // (value, index) order of the candidate lists: larger value first, then the
 // lower index
 __device__ __forceinline__ bool ahead(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-// Inserts (x, i) into a list sorted by `ahead`; x arrives with the largest
-// index seen so far, so an equal value stays behind the entries present.
-template <int KL>
-__device__ __forceinline__ void list_insert(float (&val)[KL], int (&idx)[KL], float x, int i) {
-  if (!(x > val[KL - 1])) return;
-  float cv = x;
-  int ci = i;
+// The warp's 32 values in decreasing order (lane j holds the (j+1)-th
+// largest): a bitonic sorting network over shuffles.
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
 #pragma unroll
-  for (int j = 0; j < KL; ++j) {
-    if (cv > val[j]) {
-      const float tv = val[j];
-      const int ti = idx[j];
-      val[j] = cv;
-      idx[j] = ci;
-      cv = tv;
-      ci = ti;
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, j);
+      v = (((lane & j) == 0) == ((lane & k) == 0)) ? fmaxf(v, o) : fminf(v, o);
     }
-  }
+  return v;
 }
 
-// Drops the head of a sorted list (the next entry becomes the head).
-template <int KL>
-__device__ __forceinline__ void list_pop(float (&val)[KL], int (&idx)[KL]) {
+// Inclusive prefix sum over the warp.
+__device__ __forceinline__ int warp_incl_scan(int c, int lane) {
 #pragma unroll
-  for (int j = 0; j < KL - 1; ++j) {
-    val[j] = val[j + 1];
-    idx[j] = idx[j + 1];
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, c, o);
+    if (lane >= o) c += t;
   }
-  val[KL - 1] = -INFINITY;
-  idx[KL - 1] = INT32_MAX;
+  return c;
 }
 
-// Merges the lanes' sorted lists: round j's winner (the best head over the
-// warp) goes to (out_v[j], out_i[j]) on every lane, and its lane pops it.
-template <int KL>
-__device__ __forceinline__ void warp_merge(float (&val)[KL], int (&idx)[KL], float (&out_v)[KL], int (&out_i)[KL]) {
-  const int lane = threadIdx.x & 31;
+// Warp arg-max in `ahead` order; every lane gets the winner.
+__device__ __forceinline__ void warp_best(float& bv, int& bi) {
 #pragma unroll
-  for (int j = 0; j < KL; ++j) {
-    float bv = val[0];
-    int bi = idx[0], bl = lane;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      if (ahead(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-        bl = ol;
-      }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ahead(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
     }
-    out_v[j] = bv;
-    out_i[j] = bi;
-    if (lane == bl) list_pop(val, idx);
   }
 }
 
@@ -105,7 +91,7 @@ __device__ __forceinline__ int clamp_n(const ExpandParams& p, int b) {
   return min(max(p.n_tree[b], 0), p.n_tree_max);
 }
 
-template <int KL>  // list length: the smallest of 8, 16 that holds k
+template <int KL>  // slots written per partial: the smallest of 8, 16 that holds k
 __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const ExpandParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -113,159 +99,209 @@ __global__ void __launch_bounds__(kCandThreads) cand_partial_kernel(const Expand
   const int b = row / p.w;
   const int u = p.rows[row];
   if (u < 0 || u >= clamp_n(p, b)) return;  // not a queried node: the step kernel skips the row too
-  const int64_t v0 = static_cast<int64_t>(blockIdx.y) * p.slice;
-  const int64_t v1 = min(static_cast<int64_t>(p.vocab), v0 + p.slice);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int v0 = blockIdx.y * p.slice;
+  const int v1 = min(p.vocab, v0 + p.slice);
   const float* lg = p.logits + static_cast<int64_t>(row) * p.vocab;
-  float m = -INFINITY, s = 0.f;
-  float val[KL];
-  int idx[KL];
-#pragma unroll
-  for (int j = 0; j < KL; ++j) {
-    val[j] = -INFINITY;
-    idx[j] = INT32_MAX;
+  CandPartial* out = p.part + static_cast<int64_t>(row) * p.num_slices + blockIdx.y;
+  __shared__ int2 cand[kCandCap];  // (value bits, token)
+  __shared__ int cnt_s;
+  __shared__ float wb[kCandWarps], wm[kCandWarps], wsum[kCandWarps];
+  __shared__ float red_v[kCandWarps];
+  __shared__ int red_i[kCandWarps];
+  if (tid == 0) cnt_s = 0;
+  if (tid < KL) {  // slots the ranks below do not fill (a slice shorter than k)
+    out->val[tid] = -INFINITY;
+    out->idx[tid] = INT32_MAX;
   }
-  auto push = [&](float x, int i) {
-    if (x > m) {
-      s = s * __expf(m - x) + 1.f;
-      m = x;
-    } else {
-      s += __expf(x - m);
-    }
-    list_insert<KL>(val, idx, x, i);
-  };
-  if ((p.vocab & 3) == 0) {  // 16-byte rows: slices are multiples of 1024 floats
-    // eight 16-byte loads in flight per thread, issued before any of them is
-    // consumed (the insertions branch)
-    constexpr int kLoads = 8;
-    const float4* lg4 = reinterpret_cast<const float4*>(lg);
-    const int64_t e4 = v1 / 4;
-    for (int64_t x0 = v0 / 4 + threadIdx.x; x0 < e4; x0 += kLoads * kCandThreads) {
-      float4 f[kLoads];
+  __syncthreads();
+  float m = -INFINITY, s = 0.f;
+  float bound = -INFINITY;  // warp-uniform: at most the warp's k-th largest value so far
+  const bool vec = (p.vocab & 3) == 0;  // 16-byte rows; slices are multiples of 1024 floats
+  for (int base = v0; base < v1; base += kBatch * kCandThreads) {
+    float x[kBatch];
+    int xi[kBatch];  // token, -1 past the slice
+    if (vec) {
 #pragma unroll
-      for (int q = 0; q < kLoads; ++q)
-        f[q] = x0 + q * kCandThreads < e4 ? __ldcs(lg4 + x0 + q * kCandThreads)
-                                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      // log-sum-exp of the batch: its max first, then independent exponentials
-      float bm = m;
+      for (int q = 0; q < kBatch / 4; ++q) {
+        const int t = base + 4 * (q * kCandThreads + tid);
+        const float4 f = t < v1 ? __ldcs(reinterpret_cast<const float4*>(lg + t))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        x[4 * q] = f.x;
+        x[4 * q + 1] = f.y;
+        x[4 * q + 2] = f.z;
+        x[4 * q + 3] = f.w;
 #pragma unroll
-      for (int q = 0; q < kLoads; ++q) bm = fmaxf(bm, fmaxf(fmaxf(f[q].x, f[q].y), fmaxf(f[q].z, f[q].w)));
-      if (bm > m) {
-        s *= __expf(m - bm);
-        m = bm;
+        for (int e = 0; e < 4; ++e) xi[4 * q + e] = t < v1 ? t + e : -1;
       }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int t = base + q * kCandThreads + tid;
+        x[q] = t < v1 ? __ldcs(lg + t) : -INFINITY;
+        xi[q] = t < v1 ? t : -1;
+      }
+    }
+    // log-sum-exp: the batch max first, then independent exponentials
+    float bm = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) bm = fmaxf(bm, x[q]);
+    const float lane_max = bm;
+    if (bm > m) {
+      s *= __expf(m - bm);
+      m = bm;
+    }
+    if (m > -INFINITY) {
       float es[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < kLoads; ++q) {
-        es[0] += __expf(f[q].x - m);   // -inf (past the slice) gives 0
-        es[1] += __expf(f[q].y - m);
-        es[2] += __expf(f[q].z - m);
-        es[3] += __expf(f[q].w - m);
-      }
+      for (int q = 0; q < kBatch; ++q) es[q & 3] += __expf(x[q] - m);  // -inf (past the slice) gives 0
       s += (es[0] + es[1]) + (es[2] + es[3]);
-#pragma unroll
-      for (int q = 0; q < kLoads; ++q) {
-        if (x0 + q * kCandThreads >= e4) break;
-        const int i = static_cast<int>((x0 + q * kCandThreads) * 4);
-        list_insert<KL>(val, idx, f[q].x, i);
-        list_insert<KL>(val, idx, f[q].y, i + 1);
-        list_insert<KL>(val, idx, f[q].z, i + 2);
-        list_insert<KL>(val, idx, f[q].w, i + 3);
-      }
     }
-  } else {
-    for (int64_t x = v0 + threadIdx.x; x < v1; x += kCandThreads) push(__ldcs(lg + x), static_cast<int>(x));
+    // the k-th largest lane maximum: k lanes hold a value at least that large
+    bound = fmaxf(bound, __shfl_sync(0xffffffffu, warp_sort_desc(lane_max, lane), p.k - 1));
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) c += (xi[q] >= 0 && x[q] >= bound) ? 1 : 0;
+    if (__any_sync(0xffffffffu, c > 0)) {
+      const int incl = warp_incl_scan(c, lane);
+      int pos = 0;
+      if (lane == 31) pos = atomicAdd(&cnt_s, incl);
+      pos = __shfl_sync(0xffffffffu, pos, 31) + incl - c;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q)
+        if (xi[q] >= 0 && x[q] >= bound) {
+          if (pos < kCandCap) cand[pos] = make_int2(__float_as_int(x[q]), xi[q]);
+          ++pos;
+        }
+    }
   }
-  // block: (m, s) by shuffles + shared memory; lists warp by warp, then warp 0
-  __shared__ float wm[kCandThreads / 32], wsum[kCandThreads / 32];
-  __shared__ float wv[kCandThreads / 32][KL];
-  __shared__ int wi[kCandThreads / 32][KL];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-  float tv[KL];
-  int ti[KL];
-  warp_merge<KL>(val, idx, tv, ti);
   if (lane == 0) {
     wm[warp] = m;
     wsum[warp] = s;
-#pragma unroll
-    for (int j = 0; j < KL; ++j) {
-      wv[warp][j] = tv[j];
-      wi[warp][j] = ti[j];
-    }
+    wb[warp] = bound;
   }
   __syncthreads();
-  if (warp == 0) {
-    float bm = -INFINITY, bs = 0.f;
+  if (tid == 0) {
+    float bm = wm[0], bs = wsum[0];
 #pragma unroll
-    for (int j = 0; j < KL; ++j) {
-      val[j] = -INFINITY;
-      idx[j] = INT32_MAX;
-    }
-    if (lane < kCandThreads / 32) {
-      bm = wm[lane];
-      bs = wsum[lane];
+    for (int q = 1; q < kCandWarps; ++q) lse_combine(bm, bs, wm[q], wsum[q]);
+    out->m = bm;
+    out->s = bs;
+  }
+  const int n_c = cnt_s;
+  if (n_c <= kCandCap) {
+    // Every value at or above the largest warp bound B is listed (no warp's
+    // bound ever exceeded B), and at least k are: an entry below B is not
+    // among the k best.  The rank of an entry at or above B is the number of
+    // listed entries ahead of it.
+    float bb = wb[0];
 #pragma unroll
-      for (int j = 0; j < KL; ++j) {
-        val[j] = wv[lane][j];
-        idx[j] = wi[lane][j];
+    for (int q = 1; q < kCandWarps; ++q) bb = fmaxf(bb, wb[q]);
+    for (int e = tid; e < n_c; e += kCandThreads) {
+      const int2 me = cand[e];
+      const float v = __int_as_float(me.x);
+      if (v < bb) continue;
+      int rank = 0;
+      for (int j = 0; j < n_c; ++j) {
+        const int2 o = cand[j];
+        rank += ahead(__int_as_float(o.x), o.y, v, me.y) ? 1 : 0;
+      }
+      if (rank < p.k) {
+        out->val[rank] = v;
+        out->idx[rank] = me.y;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      lse_combine(bm, bs, __shfl_xor_sync(0xffffffffu, bm, o), __shfl_xor_sync(0xffffffffu, bs, o));
-    warp_merge<KL>(val, idx, tv, ti);
-    if (lane == 0) {
-      CandPartial* out = p.part + static_cast<int64_t>(row) * p.num_slices + blockIdx.y;
-      out->m = bm;
-      out->s = bs;
-#pragma unroll
-      for (int j = 0; j < KL; ++j) {
-        out->val[j] = tv[j];
-        out->idx[j] = ti[j];
+  } else {
+    // heavy ties: k rounds, each the best value behind the previous winner
+    float pv = INFINITY;
+    int pi = -1;
+    for (int r = 0; r < p.k; ++r) {
+      float bv = -INFINITY;
+      int bi = INT32_MAX;
+      for (int t = v0 + tid; t < v1; t += kCandThreads) {
+        const float x = lg[t];
+        if (ahead(pv, pi, x, t) && ahead(x, t, bv, bi)) {
+          bv = x;
+          bi = t;
+        }
       }
+      warp_best(bv, bi);
+      if (lane == 0) {
+        red_v[warp] = bv;
+        red_i[warp] = bi;
+      }
+      __syncthreads();
+      bv = red_v[0];
+      bi = red_i[0];
+#pragma unroll
+      for (int q = 1; q < kCandWarps; ++q)
+        if (ahead(red_v[q], red_i[q], bv, bi)) {
+          bv = red_v[q];
+          bi = red_i[q];
+        }
+      __syncthreads();  // red_* is rewritten next round
+      if (bi == INT32_MAX) break;
+      if (tid == 0) {
+        out->val[r] = bv;
+        out->idx[r] = bi;
+      }
+      pv = bv;
+      pi = bi;
     }
   }
 }
 
-constexpr int kStepThreads = 2 * TS_MAX_TREE;  // thread i < n owns node i; warp r merges row r
+constexpr int kStepThreads = 256;  // 8 warps: one queried row each, then warp 0 picks
+constexpr int kMaxSlices = 16;     // candidate slices per row
 
 template <int KL>
 __global__ void __launch_bounds__(kStepThreads) expand_step_kernel(const ExpandParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t nb = static_cast<int64_t>(b) * p.n_tree_max;
   __shared__ float c_lp[TS_MAX_TREE][KL];
   __shared__ int c_tok[TS_MAX_TREE][KL];
+  __shared__ float w_s[TS_MAX_TREE];
+  __shared__ int taken_s[TS_MAX_TREE];
+  __shared__ int queried_s[TS_MAX_TREE];
   __shared__ int rows_s[K];
-  __shared__ float red_v[kStepThreads / 32];
-  __shared__ int red_i[kStepThreads / 32];
-  int n = p.n_tree[b];
+  __shared__ int2 mbuf[kStepThreads / 32][kMaxSlices * K];
+  __shared__ int n_out;
+  // The tree state is final before this kernel starts: only the step kernels
+  // write it, and the candidate pass launched between them triggers this
+  // kernel only after its own wait for the kernel before it.  Loads bypass L1.
+  int n = __ldcg(p.n_tree + b);
   if (n < 0 || n > p.n_tree_max) {
     if (tid == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
     n = min(max(n, 0), p.n_tree_max);
   }
-  if (tid < p.w) rows_s[tid] = p.rows[static_cast<int64_t>(b) * p.w + tid];
-  // each node's candidates as they stand (rows queried now are replaced below)
-  int taken = p.k;
-  const float my_w = tid < n ? p.weight[nb + tid] : 0.f;
-  if (tid < n) {
-    taken = min(max(p.cand_taken[nb + tid], 0), p.k);
-    float lp[KL];
-    int tk[KL];
+  if (tid < p.w) rows_s[tid] = __ldcg(p.rows + static_cast<int64_t>(b) * p.w + tid);
+  if (tid < TS_MAX_TREE) {
+    const int u = tid;
+    queried_s[u] = 0;
+    w_s[u] = u < n ? __ldcg(p.weight + nb + u) : -INFINITY;
+    taken_s[u] = u < n ? min(max(__ldcg(p.cand_taken + nb + u), 0), p.k) : p.k;
+    if (u < n) {
+      float lp[KL];
 #pragma unroll
-    for (int j = 0; j < KL; ++j) {  // issued together
-      lp[j] = j < p.k ? p.cand_lp[(nb + tid) * p.k + j] : -INFINITY;
-      tk[j] = j < p.k ? p.cand_tok[(nb + tid) * p.k + j] : -1;
+      for (int j = 0; j < KL; ++j) lp[j] = j < p.k ? __ldcg(p.cand_lp + (nb + u) * p.k + j) : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < KL; ++j) c_lp[u][j] = lp[j];
     }
+  } else {
+    const int u = tid - TS_MAX_TREE;
+    if (u < n) {
+      int tk[KL];
 #pragma unroll
-    for (int j = 0; j < KL; ++j) {
-      c_lp[tid][j] = lp[j];
-      c_tok[tid][j] = tk[j];
+      for (int j = 0; j < KL; ++j) tk[j] = j < p.k ? __ldcg(p.cand_tok + (nb + u) * p.k + j) : -1;
+#pragma unroll
+      for (int j = 0; j < KL; ++j) c_tok[u][j] = tk[j];
     }
   }
+  pdl_launch_dependents();
+  pdl_wait();  // the candidate partials
   __syncthreads();
   // ---- 1. the queried rows: merge the slices into k candidates (warp per row)
   for (int r = warp; r < p.w; r += kStepThreads / 32) {
@@ -284,99 +320,117 @@ __global__ void __launch_bounds__(kStepThreads) expand_step_kernel(const ExpandP
       val[j] = -INFINITY;
       idx[j] = INT32_MAX;
     }
-    if (lane < p.num_slices) {  // num_slices <= 32
+    if (lane < p.num_slices) {
       m = part[lane].m;
       s = part[lane].s;
 #pragma unroll
-      for (int j = 0; j < KL; ++j) {
-        val[j] = part[lane].val[j];
-        idx[j] = part[lane].idx[j];
-      }
+      for (int j = 0; j < KL; ++j)
+        if (j < p.k) {
+          val[j] = part[lane].val[j];
+          idx[j] = part[lane].idx[j];
+        }
+    }
+    if (lane < p.k) {
+      c_lp[u][lane] = -INFINITY;
+      c_tok[u][lane] = -1;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
     const float lse = m + logf(s);
-    float tv[KL];
-    int ti[KL];
-    warp_merge<KL>(val, idx, tv, ti);
-    if (lane < p.k) {
-      float v = -INFINITY;
-      int t = -1;
+    // a slice's k-th entry bounds the row's k-th largest from below; only a
+    // slice's first k entries can be among the row's k best
+    float kth = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < KL; ++j)
-        if (j == lane) {
-          v = tv[j];
-          t = ti[j];
-        }
-      const bool real = t != INT32_MAX && v != -INFINITY;
-      c_lp[u][lane] = real ? v - lse : -INFINITY;
-      c_tok[u][lane] = real ? t : -1;
-    }
-  }
-  __syncthreads();
-  for (int r = 0; r < p.w; ++r)
-    if (rows_s[r] == tid && tid < n) taken = 0;
-  // ---- 2. the picks: each node offers its next candidate
-  float key = (tid < n && taken < p.k && c_tok[tid][taken] >= 0) ? my_w + c_lp[tid][taken] : -INFINITY;
-  int added = 0;
-  for (int j = 0; j < p.w; ++j) {
-    if (n >= p.n_tree_max) break;  // uniform: n is the same in every thread
-    float bv = key;
-    int bi = tid;
+    for (int j = 0; j < KL; ++j)
+      if (j == p.k - 1) kth = val[j];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ahead(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
+    for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < KL; ++j) c += (j < p.k && idx[j] != INT32_MAX && val[j] >= kth) ? 1 : 0;
+    const int incl = warp_incl_scan(c, lane);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = incl - c;
+#pragma unroll
+    for (int j = 0; j < KL; ++j)
+      if (j < p.k && idx[j] != INT32_MAX && val[j] >= kth) mbuf[warp][pos++] = make_int2(__float_as_int(val[j]), idx[j]);
+    __syncwarp();
+    for (int e = lane; e < total; e += 32) {
+      const int2 me = mbuf[warp][e];
+      const float v = __int_as_float(me.x);
+      int rank = 0;
+      for (int j = 0; j < total; ++j) {
+        const int2 o = mbuf[warp][j];
+        rank += ahead(__int_as_float(o.x), o.y, v, me.y) ? 1 : 0;
+      }
+      if (rank < p.k && v != -INFINITY) {
+        c_lp[u][rank] = v - lse;
+        c_tok[u][rank] = me.y;
       }
     }
     if (lane == 0) {
-      red_v[warp] = bv;
-      red_i[warp] = bi;
+      taken_s[u] = 0;
+      queried_s[u] = 1;
     }
-    __syncthreads();
-    bv = red_v[0];
-    bi = red_i[0];
-#pragma unroll
-    for (int q = 1; q < kStepThreads / 32; ++q)
-      if (ahead(red_v[q], red_i[q], bv, bi)) {
-        bv = red_v[q];
-        bi = red_i[q];
-      }
-    __syncthreads();  // red_* is rewritten next round
-    if (bv == -INFINITY) break;
-    const int nn = n;  // the new node
-    if (tid == bi) {
-      p.parent[nb + nn] = bi;
-      p.tokens[nb + nn] = c_tok[bi][taken];
-      p.weight[nb + nn] = bv;
-      p.cand_taken[nb + nn] = p.k;
-      p.added[static_cast<int64_t>(b) * p.w + j] = nn;
-      ++taken;
-      key = (taken < p.k && c_tok[tid][taken] >= 0) ? my_w + c_lp[tid][taken] : -INFINITY;
-    }
-    if (tid == nn) {  // no candidates until its logits come
-      taken = p.k;
-      key = -INFINITY;
-    }
-    ++n;
-    ++added;
+    __syncwarp();  // mbuf is reused by the warp's next row
   }
-  if (tid < p.w && tid >= added) p.added[static_cast<int64_t>(b) * p.w + tid] = -1;
-  // write back the candidates of the queried rows and every node's taken count
+  __syncthreads();
+  // ---- 2. the picks (warp 0): each node offers its next candidate; lane l
+  // holds nodes l, l + 32, l + 64, l + 96
+  if (warp == 0) {
+    constexpr int kPer = TS_MAX_TREE / 32;
+    float key[kPer];
+    int tk[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int v = lane + 32 * q;
+      tk[q] = taken_s[v];
+      key[q] = (v < n && tk[q] < p.k && c_tok[v][tk[q]] >= 0) ? w_s[v] + c_lp[v][tk[q]] : -INFINITY;
+    }
+    int nn = n, j = 0;
+    for (; j < p.w && nn < p.n_tree_max; ++j) {
+      float bv = key[0];
+      int bi = lane;
+#pragma unroll
+      for (int q = 1; q < kPer; ++q)
+        if (key[q] > bv) {  // a tie keeps the lower node
+          bv = key[q];
+          bi = lane + 32 * q;
+        }
+      warp_best(bv, bi);
+      if (bv == -INFINITY) break;
+      if (lane == (bi & 31)) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+          if (q == (bi >> 5)) {
+            const int t = tk[q];
+            p.parent[nb + nn] = bi;
+            p.tokens[nb + nn] = c_tok[bi][t];
+            p.weight[nb + nn] = bv;
+            p.cand_taken[nb + nn] = p.k;
+            p.added[static_cast<int64_t>(b) * p.w + j] = nn;
+            tk[q] = t + 1;
+            key[q] = (t + 1 < p.k && c_tok[bi][t + 1] >= 0) ? w_s[bi] + c_lp[bi][t + 1] : -INFINITY;
+          }
+      }
+      ++nn;  // the new node: no candidates until its logits come (its key stays -inf)
+    }
+    for (int q = j + lane; q < p.w; q += 32) p.added[static_cast<int64_t>(b) * p.w + q] = -1;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) taken_s[lane + 32 * q] = tk[q];
+    if (lane == 0) n_out = nn;
+  }
+  __syncthreads();
+  // ---- 3. write back the queried rows' candidates and the old nodes' taken counts
   if (tid < n) {
-    bool queried = false;
-    for (int r = 0; r < p.w; ++r) queried = queried || rows_s[r] == tid;
-    if (queried)
+    p.cand_taken[nb + tid] = taken_s[tid];
+    if (queried_s[tid])
       for (int j = 0; j < p.k; ++j) {
         p.cand_lp[(nb + tid) * p.k + j] = c_lp[tid][j];
         p.cand_tok[(nb + tid) * p.k + j] = c_tok[tid][j];
       }
-    if (tid < n - added) p.cand_taken[nb + tid] = taken;
   }
-  if (tid == 0) p.n_tree[b] = n;
+  if (tid == 0) p.n_tree[b] = n_out;
 }
 
 __global__ void __launch_bounds__(TS_MAX_TREE) select_subtree_kernel(const SelectParams p) {

@@ -144,7 +144,7 @@ struct CandPartial {
 
 struct ExpandParams {
   int num_req, n_tree_max, vocab, w, k;
-  int slice, num_slices;   // vocab floats per candidate CTA (multiple of 1024), slices per row (<= 32)
+  int slice, num_slices;   // vocab floats per candidate CTA (multiple of 1024), slices per row (<= 16)
   const float* logits;
   const int32_t* rows;
   int32_t* n_tree;

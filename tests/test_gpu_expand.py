@@ -50,7 +50,7 @@ def _margin(avail, w):
     return min((top[i] - top[i + 1] for i in range(len(top) - 1)), default=math.inf)
 
 
-def _run(seed, B, n_max, vocab, w, k, steps, root_w=None, plant_ties=False):
+def _run(seed, B, n_max, vocab, w, k, steps, root_w=None, plant_ties=False, logits="normal"):
     rng = np.random.default_rng(seed)
     dev = "cuda"
     tree = ts.DraftTree(B, n_max, k)
@@ -66,7 +66,12 @@ def _run(seed, B, n_max, vocab, w, k, steps, root_w=None, plant_ties=False):
     rows[:, 0] = 0
     ws = None
     for step in range(steps):
-        lg = (rng.normal(size=(B, w, vocab)) * 2.0).astype(np.float32)
+        if logits == "int":      # a few distinct values: hundreds of ties at the top of every slice
+            lg = rng.integers(-1, 2, size=(B, w, vocab)).astype(np.float32)
+        elif logits == "const":  # every logit equal: the k lowest tokens, log-prob -log(vocab)
+            lg = np.full((B, w, vocab), 0.25, dtype=np.float32)
+        else:
+            lg = (rng.normal(size=(B, w, vocab)) * 2.0).astype(np.float32)
         if plant_ties:
             lg[:, :, 5 % vocab] = lg[:, :, 3 % vocab] = lg.max() + 1.0   # equal top logits: lower token first
         logits = torch.from_numpy(lg).to(dev)
@@ -125,6 +130,7 @@ def _run(seed, B, n_max, vocab, w, k, steps, root_w=None, plant_ties=False):
     (3, 1, 128, 50000, 16, 16, 6),       # the largest w and k
     (4, 5, 20, 4096, 2, 2, 12),          # growth stops at capacity
     (5, 2, 96, 128256, 8, 3, 5),
+    (10, 9, 128, 152064, 16, 16, 2),     # 144 rows: 8 slices, three batches of loads per thread
 ])
 def test_expansion_matches_oracle(seed, B, n_max, vocab, w, k, steps):
     _run(seed, B, n_max, vocab, w, k, steps)
@@ -143,6 +149,15 @@ def test_expansion_ties_go_to_the_lower_token_and_node():
     added = ts.tree_expand(tree, logits, rows)
     torch.cuda.synchronize()
     assert tree.parent[0, 3:5].tolist() == [1, 2] and added[0].tolist() == [3, 4]
+
+
+@pytest.mark.parametrize("kind,vocab,k", [("int", 20000, 8), ("int", 152064, 16), ("const", 5000, 5),
+                                           ("const", 128256, 16), ("int", 1001, 3)])
+def test_expansion_with_heavy_ties_matches_oracle(kind, vocab, k):
+    """Logits with hundreds or thousands of equal values at the top of each
+    vocab slice: the candidates are still the k largest with the lower token
+    first."""
+    _run(11, 2, 64, vocab, 4, k, 3, logits=kind)
 
 
 def test_figure2_two_nodes_per_expansion_on_gpu():
