@@ -754,7 +754,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(args)
-    traffic = measured_traffic(info["workload"], path)
+    traffic = measured_traffic(args.workload, path)
     # mean acceptance length of the last step (the inputs are the same every step)
     acceptance = None
     if info["acc_state"] is not None:
