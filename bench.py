@@ -367,23 +367,31 @@ def build_step(args, torch, ts, W, device):
 def e2e_measure(args, torch, ts, info, steps, warmup):
     """Same step through the public API with host (pinned) inputs copied in and results copied out every step.
 
-    The vocab logits (the bulk of the host->device bytes) are copied on a side
-    stream while the attention, which does not read them, runs on the main
-    stream; acceptance waits for that copy, and the next step's copy waits
-    until this step's acceptance has consumed the buffer.
+    All host->device copies of a step go on a side stream, the small inputs
+    (queries, tree metadata, draft tokens) first and the vocab logits (the bulk
+    of the bytes) after them: the copy engine takes host->device copies in the
+    order they are issued, so a small copy issued after the logits would wait
+    for all of them.  The side stream starts a step's copies once the previous
+    step's work on the main stream has finished with its inputs.  The
+    attention, which does not read the logits, starts as soon as the small
+    inputs are in and runs while the logits cross; the acceptance waits for
+    them.  The results go back on the main stream.  A step with no large
+    input and small results copies everything on the main stream.
     """
-    main_in, main_host = [], []
-    for a, ws, d, out, lse in info["attn_inputs"]:
-        main_in.append(d["q"])
+    small_in = [d["q"] for a, ws, d, out, lse in info["attn_inputs"]]
     if info["draft"] is not None:
-        main_in += info["draft"]["logits"]   # draft logits of the nodes the expansions query
+        small_in += info["draft"]["logits"]   # draft logits of the nodes the expansions query
     acc = info["acc_state"]
-    side_in = [acc[2], acc[3]] + acc[6] if acc is not None else []   # logits, tokens (+ draft logits, uniforms)
+    big_in = []
+    if acc is not None:
+        small_in.append(acc[3])               # draft tokens
+        small_in += acc[6][1:]                # uniforms (sampling)
+        big_in = [acc[2]] + acc[6][:1]        # target logits (+ draft logits, sampling)
     for st in info["comp_states"]:
-        main_in += [st[8], st[9]]          # parent, tokens (tree metadata)
+        small_in += [st[8], st[9]]          # parent, tokens (tree metadata)
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
-    main_host = [pin(t) for t in main_in]
-    side_host = [pin(t) for t in side_in]
+    small_host = [pin(t) for t in small_in]
+    big_host = [pin(t) for t in big_in]
     outs = [o for *_, o, l in info["attn_inputs"]] + [l for *_, l in info["attn_inputs"]]
     if acc is not None:
         outs += list(acc[4].values())
@@ -392,33 +400,47 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     if info["draft"] is not None:
         outs += list(info["draft"]["sel_out"].values())
     host_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(t.numel() * t.element_size() for t in main_host + side_host)
+    h2d = sum(t.numel() * t.element_size() for t in small_host + big_host)
     d2h = sum(t.numel() * t.element_size() for t in host_outs)
     side = torch.cuda.Stream()
     main = torch.cuda.current_stream()
-    consumed = torch.cuda.Event()
-    consumed.record(main)
+    done = torch.cuda.Event()   # the main stream has finished with the step's inputs
+    done.record(main)
+
+    # A side stream pays when there is something to overlap: the logits with
+    # the attention, or a step's results going out (1 MB or more) with the
+    # next step's inputs coming in.  Otherwise its events cost more than it saves.
+    use_side = bool(big_in) or d2h >= (1 << 20)
 
     def step():
-        side.wait_event(consumed)
-        with torch.cuda.stream(side):
-            for h, dv in zip(side_host, side_in):
+        if not use_side:   # copy on the main stream
+            for h, dv in zip(small_host, small_in):
                 dv.copy_(h, non_blocking=True)
-        copied = torch.cuda.Event()
-        copied.record(side)
-        for h, dv in zip(main_host, main_in):
-            dv.copy_(h, non_blocking=True)
+            for _, calls in info["phases"]:
+                for f in calls:
+                    f()
+            for dv, h in zip(outs, host_outs):
+                h.copy_(dv, non_blocking=True)
+            return
+        side.wait_event(done)
+        with torch.cuda.stream(side):
+            for h, dv in zip(small_host, small_in):
+                dv.copy_(h, non_blocking=True)
+            small = torch.cuda.Event()
+            small.record(side)
+            for h, dv in zip(big_host, big_in):
+                dv.copy_(h, non_blocking=True)
+            big = torch.cuda.Event()
+            big.record(side)
+        main.wait_event(small)
         for kind, calls in info["phases"]:
             if kind == "accept":
-                main.wait_event(copied)
+                main.wait_event(big)
                 calls = [info["accept_first"]]   # the copy the host writes into
             for f in calls:
                 f()
-            if kind == "accept":
-                consumed.record(main)
-        if acc is None:
-            main.wait_event(copied)
-            consumed.record(main)
+        main.wait_event(big)
+        done.record(main)
         for dv, h in zip(outs, host_outs):
             h.copy_(dv, non_blocking=True)
 
