@@ -94,7 +94,7 @@ def test_tcgen05_cases_match_oracle(cfg, paged):
     check_attention(case, out, lse, A.attention_case(case))
 
 
-@pytest.mark.parametrize("num_ctas", [1, 3, 64, 1000])
+@pytest.mark.parametrize("num_ctas", [1, 3, 64, 130, 1000])   # 12 units: merge share groups 1, 1, 2, 4, 8
 def test_tcgen05_split_counts_match_oracle(num_ctas):
     case = W.random_attn_case(8, num_req=3, hq=16, hkv=4, d=128, n_tree_max=40, n_query=32, prefix_range=(10, 700),
                               ragged_tree=True)
