@@ -8,11 +8,14 @@ namespace ts {
 
 // A pipeline wait: the default bound, or (the bounded-wait variant, when the
 // call gives its own bound) that bound; waits that drain copies in flight
-// after an abort always take the default bound.
+// after an abort always take the default bound.  Most pipeline waits find
+// their phase already complete, so the default instance first tests it once
+// without blocking: entering the try_wait loop costs the issuing warps even
+// then (the long-context call: 99.2 -> 95.1 us warm on one GB300).
 template <bool kBounded>
 __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if constexpr (kBounded) return mbar_wait_bounded(bar, parity, limit_ns);
-  else return mbar_wait(bar, parity);
+  else return mbar_test(bar, parity) || mbar_wait(bar, parity);
 }
 
 // Per-request lengths, clamped to the stated bounds (violations reported).
