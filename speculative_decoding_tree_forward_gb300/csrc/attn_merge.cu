@@ -20,10 +20,9 @@
 // prefetched (when that grid fits one resident wave of CTAs: many shares per
 // row, few rows), or one half-warp per row with four prefetched (twice the
 // rows in flight for the same registers, so a grid of many rows lands in
-// one wave instead of two).  The tcgen05 kernel's partials are fp16 and
-// column-blocked (columns 8 j .. 8 j + 7 of row r at (slot * 16 + j) * 128 +
-// r, 16 bytes) and merged with one thread per (row, 16 columns, group of
-// shares).
+// one wave instead of two).  The tcgen05 kernel's partials are column-blocked
+// (float4 j of row r at (slot * 32 + j) * 128 + r) and merged with one thread
+// per (row, 16 columns, group of shares).
 #include "attn_common.cuh"
 
 namespace ts {
@@ -309,9 +308,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) merge_row_per_half_warp_k
 }
 
 
-// tcgen05 layout (fp16): columns 8 j .. 8 j + 7 of row r of slot s as one
-// 16-byte word at (s * 16 + j) * 128 + r, so a warp's 32 consecutive rows
-// read 512 contiguous bytes.  A warp takes a
+// tcgen05 layout: float4 j of row r of slot s at (s * 32 + j) * 128 + r, so
+// a warp's 32 consecutive rows read 512 contiguous bytes.  A warp takes a
 // block of 32 rows x 16 columns of a unit and one of S share groups (the
 // unit's shares g, g + S, g + 2 S, ...): it requests the lse and partial
 // columns of kPrefetchTc of its shares at a time, before their weights are
@@ -348,11 +346,10 @@ __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   const bool row_ok = loc < p.rows;  // else a padding row of the tile
   auto held = [&](int c) -> bool { return c - c_lo < 32 ? ((hold >> (c - c_lo)) & 1u) != 0 : s_sp.holds(c); };
   const float* lse_col = p.part_lse + unit * kMaxRowsPerUnit + r;
-  const uint4* o_col = reinterpret_cast<const uint4*>(p.part_o) + unit * (16 * kMaxRowsPerUnit) +
-                       (2 * cb) * kMaxRowsPerUnit + r;
+  const float4* o_col = reinterpret_cast<const float4*>(p.part_o) + unit * (32 * kMaxRowsPerUnit) +
+                        (4 * cb) * kMaxRowsPerUnit + r;
   auto lse_of = [&](int c) { return __ldcg(lse_col + static_cast<int64_t>(c) * kMaxRowsPerUnit); };
-  // eight fp16 columns 16 cb + 8 j .. + 7 of share c
-  auto o_of = [&](int c, int j) { return __ldcg(o_col + (static_cast<int64_t>(c) * 16 + j) * kMaxRowsPerUnit); };
+  auto o_of = [&](int c, int j) { return __ldcg(o_col + (static_cast<int64_t>(c) * 32 + j) * kMaxRowsPerUnit); };
 
   float m = -INFINITY, ws = 0.f;
   float4 acc[4];
@@ -361,17 +358,17 @@ __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   if (row_ok) {
     for (int c0 = c_lo + g; c0 <= c_hi; c0 += kPrefetchTc * S) {
       float lx[kPrefetchTc];
-      uint4 x[kPrefetchTc][2];
+      float4 x[kPrefetchTc][4];
 #pragma unroll
       for (int q = 0; q < kPrefetchTc; ++q) {
         const int c = c0 + q * S;
         lx[q] = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) x[q][j] = make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < 4; ++j) x[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c <= c_hi && held(c)) {
           lx[q] = lse_of(c);
 #pragma unroll
-          for (int j = 0; j < 2; ++j) x[q][j] = o_of(c, j);
+          for (int j = 0; j < 4; ++j) x[q][j] = o_of(c, j);
         }
       }
       float rm = lx[0];
@@ -395,17 +392,11 @@ __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
         const float w = exp2f(lx[q] - mb);  // 0 for shares that are not held (lse -inf)
         ws += w;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float2 a0 = unpack_f16x2(x[q][j].x), a1 = unpack_f16x2(x[q][j].y);
-          const float2 a2 = unpack_f16x2(x[q][j].z), a3 = unpack_f16x2(x[q][j].w);
-          acc[2 * j].x += w * a0.x;
-          acc[2 * j].y += w * a0.y;
-          acc[2 * j].z += w * a1.x;
-          acc[2 * j].w += w * a1.y;
-          acc[2 * j + 1].x += w * a2.x;
-          acc[2 * j + 1].y += w * a2.y;
-          acc[2 * j + 1].z += w * a3.x;
-          acc[2 * j + 1].w += w * a3.y;
+        for (int j = 0; j < 4; ++j) {
+          acc[j].x += w * x[q][j].x;
+          acc[j].y += w * x[q][j].y;
+          acc[j].z += w * x[q][j].z;
+          acc[j].w += w * x[q][j].w;
         }
       }
     }

@@ -1015,14 +1015,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               }
               if (!last_seg && lane == 0) mbar_arrive(&ctl->stg_free);
             } else {
-              // fp16 partial (the weighted mean of V rows: fp16's range holds
-              // it, and its 2^-11 rounding is a quarter of the bf16 output's),
-              // written straight from registers: columns 8 j .. 8 j + 7 of row
-              // r as one 16-byte word at ((slot * 16 + j) * 128 + r), so a
-              // warp's 32 rows store 512 contiguous bytes per instruction.  No
-              // staging and no wait for the stores: both O accumulators are
-              // free as soon as the last chunk has been read from TMEM.
-              uint4* prow = reinterpret_cast<uint4*>(p.part_o) + slot * (kRowsTc * 16) + r;
+              // fp32 partial, written straight from registers: float4 j of
+              // row r at ((slot * 32 + j) * 128 + r), so a warp's 32 rows
+              // store 512 contiguous bytes per instruction.  No staging and
+              // no wait for the stores: both O accumulators are free as soon
+              // as the last chunk has been read from TMEM.
+              float4* prow = reinterpret_cast<float4*>(p.part_o) + slot * (kRowsTc * 32) + r;
               const bool write_row = loc < p.rows;
 #pragma unroll 1
               for (int ch = 0; ch < 4; ++ch) {
@@ -1036,10 +1034,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 }
                 if (write_row) {
 #pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    __stcg(prow + (ch * 4 + q) * kRowsTc,
-                           make_uint4(pack_f16x2(o[8 * q], o[8 * q + 1]), pack_f16x2(o[8 * q + 2], o[8 * q + 3]),
-                                      pack_f16x2(o[8 * q + 4], o[8 * q + 5]), pack_f16x2(o[8 * q + 6], o[8 * q + 7])));
+                  for (int q = 0; q < 8; ++q)
+                    __stcg(prow + (ch * 8 + q) * kRowsTc, make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
                 }
                 if (ch < 3) tmem_ld_wait();
               }

@@ -8,7 +8,6 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -199,16 +198,6 @@ __device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t x) {
-  __half2 v = *reinterpret_cast<__half2*>(&x);
-  return __half22float2(v);
 }
 
 // 2^x by the hardware approximation (ex2.approx, flush-to-zero): exact 0

@@ -60,7 +60,7 @@ struct AttnParams {
   float* lse;
   float scale_log2;  // softmax scale * log2(e)
   unsigned* err;     // workspace error word
-  float* part_o;     // warp-MMA path: fp32 [slots][rows_pad][head_dim]; tcgen05 path: fp16 [slots][16][128] x 8 (uint4)
+  float* part_o;     // warp-MMA path: [slots][rows_pad][head_dim]; tcgen05 path: [slots][32][128] float4
                      // (float4 j of row r at (slot * 32 + j) * 128 + r)
   float* part_lse;   // [slots][rows_pad] (log2 domain)
   uint64_t wait_ns;    // bound of each pipeline wait (the drain waits after an abort keep kWaitLimitNs)
