@@ -102,6 +102,34 @@ def test_tcgen05_split_counts_match_oracle(num_ctas):
     check_attention(case, out, lse, A.attention_case(case))
 
 
+def _scaled_bf16(bits, exp2):
+    """bf16 bit patterns times 2^exp2 (exact: only the exponent changes)."""
+    f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** exp2)
+    return W.f32_to_bf16_bits(f)
+
+
+@pytest.mark.parametrize("path,num_ctas,shape", [
+    (2, 64, "r128"), (2, 0, "r128"), (2, 64, "two_heads"), (1, 64, "r128"), (1, 7, "d64")])
+def test_large_magnitude_values_scale_exactly(path, num_ctas, shape):
+    """V scaled by 2^17 (entries up to about 2^19, split-KV partials and
+    outputs far beyond fp16's range): every fp32 step scales exactly, so the
+    output must be 2^17 times the unscaled one bit for bit, with the same
+    lse; the unscaled output is checked against the oracle.  Both kernels,
+    split and unsplit."""
+    import dataclasses
+    kw = {"r128": dict(num_req=3, hq=64, hkv=8, d=128, n_tree_max=16),
+          "two_heads": dict(num_req=3, hq=64, hkv=8, d=128, n_tree_max=5, chain=True),
+          "d64": dict(num_req=2, hq=8, hkv=2, d=64, n_tree_max=16)}[shape]
+    case = W.random_attn_case(860, prefix_range=(300, 900), **kw)
+    big = dataclasses.replace(case, v=_scaled_bf16(case.v, 17))
+    out, lse = run(case, force_path=path, num_ctas=num_ctas)
+    out_big, lse_big = run(big, force_path=path, num_ctas=num_ctas)
+    assert torch.isfinite(out_big.float()).all()
+    assert torch.equal(out_big.float(), out.float() * 2.0 ** 17)
+    assert torch.equal(lse_big, lse)
+    check_attention(case, out, lse, A.attention_case(case))
+
+
 @pytest.mark.parametrize("num_ctas", [190, 300, 400])
 def test_tcgen05_first_call_many_short_splits(num_ctas):
     """A fresh workspace and two to four tiles per CTA: every unit is combined from many partials."""
