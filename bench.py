@@ -364,6 +364,81 @@ def build_step(args, torch, ts, W, device):
     return step, info
 
 
+def phase_device_times(info, torch, peak):
+    """Device time per call of each phase of the step, from a CUDA graph of that
+    phase alone replayed back to back between one pair of events.
+
+    An event pair around a single launch adds a few microseconds to it (the
+    launch after a recorded event starts only after that event, with no
+    overlap of its set-up), and Python-side launches can fall behind
+    microsecond kernels; replaying a graph of several calls leaves the
+    kernels' own time and their programmatic-dependent overlap.  These
+    figures are supplementary: the step times and the roofline above are the
+    event-timed ones.  Inputs larger than L2 are read from DRAM; the draft
+    workload's logits and K/V (a few MB) stay in L2 across replays.
+    """
+    stream = torch.cuda.current_stream()
+
+    def graph_of(fn):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def per_replay_us(g, n):
+        vals = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            vals.append(a.elapsed_time(b) * 1e3 / n)
+        return sorted(vals)[len(vals) // 2]
+
+    out = {"method": "CUDA graph of one phase alone, replayed back to back; device microseconds per call"}
+    phases = info["phases"]
+    if info["draft"] is not None:
+        reset = phases[0][1][0]
+        exps = [calls[0] for kind, calls in phases[1:-1] if kind == "other"]
+        attns = [calls[0] for kind, calls in phases if kind == "attn"]
+
+        def seq(k, with_attn):
+            def f():
+                reset()
+                for i in range(k):
+                    exps[i]()
+                    if with_attn:
+                        attns[i]()
+            return f
+        t0 = per_replay_us(graph_of(seq(0, False)), 20)
+        te = per_replay_us(graph_of(seq(len(exps), False)), 20)
+        ta = per_replay_us(graph_of(seq(len(exps), True)), 20)
+        out["expansion_us"] = (te - t0) / len(exps)
+        out["attention_us"] = (ta - te) / len(attns)
+        out["note"] = "expansion = candidate pass + step kernel; logits and K/V L2-resident across replays"
+        return out
+    attn = [f for kind, calls in phases if kind == "attn" for f in calls]
+    reps = max(4, -(-4 * L2_BYTES // max(info["attn_bytes"], 1)))   # chained calls read more than L2 between reuses
+    t = per_replay_us(graph_of(lambda: [f() for _ in range(reps) for f in attn]), 5) / (reps * len(attn))
+    out["attention_us"] = t
+    out["attention_frac"] = info["attn_bytes"] / len(attn) / (t / 1e6) / 1e9 / peak
+    accept = [f for kind, calls in phases if kind == "accept" for f in calls]
+    if accept:
+        n = info.get("logits_copies", 1)
+        out["acceptance_us"] = per_replay_us(graph_of(lambda: [accept[0]() for _ in range(n)]), 10) / n
+    comp = [f for kind, calls in phases if kind == "other" for f in calls]
+    if comp:
+        out["compaction_us"] = per_replay_us(graph_of(lambda: [f() for _ in range(4) for f in comp]), 10) / 4
+    return out
+
+
 def e2e_measure(args, torch, ts, info, steps, warmup):
     """Same step through the public API with host (pinned) inputs copied in and results copied out every step.
 
@@ -775,6 +850,11 @@ def main():
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
     path = ts.tree_attn_selected_path(info["attn_inputs"][0][0])
 
+    # (workloads flushed between steps fit in L2: chained replays would re-read them from L2,
+    # except the draft iteration, whose figures say so)
+    phases_graph = (phase_device_times(info, torch, peak)
+                    if not args.no_graph and (flush is None or info["draft"] is not None) else None)
+
     side = None
     if not args.no_workloads and args.workload.startswith("longctx"):
         side = side_workloads(args, torch, ts, W, device, max(20, min(args.steps * 5, 200)))
@@ -827,6 +907,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": info["launches"] * args.steps,
         "graph": graph,
+        "phases_graph": phases_graph,
         "clocks": ck,
         "acceptance": acceptance,
         "workloads": side,
