@@ -467,7 +467,8 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
     small_host = [pin(t) for t in small_in]
     big_host = [pin(t) for t in big_in]
-    outs = [o for *_, o, l in info["attn_inputs"]] + [l for *_, l in info["attn_inputs"]]
+    attn_outs = [o for *_, o, l in info["attn_inputs"]] + [l for *_, l in info["attn_inputs"]]
+    outs = []
     if acc is not None:
         outs += list(acc[4].values())
     for st in info["comp_states"]:
@@ -475,9 +476,11 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     if info["draft"] is not None:
         outs += list(info["draft"]["sel_out"].values())
     host_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    host_attn_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in attn_outs]
     h2d = sum(t.numel() * t.element_size() for t in small_host + big_host)
-    d2h = sum(t.numel() * t.element_size() for t in host_outs)
+    d2h = sum(t.numel() * t.element_size() for t in host_outs + host_attn_outs)
     side = torch.cuda.Stream()
+    back = torch.cuda.Stream()   # device->host copies of the attention results
     main = torch.cuda.current_stream()
     done = torch.cuda.Event()   # the main stream has finished with the step's inputs
     done.record(main)
@@ -486,6 +489,10 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     # the attention, or a step's results going out (1 MB or more) with the
     # next step's inputs coming in.  Otherwise its events cost more than it saves.
     use_side = bool(big_in) or d2h >= (1 << 20)
+    # The attention results go back early, on a stream of their own, only
+    # while a long host->device copy is running: for a short step the extra
+    # stream and events cost more than the overlap saves.
+    use_back = sum(t.numel() * t.element_size() for t in big_host) >= (8 << 20)
 
     def step():
         if not use_side:   # copy on the main stream
@@ -494,7 +501,7 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
             for _, calls in info["phases"]:
                 for f in calls:
                     f()
-            for dv, h in zip(outs, host_outs):
+            for dv, h in zip(attn_outs + outs, host_attn_outs + host_outs):
                 h.copy_(dv, non_blocking=True)
             return
         side.wait_event(done)
@@ -508,15 +515,33 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
             big = torch.cuda.Event()
             big.record(side)
         main.wait_event(small)
+        attn_left = sum(1 for kind, _ in info["phases"] if kind == "attn")
+        back_done = None
         for kind, calls in info["phases"]:
             if kind == "accept":
                 main.wait_event(big)
                 calls = [info["accept_first"]]   # the copy the host writes into
             for f in calls:
                 f()
+            if kind == "attn" and use_back:
+                attn_left -= 1
+                if attn_left == 0:
+                    # the attention results are final: they go back on their own
+                    # stream, over the link's other direction, while the logits
+                    # are still coming in
+                    ready = torch.cuda.Event()
+                    ready.record(main)
+                    back.wait_event(ready)
+                    with torch.cuda.stream(back):
+                        for dv, h in zip(attn_outs, host_attn_outs):
+                            h.copy_(dv, non_blocking=True)
+                        back_done = torch.cuda.Event()
+                        back_done.record(back)
         main.wait_event(big)
+        if back_done is not None:
+            main.wait_event(back_done)   # the next step's attention rewrites those outputs
         done.record(main)
-        for dv, h in zip(outs, host_outs):
+        for dv, h in zip(outs if use_back else attn_outs + outs, host_outs if use_back else host_attn_outs + host_outs):
             h.copy_(dv, non_blocking=True)
 
     for _ in range(warmup):
