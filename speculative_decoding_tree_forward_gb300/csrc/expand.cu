@@ -92,16 +92,10 @@ __device__ __forceinline__ void warp_best(float& bv, int& bi) {
   }
 }
 
-// (max, sum of exp(x - max)) pairs; __expf's error is a few ulp here (its
-// argument is <= 0 and above -100 for finite logits of one distribution)
-__device__ __forceinline__ void lse_combine(float& m, float& s, float om, float os) {
-  if (om > m) {
-    s = s * __expf(m - om) + os;
-    m = om;
-  } else if (om != -INFINITY) {
-    s += os * __expf(om - m);
-  }
-}
+// Log-sum-exp is kept as (max, sum of exp(x - max)) pairs and combined by a
+// max reduction, then a sum of the pairs' sums rescaled to that max.
+// __expf's error is a few ulp here: its argument is <= 0 and above -100 for
+// finite logits of one distribution.
 
 __device__ __forceinline__ int clamp_n(const ExpandParams& p, int b) {
   return min(max(p.n_tree[b], 0), p.n_tree_max);
@@ -194,19 +188,31 @@ __device__ __forceinline__ void slice_candidates(const ExpandParams& p, const fl
         }
     }
   }
+  {  // the warp's pair: the lanes' max, then their sums rescaled to it
+    float mx = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-  if (lane == 0) {
-    wm[warp] = m;
-    wsum[warp] = s;
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sm = m != -INFINITY ? s * __expf(m - mx) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    if (lane == 0) {
+      wm[warp] = mx;
+      wsum[warp] = sm;
+    }
   }
   __syncthreads();
-  if (tid == 0) {
-    float bm = wm[0], bs = wsum[0];
+  if (warp == 0) {  // the warps' pairs: their max, then the sums rescaled to it
+    const float wmx = lane < kCandWarps ? wm[lane] : -INFINITY;
+    float mx = wmx;
 #pragma unroll
-    for (int q = 1; q < kCandWarps; ++q) lse_combine(bm, bs, wm[q], wsum[q]);
-    out->m = bm;
-    out->s = bs;
+    for (int o = kCandWarps / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sm = (lane < kCandWarps && wmx != -INFINITY) ? wsum[lane] * __expf(wmx - mx) : 0.f;
+#pragma unroll
+    for (int o = kCandWarps / 2; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    if (lane == 0) {
+      out->m = mx;
+      out->s = sm;
+    }
   }
   const int n_c = cnt_s;
   if (n_c <= kCandCap) {
@@ -227,11 +233,22 @@ __device__ __forceinline__ void slice_candidates(const ExpandParams& p, const fl
     }
     __syncthreads();
     const int n_e = n_elig_s;
-    for (int e = tid; e < n_e; e += kCandThreads) {
-      const int2 me = elig[e];
+    // the rank of each entry is counted by g adjacent lanes (g a power of two
+    // up to 32, as many as the CTA's threads allow), each over every g-th
+    // entry, and summed by shuffles within the group
+    int lg = 0;  // g = 1 << lg
+    while (lg < 5 && (2 << lg) * n_e <= kCandThreads) ++lg;
+    const int g = 1 << lg;
+    for (int x0 = 0; x0 < n_e * g; x0 += kCandThreads) {  // uniform trip count
+      const int x = x0 + tid, e = x >> lg, part = x & (g - 1);
+      int2 me = make_int2(0, 0);
       int rank = 0;
-      for (int j = 0; j < n_e; ++j) rank += ahead(elig[j], me) ? 1 : 0;
-      if (rank < p.k) {
+      if (e < n_e) {
+        me = elig[e];
+        for (int j = part; j < n_e; j += g) rank += ahead(elig[j], me) ? 1 : 0;
+      }
+      for (int o = g >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+      if (e < n_e && part == 0 && rank < p.k) {
         out->val[rank] = __int_as_float(me.x);
         out->idx[rank] = me.y;
       }
@@ -400,10 +417,14 @@ __global__ void __launch_bounds__(kStepThreads) expand_step_kernel(const ExpandP
         c_lp[u][lane] = -INFINITY;
         c_tok[u][lane] = -1;
       }
-      float m = rs.m, s = rs.s;
+      // the row's log-sum-exp from the slices' pairs: their max, then the
+      // sums rescaled to it
+      float m = rs.m;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-        lse_combine(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float s = rs.m != -INFINITY ? rs.s * __expf(rs.m - m) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       const float lse = m + logf(s);
       // Lower bounds of the row's k-th largest: any slice's k-th entry (the
       // least of its first k), and the k-th largest of the slices' heads.
