@@ -44,6 +44,7 @@ namespace {
 
 constexpr int kCompactThreads = 256;
 constexpr int kLoadsInFlight = 8;  // 16-byte loads per thread before the first store to shared memory
+constexpr int kItemPtrs = 32;      // item base pointers a CTA keeps in shared memory
 
 // One CTA's share of one request's compaction: request b of the call whose
 // parameters are p, CTA `cta` of its p.ctas.
@@ -60,14 +61,28 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
   __shared__ int cnt[kCompactThreads / 32];
   __shared__ int blk_s[TS_MAX_TREE + 2];  // paged: block-table entries of the pages holding rows P .. P + n - 1
   __shared__ int walk_cur, walk_plen, walk_all, last_ticket;
+  __shared__ void* item_ptr[kItemPtrs];   // base pointers of the CTA's first (layer, K|V) items
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t rowbase = static_cast<int64_t>(b) * p.n_tree_max;
 
-  // ---- the request's lengths and tree (clamped and reported as before)
+  // ---- the request's lengths, tree and verified tokens, requested together
+  //      (bounded by the arrays' sizes; the lengths then clamp what is used),
+  //      and the base pointers of the CTA's first (layer, K|V) items, which
+  //      only the row moves need
+  const int items = 2 * p.num_layers;
+  const int it0 = cta * p.items_per_cta;
+  const int it1 = min(items, it0 + p.items_per_cta);
   int n = p.n_tree[b];
   int m = p.m[b];
   int P = p.prefix_len[b];
+  const int ver = tid < min(p.m_max, TS_MAX_TREE + 1) ? p.verified[static_cast<int64_t>(b) * p.m_max + tid] : 0;
+  const int raw_par = tid < p.n_tree_max ? p.parent[rowbase + tid] : -1;
+  const int raw_tok = tid < p.n_tree_max ? p.tokens[rowbase + tid] : 0;
+  if (tid < min(it1 - it0, kItemPtrs)) {
+    const int it = it0 + tid;
+    item_ptr[tid] = (it & 1) ? p.v_layers[it >> 1] : p.k_layers[it >> 1];
+  }
   bool bad = false;
   if (n < 0 || n > p.n_tree_max) { n = min(max(n, 0), p.n_tree_max); bad = true; }
   if (m < 0 || m > p.m_max) { m = min(max(m, 0), p.m_max); bad = true; }
@@ -77,15 +92,15 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
   // A walk step matches at most one node, so with n <= TS_MAX_TREE nodes the
   // walk has always ended by step TS_MAX_TREE + 1: later tokens are never read.
   const int mw = min(m, TS_MAX_TREE + 1);
-  for (int j = tid; j < mw; j += kCompactThreads) ver_s[j] = p.verified[static_cast<int64_t>(b) * p.m_max + j];
+  if (tid < mw) ver_s[tid] = ver;  // mw <= TS_MAX_TREE + 1 < kCompactThreads
   int my_par = -1, my_tok = 0;
   if (tid < n) {
-    my_par = p.parent[rowbase + tid];
+    my_par = raw_par;
     if (my_par < -1 || my_par >= tid) {
       if (cta == 0) report_error(p.err, TS_DEVERR_BAD_PARENT);
       my_par = -1;
     }
-    my_tok = p.tokens[rowbase + tid];
+    my_tok = raw_tok;
     par_s[tid] = my_par;
     tok_s[tid] = my_tok;
   }
@@ -225,9 +240,6 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
   __syncthreads();  // mv_src / mv_dst complete
 
   // ---- row moves: items it0 .. it1 - 1 of this CTA, as 16-byte vectors
-  const int items = 2 * p.num_layers;
-  const int it0 = cta * p.items_per_cta;
-  const int it1 = min(items, it0 + p.items_per_cta);
   if (nmv == 0 || it0 >= it1) return;
   const int vr = p.row_bytes / 16;
   const int64_t per_item = static_cast<int64_t>(nmv) * vr;
@@ -241,7 +253,7 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
     const int k = static_cast<int>(rem / vr32), e = static_cast<int>(rem % vr32);
     const int64_t row = dst ? mv_dst[k] : mv_src[k];  // both -1 when the row does not move
     if (row < 0) return nullptr;
-    void* base = (it & 1) ? p.v_layers[it >> 1] : p.k_layers[it >> 1];
+    void* base = it - it0 < kItemPtrs ? item_ptr[it - it0] : ((it & 1) ? p.v_layers[it >> 1] : p.k_layers[it >> 1]);
     return reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + row * p.row_bytes) + e;
   };
   for (int64_t x0 = 0; x0 < nvec; x0 += p.batch_vecs) {
