@@ -97,6 +97,54 @@ def test_accept_plain_normal_logits(vocab, B, n, p_acc):
     check_accept(case, run_accept(case))
 
 
+def _normal_case(seed, B, n_max, vocab, n_tree=None, p_acc=0.7):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((B, n_max, vocab), dtype=np.float32)
+    parent = np.stack([W.random_parents(rng, n_max) for _ in range(B)]).astype(np.int32)
+    nt = np.full(B, n_max, np.int32) if n_tree is None else np.asarray(n_tree, np.int32)
+    am = np.array([T.greedy_accept(logits[b], np.zeros(n_max, np.int32), parent[b], n_max).argmax for b in range(B)],
+                  np.int32)
+    tokens = np.stack([W.draft_tokens(rng, parent[b], am[b], vocab, p_acc) for b in range(B)]).astype(np.int32)
+    return W.AcceptCase(B, n_max, vocab, nt, parent, tokens, logits, am)
+
+
+@pytest.mark.parametrize("B,n_max,vocab,n_tree", [
+    (5, 48, 32768, [48, 0, 17, 1, 30]),          # ragged and empty trees
+    (10, 30, 8192, None),                        # 300 rows, one vocab slice each
+    (8, 32, 152064, [0, 0, 0, 1, 0, 0, 0, 0]),   # one valid row among 256
+    (3, 40, 65536, [40, 39, 2]),
+])
+def test_accept_large_ragged_shapes(B, n_max, vocab, n_tree):
+    """Tens of MB of N(0, 1) logits with ragged, empty and single-node trees:
+    only rows below each request's tree size are read and reduced."""
+    case = _normal_case(B * 1000 + vocab, B, n_max, vocab, n_tree)
+    check_accept(case, run_accept(case))
+
+
+def test_accept_ties_across_vocab_slices():
+    """Equal maxima planted in each row on both sides of a boundary between
+    the vocab slices of a 152-SM launch (rows x slices = eight CTAs per SM,
+    slices rounded up to 1024 floats): on even rows the lowest lies in the
+    earlier slice, on odd rows at the start of the later one; the lowest index
+    wins."""
+    B, n_max, vocab = 4, 32, 152064
+    case = _normal_case(11, B, n_max, vocab)
+    slices = max(1, 152 * 8 // (B * n_max))
+    chunk = (vocab + slices - 1) // slices
+    chunk = (chunk + 1023) // 1024 * 1024
+    for b in range(B):
+        for i in range(n_max):
+            g = b * n_max + i
+            start = chunk * (1 + g % max(1, vocab // chunk - 1))    # a slice boundary inside the row
+            spots = [start, vocab - 4, vocab - 1] + ([start - 4] if g % 2 == 0 else [])
+            case.logits[b, i, spots] = 7.5
+    rng = np.random.default_rng(12)
+    am = [T.greedy_accept(case.logits[b], np.zeros(n_max, np.int32), case.parent[b], n_max).argmax for b in range(B)]
+    case.tokens = np.stack([W.draft_tokens(rng, case.parent[b], np.asarray(am[b], np.int32), vocab, 0.7)
+                            for b in range(B)]).astype(np.int32)
+    check_accept(case, run_accept(case))
+
+
 def test_accept_fig2_target_verify():
     with open(os.path.join(GOLDEN, "fig2_walkthrough.json")) as f:
         g = json.load(f)["target_verify"]
