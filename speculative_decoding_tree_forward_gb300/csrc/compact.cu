@@ -106,8 +106,8 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
   }
   __syncthreads();  // every read of the old metadata is done
 
-  // ---- ticket: the request's last CTA writes the new metadata (taken by
-  //      warp 1 while warp 0 walks); paged: the tree rows' block-table
+  // ---- ticket: the request's last CTA writes the new metadata (requested
+  //      by warp 1 while warp 0 walks); paged: the tree rows' block-table
   //      entries, read by warps 2.. while warp 0 walks
   const int pg0 = p.paged ? P / p.page_size : 0;
   if (p.paged && tid >= 64) {
@@ -115,13 +115,12 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
     for (int j = tid - 64; j < npg; j += kCompactThreads - 64)
       blk_s[j] = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg0 + j];
   }
+  // the ticket is taken here and its value used just before the barrier that
+  // precedes the metadata write, so the atomic's round trip overlaps the walk
+  unsigned ticket_before = 0;
   if (tid == 32) {
     __threadfence();
-    const unsigned before = atomicAdd(p.ticket + b, 1u);
-    const int last = before + 1u == static_cast<unsigned>(p.ctas);
-    if (last) p.ticket[b] = 0u;
-    __threadfence();
-    last_ticket = last;
+    ticket_before = atomicAdd(p.ticket + b, 1u);
   }
 
   // ---- 1. walk (warp 0): lane l holds nodes l, l + 32, l + 64, l + 96
@@ -190,7 +189,13 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
   const bool moves = tid < L && srcj != tid;
   const unsigned mbal = __ballot_sync(0xffffffffu, moves);
   if (lane == 0) cnt[warp] = __popc(mbal);
-  __syncthreads();
+  if (tid == 32) {
+    const int last = ticket_before + 1u == static_cast<unsigned>(p.ctas);
+    if (last) p.ticket[b] = 0u;
+    __threadfence();
+    last_ticket = last;
+  }
+  __syncthreads();  // cnt, last_ticket
   int mbefore = 0, nmv = 0;
 #pragma unroll
   for (int w = 0; w < kCompactThreads / 32; ++w) {
@@ -244,13 +249,34 @@ __device__ __forceinline__ void compact_body(const CompactParams& p, const int b
   const int vr = p.row_bytes / 16;
   const int64_t per_item = static_cast<int64_t>(nmv) * vr;
   const int64_t nvec = per_item * (it1 - it0);
-  // nvec < 2^31 (the host bounds items_per_cta), so 32-bit divisions suffice
+  // nvec < 2^31 (the host bounds items_per_cta), so 32-bit arithmetic
+  // suffices.  x / per_item is a multiply-high by a constant fixed for the CTA
+  // (division by an invariant integer, Granlund and Montgomery 1994: with
+  // l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, t = mulhi(m, x),
+  // x / d = (t + ((x - t) >> min(l, 1))) >> max(l - 1, 0), exact for every
+  // 32-bit x); a row's vector count is a power of two for the usual shapes,
+  // and then its quotient and remainder are a shift and a mask.
   const uint32_t per_item32 = static_cast<uint32_t>(per_item), vr32 = static_cast<uint32_t>(vr);
+  const uint32_t pi_l = per_item32 <= 1 ? 0u : 32u - static_cast<uint32_t>(__clz(per_item32 - 1));
+  const uint32_t pi_m =
+      static_cast<uint32_t>((4294967296ull * ((1ull << pi_l) - per_item32)) / per_item32 + 1ull);
+  const uint32_t pi_s1 = pi_l > 0 ? 1u : 0u, pi_s2 = pi_l > 0 ? pi_l - 1u : 0u;
+  const bool vr_pow2 = (vr32 & (vr32 - 1u)) == 0u;
+  const uint32_t vr_sh = static_cast<uint32_t>(__ffs(static_cast<int>(vr32)) - 1);
   auto address = [&](int64_t x, bool dst) -> uint4* {
     const uint32_t x32 = static_cast<uint32_t>(x);
-    const int it = it0 + static_cast<int>(x32 / per_item32);
-    const uint32_t rem = x32 % per_item32;
-    const int k = static_cast<int>(rem / vr32), e = static_cast<int>(rem % vr32);
+    const uint32_t t = __umulhi(pi_m, x32);
+    const uint32_t itn = (t + ((x32 - t) >> pi_s1)) >> pi_s2;  // x32 / per_item32
+    const int it = it0 + static_cast<int>(itn);
+    const uint32_t rem = x32 - itn * per_item32;
+    int k, e;
+    if (vr_pow2) {
+      k = static_cast<int>(rem >> vr_sh);
+      e = static_cast<int>(rem & (vr32 - 1u));
+    } else {
+      k = static_cast<int>(rem / vr32);
+      e = static_cast<int>(rem % vr32);
+    }
     const int64_t row = dst ? mv_dst[k] : mv_src[k];  // both -1 when the row does not move
     if (row < 0) return nullptr;
     void* base = it - it0 < kItemPtrs ? item_ptr[it - it0] : ((it & 1) ? p.v_layers[it >> 1] : p.k_layers[it >> 1]);
