@@ -174,11 +174,42 @@ __device__ __forceinline__ float residual_pass(const float* __restrict__ src, co
 }
 
 // Sums of r over blocks of kBonusBlock tokens (warp per block, coalesced),
-// into bsum[0 .. ceil(V / kBonusBlock)).
+// into bsum[0 .. ceil(V / kBonusBlock)).  16-byte rows: lane l takes tokens
+// 4l .. 4l + 3 of a block, and a warp requests kBlocksInFlight blocks before
+// it sums any, so a row of ~10^5 tokens is a few dozen dependent round trips
+// per warp rather than one per block.
+constexpr int kBlocksInFlight = 8;
 template <bool FROM_LOGITS>
 __device__ __forceinline__ void block_sums(const float* __restrict__ src, int V, float inv_t, float lt, float* bsum) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = (V + kBonusBlock - 1) / kBonusBlock;
+  if ((V & 3) == 0) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    for (int b0 = warp; b0 < nb; b0 += kBlocksInFlight * kWalkWarps) {
+      float4 f[kBlocksInFlight];
+      unsigned in = 0u;  // bit j: this lane's group of block j lies in the row
+#pragma unroll
+      for (int j = 0; j < kBlocksInFlight; ++j) {
+        const int v = (b0 + j * kWalkWarps) * kBonusBlock + 4 * lane;  // a whole 16-byte group or none: V % 4 == 0
+        f[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (b0 + j * kWalkWarps < nb && v < V) {
+          f[j] = __ldcg(s4 + v / 4);
+          in |= 1u << j;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBlocksInFlight; ++j) {
+        float t = 0.f;
+        if ((in >> j) & 1u)
+          t = (r_of<FROM_LOGITS>(f[j].x, inv_t, lt) + r_of<FROM_LOGITS>(f[j].y, inv_t, lt)) +
+              (r_of<FROM_LOGITS>(f[j].z, inv_t, lt) + r_of<FROM_LOGITS>(f[j].w, inv_t, lt));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0 && b0 + j * kWalkWarps < nb) bsum[b0 + j * kWalkWarps] = t;
+      }
+    }
+    return;
+  }
   for (int blk = warp; blk < nb; blk += kWalkWarps) {
     float t = 0.f;
 #pragma unroll
