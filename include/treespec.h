@@ -313,7 +313,11 @@ TS_API ts_status tree_cache_compact_batch(const ts_compact_args* args, int count
  *   (-1 after, optional), verified_len[b] = AL + 1 (optional).
  * The uniforms are inputs in [0, 1).  Arithmetic: fp32 (exp of scaled
  * logits minus the row's log-sum-exp); a decision within fp32 rounding of
- * its threshold may go either way.  Workspace: tree_accept_sample_workspace_size().
+ * its threshold may go either way.  Workspace: tree_accept_sample_workspace_size(),
+ * zero-filled before its first use; besides the error word it holds
+ * per-request counters that every call leaves at zero, except a call that
+ * reports TS_DEVERR_TIMEOUT (its outputs are void; zero the workspace before
+ * reusing it).
  * Errors: TS_ERR_INVALID_ARG unless temperature > 0 and finite;
  * TS_ERR_UNSUPPORTED if vocab > 262144 or n_tree_max > TS_MAX_TREE.
  * ------------------------------------------------------------------------ */

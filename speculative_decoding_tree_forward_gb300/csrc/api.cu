@@ -548,13 +548,22 @@ static int sample_slice(int vocab, int64_t rows) {
   return static_cast<int>(((vocab + slices - 1) / slices + 1023) / 1024 * 1024);
 }
 
+// CTAs per request in the walk: the SMs shared out among the requests, at
+// most kMaxWalkCtas, at least one (the leader alone).
+static int sample_walk_ctas(int num_requests) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return 1;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxWalkCtas, sms / num_requests)));
+}
+
 size_t tree_accept_sample_workspace_size(const ts_sample_args* a) {
   if (a == nullptr || a->num_requests < 1 || a->n_tree_max < 1 || a->vocab < 1) return 0;
   const int64_t rows = 2LL * a->num_requests * a->n_tree_max;
   const int slice = sample_slice(a->vocab, rows);
   const int64_t slices = (a->vocab + slice - 1) / slice;
   return kWsHeader + align256(static_cast<size_t>(rows * slices) * sizeof(float2)) +
-         align256(static_cast<size_t>(a->num_requests) * 2 * a->vocab * sizeof(float));
+         align256(static_cast<size_t>(a->num_requests) * sizeof(WalkSync)) +
+         align256(static_cast<size_t>(a->num_requests) * kMaxWalkCtas * sizeof(float));
 }
 
 ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t workspace_bytes, void* stream) {
@@ -592,7 +601,10 @@ ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t wo
   p.verified_len = a->verified_len;
   p.err = reinterpret_cast<unsigned*>(ws);
   p.part = reinterpret_cast<float2*>(ws + kWsHeader);
-  p.resid = reinterpret_cast<float*>(ws + kWsHeader + align256(static_cast<size_t>(rows * p.num_slices) * sizeof(float2)));
+  const size_t sync_off = kWsHeader + align256(static_cast<size_t>(rows * p.num_slices) * sizeof(float2));
+  p.walk_ctas = sample_walk_ctas(a->num_requests);
+  p.sync = reinterpret_cast<WalkSync*>(ws + sync_off);
+  p.walk_part = reinterpret_cast<float*>(ws + sync_off + align256(static_cast<size_t>(a->num_requests) * sizeof(WalkSync)));
   cudaError_t e = launch_sample(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }

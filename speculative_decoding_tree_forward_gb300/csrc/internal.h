@@ -175,6 +175,20 @@ struct SelectParams {
 };
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
+// One request's hand-off between the walk's leader CTA and its helpers (in
+// the workspace; zero before the first call, left at zero by every call
+// that ends without a timeout).
+struct WalkSync {
+  int seq;          // commands posted by the leader
+  int done;         // acknowledgements by the helpers, over all commands
+  int kind;         // the command: kWalkSum or kWalkStop
+  int u;            // the node whose rows the pass reads
+  float a, lt, ld;  // the pass sums max(0, p - a q), p = exp(tl / T - lt), q = exp(dl / T - ld)
+  int pad[9];       // one 64-byte line per request
+};
+constexpr int kWalkSum = 1, kWalkStop = 2;
+constexpr int kMaxWalkCtas = 16;
+
 struct SampleParams {
   int num_req, n_tree_max, vocab;
   int slice, num_slices;  // vocab floats per statistics CTA (multiple of 1024), slices per row (<= 32)
@@ -193,7 +207,9 @@ struct SampleParams {
   int32_t* verified_len;
   unsigned* err;
   float2* part;           // [2][num_req * n_tree_max][num_slices]: (max, sum of exp) of logit / T
-  float* resid;           // [num_req][2][vocab]: residual rows
+  int walk_ctas;          // CTAs per request in the walk: one leader and walk_ctas - 1 helpers
+  WalkSync* sync;         // [num_req]: the leader's commands and the helpers' acknowledgements
+  float* walk_part;       // [num_req][walk_ctas]: each CTA's slice sum of the last pass
 };
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream);
 

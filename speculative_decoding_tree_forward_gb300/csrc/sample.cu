@@ -10,15 +10,17 @@
 //
 // Kernel 1 (row statistics) streams every target and draft row of the tree
 // once in vocab slices and keeps (max, sum of exp(z - max)) of z = logit / T.
-// Kernel 2 (walk) runs one 1024-thread CTA per request: it merges a visited
-// node's slices into the two log-sum-exps, lists its children with a ballot,
-// tests the first child from two logits, and on each rejection makes one
-// coalesced pass over the vocab that writes max(0, r - q) into a workspace
-// row (two rows per request, swapped when the new residual is not all zero)
-// and sums it (four 16-byte loads per row in flight per thread).  The bonus
-// is drawn by inverse transform in three levels: coalesced sums of
-// 128-token blocks, a block scan of those sums for the block that holds the
-// target, and one warp's scan inside that block.
+// Kernel 2 (walk) runs a leader CTA and up to 15 helper CTAs per request
+// (512 threads each): the leader merges a visited node's slices into the two
+// log-sum-exps, lists its children with a ballot and tests each child from
+// two logits.  The running target after j rejections has the closed form
+// max(0, p - a_j q) / S(a_j) (derived at the walk's passes below), so a
+// rejection is one sum over the vocab and no residual row is written; the
+// request's CTAs split that sum by vocab slices, handing commands and slice
+// sums over through the workspace with bounded waits.  The bonus is drawn by
+// inverse transform: the slice that holds the target from the slice sums,
+// then coalesced sums of its 128-token blocks, a block scan of those sums,
+// and one warp's scan inside the block that holds the target.
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,8 +39,6 @@ __device__ __forceinline__ void lse_pair(float& m, float& s, float om, float os)
     s += os * expf(om - m);
   }
 }
-
-__device__ __forceinline__ int64_t nb_row(const SampleParams& p, int b) { return static_cast<int64_t>(b) * p.n_tree_max; }
 
 __device__ __forceinline__ int tree_size(const SampleParams& p, int b) {
   return min(max(p.n_tree[b], 0), p.n_tree_max);
@@ -112,129 +112,124 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// ---- the walk's passes --------------------------------------------------------
+// After j rejections at node u the running target has a closed form.  With
+// p = p_u and q = q_u, r_0 = p and r_{j+1} = norm(max(0, r_j - q)) give
+//   r_j = max(0, p - a_j q) / S(a_j),  S(a) = sum_v max(0, p(v) - a q(v)),
+//   a_0 = 0 (S(0) = 1),  a_{j+1} = a_j + S(a_j),
+// since max(0, max(0, p - a q) / S - q) = max(0, p - (a + S) q) / S; when
+// S(a_{j+1}) is 0 the residual is all zero and r_j is kept.  A rejection is
+// therefore one sum of max(0, p - a q) over the vocab, with no residual row
+// written, and the sum splits into slices: CTA k of a request's walk_ctas sums
+// slice k.  The bonus is drawn from the unnormalised max(0, p - a q).
 constexpr int kBonusBlock = 128;  // tokens per first-level block of the inverse transform
 constexpr int kBlocksPerThread = 4;
-constexpr int kMaxBonusBlocks = kBlocksPerThread * kWalkThreads;  // vocab <= 262144
+constexpr int kMaxBonusBlocks = kBlocksPerThread * kWalkThreads;  // slice <= 262144 tokens
+constexpr int kBlocksInFlight = 8;                                // a warp's block sums in flight
 
-// r(v) for the current node: from the target logits (no rejection yet) or
-// from the residual row (unnormalised)
-template <bool FROM_LOGITS>
-__device__ __forceinline__ float r_of(float x, float inv_t, float lt) {
-  return FROM_LOGITS ? expf(x * inv_t - lt) : x;
+__device__ __forceinline__ float r_of(float xt, float xd, float inv_t, float lt, float ld, float a) {
+  return fmaxf(0.f, expf(xt * inv_t - lt) - a * expf(xd * inv_t - ld));
 }
 
-// One rejection: out = max(0, r - q) over the vocab (r = src scaled by
-// r_scale), returns this thread's share of its sum.  Four 16-byte loads of
-// each row in flight per thread.
-template <bool FROM_LOGITS>
-__device__ __forceinline__ float residual_pass(const float* __restrict__ src, const float* __restrict__ dl,
-                                               float* __restrict__ out, int V, float inv_t, float lt, float ld,
-                                               float r_scale) {
+// Slice k of K of a row of V tokens: [v0, v1), v0 a multiple of 4.
+__device__ __forceinline__ void walk_slice(int V, int K, int k, int& v0, int& v1) {
+  const int len = ((V + K - 1) / K + 3) & ~3;
+  v0 = min(V, k * len);
+  v1 = min(V, v0 + len);
+}
+
+// This thread's share of sum_{v in [v0, v1)} r(v) over node u's rows tl, dl,
+// with four 16-byte loads of each row in flight per thread.
+__device__ __forceinline__ float slice_sum(const float* __restrict__ tl, const float* __restrict__ dl, int V, int v0,
+                                           int v1, float inv_t, float lt, float ld, float a) {
   float part = 0.f;
   if ((V & 3) == 0) {
     constexpr int kLoads = 4;
-    const int V4 = V / 4;
-    const float4* s4 = reinterpret_cast<const float4*>(src);
+    const float4* t4 = reinterpret_cast<const float4*>(tl);
     const float4* d4 = reinterpret_cast<const float4*>(dl);
-    float4* o4 = reinterpret_cast<float4*>(out);
-    for (int x0 = threadIdx.x; x0 < V4; x0 += kLoads * kWalkThreads) {
-      float4 a[kLoads], d[kLoads];
+    const int e4 = v1 / 4;
+    for (int x0 = v0 / 4 + static_cast<int>(threadIdx.x); x0 < e4; x0 += kLoads * kWalkThreads) {
+      float4 ft[kLoads], fd[kLoads];
 #pragma unroll
       for (int q = 0; q < kLoads; ++q) {
         const int x = x0 + q * kWalkThreads;
-        if (x < V4) {
-          a[q] = __ldcg(s4 + x);
-          d[q] = __ldcg(d4 + x);
+        if (x < e4) {
+          ft[q] = __ldcg(t4 + x);
+          fd[q] = __ldcg(d4 + x);
         }
       }
 #pragma unroll
-      for (int q = 0; q < kLoads; ++q) {
-        const int x = x0 + q * kWalkThreads;
-        if (x < V4) {
-          float4 o;
-          o.x = fmaxf(0.f, r_of<FROM_LOGITS>(a[q].x, inv_t, lt) * r_scale - expf(d[q].x * inv_t - ld));
-          o.y = fmaxf(0.f, r_of<FROM_LOGITS>(a[q].y, inv_t, lt) * r_scale - expf(d[q].y * inv_t - ld));
-          o.z = fmaxf(0.f, r_of<FROM_LOGITS>(a[q].z, inv_t, lt) * r_scale - expf(d[q].z * inv_t - ld));
-          o.w = fmaxf(0.f, r_of<FROM_LOGITS>(a[q].w, inv_t, lt) * r_scale - expf(d[q].w * inv_t - ld));
-          o4[x] = o;
-          part += (o.x + o.y) + (o.z + o.w);
-        }
-      }
+      for (int q = 0; q < kLoads; ++q)
+        if (x0 + q * kWalkThreads < e4)
+          part += (r_of(ft[q].x, fd[q].x, inv_t, lt, ld, a) + r_of(ft[q].y, fd[q].y, inv_t, lt, ld, a)) +
+                  (r_of(ft[q].z, fd[q].z, inv_t, lt, ld, a) + r_of(ft[q].w, fd[q].w, inv_t, lt, ld, a));
     }
   } else {
 #pragma unroll 4
-    for (int v = threadIdx.x; v < V; v += kWalkThreads) {
-      const float res = fmaxf(0.f, r_of<FROM_LOGITS>(__ldcg(src + v), inv_t, lt) * r_scale -
-                                       expf(__ldcg(dl + v) * inv_t - ld));
-      out[v] = res;
-      part += res;
-    }
+    for (int v = v0 + static_cast<int>(threadIdx.x); v < v1; v += kWalkThreads)
+      part += r_of(__ldcg(tl + v), __ldcg(dl + v), inv_t, lt, ld, a);
   }
   return part;
 }
 
-// Sums of r over blocks of kBonusBlock tokens (warp per block, coalesced),
-// into bsum[0 .. ceil(V / kBonusBlock)).  16-byte rows: lane l takes tokens
-// 4l .. 4l + 3 of a block, and a warp requests kBlocksInFlight blocks before
-// it sums any, so a row of ~10^5 tokens is a few dozen dependent round trips
-// per warp rather than one per block.
-constexpr int kBlocksInFlight = 8;
-template <bool FROM_LOGITS>
-__device__ __forceinline__ void block_sums(const float* __restrict__ src, int V, float inv_t, float lt, float* bsum) {
+// Sums of r over the slice's blocks of kBonusBlock tokens (block i is
+// [v0 + 128 i, ...)), warp per block with kBlocksInFlight blocks of a warp
+// requested before any is summed, into bsum[0 .. ceil((v1 - v0) / 128)).
+__device__ __forceinline__ void slice_block_sums(const float* __restrict__ tl, const float* __restrict__ dl, int V,
+                                                 int v0, int v1, float inv_t, float lt, float ld, float a, float* bsum) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = (V + kBonusBlock - 1) / kBonusBlock;
-  if ((V & 3) == 0) {
-    const float4* s4 = reinterpret_cast<const float4*>(src);
-    for (int b0 = warp; b0 < nb; b0 += kBlocksInFlight * kWalkWarps) {
-      float4 f[kBlocksInFlight];
-      unsigned in = 0u;  // bit j: this lane's group of block j lies in the row
+  const int nb = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
+  for (int b0 = warp; b0 < nb; b0 += kBlocksInFlight * kWalkWarps) {
+    float t[kBlocksInFlight];
+    if ((V & 3) == 0) {  // lane l: tokens 4l .. 4l + 3 of the block, whole 16-byte groups (v1 - v0 % 4 == 0)
+      float4 ft[kBlocksInFlight], fd[kBlocksInFlight];
+      unsigned in = 0u;
 #pragma unroll
       for (int j = 0; j < kBlocksInFlight; ++j) {
-        const int v = (b0 + j * kWalkWarps) * kBonusBlock + 4 * lane;  // a whole 16-byte group or none: V % 4 == 0
-        f[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (b0 + j * kWalkWarps < nb && v < V) {
-          f[j] = __ldcg(s4 + v / 4);
+        const int v = v0 + (b0 + j * kWalkWarps) * kBonusBlock + 4 * lane;
+        if (b0 + j * kWalkWarps < nb && v < v1) {
+          ft[j] = __ldcg(reinterpret_cast<const float4*>(tl + v));
+          fd[j] = __ldcg(reinterpret_cast<const float4*>(dl + v));
           in |= 1u << j;
         }
       }
 #pragma unroll
-      for (int j = 0; j < kBlocksInFlight; ++j) {
-        float t = 0.f;
-        if ((in >> j) & 1u)
-          t = (r_of<FROM_LOGITS>(f[j].x, inv_t, lt) + r_of<FROM_LOGITS>(f[j].y, inv_t, lt)) +
-              (r_of<FROM_LOGITS>(f[j].z, inv_t, lt) + r_of<FROM_LOGITS>(f[j].w, inv_t, lt));
+      for (int j = 0; j < kBlocksInFlight; ++j)
+        t[j] = ((in >> j) & 1u) ? (r_of(ft[j].x, fd[j].x, inv_t, lt, ld, a) + r_of(ft[j].y, fd[j].y, inv_t, lt, ld, a)) +
+                                      (r_of(ft[j].z, fd[j].z, inv_t, lt, ld, a) + r_of(ft[j].w, fd[j].w, inv_t, lt, ld, a))
+                                : 0.f;
+    } else {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0 && b0 + j * kWalkWarps < nb) bsum[b0 + j * kWalkWarps] = t;
+      for (int j = 0; j < kBlocksInFlight; ++j) {
+        t[j] = 0.f;
+#pragma unroll
+        for (int e = 0; e < kBonusBlock / 32; ++e) {
+          const int v = v0 + (b0 + j * kWalkWarps) * kBonusBlock + e * 32 + lane;
+          if (b0 + j * kWalkWarps < nb && v < v1) t[j] += r_of(__ldcg(tl + v), __ldcg(dl + v), inv_t, lt, ld, a);
+        }
       }
     }
-    return;
-  }
-  for (int blk = warp; blk < nb; blk += kWalkWarps) {
-    float t = 0.f;
 #pragma unroll
-    for (int e = 0; e < kBonusBlock / 32; ++e) {
-      const int v = blk * kBonusBlock + e * 32 + lane;
-      if (v < V) t += r_of<FROM_LOGITS>(__ldcg(src + v), inv_t, lt);
+    for (int j = 0; j < kBlocksInFlight; ++j) {
+      float x = t[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0 && b0 + j * kWalkWarps < nb) bsum[b0 + j * kWalkWarps] = x;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) bsum[blk] = t;
   }
 }
 
-// Inside one block: the smallest token with excl + r(blk start .. v) > target
-// (warp-wide: lane l holds tokens 4l .. 4l + 3 of the block), or -1.
-template <bool FROM_LOGITS>
-__device__ __forceinline__ int scan_block(const float* __restrict__ src, int V, float inv_t, float lt, int blk,
-                                          float excl, float target) {
+// Inside block blk of the slice: the smallest token with excl + r(block start
+// .. v) > target (warp-wide: lane l holds tokens 4l .. 4l + 3 of the block), or -1.
+__device__ __forceinline__ int scan_block(const float* __restrict__ tl, const float* __restrict__ dl, int v0, int v1,
+                                          float inv_t, float lt, float ld, float a, int blk, float excl, float target) {
   const int lane = threadIdx.x & 31;
   float r4[4];
   float mine = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int v = blk * kBonusBlock + lane * 4 + e;
-    r4[e] = v < V ? r_of<FROM_LOGITS>(__ldcg(src + v), inv_t, lt) : 0.f;
+    const int v = v0 + blk * kBonusBlock + lane * 4 + e;
+    r4[e] = v < v1 ? r_of(__ldcg(tl + v), __ldcg(dl + v), inv_t, lt, ld, a) : 0.f;
     mine += r4[e];
   }
   float inc = mine;
@@ -248,30 +243,105 @@ __device__ __forceinline__ int scan_block(const float* __restrict__ src, int V, 
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     acc += r4[e];
-    if (pick < 0 && acc > target) pick = blk * kBonusBlock + lane * 4 + e;
+    if (pick < 0 && acc > target) pick = v0 + blk * kBonusBlock + lane * 4 + e;
   }
   const unsigned hit = __ballot_sync(0xffffffffu, pick >= 0);
   return hit ? __shfl_sync(0xffffffffu, pick, __ffs(hit) - 1) : -1;
 }
 
+// Global-memory hand-off between a request's leader and helper CTAs.
+__device__ __forceinline__ int ld_acquire(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* ptr, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+// Waits until *ptr >= target, for at most kWaitLimitNs of %globaltimer.
+__device__ __forceinline__ bool poll_at_least(const int* ptr, int target) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire(ptr) < target)
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// The walk: walk_ctas CTAs per request.  CTA 0 (the leader) walks the tree;
+// every pass (a rejection, or the bonus draw's slice totals) is a sum of
+// max(0, p - a q) that the leader and its helpers compute over their slices:
+// the leader posts the pass in the request's WalkSync (fields, then seq with
+// release), each helper sums its slice, stores it and acknowledges (fence,
+// then done += 1), and the leader reads the slice sums once done reaches
+// seq x helpers, adding them in slice order.  A helper handles every command
+// in order (the leader posts the next only after all have acknowledged this
+// one) until the stop command.  Every wait is bounded; a wait that runs out
+// reports TS_DEVERR_TIMEOUT and ends the walk (the call's outputs are then
+// void and the workspace must be zeroed before its next use).  No CTA reads
+// another's shared memory.
 __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleParams p) {
   pdl_wait();
   pdl_launch_dependents();
-  const int b = blockIdx.x;
+  const int K = p.walk_ctas;
+  const int b = blockIdx.x / K, part = blockIdx.x % K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t nb = static_cast<int64_t>(b) * p.n_tree_max;
   const int rows = p.num_req * p.n_tree_max;
   const int V = p.vocab;
+  WalkSync* const sync = p.sync + b;
+  float* const wpart = p.walk_part + static_cast<int64_t>(b) * K;
+  __shared__ float red[kWalkWarps];
+  __shared__ int s_ok;
+  const int n = tree_size(p, b);  // the same for every CTA of the request
+  // ======================= helpers =======================
+  if (part > 0) {
+    if (n == 0) return;  // the leader posts nothing
+    __shared__ int s_kind, s_u;
+    __shared__ float s_a, s_lt, s_ld;
+    int v0, v1;
+    walk_slice(V, K, part, v0, v1);
+    for (int cmd = 1;; ++cmd) {
+      if (tid == 0) {
+        s_ok = poll_at_least(&sync->seq, cmd);
+        if (s_ok) {
+          s_kind = sync->kind;
+          s_u = sync->u;
+          s_a = sync->a;
+          s_lt = sync->lt;
+          s_ld = sync->ld;
+        } else {
+          report_error(p.err, TS_DEVERR_TIMEOUT);
+        }
+      }
+      __syncthreads();
+      if (!s_ok) return;
+      const int kind = s_kind;
+      if (kind == kWalkStop) {
+        if (tid == 0) {
+          __threadfence();
+          atomicAdd(&sync->done, 1);
+        }
+        return;
+      }
+      const int64_t row = (nb + s_u) * V;
+      const float t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, s_lt, s_ld, s_a), red);
+      if (tid == 0) {
+        wpart[part] = t;
+        __threadfence();
+        atomicAdd(&sync->done, 1);
+      }
+      __syncthreads();  // s_* are rewritten by the next command
+    }
+  }
+  // ======================= leader =======================
   __shared__ int par_s[TS_MAX_TREE], tok_s[TS_MAX_TREE], kids[TS_MAX_TREE], path_s[TS_MAX_TREE];
   __shared__ int cnt[kWalkWarps];
-  __shared__ float red[kWalkWarps];
   __shared__ float lse_t, lse_d;
   __shared__ int s_accept;
-  __shared__ int s_bonus, s_blk;
-  __shared__ float s_blk_excl;
+  __shared__ int s_bonus, s_blk, s_slice;
+  __shared__ float s_blk_excl, s_slice_excl;
   __shared__ float s_scan[kWalkWarps];
+  __shared__ float s_tot[kMaxWalkCtas];  // slice sums of the last pass
   __shared__ float bsum[kMaxBonusBlocks];
-  const int n = tree_size(p, b);
   if (n != p.n_tree[b] && tid == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
   if (tid < n) {
     int q = p.parent[nb + tid];
@@ -287,30 +357,63 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     }
     tok_s[tid] = t;
   }
+  if (tid == 0) s_ok = 1;
   __syncthreads();
-  float* const row0 = p.resid + static_cast<int64_t>(b) * 2 * V;
-  float* const row1 = row0 + V;
+  int seq = 0;  // commands posted
+  // One pass: the slice sums of max(0, p - a q) over node u's rows into
+  // s_tot[0 .. K), the leader's own slice first.  Returns their sum (slice order).
+  auto pass = [&](int u, float a, float lt, float ld) -> float {
+    const int64_t row = (nb + u) * V;
+    if (K > 1 && tid == 0) {
+      sync->kind = kWalkSum;
+      sync->u = u;
+      sync->a = a;
+      sync->lt = lt;
+      sync->ld = ld;
+      st_release(&sync->seq, ++seq);
+    } else if (K > 1) {
+      ++seq;
+    }
+    int v0, v1;
+    walk_slice(V, K, 0, v0, v1);
+    const float mine = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, lt, ld, a), red);
+    if (tid == 0) {
+      s_tot[0] = mine;
+      if (K > 1) {
+        if (poll_at_least(&sync->done, seq * (K - 1))) {
+          for (int k = 1; k < K; ++k) s_tot[k] = __ldcg(wpart + k);
+        } else {
+          report_error(p.err, TS_DEVERR_TIMEOUT);
+          s_ok = 0;
+        }
+      }
+    }
+    __syncthreads();
+    float total = 0.f;
+    for (int k = 0; k < K; ++k) total += s_tot[k];
+    return total;
+  };
   int len = 0, bonus = -1;
   if (n > 0) {
     int u = 0;
     len = 1;
     if (tid == 0) path_s[0] = 0;
-    for (int guard = 0; guard < n; ++guard) {
+    for (int guard = 0; guard < n && s_ok; ++guard) {
       // ---- the two log-sum-exps of node u (scaled logits)
       if (warp == 0) {
         for (int which = 0; which < 2; ++which) {
-          float m = -INFINITY, s = 0.f;
+          float m = -INFINITY, sm = 0.f;
           if (lane < p.num_slices) {  // num_slices <= 32
             const float2 ms = p.part[(static_cast<int64_t>(which) * rows + nb + u) * p.num_slices + lane];
             m = ms.x;
-            s = ms.y;
+            sm = ms.y;
           }
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1)
-            lse_pair(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+            lse_pair(m, sm, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sm, o));
           if (lane == 0) {
-            if (which == 0) lse_t = m + logf(s);
-            else lse_d = m + logf(s);
+            if (which == 0) lse_t = m + logf(sm);
+            else lse_d = m + logf(sm);
           }
         }
       }
@@ -329,17 +432,17 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       const float* tl = p.tl + (nb + u) * V;
       const float* dl = p.dl + (nb + u) * V;
       const float lt = lse_t, ld = lse_d;
-      int mode = 0, cur = 0;  // mode 0: r = p_u (from the logits); 1: r = (residual row cur) / rsum
-      float rsum = 1.f;
+      float a = 0.f, sa = 1.f;  // r = max(0, p - a q) / sa: r = p before any rejection
+      float tot_a = -1.f;       // the a that s_tot holds slice sums for (none yet)
       int next = -1;
-      for (int k = 0; k < nk; ++k) {
+      for (int k = 0; k < nk && s_ok; ++k) {
         const int c = kids[k];
         if (tid == 0) {
           const int t = tok_s[c];
           bool acc = false;
           if (t >= 0) {
-            const float rt = mode == 0 ? expf(tl[t] * p.inv_t - lt) : (cur ? row1 : row0)[t] / rsum;
             const float qt = expf(dl[t] * p.inv_t - ld);
+            const float rt = fmaxf(0.f, expf(tl[t] * p.inv_t - lt) - a * qt) / sa;
             acc = qt > 0.f ? (p.u_acc[nb + c] < rt / qt) : rt > 0.f;
           }
           s_accept = acc;
@@ -349,17 +452,18 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
           next = c;
           break;
         }
-        // rejected: the next r is norm(max(0, r - q)), written to the other row
-        float* const dst = cur ? row0 : row1;
-        const float part = mode == 0 ? residual_pass<true>(tl, dl, dst, V, p.inv_t, lt, ld, 1.f)
-                                     : residual_pass<false>(cur ? row1 : row0, dl, dst, V, p.inv_t, lt, ld, 1.f / rsum);
-        const float z = block_sum(part, red);  // also orders the writes before later reads
+        // rejected: r becomes max(0, p - (a + sa) q) / S(a + sa), kept if S is 0
+        const float an = a + sa;
+        const float z = pass(u, an, lt, ld);
         if (z > 0.f) {
-          mode = 1;
-          cur ^= 1;
-          rsum = z;
+          a = an;
+          sa = z;
+          tot_a = an;
+        } else {
+          tot_a = -1.f;  // s_tot now holds the sums for an, not for the a that is kept
         }
       }
+      if (!s_ok) break;
       if (next >= 0) {
         u = next;
         if (tid == 0) path_s[len] = u;
@@ -367,89 +471,134 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
         __syncthreads();
         continue;
       }
-      // ---- the bonus: smallest v with r(0) + ... + r(v) > U * sum(r):
-      //      block sums, a scan of them for the block, a scan inside it
-      const float* src = mode == 0 ? tl : (cur ? row1 : row0);
-      if (mode == 0) block_sums<true>(src, V, p.inv_t, lt, bsum);
-      else block_sums<false>(src, V, p.inv_t, lt, bsum);
-      __syncthreads();
-      const int nb = (V + kBonusBlock - 1) / kBonusBlock;
-      // consecutive block sums per thread (nb <= kMaxBonusBlocks), block exclusive scan
-      const int per = (nb + kWalkThreads - 1) / kWalkThreads;
-      float bs[kBlocksPerThread];
-      float mine = 0.f;
-#pragma unroll
-      for (int e = 0; e < kBlocksPerThread; ++e) {
-        bs[e] = (e < per && tid * per + e < nb) ? bsum[tid * per + e] : 0.f;
-        mine += bs[e];
-      }
-      float inc = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-      }
-      if (lane == 31) s_scan[warp] = inc;
+      // ---- the bonus: the smallest v with r(0) + ... + r(v) > U * sum(r),
+      //      r = max(0, p - a q) unnormalised: the slice that holds the
+      //      target from the slice sums, then block sums, a scan of them for
+      //      the block, and a scan inside it
+      const float total = tot_a == a ? [&] {
+        float t = 0.f;
+        for (int k = 0; k < K; ++k) t += s_tot[k];
+        return t;
+      }()
+                                     : pass(u, a, lt, ld);
+      if (!s_ok) break;
+      const float target = p.u_bonus[nb + u] * total;
       if (tid == 0) {
+        float excl = 0.f;
+        int sl = -1, last_pos = -1;
+        for (int k = 0; k < K; ++k) {
+          if (s_tot[k] > 0.f) {
+            last_pos = k;
+            if (sl < 0 && excl <= target && target < excl + s_tot[k]) {
+              sl = k;
+              s_slice_excl = excl;
+            }
+          }
+          excl += s_tot[k];
+        }
+        if (sl < 0) {  // rounding put the target at or past the total: the last slice with r > 0
+          sl = last_pos;
+          s_slice_excl = -1.f;  // take its last token with r > 0
+        }
+        s_slice = sl;
         s_bonus = -1;
         s_blk = -1;
       }
       __syncthreads();
-      if (warp == 0) {
-        float w = lane < kWalkWarps ? s_scan[lane] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, w, o);
-          if (lane >= o) w += y;
-        }
-        if (lane < kWalkWarps) s_scan[lane] = w;  // inclusive warp totals
-      }
-      __syncthreads();
-      const float total = s_scan[kWalkWarps - 1];
-      const float target = p.u_bonus[nb_row(p, b) + u] * total;
-      float excl = (warp > 0 ? s_scan[warp - 1] : 0.f) + inc - mine;
-#pragma unroll
-      for (int e = 0; e < kBlocksPerThread; ++e) {
-        if (bs[e] > 0.f && excl <= target && target < excl + bs[e]) {
-          s_blk = tid * per + e;
-          s_blk_excl = excl;
-        }
-        excl += bs[e];
-      }
-      __syncthreads();
-      if (warp == 0 && s_blk >= 0) {
-        const int v = mode == 0 ? scan_block<true>(src, V, p.inv_t, lt, s_blk, s_blk_excl, target)
-                                : scan_block<false>(src, V, p.inv_t, lt, s_blk, s_blk_excl, target);
-        if (lane == 0) s_bonus = v;
-      }
-      __syncthreads();
-      if (s_bonus < 0) {  // rounding put the target at or past the total: the last token with r > 0
-        int last = -1;
-        for (int blk = nb - 1 - tid; blk >= 0; blk -= kWalkThreads)
-          if (bsum[blk] > 0.f) {
-            last = blk;
-            break;
-          }
-        last = __reduce_max_sync(0xffffffffu, last);
-        if (lane == 0) cnt[warp] = last;
+      const int sl = s_slice;
+      if (sl >= 0) {
+        int v0, v1;
+        walk_slice(V, K, sl, v0, v1);
+        const bool take_last = s_slice_excl < 0.f;
+        const float ltarget = target - (take_last ? 0.f : s_slice_excl);
+        slice_block_sums(tl, dl, V, v0, v1, p.inv_t, lt, ld, a, bsum);
         __syncthreads();
-        if (warp == 0) {
-          int blk = lane < kWalkWarps ? cnt[lane] : -1;
-          blk = __reduce_max_sync(0xffffffffu, blk);
-          int v = -1;
-          if (blk >= 0) {
-            for (int e = lane; e < kBonusBlock; e += 32) {
-              const int t = blk * kBonusBlock + e;
-              if (t < V && (mode == 0 ? expf(__ldcg(src + t) * p.inv_t - lt) : __ldcg(src + t)) > 0.f) v = t;
+        const int nbk = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
+        if (!take_last) {
+          // consecutive block sums per thread (nbk <= kMaxBonusBlocks), block exclusive scan
+          const int per = (nbk + kWalkThreads - 1) / kWalkThreads;
+          float bs[kBlocksPerThread];
+          float mine = 0.f;
+#pragma unroll
+          for (int e = 0; e < kBlocksPerThread; ++e) {
+            bs[e] = (e < per && tid * per + e < nbk) ? bsum[tid * per + e] : 0.f;
+            mine += bs[e];
+          }
+          float inc = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          if (lane == 31) s_scan[warp] = inc;
+          __syncthreads();
+          if (warp == 0) {
+            float w = lane < kWalkWarps ? s_scan[lane] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const float y = __shfl_up_sync(0xffffffffu, w, o);
+              if (lane >= o) w += y;
             }
+            if (lane < kWalkWarps) s_scan[lane] = w;  // inclusive warp totals
           }
-          v = __reduce_max_sync(0xffffffffu, v);
-          if (lane == 0) s_bonus = v;
+          __syncthreads();
+          float excl = (warp > 0 ? s_scan[warp - 1] : 0.f) + inc - mine;
+#pragma unroll
+          for (int e = 0; e < kBlocksPerThread; ++e) {
+            if (bs[e] > 0.f && excl <= ltarget && ltarget < excl + bs[e]) {
+              s_blk = tid * per + e;
+              s_blk_excl = excl;
+            }
+            excl += bs[e];
+          }
+          __syncthreads();
+          if (warp == 0 && s_blk >= 0) {
+            const int v = scan_block(tl, dl, v0, v1, p.inv_t, lt, ld, a, s_blk, s_blk_excl, ltarget);
+            if (lane == 0) s_bonus = v;
+          }
+          __syncthreads();
         }
-        __syncthreads();
+        if (s_bonus < 0) {  // the last token of the slice with r > 0
+          int lastb = -1;
+          for (int blk = nbk - 1 - tid; blk >= 0; blk -= kWalkThreads)
+            if (bsum[blk] > 0.f) {
+              lastb = blk;
+              break;
+            }
+          lastb = __reduce_max_sync(0xffffffffu, lastb);
+          if (lane == 0) cnt[warp] = lastb;
+          __syncthreads();
+          if (warp == 0) {
+            int blk = lane < kWalkWarps ? cnt[lane] : -1;
+            blk = __reduce_max_sync(0xffffffffu, blk);
+            int v = -1;
+            if (blk >= 0) {
+              for (int e = lane; e < kBonusBlock; e += 32) {
+                const int t = v0 + blk * kBonusBlock + e;
+                if (t < v1 && r_of(__ldcg(tl + t), __ldcg(dl + t), p.inv_t, lt, ld, a) > 0.f) v = t;
+              }
+            }
+            v = __reduce_max_sync(0xffffffffu, v);
+            if (lane == 0) s_bonus = v;
+          }
+          __syncthreads();
+        }
       }
       bonus = s_bonus;
       break;
+    }
+    // the helpers stop; with every acknowledgement in, the counters go back to zero
+    if (K > 1 && tid == 0) {
+      if (s_ok) {
+        sync->kind = kWalkStop;
+        st_release(&sync->seq, seq + 1);
+        if (poll_at_least(&sync->done, (seq + 1) * (K - 1))) {
+          st_release(&sync->done, 0);
+          st_release(&sync->seq, 0);
+        } else {
+          report_error(p.err, TS_DEVERR_TIMEOUT);
+        }
+      }
     }
   }
   __syncthreads();
@@ -473,7 +622,7 @@ cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream) {
   const dim3 grid(2 * p.num_req * p.n_tree_max, p.num_slices);
   cudaError_t e = launch_pdl(sample_lse_kernel, grid, dim3(kLseThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(sample_walk_kernel, dim3(p.num_req), dim3(kWalkThreads), 0, stream, p);
+  return launch_pdl(sample_walk_kernel, dim3(p.num_req * p.walk_ctas), dim3(kWalkThreads), 0, stream, p);
 }
 
 }  // namespace ts
