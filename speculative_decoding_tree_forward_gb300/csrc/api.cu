@@ -562,8 +562,7 @@ size_t tree_accept_sample_workspace_size(const ts_sample_args* a) {
   const int slice = sample_slice(a->vocab, rows);
   const int64_t slices = (a->vocab + slice - 1) / slice;
   return kWsHeader + align256(static_cast<size_t>(rows * slices) * sizeof(float2)) +
-         align256(static_cast<size_t>(a->num_requests) * sizeof(WalkSync)) +
-         align256(static_cast<size_t>(a->num_requests) * kMaxWalkCtas * sizeof(float));
+         align256(static_cast<size_t>(a->num_requests) * sizeof(WalkSync));
 }
 
 ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t workspace_bytes, void* stream) {
@@ -604,7 +603,6 @@ ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t wo
   const size_t sync_off = kWsHeader + align256(static_cast<size_t>(rows * p.num_slices) * sizeof(float2));
   p.walk_ctas = sample_walk_ctas(a->num_requests);
   p.sync = reinterpret_cast<WalkSync*>(ws + sync_off);
-  p.walk_part = reinterpret_cast<float*>(ws + sync_off + align256(static_cast<size_t>(a->num_requests) * sizeof(WalkSync)));
   cudaError_t e = launch_sample(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }

@@ -177,16 +177,16 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
 // One request's hand-off between the walk's leader CTA and its helpers (in
 // the workspace; zero before the first call, left at zero by every call
-// that ends without a timeout).
+// that ends without a timeout).  A command is one 64-bit word: its sequence
+// number (bits 48..63, from 1), the node (bits 32..47; kWalkStopNode to
+// stop) and the pass's threshold a (bits 0..31, fp32); helper k answers in
+// slot[k]: the sequence number (bits 32..63) and its slice sum (fp32).
 struct WalkSync {
-  int seq;          // commands posted by the leader
-  int done;         // acknowledgements by the helpers, over all commands
-  int kind;         // the command: kWalkSum or kWalkStop
-  int u;            // the node whose rows the pass reads
-  float a, lt, ld;  // the pass sums max(0, p - a q), p = exp(tl / T - lt), q = exp(dl / T - ld)
-  int pad[9];       // one 64-byte line per request
+  unsigned long long cmd;
+  unsigned long long slot[16];
+  unsigned long long pad[15];  // 256 bytes per request
 };
-constexpr int kWalkSum = 1, kWalkStop = 2;
+constexpr int kWalkStopNode = 0xffff;
 constexpr int kMaxWalkCtas = 16;
 
 struct SampleParams {
@@ -208,8 +208,7 @@ struct SampleParams {
   unsigned* err;
   float2* part;           // [2][num_req * n_tree_max][num_slices]: (max, sum of exp) of logit / T
   int walk_ctas;          // CTAs per request in the walk: one leader and walk_ctas - 1 helpers
-  WalkSync* sync;         // [num_req]: the leader's commands and the helpers' acknowledgements
-  float* walk_part;       // [num_req][walk_ctas]: each CTA's slice sum of the last pass
+  WalkSync* sync;         // [num_req]: the leader's commands and the helpers' slice sums
 };
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream);
 

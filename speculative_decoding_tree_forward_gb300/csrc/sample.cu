@@ -249,35 +249,50 @@ __device__ __forceinline__ int scan_block(const float* __restrict__ tl, const fl
   return hit ? __shfl_sync(0xffffffffu, pick, __ffs(hit) - 1) : -1;
 }
 
-// Global-memory hand-off between a request's leader and helper CTAs.
-__device__ __forceinline__ int ld_acquire(const int* ptr) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+// Global-memory hand-off between a request's leader and helper CTAs: one
+// 64-bit word each way, written with release and polled with acquire, so a
+// command and its answer each cost one one-way latency.
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* ptr) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release(int* ptr, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+__device__ __forceinline__ void st_release64(unsigned long long* ptr, unsigned long long v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
 }
-// Waits until *ptr >= target, for at most kWaitLimitNs of %globaltimer.
-__device__ __forceinline__ bool poll_at_least(const int* ptr, int target) {
+// Waits until the word's bits from `shift` up equal `want`, for at most
+// kWaitLimitNs of %globaltimer; the word read last goes to *got.
+__device__ __forceinline__ bool poll_tag(const unsigned long long* ptr, int shift, unsigned long long want,
+                                         unsigned long long* got) {
   const uint64_t t0 = globaltimer_ns();
-  while (ld_acquire(ptr) < target)
+  for (;;) {
+    const unsigned long long v = ld_acquire64(ptr);
+    if ((v >> shift) == want) {
+      *got = v;
+      return true;
+    }
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  return true;
+  }
+}
+__device__ __forceinline__ unsigned long long walk_cmd(int seq, int u, float a) {
+  return (static_cast<unsigned long long>(seq & 0xffff) << 48) | (static_cast<unsigned long long>(u & 0xffff) << 32) |
+         __float_as_uint(a);
 }
 
 // The walk: walk_ctas CTAs per request.  CTA 0 (the leader) walks the tree;
 // every pass (a rejection, or the bonus draw's slice totals) is a sum of
-// max(0, p - a q) that the leader and its helpers compute over their slices:
-// the leader posts the pass in the request's WalkSync (fields, then seq with
-// release), each helper sums its slice, stores it and acknowledges (fence,
-// then done += 1), and the leader reads the slice sums once done reaches
-// seq x helpers, adding them in slice order.  A helper handles every command
-// in order (the leader posts the next only after all have acknowledged this
-// one) until the stop command.  Every wait is bounded; a wait that runs out
-// reports TS_DEVERR_TIMEOUT and ends the walk (the call's outputs are then
-// void and the workspace must be zeroed before its next use).  No CTA reads
-// another's shared memory.
+// max(0, p - a q) over the vocab that the leader and its helpers compute
+// over their slices: the leader posts (seq, node, a) in the request's command
+// word, helper k answers (seq, slice sum) in its slot, and the leader adds
+// the slice sums in slice order.  A helper handles every command in order
+// (the leader posts the next only after every helper has answered this one)
+// until the stop command; the leader then zeroes the words.  Every CTA first
+// forms the log-sum-exps of all the request's nodes, and the leader p and q
+// of every node's own token under its parent, so a visited node costs no
+// memory round trip.  Every wait is bounded; one that runs out reports
+// TS_DEVERR_TIMEOUT and ends the walk (the call's outputs are void and the
+// workspace must be zeroed before its next use).  No CTA reads another's
+// shared memory.
 __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -288,54 +303,65 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
   const int rows = p.num_req * p.n_tree_max;
   const int V = p.vocab;
   WalkSync* const sync = p.sync + b;
-  float* const wpart = p.walk_part + static_cast<int64_t>(b) * K;
   __shared__ float red[kWalkWarps];
+  __shared__ float lt_s[TS_MAX_TREE], ld_s[TS_MAX_TREE];  // log-sum-exps of every node's rows
   __shared__ int s_ok;
   const int n = tree_size(p, b);  // the same for every CTA of the request
+  if (tid < n) {                  // node tid's two log-sum-exps from the statistics partials
+    float m[2] = {-INFINITY, -INFINITY}, sm[2] = {0.f, 0.f};
+    for (int j0 = 0; j0 < p.num_slices; j0 += 8) {  // eight slices of both rows requested together
+      float2 x[2][8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+        for (int which = 0; which < 2; ++which)
+          x[which][jj] = j0 + jj < p.num_slices
+                             ? p.part[(static_cast<int64_t>(which) * rows + nb + tid) * p.num_slices + j0 + jj]
+                             : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+        for (int which = 0; which < 2; ++which) lse_pair(m[which], sm[which], x[which][jj].x, x[which][jj].y);
+    }
+    lt_s[tid] = m[0] + logf(sm[0]);
+    ld_s[tid] = m[1] + logf(sm[1]);
+  }
+  __syncthreads();
   // ======================= helpers =======================
   if (part > 0) {
     if (n == 0) return;  // the leader posts nothing
-    __shared__ int s_kind, s_u;
-    __shared__ float s_a, s_lt, s_ld;
+    __shared__ int s_u;
+    __shared__ float s_a;
     int v0, v1;
     walk_slice(V, K, part, v0, v1);
-    for (int cmd = 1;; ++cmd) {
+    for (int seq = 1;; ++seq) {
       if (tid == 0) {
-        s_ok = poll_at_least(&sync->seq, cmd);
-        if (s_ok) {
-          s_kind = sync->kind;
-          s_u = sync->u;
-          s_a = sync->a;
-          s_lt = sync->lt;
-          s_ld = sync->ld;
-        } else {
-          report_error(p.err, TS_DEVERR_TIMEOUT);
-        }
+        unsigned long long c = 0;
+        s_ok = poll_tag(&sync->cmd, 48, static_cast<unsigned long long>(seq & 0xffff), &c);
+        s_u = static_cast<int>((c >> 32) & 0xffff);
+        s_a = __uint_as_float(static_cast<unsigned>(c));
+        if (!s_ok) report_error(p.err, TS_DEVERR_TIMEOUT);
       }
       __syncthreads();
       if (!s_ok) return;
-      const int kind = s_kind;
-      if (kind == kWalkStop) {
-        if (tid == 0) {
-          __threadfence();
-          atomicAdd(&sync->done, 1);
-        }
-        return;
+      const int u = s_u;
+      float t = 0.f;
+      if (u != kWalkStopNode) {
+        const int64_t row = (nb + u) * V;
+        t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, lt_s[u], ld_s[u], s_a), red);
       }
-      const int64_t row = (nb + s_u) * V;
-      const float t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, s_lt, s_ld, s_a), red);
-      if (tid == 0) {
-        wpart[part] = t;
-        __threadfence();
-        atomicAdd(&sync->done, 1);
-      }
-      __syncthreads();  // s_* are rewritten by the next command
+      if (tid == 0)
+        st_release64(&sync->slot[part],
+                     (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(t));
+      if (u == kWalkStopNode) return;
+      __syncthreads();  // s_u, s_a are rewritten by the next command
     }
   }
   // ======================= leader =======================
   __shared__ int par_s[TS_MAX_TREE], tok_s[TS_MAX_TREE], kids[TS_MAX_TREE], path_s[TS_MAX_TREE];
+  __shared__ float pc_s[TS_MAX_TREE], qc_s[TS_MAX_TREE];  // p and q of node c's token under its parent
+  __shared__ float ua_s[TS_MAX_TREE], ub_s[TS_MAX_TREE];  // the uniforms of every node
   __shared__ int cnt[kWalkWarps];
-  __shared__ float lse_t, lse_d;
   __shared__ int s_accept;
   __shared__ int s_bonus, s_blk, s_slice;
   __shared__ float s_blk_excl, s_slice_excl;
@@ -356,36 +382,37 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       t = -1;
     }
     tok_s[tid] = t;
+    float pc = 0.f, qc = 0.f;
+    if (q >= 0 && t >= 0) {
+      const int64_t row = (nb + q) * V;
+      pc = expf(p.tl[row + t] * p.inv_t - lt_s[q]);
+      qc = expf(p.dl[row + t] * p.inv_t - ld_s[q]);
+    }
+    pc_s[tid] = pc;
+    qc_s[tid] = qc;
+    ua_s[tid] = p.u_acc[nb + tid];
+    ub_s[tid] = p.u_bonus[nb + tid];
   }
   if (tid == 0) s_ok = 1;
   __syncthreads();
   int seq = 0;  // commands posted
   // One pass: the slice sums of max(0, p - a q) over node u's rows into
   // s_tot[0 .. K), the leader's own slice first.  Returns their sum (slice order).
-  auto pass = [&](int u, float a, float lt, float ld) -> float {
+  auto pass = [&](int u, float a) -> float {
+    ++seq;
+    if (K > 1 && tid == 0) st_release64(&sync->cmd, walk_cmd(seq, u, a));
     const int64_t row = (nb + u) * V;
-    if (K > 1 && tid == 0) {
-      sync->kind = kWalkSum;
-      sync->u = u;
-      sync->a = a;
-      sync->lt = lt;
-      sync->ld = ld;
-      st_release(&sync->seq, ++seq);
-    } else if (K > 1) {
-      ++seq;
-    }
     int v0, v1;
     walk_slice(V, K, 0, v0, v1);
-    const float mine = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, lt, ld, a), red);
-    if (tid == 0) {
-      s_tot[0] = mine;
-      if (K > 1) {
-        if (poll_at_least(&sync->done, seq * (K - 1))) {
-          for (int k = 1; k < K; ++k) s_tot[k] = __ldcg(wpart + k);
-        } else {
-          report_error(p.err, TS_DEVERR_TIMEOUT);
-          s_ok = 0;
-        }
+    const float mine = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, lt_s[u], ld_s[u], a), red);
+    if (tid == 0) s_tot[0] = mine;
+    if (warp == 0 && lane + 1 < K) {  // lane k - 1 collects helper k's answer
+      unsigned long long v = 0;
+      if (poll_tag(&sync->slot[lane + 1], 32, static_cast<unsigned long long>(seq), &v)) {
+        s_tot[lane + 1] = __uint_as_float(static_cast<unsigned>(v));
+      } else {
+        report_error(p.err, TS_DEVERR_TIMEOUT);
+        s_ok = 0;
       }
     }
     __syncthreads();
@@ -399,24 +426,6 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     len = 1;
     if (tid == 0) path_s[0] = 0;
     for (int guard = 0; guard < n && s_ok; ++guard) {
-      // ---- the two log-sum-exps of node u (scaled logits)
-      if (warp == 0) {
-        for (int which = 0; which < 2; ++which) {
-          float m = -INFINITY, sm = 0.f;
-          if (lane < p.num_slices) {  // num_slices <= 32
-            const float2 ms = p.part[(static_cast<int64_t>(which) * rows + nb + u) * p.num_slices + lane];
-            m = ms.x;
-            sm = ms.y;
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-            lse_pair(m, sm, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sm, o));
-          if (lane == 0) {
-            if (which == 0) lse_t = m + logf(sm);
-            else lse_d = m + logf(sm);
-          }
-        }
-      }
       // ---- children of u in index order
       const bool kid = tid < n && par_s[tid] == u;
       const unsigned bal = __ballot_sync(0xffffffffu, kid);
@@ -431,19 +440,18 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       __syncthreads();
       const float* tl = p.tl + (nb + u) * V;
       const float* dl = p.dl + (nb + u) * V;
-      const float lt = lse_t, ld = lse_d;
+      const float lt = lt_s[u], ld = ld_s[u];
       float a = 0.f, sa = 1.f;  // r = max(0, p - a q) / sa: r = p before any rejection
       float tot_a = -1.f;       // the a that s_tot holds slice sums for (none yet)
       int next = -1;
       for (int k = 0; k < nk && s_ok; ++k) {
         const int c = kids[k];
         if (tid == 0) {
-          const int t = tok_s[c];
           bool acc = false;
-          if (t >= 0) {
-            const float qt = expf(dl[t] * p.inv_t - ld);
-            const float rt = fmaxf(0.f, expf(tl[t] * p.inv_t - lt) - a * qt) / sa;
-            acc = qt > 0.f ? (p.u_acc[nb + c] < rt / qt) : rt > 0.f;
+          if (tok_s[c] >= 0) {
+            const float qt = qc_s[c];
+            const float rt = fmaxf(0.f, pc_s[c] - a * qt) / sa;
+            acc = qt > 0.f ? (ua_s[c] < rt / qt) : rt > 0.f;
           }
           s_accept = acc;
         }
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
         }
         // rejected: r becomes max(0, p - (a + sa) q) / S(a + sa), kept if S is 0
         const float an = a + sa;
-        const float z = pass(u, an, lt, ld);
+        const float z = pass(u, an);
         if (z > 0.f) {
           a = an;
           sa = z;
@@ -475,14 +483,14 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       //      r = max(0, p - a q) unnormalised: the slice that holds the
       //      target from the slice sums, then block sums, a scan of them for
       //      the block, and a scan inside it
-      const float total = tot_a == a ? [&] {
-        float t = 0.f;
-        for (int k = 0; k < K; ++k) t += s_tot[k];
-        return t;
-      }()
-                                     : pass(u, a, lt, ld);
+      float total = 0.f;
+      if (tot_a == a) {
+        for (int k = 0; k < K; ++k) total += s_tot[k];
+      } else {
+        total = pass(u, a);
+      }
       if (!s_ok) break;
-      const float target = p.u_bonus[nb + u] * total;
+      const float target = ub_s[u] * total;
       if (tid == 0) {
         float excl = 0.f;
         int sl = -1, last_pos = -1;
@@ -587,16 +595,20 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       bonus = s_bonus;
       break;
     }
-    // the helpers stop; with every acknowledgement in, the counters go back to zero
-    if (K > 1 && tid == 0) {
-      if (s_ok) {
-        sync->kind = kWalkStop;
-        st_release(&sync->seq, seq + 1);
-        if (poll_at_least(&sync->done, (seq + 1) * (K - 1))) {
-          st_release(&sync->done, 0);
-          st_release(&sync->seq, 0);
-        } else {
-          report_error(p.err, TS_DEVERR_TIMEOUT);
+    // the helpers stop; with every answer in, the words go back to zero
+    if (K > 1 && s_ok) {
+      ++seq;
+      if (tid == 0) st_release64(&sync->cmd, walk_cmd(seq, kWalkStopNode, 0.f));
+      if (warp == 0) {
+        bool all = true;
+        if (lane + 1 < K) {
+          unsigned long long v = 0;
+          all = poll_tag(&sync->slot[lane + 1], 32, static_cast<unsigned long long>(seq), &v);
+          if (!all) report_error(p.err, TS_DEVERR_TIMEOUT);
+        }
+        if (__all_sync(0xffffffffu, all)) {
+          if (lane + 1 < K) st_release64(&sync->slot[lane + 1], 0ull);
+          if (lane == 0) st_release64(&sync->cmd, 0ull);
         }
       }
     }
