@@ -311,15 +311,17 @@ TS_API ts_status tree_cache_compact_batch(const ts_compact_args* args, int count
  *   path[b][0..AL) = accepted nodes (root first, -1 after), accept_len[b] =
  *   AL in [1, 1 + depth], bonus[b]; verified[b] = tokens(path) ++ bonus
  *   (-1 after, optional), verified_len[b] = AL + 1 (optional).
- * The uniforms are inputs in [0, 1).  Arithmetic: fp32 (exp of scaled
- * logits minus the row's log-sum-exp); a decision within fp32 rounding of
- * its threshold may go either way.  Workspace: tree_accept_sample_workspace_size(),
+ * The uniforms are inputs in [0, 1).  Arithmetic: fp32, each probability
+ * 2^(logit * log2(e) / T - the row's base-2 log-sum-exp) by the hardware's
+ * approximate 2^x (relative error about 2^-22; below 2^-126 it is 0); a
+ * decision within that rounding of its threshold may go either way.  Workspace: tree_accept_sample_workspace_size(),
  * zero-filled before its first use; besides the error word it holds
  * per-request counters that every call leaves at zero, except a call that
  * reports TS_DEVERR_TIMEOUT (its outputs are void; zero the workspace before
  * reusing it).
  * Errors: TS_ERR_INVALID_ARG unless temperature > 0 and finite;
- * TS_ERR_UNSUPPORTED if vocab > 262144 or n_tree_max > TS_MAX_TREE.
+ * TS_ERR_UNSUPPORTED if vocab > 262144 or n_tree_max > TS_MAX_TREE, or if
+ * log2(e) / temperature overflows fp32 (a temperature below about 4e-39).
  * ------------------------------------------------------------------------ */
 typedef struct ts_sample_args {
   int num_requests;           /* >= 1 */

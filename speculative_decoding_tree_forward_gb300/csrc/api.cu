@@ -585,7 +585,8 @@ ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t wo
   p.vocab = a->vocab;
   p.slice = sample_slice(a->vocab, rows);
   p.num_slices = (a->vocab + p.slice - 1) / p.slice;
-  p.inv_t = 1.0f / a->temperature;
+  p.scale2 = static_cast<float>(1.4426950408889634 / static_cast<double>(a->temperature));  // log2(e) / T
+  if (!std::isfinite(p.scale2)) return TS_ERR_UNSUPPORTED;
   p.tl = a->target_logits;
   p.dl = a->draft_logits;
   p.tokens = a->tokens;

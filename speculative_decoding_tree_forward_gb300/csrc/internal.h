@@ -192,7 +192,7 @@ constexpr int kMaxWalkCtas = 16;
 struct SampleParams {
   int num_req, n_tree_max, vocab;
   int slice, num_slices;  // vocab floats per statistics CTA (multiple of 1024), slices per row (<= 32)
-  float inv_t;            // 1 / temperature
+  float scale2;           // log2(e) / temperature: every exponential is 2^(x scale2 - lse2)
   const float* tl;
   const float* dl;
   const int32_t* tokens;

@@ -9,7 +9,7 @@
 // current node; when all are rejected the bonus is drawn from r.
 //
 // Kernel 1 (row statistics) streams every target and draft row of the tree
-// once in vocab slices and keeps (max, sum of exp(z - max)) of z = logit / T.
+// once in vocab slices and keeps (max, sum of 2^(z - max)) of z = logit log2(e) / T.
 // Kernel 2 (walk) runs a leader CTA and up to 15 helper CTAs per request
 // (512 threads each): the leader merges a visited node's slices into the two
 // log-sum-exps, lists its children with a ballot and tests each child from
@@ -31,12 +31,17 @@ constexpr int kLseThreads = 256;
 constexpr int kWalkThreads = 512;
 constexpr int kWalkWarps = kWalkThreads / 32;
 
+// Logits enter every exponential as x * scale2 with scale2 = log2(e) / T, so
+// a row's statistics are (m, s) with m = max_v x_v scale2 and
+// s = sum_v 2^(x_v scale2 - m), its log-sum-exp in base 2 is m + log2(s), and
+// p(v) = 2^(x_v scale2 - lse2): the same softmax at temperature T, each
+// exponential one ex2 instruction.
 __device__ __forceinline__ void lse_pair(float& m, float& s, float om, float os) {
   if (om > m) {
-    s = s * expf(m - om) + os;
+    s = s * ex2_approx(m - om) + os;
     m = om;
   } else if (om != -INFINITY) {
-    s += os * expf(om - m);
+    s += os * ex2_approx(om - m);
   }
 }
 
@@ -70,18 +75,18 @@ __global__ void __launch_bounds__(kLseThreads, 8) sample_lse_kernel(const Sample
       float bm = m;
 #pragma unroll
       for (int q = 0; q < kLoads; ++q)
-        bm = fmaxf(bm, fmaxf(fmaxf(f[q].x, f[q].y), fmaxf(f[q].z, f[q].w)) * p.inv_t);
+        bm = fmaxf(bm, fmaxf(fmaxf(f[q].x, f[q].y), fmaxf(f[q].z, f[q].w)) * p.scale2);
       if (bm > m) {
-        s *= expf(m - bm);
+        s *= ex2_approx(m - bm);
         m = bm;
       }
 #pragma unroll
       for (int q = 0; q < kLoads; ++q)
-        s += (expf(f[q].x * p.inv_t - m) + expf(f[q].y * p.inv_t - m)) +
-             (expf(f[q].z * p.inv_t - m) + expf(f[q].w * p.inv_t - m));
+        s += (ex2_approx(fmaf(f[q].x, p.scale2, -m)) + ex2_approx(fmaf(f[q].y, p.scale2, -m))) +
+             (ex2_approx(fmaf(f[q].z, p.scale2, -m)) + ex2_approx(fmaf(f[q].w, p.scale2, -m)));
     }
   } else {
-    for (int64_t x = v0 + threadIdx.x; x < v1; x += kLseThreads) lse_pair(m, s, __ldcs(lg + x) * p.inv_t, 1.f);
+    for (int64_t x = v0 + threadIdx.x; x < v1; x += kLseThreads) lse_pair(m, s, __ldcs(lg + x) * p.scale2, 1.f);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lse_pair(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
@@ -127,8 +132,8 @@ constexpr int kBlocksPerThread = 4;
 constexpr int kMaxBonusBlocks = kBlocksPerThread * kWalkThreads;  // slice <= 262144 tokens
 constexpr int kBlocksInFlight = 8;                                // a warp's block sums in flight
 
-__device__ __forceinline__ float r_of(float xt, float xd, float inv_t, float lt, float ld, float a) {
-  return fmaxf(0.f, expf(xt * inv_t - lt) - a * expf(xd * inv_t - ld));
+__device__ __forceinline__ float r_of(float xt, float xd, float scale2, float lt, float ld, float a) {
+  return fmaxf(0.f, ex2_approx(fmaf(xt, scale2, -lt)) - a * ex2_approx(fmaf(xd, scale2, -ld)));
 }
 
 // Slice k of K of a row of V tokens: [v0, v1), v0 a multiple of 4.
@@ -141,7 +146,7 @@ __device__ __forceinline__ void walk_slice(int V, int K, int k, int& v0, int& v1
 // This thread's share of sum_{v in [v0, v1)} r(v) over node u's rows tl, dl,
 // with four 16-byte loads of each row in flight per thread.
 __device__ __forceinline__ float slice_sum(const float* __restrict__ tl, const float* __restrict__ dl, int V, int v0,
-                                           int v1, float inv_t, float lt, float ld, float a) {
+                                           int v1, float scale2, float lt, float ld, float a) {
   float part = 0.f;
   if ((V & 3) == 0) {
     constexpr int kLoads = 4;
@@ -161,13 +166,13 @@ __device__ __forceinline__ float slice_sum(const float* __restrict__ tl, const f
 #pragma unroll
       for (int q = 0; q < kLoads; ++q)
         if (x0 + q * kWalkThreads < e4)
-          part += (r_of(ft[q].x, fd[q].x, inv_t, lt, ld, a) + r_of(ft[q].y, fd[q].y, inv_t, lt, ld, a)) +
-                  (r_of(ft[q].z, fd[q].z, inv_t, lt, ld, a) + r_of(ft[q].w, fd[q].w, inv_t, lt, ld, a));
+          part += (r_of(ft[q].x, fd[q].x, scale2, lt, ld, a) + r_of(ft[q].y, fd[q].y, scale2, lt, ld, a)) +
+                  (r_of(ft[q].z, fd[q].z, scale2, lt, ld, a) + r_of(ft[q].w, fd[q].w, scale2, lt, ld, a));
     }
   } else {
 #pragma unroll 4
     for (int v = v0 + static_cast<int>(threadIdx.x); v < v1; v += kWalkThreads)
-      part += r_of(__ldcg(tl + v), __ldcg(dl + v), inv_t, lt, ld, a);
+      part += r_of(__ldcg(tl + v), __ldcg(dl + v), scale2, lt, ld, a);
   }
   return part;
 }
@@ -176,7 +181,7 @@ __device__ __forceinline__ float slice_sum(const float* __restrict__ tl, const f
 // [v0 + 128 i, ...)), warp per block with kBlocksInFlight blocks of a warp
 // requested before any is summed, into bsum[0 .. ceil((v1 - v0) / 128)).
 __device__ __forceinline__ void slice_block_sums(const float* __restrict__ tl, const float* __restrict__ dl, int V,
-                                                 int v0, int v1, float inv_t, float lt, float ld, float a, float* bsum) {
+                                                 int v0, int v1, float scale2, float lt, float ld, float a, float* bsum) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
   for (int b0 = warp; b0 < nb; b0 += kBlocksInFlight * kWalkWarps) {
@@ -195,8 +200,8 @@ __device__ __forceinline__ void slice_block_sums(const float* __restrict__ tl, c
       }
 #pragma unroll
       for (int j = 0; j < kBlocksInFlight; ++j)
-        t[j] = ((in >> j) & 1u) ? (r_of(ft[j].x, fd[j].x, inv_t, lt, ld, a) + r_of(ft[j].y, fd[j].y, inv_t, lt, ld, a)) +
-                                      (r_of(ft[j].z, fd[j].z, inv_t, lt, ld, a) + r_of(ft[j].w, fd[j].w, inv_t, lt, ld, a))
+        t[j] = ((in >> j) & 1u) ? (r_of(ft[j].x, fd[j].x, scale2, lt, ld, a) + r_of(ft[j].y, fd[j].y, scale2, lt, ld, a)) +
+                                      (r_of(ft[j].z, fd[j].z, scale2, lt, ld, a) + r_of(ft[j].w, fd[j].w, scale2, lt, ld, a))
                                 : 0.f;
     } else {
 #pragma unroll
@@ -205,7 +210,7 @@ __device__ __forceinline__ void slice_block_sums(const float* __restrict__ tl, c
 #pragma unroll
         for (int e = 0; e < kBonusBlock / 32; ++e) {
           const int v = v0 + (b0 + j * kWalkWarps) * kBonusBlock + e * 32 + lane;
-          if (b0 + j * kWalkWarps < nb && v < v1) t[j] += r_of(__ldcg(tl + v), __ldcg(dl + v), inv_t, lt, ld, a);
+          if (b0 + j * kWalkWarps < nb && v < v1) t[j] += r_of(__ldcg(tl + v), __ldcg(dl + v), scale2, lt, ld, a);
         }
       }
     }
@@ -222,14 +227,14 @@ __device__ __forceinline__ void slice_block_sums(const float* __restrict__ tl, c
 // Inside block blk of the slice: the smallest token with excl + r(block start
 // .. v) > target (warp-wide: lane l holds tokens 4l .. 4l + 3 of the block), or -1.
 __device__ __forceinline__ int scan_block(const float* __restrict__ tl, const float* __restrict__ dl, int v0, int v1,
-                                          float inv_t, float lt, float ld, float a, int blk, float excl, float target) {
+                                          float scale2, float lt, float ld, float a, int blk, float excl, float target) {
   const int lane = threadIdx.x & 31;
   float r4[4];
   float mine = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int v = v0 + blk * kBonusBlock + lane * 4 + e;
-    r4[e] = v < v1 ? r_of(__ldcg(tl + v), __ldcg(dl + v), inv_t, lt, ld, a) : 0.f;
+    r4[e] = v < v1 ? r_of(__ldcg(tl + v), __ldcg(dl + v), scale2, lt, ld, a) : 0.f;
     mine += r4[e];
   }
   float inc = mine;
@@ -323,8 +328,8 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
 #pragma unroll
         for (int which = 0; which < 2; ++which) lse_pair(m[which], sm[which], x[which][jj].x, x[which][jj].y);
     }
-    lt_s[tid] = m[0] + logf(sm[0]);
-    ld_s[tid] = m[1] + logf(sm[1]);
+    lt_s[tid] = m[0] + log2f(sm[0]);
+    ld_s[tid] = m[1] + log2f(sm[1]);
   }
   __syncthreads();
   // ======================= helpers =======================
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       float t = 0.f;
       if (u != kWalkStopNode) {
         const int64_t row = (nb + u) * V;
-        t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, lt_s[u], ld_s[u], s_a), red);
+        t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], s_a), red);
       }
       if (tid == 0)
         st_release64(&sync->slot[part],
@@ -385,8 +390,8 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     float pc = 0.f, qc = 0.f;
     if (q >= 0 && t >= 0) {
       const int64_t row = (nb + q) * V;
-      pc = expf(p.tl[row + t] * p.inv_t - lt_s[q]);
-      qc = expf(p.dl[row + t] * p.inv_t - ld_s[q]);
+      pc = ex2_approx(fmaf(p.tl[row + t], p.scale2, -lt_s[q]));
+      qc = ex2_approx(fmaf(p.dl[row + t], p.scale2, -ld_s[q]));
     }
     pc_s[tid] = pc;
     qc_s[tid] = qc;
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     const int64_t row = (nb + u) * V;
     int v0, v1;
     walk_slice(V, K, 0, v0, v1);
-    const float mine = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.inv_t, lt_s[u], ld_s[u], a), red);
+    const float mine = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], a), red);
     if (tid == 0) s_tot[0] = mine;
     if (warp == 0 && lane + 1 < K) {  // lane k - 1 collects helper k's answer
       unsigned long long v = 0;
@@ -519,7 +524,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
         walk_slice(V, K, sl, v0, v1);
         const bool take_last = s_slice_excl < 0.f;
         const float ltarget = target - (take_last ? 0.f : s_slice_excl);
-        slice_block_sums(tl, dl, V, v0, v1, p.inv_t, lt, ld, a, bsum);
+        slice_block_sums(tl, dl, V, v0, v1, p.scale2, lt, ld, a, bsum);
         __syncthreads();
         const int nbk = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
         if (!take_last) {
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
           }
           __syncthreads();
           if (warp == 0 && s_blk >= 0) {
-            const int v = scan_block(tl, dl, v0, v1, p.inv_t, lt, ld, a, s_blk, s_blk_excl, ltarget);
+            const int v = scan_block(tl, dl, v0, v1, p.scale2, lt, ld, a, s_blk, s_blk_excl, ltarget);
             if (lane == 0) s_bonus = v;
           }
           __syncthreads();
@@ -583,7 +588,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
             if (blk >= 0) {
               for (int e = lane; e < kBonusBlock; e += 32) {
                 const int t = v0 + blk * kBonusBlock + e;
-                if (t < v1 && r_of(__ldcg(tl + t), __ldcg(dl + t), p.inv_t, lt, ld, a) > 0.f) v = t;
+                if (t < v1 && r_of(__ldcg(tl + t), __ldcg(dl + t), p.scale2, lt, ld, a) > 0.f) v = t;
               }
             }
             v = __reduce_max_sync(0xffffffffu, v);
