@@ -341,7 +341,9 @@ __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   const int c_lo = s_sp.c_lo, c_hi = s_sp.c_hi;
   const unsigned hold = s_hold;
   pdl_wait();
-  pdl_launch_dependents();
+  // No early trigger: the next kernel's CTAs are placed as these exit, so
+  // they spread over every SM instead of piling onto the SMs that hold no
+  // merge CTA (a streaming kernel after this one is bound by its busiest SM).
   if (c_lo == c_hi) return;  // one CTA held the whole unit and wrote it
   const bool row_ok = loc < p.rows;  // else a padding row of the tile
   auto held = [&](int c) -> bool { return c - c_lo < 32 ? ((hold >> (c - c_lo)) & 1u) != 0 : s_sp.holds(c); };
