@@ -316,9 +316,10 @@ TS_API ts_status tree_cache_compact_batch(const ts_compact_args* args, int count
  * approximate 2^x (relative error about 2^-22; below 2^-126 it is 0); a
  * decision within that rounding of its threshold may go either way.  Workspace: tree_accept_sample_workspace_size(),
  * zero-filled before its first use; besides the error word it holds
- * per-request counters that every call leaves at zero, except a call that
- * reports TS_DEVERR_TIMEOUT (its outputs are void; zero the workspace before
- * reusing it).
+ * per-request command words whose numbering carries on from one call to the
+ * next, so a workspace serves calls of one shape (num_requests, n_tree_max,
+ * vocab) on one stream: zero it again before a call of another shape, and
+ * after a call that reports TS_DEVERR_TIMEOUT (its outputs are void).
  * Errors: TS_ERR_INVALID_ARG unless temperature > 0 and finite;
  * TS_ERR_UNSUPPORTED if vocab > 262144 or n_tree_max > TS_MAX_TREE, or if
  * log2(e) / temperature overflows fp32 (a temperature below about 4e-39).

@@ -184,7 +184,8 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 struct WalkSync {
   unsigned long long cmd;
   unsigned long long slot[16];
-  unsigned long long pad[15];  // 256 bytes per request
+  unsigned long long last;     // the last command number of the previous call
+  unsigned long long pad[14];  // 256 bytes per request
 };
 constexpr int kWalkStopNode = 0xffff;
 constexpr int kMaxWalkCtas = 16;

@@ -279,28 +279,44 @@ __device__ __forceinline__ bool poll_tag(const unsigned long long* ptr, int shif
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
-__device__ __forceinline__ unsigned long long walk_cmd(int seq, int u, float a) {
-  return (static_cast<unsigned long long>(seq & 0xffff) << 48) | (static_cast<unsigned long long>(u & 0xffff) << 32) |
+__device__ __forceinline__ unsigned long long walk_cmd(unsigned seq, int u, float a) {
+  return (static_cast<unsigned long long>(seq & 0xffffu) << 48) | (static_cast<unsigned long long>(u & 0xffff) << 32) |
          __float_as_uint(a);
+}
+
+// Node u's next child after node `after` (children in index order; parent[j]
+// < j, so they all follow u), or -1: warp-wide, one ballot per 32 nodes.
+__device__ __forceinline__ int next_child(const int* par_s, int n, int u, int after, int lane) {
+  for (int w0 = (after + 1) & ~31; w0 < n; w0 += 32) {
+    const int j = w0 + lane;
+    const unsigned bal = __ballot_sync(0xffffffffu, j > after && j < n && par_s[j] == u);
+    if (bal) return w0 + __ffs(bal) - 1;
+  }
+  return -1;
 }
 
 // The walk: walk_ctas CTAs per request.  CTA 0 (the leader) walks the tree;
 // every pass (a rejection, or the bonus draw's slice totals) is a sum of
 // max(0, p - a q) over the vocab that the leader and its helpers compute
-// over their slices: the leader posts (seq, node, a) in the request's command
-// word, helper k answers (seq, slice sum) in its slot, and the leader adds
-// the slice sums in slice order.  A helper handles every command in order
-// (the leader posts the next only after every helper has answered this one)
-// until the stop command; the leader then zeroes the words.  Every CTA first
-// forms the log-sum-exps of all the request's nodes, and the leader p and q
-// of every node's own token under its parent, so a visited node costs no
-// memory round trip.  Every wait is bounded; one that runs out reports
-// TS_DEVERR_TIMEOUT and ends the walk (the call's outputs are void and the
-// workspace must be zeroed before its next use).  No CTA reads another's
-// shared memory.
+// over their slices: the leader posts (command number, node, a) in the
+// request's command word, helper k answers (command number, slice sum) in
+// its slot, and the leader adds the slice sums in slice order.  A helper
+// handles every command in order (the leader posts the next only after every
+// helper has answered this one) until the stop command, which it does not
+// answer.  Command numbers continue from one call to the next (the leader
+// leaves the last one in the request's words), so no word is reset and a
+// stale word never carries the number a CTA waits for.  The tree, the
+// uniforms and the logits at the draft tokens are inputs of the call, final
+// before the statistics kernel passed its own wait, which precedes this
+// grid's launch: the leader reads them before waiting.  After the wait every
+// CTA forms the log-sum-exps of all the request's nodes, and the leader p and
+// q of every node's own token under its parent, so testing a child costs no
+// memory round trip.  Warp 0 of the leader walks alone (a ballot lists a
+// node's children) and the whole CTA joins it for each pass.  Every wait is
+// bounded; one that runs out reports TS_DEVERR_TIMEOUT and ends the walk
+// (the call's outputs are void and the workspace must be zeroed before its
+// next use).  No CTA reads another's shared memory.
 __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
   const int K = p.walk_ctas;
   const int b = blockIdx.x / K, part = blockIdx.x % K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -309,10 +325,43 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
   const int V = p.vocab;
   WalkSync* const sync = p.sync + b;
   __shared__ float red[kWalkWarps];
-  __shared__ float lt_s[TS_MAX_TREE], ld_s[TS_MAX_TREE];  // log-sum-exps of every node's rows
+  __shared__ float lt_s[TS_MAX_TREE], ld_s[TS_MAX_TREE];  // base-2 log-sum-exps of every node's rows
+  __shared__ int par_s[TS_MAX_TREE], tok_s[TS_MAX_TREE];
+  __shared__ float pc_s[TS_MAX_TREE], qc_s[TS_MAX_TREE];  // logits of node c's token under its parent, then p and q
   __shared__ int s_ok;
   const int n = tree_size(p, b);  // the same for every CTA of the request
-  if (tid < n) {                  // node tid's two log-sum-exps from the statistics partials
+  float ua = 0.f, ub = 0.f;
+  if (part == 0) {
+    if (n != p.n_tree[b] && tid == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
+    if (tid < n) {
+      int q = p.parent[nb + tid];
+      if (q < -1 || q >= tid) {
+        report_error(p.err, TS_DEVERR_BAD_PARENT);
+        q = -1;
+      }
+      par_s[tid] = q;
+      int t = p.tokens[nb + tid];
+      if (t < 0 || t >= V) {
+        if (tid > 0) report_error(p.err, TS_DEVERR_BAD_TOKEN);  // the root's own token is not tested
+        t = -1;
+      }
+      tok_s[tid] = t;
+      float xt = 0.f, xd = 0.f;
+      if (q >= 0 && t >= 0) {
+        const int64_t row = (nb + q) * V;
+        xt = p.tl[row + t];
+        xd = p.dl[row + t];
+      }
+      pc_s[tid] = xt;
+      qc_s[tid] = xd;
+      ua = p.u_acc[nb + tid];
+      ub = p.u_bonus[nb + tid];
+    }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  const unsigned base = static_cast<unsigned>(sync->last);  // the previous call's last command number
+  if (tid < n) {  // node tid's two log-sum-exps from the statistics partials
     float m[2] = {-INFINITY, -INFINITY}, sm[2] = {0.f, 0.f};
     for (int j0 = 0; j0 < p.num_slices; j0 += 8) {  // eight slices of both rows requested together
       float2 x[2][8];
@@ -339,10 +388,10 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     __shared__ float s_a;
     int v0, v1;
     walk_slice(V, K, part, v0, v1);
-    for (int seq = 1;; ++seq) {
+    for (unsigned seq = base + 1;; ++seq) {
       if (tid == 0) {
         unsigned long long c = 0;
-        s_ok = poll_tag(&sync->cmd, 48, static_cast<unsigned long long>(seq & 0xffff), &c);
+        s_ok = poll_tag(&sync->cmd, 48, static_cast<unsigned long long>(seq & 0xffffu), &c);
         s_u = static_cast<int>((c >> 32) & 0xffff);
         s_a = __uint_as_float(static_cast<unsigned>(c));
         if (!s_ok) report_error(p.err, TS_DEVERR_TIMEOUT);
@@ -350,57 +399,39 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       __syncthreads();
       if (!s_ok) return;
       const int u = s_u;
-      float t = 0.f;
-      if (u != kWalkStopNode) {
-        const int64_t row = (nb + u) * V;
-        t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], s_a), red);
-      }
-      if (tid == 0)
-        st_release64(&sync->slot[part],
-                     (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(t));
       if (u == kWalkStopNode) return;
+      const int64_t row = (nb + u) * V;
+      const float t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], s_a), red);
+      if (tid == 0)
+        st_release64(&sync->slot[part], (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(t));
       __syncthreads();  // s_u, s_a are rewritten by the next command
     }
   }
   // ======================= leader =======================
-  __shared__ int par_s[TS_MAX_TREE], tok_s[TS_MAX_TREE], kids[TS_MAX_TREE], path_s[TS_MAX_TREE];
-  __shared__ float pc_s[TS_MAX_TREE], qc_s[TS_MAX_TREE];  // p and q of node c's token under its parent
+  __shared__ int path_s[TS_MAX_TREE];
   __shared__ float ua_s[TS_MAX_TREE], ub_s[TS_MAX_TREE];  // the uniforms of every node
   __shared__ int cnt[kWalkWarps];
-  __shared__ int s_accept;
+  __shared__ int s_op, s_u, s_len;
+  __shared__ float s_a;
   __shared__ int s_bonus, s_blk, s_slice;
   __shared__ float s_blk_excl, s_slice_excl;
   __shared__ float s_scan[kWalkWarps];
   __shared__ float s_tot[kMaxWalkCtas];  // slice sums of the last pass
   __shared__ float bsum[kMaxBonusBlocks];
-  if (n != p.n_tree[b] && tid == 0) report_error(p.err, TS_DEVERR_BAD_LENGTH);
   if (tid < n) {
-    int q = p.parent[nb + tid];
-    if (q < -1 || q >= tid) {
-      report_error(p.err, TS_DEVERR_BAD_PARENT);
-      q = -1;
-    }
-    par_s[tid] = q;
-    int t = p.tokens[nb + tid];
-    if (t < 0 || t >= V) {
-      if (tid > 0) report_error(p.err, TS_DEVERR_BAD_TOKEN);  // the root's own token is not tested
-      t = -1;
-    }
-    tok_s[tid] = t;
-    float pc = 0.f, qc = 0.f;
-    if (q >= 0 && t >= 0) {
-      const int64_t row = (nb + q) * V;
-      pc = ex2_approx(fmaf(p.tl[row + t], p.scale2, -lt_s[q]));
-      qc = ex2_approx(fmaf(p.dl[row + t], p.scale2, -ld_s[q]));
-    }
-    pc_s[tid] = pc;
-    qc_s[tid] = qc;
-    ua_s[tid] = p.u_acc[nb + tid];
-    ub_s[tid] = p.u_bonus[nb + tid];
+    const int q = par_s[tid], t = tok_s[tid];
+    const bool real = q >= 0 && t >= 0;
+    pc_s[tid] = real ? ex2_approx(fmaf(pc_s[tid], p.scale2, -lt_s[q])) : 0.f;
+    qc_s[tid] = real ? ex2_approx(fmaf(qc_s[tid], p.scale2, -ld_s[q])) : 0.f;
+    ua_s[tid] = ua;
+    ub_s[tid] = ub;
   }
-  if (tid == 0) s_ok = 1;
+  if (tid == 0) {
+    s_ok = 1;
+    path_s[0] = 0;
+  }
   __syncthreads();
-  int seq = 0;  // commands posted
+  unsigned seq = base;  // commands posted
   // One pass: the slice sums of max(0, p - a q) over node u's rows into
   // s_tot[0 .. K), the leader's own slice first.  Returns their sum (slice order).
   auto pass = [&](int u, float a) -> float {
@@ -427,74 +458,78 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
   };
   int len = 0, bonus = -1;
   if (n > 0) {
-    int u = 0;
-    len = 1;
-    if (tid == 0) path_s[0] = 0;
-    for (int guard = 0; guard < n && s_ok; ++guard) {
-      // ---- children of u in index order
-      const bool kid = tid < n && par_s[tid] == u;
-      const unsigned bal = __ballot_sync(0xffffffffu, kid);
-      if (lane == 0 && warp < TS_MAX_TREE / 32) cnt[warp] = __popc(bal);
-      __syncthreads();
-      int before = 0, nk = 0;
-      for (int w = 0; w < TS_MAX_TREE / 32; ++w) {
-        if (w < warp) before += cnt[w];
-        nk += cnt[w];
-      }
-      if (kid) kids[before + __popc(bal & ((1u << lane) - 1u))] = tid;
-      __syncthreads();
-      const float* tl = p.tl + (nb + u) * V;
-      const float* dl = p.dl + (nb + u) * V;
-      const float lt = lt_s[u], ld = ld_s[u];
-      float a = 0.f, sa = 1.f;  // r = max(0, p - a q) / sa: r = p before any rejection
-      float tot_a = -1.f;       // the a that s_tot holds slice sums for (none yet)
-      int next = -1;
-      for (int k = 0; k < nk && s_ok; ++k) {
-        const int c = kids[k];
-        if (tid == 0) {
+    // Warp 0's walk state (the same in every lane): node wu, the last child
+    // tried at wu, and r = max(0, p - wa q) / sa at wu; tot_a is the a that
+    // s_tot holds slice sums for (-1: none).
+    int wu = 0, after = 0, wlen = 1;
+    float wa = 0.f, sa = 1.f, tot_a = -1.f;
+    constexpr int kOpReject = 1, kOpBonusSums = 2, kOpBonus = 3;
+    for (;;) {
+      if (warp == 0) {
+        int op = kOpBonus;
+        float pa = 0.f;  // the pass's a
+        for (;;) {  // children of wu in index order, until a rejection or none is left
+          const int c = next_child(par_s, n, wu, after, lane);
+          if (c < 0) break;
           bool acc = false;
           if (tok_s[c] >= 0) {
             const float qt = qc_s[c];
-            const float rt = fmaxf(0.f, pc_s[c] - a * qt) / sa;
+            const float rt = fmaxf(0.f, pc_s[c] - wa * qt) / sa;
             acc = qt > 0.f ? (ua_s[c] < rt / qt) : rt > 0.f;
           }
-          s_accept = acc;
-        }
-        __syncthreads();
-        if (s_accept) {
-          next = c;
+          after = c;
+          if (acc) {  // c becomes the current node, with r = p at c
+            if (lane == 0) path_s[wlen] = c;
+            ++wlen;
+            wu = c;
+            wa = 0.f;
+            sa = 1.f;
+            tot_a = -1.f;
+            continue;
+          }
+          op = kOpReject;  // r becomes max(0, p - (wa + sa) q) / S(wa + sa), kept if S is 0
+          pa = wa + sa;
           break;
         }
-        // rejected: r becomes max(0, p - (a + sa) q) / S(a + sa), kept if S is 0
-        const float an = a + sa;
-        const float z = pass(u, an);
-        if (z > 0.f) {
-          a = an;
-          sa = z;
-          tot_a = an;
-        } else {
-          tot_a = -1.f;  // s_tot now holds the sums for an, not for the a that is kept
+        if (op == kOpBonus) {
+          pa = wa;  // the bonus draws from r at the node where the walk ended
+          if (tot_a != wa) op = kOpBonusSums;  // and needs its slice sums
+        }
+        if (lane == 0) {
+          s_op = op;
+          s_u = wu;
+          s_a = pa;
+          s_len = wlen;
         }
       }
-      if (!s_ok) break;
-      if (next >= 0) {
-        u = next;
-        if (tid == 0) path_s[len] = u;
-        ++len;
-        __syncthreads();
-        continue;
+      __syncthreads();
+      const int op = s_op;
+      if (op == kOpBonus) break;
+      const float z = pass(s_u, s_a);
+      if (!s_ok || op == kOpBonusSums) break;
+      if (warp == 0) {
+        if (z > 0.f) {
+          wa += sa;  // the pass's a
+          sa = z;
+          tot_a = wa;
+        } else {
+          tot_a = -1.f;  // s_tot holds the sums for wa + sa, not for the wa that is kept
+        }
       }
+    }
+    len = s_len;
+    if (s_ok) {
       // ---- the bonus: the smallest v with r(0) + ... + r(v) > U * sum(r),
       //      r = max(0, p - a q) unnormalised: the slice that holds the
       //      target from the slice sums, then block sums, a scan of them for
       //      the block, and a scan inside it
+      const int u = s_u;
+      const float a = s_a;
+      const float* tl = p.tl + (nb + u) * V;
+      const float* dl = p.dl + (nb + u) * V;
+      const float lt = lt_s[u], ld = ld_s[u];
       float total = 0.f;
-      if (tot_a == a) {
-        for (int k = 0; k < K; ++k) total += s_tot[k];
-      } else {
-        total = pass(u, a);
-      }
-      if (!s_ok) break;
+      for (int k = 0; k < K; ++k) total += s_tot[k];
       const float target = ub_s[u] * total;
       if (tid == 0) {
         float excl = 0.f;
@@ -598,24 +633,11 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
         }
       }
       bonus = s_bonus;
-      break;
     }
-    // the helpers stop; with every answer in, the words go back to zero
-    if (K > 1 && s_ok) {
-      ++seq;
-      if (tid == 0) st_release64(&sync->cmd, walk_cmd(seq, kWalkStopNode, 0.f));
-      if (warp == 0) {
-        bool all = true;
-        if (lane + 1 < K) {
-          unsigned long long v = 0;
-          all = poll_tag(&sync->slot[lane + 1], 32, static_cast<unsigned long long>(seq), &v);
-          if (!all) report_error(p.err, TS_DEVERR_TIMEOUT);
-        }
-        if (__all_sync(0xffffffffu, all)) {
-          if (lane + 1 < K) st_release64(&sync->slot[lane + 1], 0ull);
-          if (lane == 0) st_release64(&sync->cmd, 0ull);
-        }
-      }
+    // the helpers stop (without answering); the next call's commands continue from here
+    if (K > 1 && s_ok && tid == 0) {
+      st_release64(&sync->cmd, walk_cmd(seq + 1, kWalkStopNode, 0.f));
+      sync->last = seq + 1;
     }
   }
   __syncthreads();

@@ -133,6 +133,40 @@ def test_stochastic_acceptance_matches_oracle(seed, B, n_max, vocab, noise, temp
     assert compared >= B // 2
 
 
+def test_one_workspace_over_many_calls():
+    """The walk's command words are not reset between calls (their numbering
+    carries on): six calls of one shape on one workspace, each checked
+    against the oracle, the last two on the inputs of the first two."""
+    B, n_max, vocab = 4, 24, 20000
+    cases = [_case(40 + k, B, n_max, vocab, 0.6, plain=(k % 2 == 1)) for k in range(4)]
+    cases += cases[:2]
+    ws = None
+    for acc, tl, dl, u_acc, u_bonus in cases:
+        dev = "cuda"
+        a = [torch.from_numpy(tl).to(dev), torch.from_numpy(dl).to(dev), i32_dev(acc.tokens), i32_dev(acc.parent),
+             i32_dev(acc.n_tree), torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_bonus).to(dev)]
+        if ws is None:
+            dummy = {k: torch.empty(1, dtype=torch.int32, device=dev)
+                     for k in ("path", "accept_len", "bonus", "verified", "verified_len")}
+            probe = ts.sample_args(*a, 1.0, dummy)
+            ws = ts.new_workspace(ts.tree_accept_sample_workspace_size(probe), dev)
+        got = ts.tree_accept_sample(*a, 1.0, workspace=ws)
+        torch.cuda.synchronize()
+        got = {k: v.cpu().numpy() for k, v in got.items()}
+        assert ts.read_device_error(ws) == 0
+        for b in range(B):
+            n = int(acc.n_tree[b])
+            if n == 0:
+                assert got["accept_len"][b] == 0
+                continue
+            args = (tl[b][:n].astype(np.float64), dl[b][:n].astype(np.float64), acc.tokens[b], acc.parent[b], n, 1.0,
+                    u_acc[b], u_bonus[b])
+            opath, margin, r, target = _walk(*args)
+            al = int(got["accept_len"][b])
+            if margin > MARGIN:
+                assert list(got["path"][b][:al]) == opath
+
+
 def test_near_zero_temperature_is_greedy_acceptance_on_gpu():
     acc, tl, dl, u_acc, u_bonus = _case(7, 6, 24, 2000, 1.0)
     got = _run_gpu(acc, tl, dl, u_acc, u_bonus, 1e-3)
