@@ -181,14 +181,14 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 // number (bits 48..63, from 1), the node (bits 32..47; kWalkStopNode to
 // stop) and the pass's threshold a (bits 0..31, fp32); helper k answers in
 // slot[k]: the sequence number (bits 32..63) and its slice sum (fp32).
+constexpr int kMaxWalkCtas = 16;
 struct WalkSync {
   unsigned long long cmd;
-  unsigned long long slot[16];
-  unsigned long long last;     // the last command number of the previous call
-  unsigned long long pad[14];  // 256 bytes per request
+  unsigned long long slot[kMaxWalkCtas];  // slot k: helper k's answer (slot 0 unused)
+  unsigned long long last;                // the last command number of the previous call
+  unsigned long long pad[32 - 2 - kMaxWalkCtas];  // 256 bytes per request
 };
 constexpr int kWalkStopNode = 0xffff;
-constexpr int kMaxWalkCtas = 16;
 
 struct SampleParams {
   int num_req, n_tree_max, vocab;

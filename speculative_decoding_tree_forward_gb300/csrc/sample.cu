@@ -11,9 +11,9 @@
 // Kernel 1 (row statistics) streams every target and draft row of the tree
 // once in vocab slices and keeps (max, sum of 2^(z - max)) of z = logit log2(e) / T.
 // Kernel 2 (walk) runs a leader CTA and up to 15 helper CTAs per request
-// (512 threads each): the leader merges a visited node's slices into the two
-// log-sum-exps, lists its children with a ballot and tests each child from
-// two logits.  The running target after j rejections has the closed form
+// (512 threads each): every CTA folds all nodes' slice statistics into their
+// log-sum-exps, and warp 0 of the leader lists a node's children with ballots
+// and tests each child from p and q at its token.  The running target after j rejections has the closed form
 // max(0, p - a_j q) / S(a_j) (derived at the walk's passes below), so a
 // rejection is one sum over the vocab and no residual row is written; the
 // request's CTAs split that sum by vocab slices, handing commands and slice
@@ -255,28 +255,32 @@ __device__ __forceinline__ int scan_block(const float* __restrict__ tl, const fl
 }
 
 // Global-memory hand-off between a request's leader and helper CTAs: one
-// 64-bit word each way, written with release and polled with acquire, so a
-// command and its answer each cost one one-way latency.
-__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* ptr) {
+// 64-bit word each way.  A word carries its whole message (the command
+// number with the node and a, or with the slice sum) and neither side reads
+// any other memory the other writes, so the words need no ordering against
+// other accesses: relaxed loads and stores at GPU scope (single-copy atomic
+// for an aligned 64-bit word), with no fence and no L1 invalidation per poll.
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* ptr) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release64(unsigned long long* ptr, unsigned long long v) {
-  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed64(unsigned long long* ptr, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
 }
 // Waits until the word's bits from `shift` up equal `want`, for at most
-// kWaitLimitNs of %globaltimer; the word read last goes to *got.
+// kWaitLimitNs of %globaltimer (read every 32 polls); the word read last goes
+// to *got.
 __device__ __forceinline__ bool poll_tag(const unsigned long long* ptr, int shift, unsigned long long want,
                                          unsigned long long* got) {
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    const unsigned long long v = ld_acquire64(ptr);
+  for (unsigned i = 1;; ++i) {
+    const unsigned long long v = ld_relaxed64(ptr);
     if ((v >> shift) == want) {
       *got = v;
       return true;
     }
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 31u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 __device__ __forceinline__ unsigned long long walk_cmd(unsigned seq, int u, float a) {
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       const int64_t row = (nb + u) * V;
       const float t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], s_a), red);
       if (tid == 0)
-        st_release64(&sync->slot[part], (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(t));
+        st_relaxed64(&sync->slot[part], (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(t));
       __syncthreads();  // s_u, s_a are rewritten by the next command
     }
   }
@@ -436,7 +440,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
   // s_tot[0 .. K), the leader's own slice first.  Returns their sum (slice order).
   auto pass = [&](int u, float a) -> float {
     ++seq;
-    if (K > 1 && tid == 0) st_release64(&sync->cmd, walk_cmd(seq, u, a));
+    if (K > 1 && tid == 0) st_relaxed64(&sync->cmd, walk_cmd(seq, u, a));
     const int64_t row = (nb + u) * V;
     int v0, v1;
     walk_slice(V, K, 0, v0, v1);
@@ -636,7 +640,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     }
     // the helpers stop (without answering); the next call's commands continue from here
     if (K > 1 && s_ok && tid == 0) {
-      st_release64(&sync->cmd, walk_cmd(seq + 1, kWalkStopNode, 0.f));
+      st_relaxed64(&sync->cmd, walk_cmd(seq + 1, kWalkStopNode, 0.f));
       sync->last = seq + 1;
     }
   }
