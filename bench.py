@@ -257,6 +257,8 @@ def build_step(args, torch, ts, W, device):
         # larger than L2), the acceptance reads one of several copies of the
         # logits in turn, so that every step streams them from DRAM.
         n_rep = 1 if attn_bytes < 2 * L2_BYTES else min(8, -(-3 * L2_BYTES // A.logits.nbytes))
+        if A.logits.nbytes >= (8 << 20):
+            n_rep = max(n_rep, 2)   # the end-to-end leg copies large logits into two device copies in turn
         reps = [logits] + [logits.clone() for _ in range(n_rep - 1)]
         tok = i32_dev(A.tokens)
         res = {k: torch.empty(s, dtype=torch.int32, device=device) for k, s in [
@@ -279,12 +281,14 @@ def build_step(args, torch, ts, W, device):
             aws = ts.new_workspace(ts.tree_accept_sample_workspace_size(aas[0]), device)
             acc_state = (aas, aws, logits, tok, res, "sample", [dlog, u_acc, u_bon])
             info["logits_keep"] = reps + dreps   # the copies the argument structs point at stay alive
+            info["logits_sets"] = [[x, y] for x, y in zip(reps, dreps)]   # copy k: what the k-th call reads
             info["accept_bytes"] = 2 * A.logits.nbytes
         else:
             aas = [ts.accept_args(x, tok, par, ntree, **res) for x in reps]
             aws = ts.new_workspace(ts.tree_accept_workspace_size(aas[0]), device)
             acc_state = (aas, aws, logits, tok, res, "greedy", [])
             info["logits_keep"] = reps   # the copies the argument structs point at stay alive
+            info["logits_sets"] = [[x] for x in reps]
         info["logits_copies"] = n_rep
         launches += 2
         info.setdefault("accept_bytes", A.logits.nbytes)
@@ -345,6 +349,7 @@ def build_step(args, torch, ts, W, device):
             accept_call(a, acc_state[1])
         phases.append(("accept", [accept_next]))
         info["accept_first"] = lambda: accept_call(acc_state[0][0], acc_state[1])
+        info["accept_copy"] = lambda k: accept_call(acc_state[0][k], acc_state[1])
     if len(comp_states) == 2 and not args.serial_compaction:
         # the target- and draft-side caches and their metadata are disjoint:
         # both compactions run as one launch (tree_cache_compact_batch)
@@ -448,10 +453,13 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     order they are issued, so a small copy issued after the logits would wait
     for all of them.  The side stream starts a step's copies once the previous
     step's work on the main stream has finished with its inputs.  The
-    attention, which does not read the logits, starts as soon as the small
-    inputs are in and runs while the logits cross; the acceptance waits for
-    them.  The results go back on the main stream.  A step with no large
-    input and small results copies everything on the main stream.
+    logits go to one of two device copies in turn: step k + 1's logits are
+    copied while step k computes (after the acceptance that last read that
+    copy), so the link carries one step's inputs per step without pauses.
+    The attention, which does not read the logits, starts as soon as the
+    small inputs are in; the acceptance waits for its logits.  The results go
+    back on the main stream.  A step with no large input and small results
+    copies everything on the main stream.
     """
     small_in = [d["q"] for a, ws, d, out, lse in info["attn_inputs"]]
     if info["draft"] is not None:
@@ -494,6 +502,27 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
     # stream and events cost more than the overlap saves.
     use_back = sum(t.numel() * t.element_size() for t in big_host) >= (8 << 20)
 
+    # With two device copies of the large inputs (the logits), step k + 1's
+    # copy crosses the link while step k computes: the copy engine is never
+    # idle, and the step's period is the link time of its inputs.  Every step
+    # still copies all of its inputs in and its results out.
+    sets = info.get("logits_sets") or []
+    dbl = use_side and bool(big_in) and len(sets) >= 2
+    big_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    acc_done = [torch.cuda.Event(), torch.cuda.Event()]
+    for ev in acc_done:
+        ev.record(main)
+    turn = {"k": 0, "primed": False}
+
+    def copy_big(k):
+        # step k's large inputs into device copy k % 2, once the acceptance
+        # that read that copy (step k - 2) is done
+        side.wait_event(acc_done[k % 2])
+        with torch.cuda.stream(side):
+            for h, dv in zip(big_host, sets[k % 2]):
+                dv.copy_(h, non_blocking=True)
+            big_ready[k % 2].record(side)
+
     def step():
         if not use_side:   # copy on the main stream
             for h, dv in zip(small_host, small_in):
@@ -504,25 +533,38 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
             for dv, h in zip(attn_outs + outs, host_attn_outs + host_outs):
                 h.copy_(dv, non_blocking=True)
             return
+        k = turn["k"]
+        if dbl and not turn["primed"]:
+            copy_big(k)
+            turn["primed"] = True
         side.wait_event(done)
         with torch.cuda.stream(side):
             for h, dv in zip(small_host, small_in):
                 dv.copy_(h, non_blocking=True)
             small = torch.cuda.Event()
             small.record(side)
-            for h, dv in zip(big_host, big_in):
-                dv.copy_(h, non_blocking=True)
-            big = torch.cuda.Event()
-            big.record(side)
+            if not dbl:
+                for h, dv in zip(big_host, big_in):
+                    dv.copy_(h, non_blocking=True)
+                big = torch.cuda.Event()
+                big.record(side)
+        if dbl:
+            copy_big(k + 1)   # the next step's logits cross while this step computes
         main.wait_event(small)
         attn_left = sum(1 for kind, _ in info["phases"] if kind == "attn")
         back_done = None
         for kind, calls in info["phases"]:
             if kind == "accept":
-                main.wait_event(big)
-                calls = [info["accept_first"]]   # the copy the host writes into
+                if dbl:
+                    main.wait_event(big_ready[k % 2])
+                    calls = [lambda: info["accept_copy"](k % 2)]
+                else:
+                    main.wait_event(big)
+                    calls = [info["accept_first"]]   # the copy the host writes into
             for f in calls:
                 f()
+            if kind == "accept" and dbl:
+                acc_done[k % 2].record(main)
             if kind == "attn" and use_back:
                 attn_left -= 1
                 if attn_left == 0:
@@ -537,12 +579,14 @@ def e2e_measure(args, torch, ts, info, steps, warmup):
                             h.copy_(dv, non_blocking=True)
                         back_done = torch.cuda.Event()
                         back_done.record(back)
-        main.wait_event(big)
+        if not dbl:
+            main.wait_event(big)
         if back_done is not None:
             main.wait_event(back_done)   # the next step's attention rewrites those outputs
         done.record(main)
         for dv, h in zip(outs if use_back else attn_outs + outs, host_outs if use_back else host_attn_outs + host_outs):
             h.copy_(dv, non_blocking=True)
+        turn["k"] = k + 1
 
     for _ in range(warmup):
         step()
@@ -845,7 +889,10 @@ def main():
     # latency off the host; the kernels and their dependencies are the same)
     graph = None
     if not args.no_graph:
-        per_graph = info.get("logits_copies", 1)   # one captured step per copy of the logits
+        # one captured step per copy of the logits; one step when L2 is flushed
+        # before every replay (a second step in the graph would find the first's
+        # inputs in L2)
+        per_graph = info.get("logits_copies", 1) if flush is None else 1
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for _ in range(per_graph):
