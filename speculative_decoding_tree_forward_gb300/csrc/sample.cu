@@ -475,12 +475,11 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
         for (;;) {  // children of wu in index order, until a rejection or none is left
           const int c = next_child(par_s, n, wu, after, lane);
           if (c < 0) break;
-          bool acc = false;
-          if (tok_s[c] >= 0) {
-            const float qt = qc_s[c];
-            const float rt = fmaxf(0.f, pc_s[c] - wa * qt) / sa;
-            acc = qt > 0.f ? (ua_s[c] < rt / qt) : rt > 0.f;
-          }
+          // U < r(t) / q(t) with r = max(0, p - wa q) / sa, as U q(t) sa <
+          // max(0, p(t) - wa q(t)) (sa > 0): no division, and with q(t) = 0 it
+          // reads r(t) > 0
+          const float qt = qc_s[c];
+          const bool acc = tok_s[c] >= 0 && ua_s[c] * qt * sa < fmaxf(0.f, pc_s[c] - wa * qt);
           after = c;
           if (acc) {  // c becomes the current node, with r = p at c
             if (lane == 0) path_s[wlen] = c;
