@@ -12,15 +12,16 @@
 // once in vocab slices and keeps (max, sum of 2^(z - max)) of z = logit log2(e) / T.
 // Kernel 2 (walk) runs a leader CTA and up to 15 helper CTAs per request
 // (512 threads each): every CTA folds all nodes' slice statistics into their
-// log-sum-exps, and warp 0 of the leader lists a node's children with ballots
-// and tests each child from p and q at its token.  The running target after j rejections has the closed form
-// max(0, p - a_j q) / S(a_j) (derived at the walk's passes below), so a
-// rejection is one sum over the vocab and no residual row is written; the
-// request's CTAs split that sum by vocab slices, handing commands and slice
+// log-sum-exps, and warp 0 of the leader lists a node's children with
+// ballots and tests each child from p and q at its token.  The running target
+// after j rejections has the closed form max(0, p - a_j q) / S(a_j) (derived
+// at the walk's passes below), so a rejection is one sum over the vocab and no
+// residual row is written; the request's CTAs split that sum by vocab slices,
+// each keeping its slice's 128-token block sums, and hand commands and slice
 // sums over through the workspace with bounded waits.  The bonus is drawn by
-// inverse transform: the slice that holds the target from the slice sums,
-// then coalesced sums of its 128-token blocks, a block scan of those sums,
-// and one warp's scan inside the block that holds the target.
+// inverse transform: the slice that holds the target from the slice sums of
+// the last pass, then, in the CTA that owns that slice, a block scan of its
+// block sums and one warp's scan inside the block that holds the target.
 #include "common.cuh"
 #include "internal.h"
 
@@ -143,40 +144,6 @@ __device__ __forceinline__ void walk_slice(int V, int K, int k, int& v0, int& v1
   v1 = min(V, v0 + len);
 }
 
-// This thread's share of sum_{v in [v0, v1)} r(v) over node u's rows tl, dl,
-// with four 16-byte loads of each row in flight per thread.
-__device__ __forceinline__ float slice_sum(const float* __restrict__ tl, const float* __restrict__ dl, int V, int v0,
-                                           int v1, float scale2, float lt, float ld, float a) {
-  float part = 0.f;
-  if ((V & 3) == 0) {
-    constexpr int kLoads = 4;
-    const float4* t4 = reinterpret_cast<const float4*>(tl);
-    const float4* d4 = reinterpret_cast<const float4*>(dl);
-    const int e4 = v1 / 4;
-    for (int x0 = v0 / 4 + static_cast<int>(threadIdx.x); x0 < e4; x0 += kLoads * kWalkThreads) {
-      float4 ft[kLoads], fd[kLoads];
-#pragma unroll
-      for (int q = 0; q < kLoads; ++q) {
-        const int x = x0 + q * kWalkThreads;
-        if (x < e4) {
-          ft[q] = __ldcg(t4 + x);
-          fd[q] = __ldcg(d4 + x);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kLoads; ++q)
-        if (x0 + q * kWalkThreads < e4)
-          part += (r_of(ft[q].x, fd[q].x, scale2, lt, ld, a) + r_of(ft[q].y, fd[q].y, scale2, lt, ld, a)) +
-                  (r_of(ft[q].z, fd[q].z, scale2, lt, ld, a) + r_of(ft[q].w, fd[q].w, scale2, lt, ld, a));
-    }
-  } else {
-#pragma unroll 4
-    for (int v = v0 + static_cast<int>(threadIdx.x); v < v1; v += kWalkThreads)
-      part += r_of(__ldcg(tl + v), __ldcg(dl + v), scale2, lt, ld, a);
-  }
-  return part;
-}
-
 // Sums of r over the slice's blocks of kBonusBlock tokens (block i is
 // [v0 + 128 i, ...)), warp per block with kBlocksInFlight blocks of a warp
 // requested before any is summed, into bsum[0 .. ceil((v1 - v0) / 128)).
@@ -254,6 +221,117 @@ __device__ __forceinline__ int scan_block(const float* __restrict__ tl, const fl
   return hit ? __shfl_sync(0xffffffffu, pick, __ffs(hit) - 1) : -1;
 }
 
+// Shared scratch of a bonus draw inside one slice.
+struct DrawScratch {
+  float scan[kWalkWarps];
+  int cnt[kWalkWarps];
+  int blk, bonus;
+  float blk_excl;
+};
+
+// This CTA's part of a pass over node rows tl, dl: r's 128-token block sums
+// over its slice [v0, v1) into bsum (kept for a bonus draw in the slice) and
+// their total, which every thread returns.
+__device__ __forceinline__ float slice_pass(const float* __restrict__ tl, const float* __restrict__ dl, int V, int v0,
+                                            int v1, float scale2, float lt, float ld, float a, float* bsum, float* red) {
+  __syncthreads();  // bsum may still be read from the previous pass
+  slice_block_sums(tl, dl, V, v0, v1, scale2, lt, ld, a, bsum);
+  __syncthreads();
+  const int nbk = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
+  float t = 0.f;
+  for (int i = static_cast<int>(threadIdx.x); i < nbk; i += kWalkThreads) t += bsum[i];
+  return block_sum(t, red);
+}
+
+// The bonus inside slice [v0, v1) of node rows tl, dl, from the block sums
+// in bsum (those of a pass at the same a): the smallest v whose sum of r over
+// [v0, v] exceeds ltarget; with take_last, or when rounding leaves no such v,
+// the slice's last token with r > 0 (-1 if there is none).  Every thread
+// returns it.
+__device__ int draw_in_slice(const float* __restrict__ tl, const float* __restrict__ dl, int v0, int v1, float scale2,
+                             float lt, float ld, float a, const float* bsum, float ltarget, bool take_last,
+                             DrawScratch& ds) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nbk = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
+  if (tid == 0) {
+    ds.bonus = -1;
+    ds.blk = -1;
+  }
+  __syncthreads();
+  if (!take_last) {
+    // consecutive block sums per thread (nbk <= kMaxBonusBlocks), block exclusive scan
+    const int per = (nbk + kWalkThreads - 1) / kWalkThreads;
+    float bs[kBlocksPerThread];
+    float mine = 0.f;
+#pragma unroll
+    for (int e = 0; e < kBlocksPerThread; ++e) {
+      bs[e] = (e < per && tid * per + e < nbk) ? bsum[tid * per + e] : 0.f;
+      mine += bs[e];
+    }
+    float inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) ds.scan[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      float w = lane < kWalkWarps ? ds.scan[lane] : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < kWalkWarps) ds.scan[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    float excl = (warp > 0 ? ds.scan[warp - 1] : 0.f) + inc - mine;
+#pragma unroll
+    for (int e = 0; e < kBlocksPerThread; ++e) {
+      if (bs[e] > 0.f && excl <= ltarget && ltarget < excl + bs[e]) {
+        ds.blk = tid * per + e;
+        ds.blk_excl = excl;
+      }
+      excl += bs[e];
+    }
+    __syncthreads();
+    if (warp == 0 && ds.blk >= 0) {
+      const int v = scan_block(tl, dl, v0, v1, scale2, lt, ld, a, ds.blk, ds.blk_excl, ltarget);
+      if (lane == 0) ds.bonus = v;
+    }
+    __syncthreads();
+  }
+  if (ds.bonus < 0) {  // the last token of the slice with r > 0
+    int lastb = -1;
+    for (int blk = nbk - 1 - tid; blk >= 0; blk -= kWalkThreads)
+      if (bsum[blk] > 0.f) {
+        lastb = blk;
+        break;
+      }
+    lastb = __reduce_max_sync(0xffffffffu, lastb);
+    if (lane == 0) ds.cnt[warp] = lastb;
+    __syncthreads();
+    if (warp == 0) {
+      int blk = lane < kWalkWarps ? ds.cnt[lane] : -1;
+      blk = __reduce_max_sync(0xffffffffu, blk);
+      int v = -1;
+      if (blk >= 0) {
+        for (int e = lane; e < kBonusBlock; e += 32) {
+          const int t = v0 + blk * kBonusBlock + e;
+          if (t < v1 && r_of(__ldcg(tl + t), __ldcg(dl + t), scale2, lt, ld, a) > 0.f) v = t;
+        }
+      }
+      v = __reduce_max_sync(0xffffffffu, v);
+      if (lane == 0) ds.bonus = v;
+    }
+    __syncthreads();
+  }
+  const int v = ds.bonus;
+  __syncthreads();  // ds is rewritten by the next draw
+  return v;
+}
+
 // Global-memory hand-off between a request's leader and helper CTAs: one
 // 64-bit word each way.  A word carries its whole message (the command
 // number with the node and a, or with the slice sum) and neither side reads
@@ -287,6 +365,14 @@ __device__ __forceinline__ unsigned long long walk_cmd(unsigned seq, int u, floa
   return (static_cast<unsigned long long>(seq & 0xffffu) << 48) | (static_cast<unsigned long long>(u & 0xffff) << 32) |
          __float_as_uint(a);
 }
+// A bonus command in the node field: the flag, the slice whose owner draws
+// (bits 10..14) and the path length (bits 0..9, at most TS_MAX_TREE, so never
+// the stop word's 1023); the float is the target within that slice, or -1 for
+// the slice's last token with r > 0.
+constexpr int kWalkBonusFlag = 0x8000;
+__device__ __forceinline__ unsigned long long walk_bonus_cmd(unsigned seq, int slice, int len, float ltarget) {
+  return walk_cmd(seq, kWalkBonusFlag | (slice << 10) | len, ltarget);
+}
 
 // Node u's next child after node `after` (children in index order; parent[j]
 // < j, so they all follow u), or -1: warp-wide, one ballot per 32 nodes.
@@ -306,8 +392,11 @@ __device__ __forceinline__ int next_child(const int* par_s, int n, int u, int af
 // request's command word, helper k answers (command number, slice sum) in
 // its slot, and the leader adds the slice sums in slice order.  A helper
 // handles every command in order (the leader posts the next only after every
-// helper has answered this one) until the stop command, which it does not
-// answer.  Command numbers continue from one call to the next (the leader
+// helper has answered this one) until the last one, which it does not
+// answer: the stop, or the bonus command, on which the helper that owns the
+// bonus's slice draws it from its block sums and writes it while the others
+// stop (when the leader owns that slice it draws the bonus itself and posts
+// the stop).  Command numbers continue from one call to the next (the leader
 // leaves the last one in the request's words), so no word is reset and a
 // stale word never carries the number a CTA waits for.  The tree, the
 // uniforms and the logits at the draft tokens are inputs of the call, final
@@ -333,6 +422,8 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
   __shared__ int par_s[TS_MAX_TREE], tok_s[TS_MAX_TREE];
   __shared__ float pc_s[TS_MAX_TREE], qc_s[TS_MAX_TREE];  // logits of node c's token under its parent, then p and q
   __shared__ int s_ok;
+  __shared__ float bsum[kMaxBonusBlocks];  // this CTA's block sums of the last pass
+  __shared__ DrawScratch ds;
   const int n = tree_size(p, b);  // the same for every CTA of the request
   float ua = 0.f, ub = 0.f;
   if (part == 0) {
@@ -392,6 +483,8 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     __shared__ float s_a;
     int v0, v1;
     walk_slice(V, K, part, v0, v1);
+    int last_u = 0;      // the node and a of the last pass
+    float last_a = 0.f;
     for (unsigned seq = base + 1;; ++seq) {
       if (tid == 0) {
         unsigned long long c = 0;
@@ -404,8 +497,24 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
       if (!s_ok) return;
       const int u = s_u;
       if (u == kWalkStopNode) return;
+      if (u & kWalkBonusFlag) {  // the bonus: drawn by the slice's owner from its last pass; the others stop
+        if (((u >> 10) & 31) != part) return;
+        const float ltarget = s_a;
+        const int len = u & 1023;
+        const int64_t row = (nb + last_u) * V;
+        const int v = draw_in_slice(p.tl + row, p.dl + row, v0, v1, p.scale2, lt_s[last_u], ld_s[last_u], last_a, bsum,
+                                    ltarget, ltarget < 0.f, ds);
+        if (tid == 0) {
+          p.bonus[b] = v;
+          if (p.verified != nullptr) p.verified[static_cast<int64_t>(b) * (p.n_tree_max + 1) + len] = v;
+          if (p.verified_len != nullptr) p.verified_len[b] = len + 1;
+        }
+        return;
+      }
       const int64_t row = (nb + u) * V;
-      const float t = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], s_a), red);
+      last_u = u;
+      last_a = s_a;
+      const float t = slice_pass(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], last_a, bsum, red);
       if (tid == 0)
         st_relaxed64(&sync->slot[part], (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(t));
       __syncthreads();  // s_u, s_a are rewritten by the next command
@@ -414,14 +523,11 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
   // ======================= leader =======================
   __shared__ int path_s[TS_MAX_TREE];
   __shared__ float ua_s[TS_MAX_TREE], ub_s[TS_MAX_TREE];  // the uniforms of every node
-  __shared__ int cnt[kWalkWarps];
   __shared__ int s_op, s_u, s_len;
   __shared__ float s_a;
-  __shared__ int s_bonus, s_blk, s_slice;
-  __shared__ float s_blk_excl, s_slice_excl;
-  __shared__ float s_scan[kWalkWarps];
+  __shared__ int s_slice;
+  __shared__ float s_slice_excl;
   __shared__ float s_tot[kMaxWalkCtas];  // slice sums of the last pass
-  __shared__ float bsum[kMaxBonusBlocks];
   if (tid < n) {
     const int q = par_s[tid], t = tok_s[tid];
     const bool real = q >= 0 && t >= 0;
@@ -444,7 +550,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     const int64_t row = (nb + u) * V;
     int v0, v1;
     walk_slice(V, K, 0, v0, v1);
-    const float mine = block_sum(slice_sum(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], a), red);
+    const float mine = slice_pass(p.tl + row, p.dl + row, V, v0, v1, p.scale2, lt_s[u], ld_s[u], a, bsum, red);
     if (tid == 0) s_tot[0] = mine;
     if (warp == 0 && lane + 1 < K) {  // lane k - 1 collects helper k's answer
       unsigned long long v = 0;
@@ -461,6 +567,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     return total;
   };
   int len = 0, bonus = -1;
+  bool drawn_by_helper = false;
   if (n > 0) {
     // Warp 0's walk state (the same in every lane): node wu, the last child
     // tried at wu, and r = max(0, p - wa q) / sa at wu; tot_a is the a that
@@ -524,13 +631,11 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     if (s_ok) {
       // ---- the bonus: the smallest v with r(0) + ... + r(v) > U * sum(r),
       //      r = max(0, p - a q) unnormalised: the slice that holds the
-      //      target from the slice sums, then block sums, a scan of them for
-      //      the block, and a scan inside it
+      //      target from the last pass's slice sums (a pass at this a), then,
+      //      in the CTA that owns that slice, a scan of its block sums from
+      //      that pass and a scan inside the block
       const int u = s_u;
       const float a = s_a;
-      const float* tl = p.tl + (nb + u) * V;
-      const float* dl = p.dl + (nb + u) * V;
-      const float lt = lt_s[u], ld = ld_s[u];
       float total = 0.f;
       for (int k = 0; k < K; ++k) total += s_tot[k];
       const float target = ub_s[u] * total;
@@ -552,109 +657,49 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
           s_slice_excl = -1.f;  // take its last token with r > 0
         }
         s_slice = sl;
-        s_bonus = -1;
-        s_blk = -1;
       }
       __syncthreads();
       const int sl = s_slice;
-      if (sl >= 0) {
+      const bool take_last = s_slice_excl < 0.f;
+      const float ltarget = take_last ? -1.f : fmaxf(0.f, target - s_slice_excl);
+      if (sl == 0) {  // the leader's own slice
         int v0, v1;
-        walk_slice(V, K, sl, v0, v1);
-        const bool take_last = s_slice_excl < 0.f;
-        const float ltarget = target - (take_last ? 0.f : s_slice_excl);
-        slice_block_sums(tl, dl, V, v0, v1, p.scale2, lt, ld, a, bsum);
-        __syncthreads();
-        const int nbk = (v1 - v0 + kBonusBlock - 1) / kBonusBlock;
-        if (!take_last) {
-          // consecutive block sums per thread (nbk <= kMaxBonusBlocks), block exclusive scan
-          const int per = (nbk + kWalkThreads - 1) / kWalkThreads;
-          float bs[kBlocksPerThread];
-          float mine = 0.f;
-#pragma unroll
-          for (int e = 0; e < kBlocksPerThread; ++e) {
-            bs[e] = (e < per && tid * per + e < nbk) ? bsum[tid * per + e] : 0.f;
-            mine += bs[e];
-          }
-          float inc = mine;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
-          }
-          if (lane == 31) s_scan[warp] = inc;
-          __syncthreads();
-          if (warp == 0) {
-            float w = lane < kWalkWarps ? s_scan[lane] : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const float y = __shfl_up_sync(0xffffffffu, w, o);
-              if (lane >= o) w += y;
-            }
-            if (lane < kWalkWarps) s_scan[lane] = w;  // inclusive warp totals
-          }
-          __syncthreads();
-          float excl = (warp > 0 ? s_scan[warp - 1] : 0.f) + inc - mine;
-#pragma unroll
-          for (int e = 0; e < kBlocksPerThread; ++e) {
-            if (bs[e] > 0.f && excl <= ltarget && ltarget < excl + bs[e]) {
-              s_blk = tid * per + e;
-              s_blk_excl = excl;
-            }
-            excl += bs[e];
-          }
-          __syncthreads();
-          if (warp == 0 && s_blk >= 0) {
-            const int v = scan_block(tl, dl, v0, v1, p.scale2, lt, ld, a, s_blk, s_blk_excl, ltarget);
-            if (lane == 0) s_bonus = v;
-          }
-          __syncthreads();
-        }
-        if (s_bonus < 0) {  // the last token of the slice with r > 0
-          int lastb = -1;
-          for (int blk = nbk - 1 - tid; blk >= 0; blk -= kWalkThreads)
-            if (bsum[blk] > 0.f) {
-              lastb = blk;
-              break;
-            }
-          lastb = __reduce_max_sync(0xffffffffu, lastb);
-          if (lane == 0) cnt[warp] = lastb;
-          __syncthreads();
-          if (warp == 0) {
-            int blk = lane < kWalkWarps ? cnt[lane] : -1;
-            blk = __reduce_max_sync(0xffffffffu, blk);
-            int v = -1;
-            if (blk >= 0) {
-              for (int e = lane; e < kBonusBlock; e += 32) {
-                const int t = v0 + blk * kBonusBlock + e;
-                if (t < v1 && r_of(__ldcg(tl + t), __ldcg(dl + t), p.scale2, lt, ld, a) > 0.f) v = t;
-              }
-            }
-            v = __reduce_max_sync(0xffffffffu, v);
-            if (lane == 0) s_bonus = v;
-          }
-          __syncthreads();
+        walk_slice(V, K, 0, v0, v1);
+        const int64_t row = (nb + u) * V;
+        bonus = draw_in_slice(p.tl + row, p.dl + row, v0, v1, p.scale2, lt_s[u], ld_s[u], a, bsum, ltarget, take_last,
+                              ds);
+      } else if (sl > 0) {  // helper sl draws and writes the bonus; the command stops the other helpers
+        drawn_by_helper = true;
+        if (tid == 0) {
+          st_relaxed64(&sync->cmd, walk_bonus_cmd(seq + 1, sl, len, ltarget));
+          sync->last = seq + 1;
         }
       }
-      bonus = s_bonus;
     }
     // the helpers stop (without answering); the next call's commands continue from here
-    if (K > 1 && s_ok && tid == 0) {
+    if (K > 1 && s_ok && !drawn_by_helper && tid == 0) {
       st_relaxed64(&sync->cmd, walk_cmd(seq + 1, kWalkStopNode, 0.f));
       sync->last = seq + 1;
     }
   }
   __syncthreads();
-  // ---- outputs (the path written from shared memory)
+  // ---- outputs (the path written from shared memory; the bonus, its place
+  //      in `verified` and verified_len by the helper that drew it, if one did)
   for (int j = tid; j < p.n_tree_max; j += kWalkThreads) p.path[nb + j] = j < len ? path_s[j] : -1;
   if (p.verified != nullptr) {
     int32_t* vrow = p.verified + static_cast<int64_t>(b) * (p.n_tree_max + 1);
-    for (int j = tid; j <= p.n_tree_max; j += kWalkThreads)
-      vrow[j] = j < len ? p.tokens[nb + path_s[j]] : (j == len && n > 0 ? bonus : -1);
+    for (int j = tid; j <= p.n_tree_max; j += kWalkThreads) {
+      if (j < len) vrow[j] = p.tokens[nb + path_s[j]];
+      else if (j > len || n == 0) vrow[j] = -1;
+      else if (!drawn_by_helper) vrow[j] = bonus;
+    }
   }
   if (tid == 0) {
     p.accept_len[b] = len;
-    p.bonus[b] = bonus;
-    if (p.verified_len != nullptr) p.verified_len[b] = n > 0 ? len + 1 : 0;
+    if (!drawn_by_helper) {
+      p.bonus[b] = bonus;
+      if (p.verified_len != nullptr) p.verified_len[b] = n > 0 ? len + 1 : 0;
+    }
   }
 }
 
