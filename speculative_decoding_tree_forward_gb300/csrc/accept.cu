@@ -114,13 +114,23 @@ __global__ void __launch_bounds__(TS_MAX_TREE) accept_scan_kernel(const AcceptPa
   pdl_launch_dependents();
   // argmax per node from the chunk partials
   int am = -1;
-  if (i < n) {
+  if (i < n) {  // sixteen chunks' partials requested together: one round trip for up to 16 chunks
     float bv = -INFINITY;
     int bi = INT32_MAX;
     const float* pv = p.part_val + (rowbase + i) * p.num_chunks;
     const int* pi = p.part_idx + (rowbase + i) * p.num_chunks;
-#pragma unroll 8
-    for (int c = 0; c < p.num_chunks; ++c) better(bv, bi, pv[c], pi[c]);
+    for (int c0 = 0; c0 < p.num_chunks; c0 += 16) {
+      float v[16];
+      int x[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const bool in = c0 + q < p.num_chunks;
+        v[q] = in ? pv[c0 + q] : -INFINITY;
+        x[q] = in ? pi[c0 + q] : INT32_MAX;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) better(bv, bi, v[q], x[q]);
+    }
     am = bi;
   }
   if (i < p.n_tree_max) p.argmax[rowbase + i] = (i < n) ? am : -1;
