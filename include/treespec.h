@@ -64,6 +64,8 @@ typedef enum ts_kv_layout {
 #define TS_DEVERR_BAD_BLOCK 0x4u    /* block_table entry outside [0, num_blocks): rows read as zero / not moved */
 #define TS_DEVERR_TIMEOUT 0x8u      /* a bounded wait inside a kernel expired; outputs are invalid */
 #define TS_DEVERR_BAD_TOKEN 0x10u   /* a draft token outside [0, vocab): never accepted */
+#define TS_DEVERR_BAD_WORKSPACE 0x20u /* a workspace word holds what no call wrote (not zeroed before use,
+                                       or last used by a call of another shape): ignored, outputs invalid */
 
 /* Largest tree the kernels accept (ancestor sets are 128-bit masks). */
 #define TS_MAX_TREE 128
@@ -341,6 +343,10 @@ typedef struct ts_sample_args {
   int32_t* bonus;              /* device [num_requests] (out) */
   int32_t* verified;           /* device [num_requests][n_tree_max + 1] (out) or NULL */
   int32_t* verified_len;       /* device [num_requests] (out) or NULL */
+  unsigned wait_limit_ns;      /* testing: bound of each wait in the walk's hand-offs between CTAs, in ns
+                                  (0 = the default, 2 s).  A wait that runs out sets TS_DEVERR_TIMEOUT and
+                                  its CTA returns; the call's outputs are void and the workspace must be
+                                  zeroed before its next use. */
 } ts_sample_args;
 
 TS_API size_t tree_accept_sample_workspace_size(const ts_sample_args* args);

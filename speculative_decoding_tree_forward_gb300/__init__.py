@@ -23,6 +23,7 @@ TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_WORKSPACE = r
 TS_KV_CONTIGUOUS, TS_KV_PAGED = 0, 1
 TS_DEVERR_BAD_PARENT, TS_DEVERR_BAD_LENGTH, TS_DEVERR_BAD_BLOCK, TS_DEVERR_TIMEOUT = 1, 2, 4, 8
 TS_DEVERR_BAD_TOKEN = 16
+TS_DEVERR_BAD_WORKSPACE = 32
 TS_MAX_TREE = 128
 
 if not os.path.exists(LIB_PATH):
@@ -64,7 +65,7 @@ class SampleArgs(ctypes.Structure):
     _fields_ = [("num_requests", _i32), ("n_tree_max", _i32), ("vocab", _i32), ("temperature", ctypes.c_float),
                 ("target_logits", _vp), ("draft_logits", _vp), ("tokens", _vp), ("parent", _vp), ("n_tree", _vp),
                 ("u_accept", _vp), ("u_bonus", _vp), ("path", _vp), ("accept_len", _vp), ("bonus", _vp),
-                ("verified", _vp), ("verified_len", _vp)]
+                ("verified", _vp), ("verified_len", _vp), ("wait_limit_ns", ctypes.c_uint)]
 
 
 class ExpandArgs(ctypes.Structure):
@@ -464,7 +465,7 @@ def tree_select_subtree(n_tree, parent, tokens, weight, bs: int, workspace=None,
 
 # ------------------------------------------------------------------ stochastic acceptance
 def sample_args(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature: float,
-                out: dict) -> SampleArgs:
+                out: dict, wait_limit_ns: int = 0) -> SampleArgs:
     """target_logits / draft_logits fp32 [B][n_max][V]; u_accept / u_bonus fp32 [B][n_max] in [0, 1)."""
     B, n_max, V = target_logits.shape
     a = SampleArgs()
@@ -474,6 +475,7 @@ def sample_args(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u
     a.u_accept, a.u_bonus = u_accept.data_ptr(), u_bonus.data_ptr()
     a.path, a.accept_len, a.bonus = out["path"].data_ptr(), out["accept_len"].data_ptr(), out["bonus"].data_ptr()
     a.verified, a.verified_len = out["verified"].data_ptr(), out["verified_len"].data_ptr()
+    a.wait_limit_ns = wait_limit_ns
     return a
 
 
@@ -489,8 +491,9 @@ def tree_accept_sample_args(args: SampleArgs, workspace: torch.Tensor, stream=No
 
 
 def tree_accept_sample(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature: float,
-                       workspace=None, stream=None) -> dict:
-    """Stochastic tree acceptance; returns dict of path, accept_len, bonus, verified, verified_len."""
+                       workspace=None, stream=None, wait_limit_ns: int = 0) -> dict:
+    """Stochastic tree acceptance; returns dict of path, accept_len, bonus, verified, verified_len.
+    wait_limit_ns > 0 bounds each wait of the walk's hand-offs (testing)."""
     B, n_max, _ = target_logits.shape
     dev = target_logits.device
     out = {"path": torch.empty((B, n_max), dtype=torch.int32, device=dev),
@@ -498,7 +501,8 @@ def tree_accept_sample(target_logits, draft_logits, tokens, parent, n_tree, u_ac
            "bonus": torch.empty(B, dtype=torch.int32, device=dev),
            "verified": torch.empty((B, n_max + 1), dtype=torch.int32, device=dev),
            "verified_len": torch.empty(B, dtype=torch.int32, device=dev)}
-    a = sample_args(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature, out)
+    a = sample_args(target_logits, draft_logits, tokens, parent, n_tree, u_accept, u_bonus, temperature, out,
+                    wait_limit_ns)
     if workspace is None:
         workspace = new_workspace(tree_accept_sample_workspace_size(a), dev)
     tree_accept_sample_args(a, workspace, stream)

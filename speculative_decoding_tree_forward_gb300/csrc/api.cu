@@ -587,6 +587,7 @@ ts_status tree_accept_sample(const ts_sample_args* a, void* workspace, size_t wo
   p.num_slices = (a->vocab + p.slice - 1) / p.slice;
   p.scale2 = static_cast<float>(1.4426950408889634 / static_cast<double>(a->temperature));  // log2(e) / T
   if (!std::isfinite(p.scale2)) return TS_ERR_UNSUPPORTED;
+  p.wait_ns = a->wait_limit_ns > 0 ? static_cast<uint64_t>(a->wait_limit_ns) : kWaitLimitNsHost;
   p.tl = a->target_logits;
   p.dl = a->draft_logits;
   p.tokens = a->tokens;

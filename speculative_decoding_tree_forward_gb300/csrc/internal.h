@@ -194,6 +194,7 @@ struct SampleParams {
   int num_req, n_tree_max, vocab;
   int slice, num_slices;  // vocab floats per statistics CTA (multiple of 1024), slices per row (<= 32)
   float scale2;           // log2(e) / temperature: every exponential is 2^(x scale2 - lse2)
+  uint64_t wait_ns;       // bound of each wait in the walk's hand-offs
   const float* tl;
   const float* dl;
   const int32_t* tokens;

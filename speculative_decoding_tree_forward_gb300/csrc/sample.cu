@@ -347,10 +347,10 @@ __device__ __forceinline__ void st_relaxed64(unsigned long long* ptr, unsigned l
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
 }
 // Waits until the word's bits from `shift` up equal `want`, for at most
-// kWaitLimitNs of %globaltimer (read every 32 polls); the word read last goes
-// to *got.
+// limit_ns of %globaltimer (read after the first poll, then every 32); the
+// word read last goes to *got.
 __device__ __forceinline__ bool poll_tag(const unsigned long long* ptr, int shift, unsigned long long want,
-                                         unsigned long long* got) {
+                                         unsigned long long* got, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (unsigned i = 1;; ++i) {
     const unsigned long long v = ld_relaxed64(ptr);
@@ -358,7 +358,7 @@ __device__ __forceinline__ bool poll_tag(const unsigned long long* ptr, int shif
       *got = v;
       return true;
     }
-    if ((i & 31u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 31u) == 1u && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ unsigned long long walk_cmd(unsigned seq, int u, float a) {
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     for (unsigned seq = base + 1;; ++seq) {
       if (tid == 0) {
         unsigned long long c = 0;
-        s_ok = poll_tag(&sync->cmd, 48, static_cast<unsigned long long>(seq & 0xffffu), &c);
+        s_ok = poll_tag(&sync->cmd, 48, static_cast<unsigned long long>(seq & 0xffffu), &c, p.wait_ns);
         s_u = static_cast<int>((c >> 32) & 0xffff);
         s_a = __uint_as_float(static_cast<unsigned>(c));
         if (!s_ok) report_error(p.err, TS_DEVERR_TIMEOUT);
@@ -501,6 +501,10 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
         if (((u >> 10) & 31) != part) return;
         const float ltarget = s_a;
         const int len = u & 1023;
+        if (len < 1 || len > n || seq == base + 1) {  // no call posts this: a word the workspace held before
+          if (tid == 0) report_error(p.err, TS_DEVERR_BAD_WORKSPACE);
+          return;
+        }
         const int64_t row = (nb + last_u) * V;
         const int v = draw_in_slice(p.tl + row, p.dl + row, v0, v1, p.scale2, lt_s[last_u], ld_s[last_u], last_a, bsum,
                                     ltarget, ltarget < 0.f, ds);
@@ -509,6 +513,10 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
           if (p.verified != nullptr) p.verified[static_cast<int64_t>(b) * (p.n_tree_max + 1) + len] = v;
           if (p.verified_len != nullptr) p.verified_len[b] = len + 1;
         }
+        return;
+      }
+      if (u >= n) {  // no call posts this: a word the workspace held before
+        if (tid == 0) report_error(p.err, TS_DEVERR_BAD_WORKSPACE);
         return;
       }
       const int64_t row = (nb + u) * V;
@@ -554,7 +562,7 @@ __global__ void __launch_bounds__(kWalkThreads) sample_walk_kernel(const SampleP
     if (tid == 0) s_tot[0] = mine;
     if (warp == 0 && lane + 1 < K) {  // lane k - 1 collects helper k's answer
       unsigned long long v = 0;
-      if (poll_tag(&sync->slot[lane + 1], 32, static_cast<unsigned long long>(seq), &v)) {
+      if (poll_tag(&sync->slot[lane + 1], 32, static_cast<unsigned long long>(seq), &v, p.wait_ns)) {
         s_tot[lane + 1] = __uint_as_float(static_cast<unsigned>(v));
       } else {
         report_error(p.err, TS_DEVERR_TIMEOUT);

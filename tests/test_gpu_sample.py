@@ -167,6 +167,40 @@ def test_one_workspace_over_many_calls():
                 assert list(got["path"][b][:al]) == opath
 
 
+def test_a_walk_wait_that_runs_out_returns_and_the_next_call_is_right():
+    """With the walk's hand-off waits bounded by 1 ns, a helper CTA that polls
+    for the first command before the leader has posted it gives up
+    (TS_DEVERR_TIMEOUT) and returns, and the leader's wait for that helper's
+    answer runs out in turn: the call's outputs are void and the context stays
+    usable.  On the workspace zeroed again, a call with the default bound
+    matches the oracle."""
+    B, n_max, vocab = 4, 24, 20000
+    acc, tl, dl, u_acc, u_bonus = _case(60, B, n_max, vocab, 0.6)
+    dev = "cuda"
+    a = [torch.from_numpy(tl).to(dev), torch.from_numpy(dl).to(dev), i32_dev(acc.tokens), i32_dev(acc.parent),
+         i32_dev(acc.n_tree), torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_bonus).to(dev)]
+    dummy = {k: torch.empty(1, dtype=torch.int32, device=dev) for k in ("path", "accept_len", "bonus", "verified",
+                                                                        "verified_len")}
+    ws = ts.new_workspace(ts.tree_accept_sample_workspace_size(ts.sample_args(*a, 1.0, dummy)), dev)
+    ts.tree_accept_sample(*a, 1.0, workspace=ws, wait_limit_ns=1)
+    torch.cuda.synchronize()
+    assert ts.read_device_error(ws) & ts.TS_DEVERR_TIMEOUT
+    ws.zero_()
+    got = ts.tree_accept_sample(*a, 1.0, workspace=ws)
+    torch.cuda.synchronize()
+    got = {k: v.cpu().numpy() for k, v in got.items()}
+    assert ts.read_device_error(ws) == 0
+    for b in range(B):
+        n = int(acc.n_tree[b])
+        if n == 0:
+            continue
+        args = (tl[b][:n].astype(np.float64), dl[b][:n].astype(np.float64), acc.tokens[b], acc.parent[b], n, 1.0,
+                u_acc[b], u_bonus[b])
+        opath, margin, r, target = _walk(*args)
+        if margin > MARGIN:
+            assert list(got["path"][b][:int(got["accept_len"][b])]) == opath
+
+
 def test_near_zero_temperature_is_greedy_acceptance_on_gpu():
     acc, tl, dl, u_acc, u_bonus = _case(7, 6, 24, 2000, 1.0)
     got = _run_gpu(acc, tl, dl, u_acc, u_bonus, 1e-3)
