@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4) merge_row_per_half_warp_k
 // 256 threads: 8 / S blocks per CTA.
 constexpr int kPrefetchTc = 4;
 constexpr int kMaxShareGroups = 8;
+static_assert(kPrefetchTc * kMaxShareGroups == kMergeSharesPerRound, "the host caps a unit's shares at one round");
 
 __global__ void __launch_bounds__(256, 2) merge_tc_kernel(const AttnParams p) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;

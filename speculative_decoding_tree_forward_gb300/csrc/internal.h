@@ -33,6 +33,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 constexpr int kBlockN = 64;        // keys per K/V tile
 constexpr int kMaxRowsPerUnit = 128;  // packed query rows handled by one CTA
+// Shares of one unit the tcgen05 path's merge reads in one round of loads
+// (its share groups x shares prefetched per group).
+constexpr int kMergeSharesPerRound = 32;
 constexpr int kMaxRequestsAttn = 1024;
 constexpr size_t kWsHeader = 256;  // error word + padding at the start of every workspace
 constexpr int64_t kCompactBatchBytes = 96 * 1024;  // row-move staging per CTA (two CTAs per SM)
