@@ -201,6 +201,36 @@ def test_a_walk_wait_that_runs_out_returns_and_the_next_call_is_right():
             assert list(got["path"][b][:int(got["accept_len"][b])]) == opath
 
 
+@pytest.mark.parametrize("u_value", [0.0, float(np.float32(1.0) - np.float32(2.0 ** -24))])
+def test_bonus_at_either_end_of_the_distribution(u_value):
+    """Bonus uniforms of 0 (the first token with r > 0: in the leader's own
+    vocab slice) and of the largest float below 1 (the last tokens with
+    r > 0: the last slice, where fp32 rounding can put the target past the
+    slice sums and the slice's last token with r > 0 is taken), checked
+    against the oracle's CDF interval like every bonus."""
+    B, n_max, vocab = 4, 16, 30000
+    acc, tl, dl, u_acc, u_bonus = _case(70, B, n_max, vocab, 0.8)
+    u_bonus = np.full_like(u_bonus, u_value)
+    got = _run_gpu(acc, tl, dl, u_acc, u_bonus, 1.0)
+    for b in range(B):
+        n = int(acc.n_tree[b])
+        if n == 0:
+            continue
+        args = (tl[b][:n].astype(np.float64), dl[b][:n].astype(np.float64), acc.tokens[b], acc.parent[b], n, 1.0,
+                u_acc[b], u_bonus[b])
+        opath, margin, r, target = _walk(*args)
+        if margin <= MARGIN:
+            continue
+        al = int(got["accept_len"][b])
+        assert list(got["path"][b][:al]) == opath
+        c = np.cumsum(r)
+        v = int(got["bonus"][b])
+        assert 0 <= v < vocab
+        lo = c[v - 1] if v > 0 else 0.0
+        assert lo - BONUS_EPS * c[-1] <= target <= c[v] + BONUS_EPS * c[-1], f"request {b} bonus {v}"
+        assert got["verified"][b][al] == v and got["verified_len"][b] == al + 1
+
+
 def test_near_zero_temperature_is_greedy_acceptance_on_gpu():
     acc, tl, dl, u_acc, u_bonus = _case(7, 6, 24, 2000, 1.0)
     got = _run_gpu(acc, tl, dl, u_acc, u_bonus, 1e-3)
